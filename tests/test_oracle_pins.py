@@ -1,0 +1,419 @@
+"""Pins of the CPU oracle against things other than itself.
+
+Each check ties the oracle to a fact fixed outside it: numpy / torch library
+routines (explicit padding + tap sums, torch fp64 conv3d, matmul, bf16
+rounding, F.normalize, F.silu), closed forms, the T=1 causal identity from the
+ROCm/FlyDSL PR "[Flydsl] Add Qwen-Image VAE classic conv shapes to conv3d
+tests" ("T=1 degeneration"), the output-shape rules of the cuDNN frontend doc
+"Fused Conv3D + Bias + Residual + RMSNorm + SiLU" ("Raw Conv3D Variant",
+"Spatial Padding Variant") and hand-worked epilogue values
+(tests/golden/epilogue_cases.txt).
+"""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_bits_from_f32(a):
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def rand_bf16(rng, shape, scale=1.0):
+    return bf16_bits_from_f32(rng.standard_normal(shape).astype(np.float32) * scale)
+
+
+def to_f64(orc, bits):
+    return orc.bf16_to_f32(bits).astype(np.float64)
+
+
+# ---- brute force: explicit padding, then a tap-by-tap valid correlation --------------
+
+def brute_conv(x_ncdhw, w, stride, pads):
+    """float64 reference written without the oracle's index arithmetic:
+    materialise the padded tensor with numpy.pad, then sum shifted slices."""
+    xp = x_ncdhw
+    for axis, (b, a, mode) in zip((2, 3, 4), pads):
+        widths = [(0, 0)] * 5
+        widths[axis] = (b, a)
+        xp = np.pad(xp, widths, mode="reflect" if mode == wl.REFLECT else "constant")
+    N, C, D, H, W = xp.shape
+    Co, _, KT, KR, KS = w.shape
+    st, sh, sw = stride
+    Do = (D - KT) // st + 1
+    Ho = (H - KR) // sh + 1
+    Wo = (W - KS) // sw + 1
+    out = np.zeros((N, Co, Do, Ho, Wo), dtype=np.float64)
+    for t in range(KT):
+        for r in range(KR):
+            for s in range(KS):
+                sl = xp[:, :, t:t + st * (Do - 1) + 1:st, r:r + sh * (Ho - 1) + 1:sh,
+                        s:s + sw * (Wo - 1) + 1:sw]
+                out += np.einsum("ncdhw,oc->nodhw", sl, w[:, :, t, r, s])
+    return out.transpose(0, 2, 3, 4, 1)  # NDHWC
+
+
+def torch_conv(x_ncdhw, w, stride, pads):
+    """float64 torch.nn.functional.conv3d after F.pad (reflect and zero)."""
+    x = torch.from_numpy(x_ncdhw)
+    (tb, ta, tm), (hb, ha, hm), (wb, wa, wm) = pads
+    # spatial pads first (reflect or zero), then the temporal pad
+    if hm == wl.REFLECT or wm == wl.REFLECT:
+        assert hm == wm
+        x = F.pad(x, (wb, wa, hb, ha, 0, 0), mode="reflect")
+    else:
+        x = F.pad(x, (wb, wa, hb, ha, 0, 0))
+    if tm == wl.REFLECT:
+        x = F.pad(x, (0, 0, 0, 0, tb, ta), mode="reflect")
+    else:
+        x = F.pad(x, (0, 0, 0, 0, tb, ta))
+    y = F.conv3d(x, torch.from_numpy(w), stride=stride)
+    return y.numpy().transpose(0, 2, 3, 4, 1)
+
+
+CASES = [
+    # (N, C, D, H, W, Co, kernel, stride, pads)
+    (1, 3, 3, 5, 6, 4, (3, 3, 3), (1, 1, 1), ((0, 0, 0),) * 3),
+    (2, 5, 4, 6, 5, 3, (3, 3, 3), (1, 1, 1), ((1, 1, 0),) * 3),
+    (1, 16, 5, 6, 6, 8, (3, 3, 3), (1, 1, 1), ((2, 0, 0), (1, 1, 1), (1, 1, 1))),
+    (1, 1, 6, 5, 4, 2, (3, 3, 3), (2, 2, 2), ((2, 0, 0), (1, 1, 1), (1, 1, 1))),
+    (1, 3, 2, 6, 6, 5, (1, 3, 3), (1, 2, 2), ((0, 0, 0), (0, 0, 0), (0, 0, 0))),
+    (1, 5, 3, 7, 7, 2, (3, 3, 3), (1, 2, 2), ((2, 0, 0), (1, 1, 1), (1, 1, 1))),
+    (2, 3, 1, 4, 4, 3, (1, 3, 3), (1, 1, 1), ((0, 0, 0), (1, 1, 0), (1, 1, 0))),
+    (1, 4, 3, 3, 3, 4, (1, 1, 1), (1, 1, 1), ((0, 0, 0),) * 3),
+    (1, 2, 4, 2, 2, 3, (3, 3, 3), (1, 1, 1), ((2, 0, 0), (1, 1, 1), (1, 1, 1))),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+@pytest.mark.parametrize("layout", [wl.NCDHW, wl.NDHWC])
+def test_brute_force_and_torch(orc, case, layout):
+    N, C, D, H, W, Co, k, stride, pads = case
+    rng = np.random.default_rng(hash((case, layout)) % (2 ** 32))
+    xb = rand_bf16(rng, (N, C, D, H, W))
+    wb = rand_bf16(rng, (Co, C) + k, 0.3)
+    x_in = xb if layout == wl.NCDHW else np.ascontiguousarray(xb.transpose(0, 2, 3, 4, 1))
+    acc = orc.conv3d_acc(x_in, layout, wb, stride, pads)
+    ref_b = brute_conv(to_f64(orc, xb), to_f64(orc, wb), stride, pads)
+    ref_t = torch_conv(to_f64(orc, xb), to_f64(orc, wb), stride, pads)
+    assert acc.shape == ref_b.shape
+    # bf16 products are exact in fp64 and these sums stay far inside 53 bits,
+    # so all three agree exactly once rounded to fp32.
+    np.testing.assert_array_equal(acc, ref_b.astype(np.float32))
+    np.testing.assert_array_equal(acc, ref_t.astype(np.float32))
+
+
+def test_points_match_full(orc):
+    rng = np.random.default_rng(7)
+    xb = rand_bf16(rng, (2, 8, 5, 7, 9))
+    wb = rand_bf16(rng, (6, 8, 3, 3, 3), 0.2)
+    pads = ((2, 0, 0), (1, 1, 1), (1, 1, 1))
+    full = orc.conv3d_acc(xb, wl.NCDHW, wb, (1, 1, 1), pads)
+    pts = np.array([[0, 0, 0, 0], [1, 4, 6, 8], [0, 2, 3, 0], [1, 0, 6, 4]], dtype=np.int64)
+    sel = orc.conv3d_acc_points(xb, wl.NCDHW, wb, pts, (1, 1, 1), pads)
+    for i, (n, d, h, w) in enumerate(pts):
+        np.testing.assert_array_equal(sel[i], full[n, d, h, w])
+
+
+# ---- special cases and closed forms ---------------------------------------------------
+
+def test_t1_causal_identity(orc):
+    """CausalConv3d(x, W) == Conv2d(x.squeeze(T), W[:, :, 2], padding=1) at T=1."""
+    rng = np.random.default_rng(11)
+    x = rand_bf16(rng, (1, 6, 1, 9, 10))
+    w = rand_bf16(rng, (5, 6, 3, 3, 3), 0.3)
+    causal = ((2, 0, 0), (1, 1, 0), (1, 1, 0))
+    y5 = orc.conv3d_acc(x, wl.NCDHW, w, (1, 1, 1), causal)
+    w2 = np.ascontiguousarray(w[:, :, 2:3])
+    y2 = orc.conv3d_acc(x, wl.NCDHW, w2, (1, 1, 1), ((0, 0, 0), (1, 1, 0), (1, 1, 0)))
+    np.testing.assert_array_equal(y5, y2)
+    # and a symmetric temporal pad is NOT that identity (it would use W[:, :, 1])
+    ysym = orc.conv3d_acc(x, wl.NCDHW, w, (1, 1, 1), ((1, 1, 0), (1, 1, 0), (1, 1, 0)))
+    assert not np.array_equal(ysym, y2)
+
+
+def test_1x1x1_is_gemm(orc):
+    rng = np.random.default_rng(3)
+    x = rand_bf16(rng, (2, 3, 4, 5, 24))  # NDHWC
+    w = rand_bf16(rng, (7, 24, 1, 1, 1), 0.2)
+    y = orc.conv3d_acc(x, wl.NDHWC, w)
+    ref = to_f64(orc, x).reshape(-1, 24) @ to_f64(orc, w).reshape(7, 24).T
+    np.testing.assert_array_equal(y.reshape(-1, 7), ref.astype(np.float32))
+
+
+def test_layout_round_trip(orc):
+    rng = np.random.default_rng(5)
+    xb = rand_bf16(rng, (1, 9, 4, 6, 7))
+    wb = rand_bf16(rng, (4, 9, 3, 3, 3), 0.2)
+    pads = ((2, 0, 0), (1, 1, 1), (1, 1, 1))
+    a = orc.conv3d_acc(xb, wl.NCDHW, wb, (1, 1, 1), pads)
+    b = orc.conv3d_acc(np.ascontiguousarray(xb.transpose(0, 2, 3, 4, 1)), wl.NDHWC, wb,
+                       (1, 1, 1), pads)
+    np.testing.assert_array_equal(a, b)
+    y = orc.round_bf16(a)
+    np.testing.assert_array_equal(orc.from_layout(orc.to_layout(y, wl.NCDHW), wl.NCDHW), y)
+
+
+def _ones(shape):
+    return np.full(shape, 0x3F80, dtype=np.uint16)  # bf16 1.0
+
+
+def test_closed_form_ones_zero_pad(orc):
+    C, D, H, W = 3, 4, 5, 6
+    x = _ones((1, C, D, H, W))
+    w = _ones((2, C, 3, 3, 3))
+    y = orc.conv3d_acc(x, wl.NCDHW, w, (1, 1, 1), ((1, 1, 0),) * 3)
+    # each output counts the in-bounds taps: prod over dims of the window overlap
+    def cnt(o, L):
+        return min(o + 1, L - 1) - max(o - 1, 0) + 1
+    for d in range(D):
+        for h in range(H):
+            for ww in range(W):
+                expect = C * cnt(d, D) * cnt(h, H) * cnt(ww, W)
+                assert y[0, d, h, ww, 0] == expect and y[0, d, h, ww, 1] == expect
+    assert y[0, 1, 1, 1, 0] == C * 27
+
+
+def test_closed_form_ones_reflect(orc):
+    x = _ones((1, 2, 3, 4, 5))
+    w = _ones((1, 2, 3, 3, 3))
+    y = orc.conv3d_acc(x, wl.NCDHW, w, (1, 1, 1), ((1, 1, 1),) * 3)
+    assert np.all(y == 2 * 27)
+    # causal temporal zero pad + reflect spatial: planes 0 and 1 see 1 and 2 frames
+    y = orc.conv3d_acc(x, wl.NCDHW, w, (1, 1, 1), ((2, 0, 0), (1, 1, 1), (1, 1, 1)))
+    assert np.all(y[0, 0] == 2 * 9) and np.all(y[0, 1] == 2 * 18) and np.all(y[0, 2] == 2 * 27)
+
+
+def test_closed_form_one_hot(orc):
+    """A one-hot input at (p, ci) gives out[p - tap + pad] = W[:, ci, tap]:
+    pins the correlation orientation and the causal direction."""
+    rng = np.random.default_rng(9)
+    C, D, H, W = 4, 5, 6, 7
+    w = rand_bf16(rng, (3, C, 3, 3, 3))
+    x = np.zeros((1, C, D, H, W), dtype=np.uint16)
+    p = (2, 3, 4)
+    ci = 2
+    x[0, ci, p[0], p[1], p[2]] = 0x3F80
+    pads = ((2, 0, 0), (1, 1, 0), (1, 1, 0))
+    y = orc.conv3d_acc(x, wl.NCDHW, w, (1, 1, 1), pads)
+    wf = orc.bf16_to_f32(w)
+    seen = 0
+    for t in range(3):
+        for r in range(3):
+            for s in range(3):
+                o = (p[0] - t + 2, p[1] - r + 1, p[2] - s + 1)
+                if 0 <= o[0] < D and 0 <= o[1] < H and 0 <= o[2] < W:
+                    np.testing.assert_array_equal(y[0, o[0], o[1], o[2]], wf[:, ci, t, r, s])
+                    seen += 1
+    assert seen == 27
+    assert np.count_nonzero(np.any(y != 0, axis=-1)) == 27
+
+
+@pytest.mark.parametrize("pads", [((0, 0, 0),) * 3, ((1, 1, 0),) * 3])
+def test_stride_is_subsampling(orc, pads):
+    rng = np.random.default_rng(13)
+    x = rand_bf16(rng, (1, 3, 7, 9, 8))
+    w = rand_bf16(rng, (2, 3, 3, 3, 3), 0.3)
+    full = orc.conv3d_acc(x, wl.NCDHW, w, (1, 1, 1), pads)
+    s2 = orc.conv3d_acc(x, wl.NCDHW, w, (2, 2, 2), pads)
+    np.testing.assert_array_equal(s2, full[:, ::2, ::2, ::2][:, :s2.shape[1], :s2.shape[2],
+                                                              :s2.shape[3]])
+
+
+def test_output_shape_rules(orc):
+    # valid 3x3x3: [N,T,H,W] -> [N,T-2,H-2,W-2] (cuDNN doc, "Raw Conv3D Variant")
+    assert orc.out_dims(8, 106, 182, 3, 3, 3, (1, 1, 1), ((0, 0, 0),) * 3) == (6, 104, 180)
+    # Wan dominant shapes with the pad applied outside (valid)
+    assert orc.out_dims(6, 354, 642, 3, 3, 3, (1, 1, 1), ((0, 0, 0),) * 3) == (4, 352, 640)
+    assert orc.out_dims(3, 46, 82, 3, 3, 3, (1, 1, 1), ((0, 0, 0),) * 3) == (1, 44, 80)
+    # encoder ladder: causal T pad 2 + reflect 1 keeps size; stride 2 halves
+    cr = ((2, 0, 0), (1, 1, 1), (1, 1, 1))
+    assert orc.out_dims(17, 256, 256, 3, 3, 3, (1, 1, 1), cr) == (17, 256, 256)
+    assert orc.out_dims(17, 256, 256, 3, 3, 3, (1, 2, 2), cr) == (17, 128, 128)
+    assert orc.out_dims(17, 128, 128, 3, 3, 3, (2, 2, 2), cr) == (9, 64, 64)
+    assert orc.out_dims(9, 64, 64, 3, 3, 3, (2, 2, 2), cr) == (5, 32, 32)
+    # ZeroPad2d((0,1,0,1)) then k=3 s=2 p=0: 1025 -> 512
+    assert orc.out_dims(1, 1025, 1025, 1, 3, 3, (1, 2, 2), ((0, 0, 0),) * 3) == (1, 512, 512)
+    assert orc.out_dims(1, 257, 257, 1, 3, 3, (1, 2, 2), ((0, 0, 0),) * 3) == (1, 128, 128)
+    with pytest.raises(ValueError):
+        orc.out_dims(1, 4, 4, 1, 3, 3, (1, 1, 1), ((0, 0, 0), (4, 4, 1), (0, 0, 0)))
+
+
+def test_pad_bottom_right(orc):
+    y = np.arange(2 * 3 * 4 * 5, dtype=np.uint16).reshape(1, 2, 3, 4, 5)
+    p = orc.pad_bottom_right(y)
+    assert p.shape == (1, 2, 4, 5, 5)
+    np.testing.assert_array_equal(p[:, :, :3, :4], y)
+    assert np.all(p[:, :, 3] == 0) and np.all(p[:, :, :, 4] == 0)
+
+
+# ---- bf16 rounding, pack ----------------------------------------------------------------
+
+def test_round_bf16_matches_torch(orc):
+    rng = np.random.default_rng(1)
+    mags = (10.0 ** rng.integers(-30, 30, 200000)).astype(np.float32)
+    vals = [rng.standard_normal(200000).astype(np.float32) * mags]
+    # exact ties, subnormals, signed zero, infinities, near-overflow
+    base = np.arange(0, 1 << 16, dtype=np.uint32) << 16
+    vals.append((base | 0x8000).view(np.float32))
+    vals.append((base | 0x7FFF).view(np.float32))
+    vals.append((base | 0x8001).view(np.float32))
+    vals.append(np.array([0.0, -0.0, np.inf, -np.inf, 3.3895e38, -3.3895e38, 1e-40, -1e-45],
+                         dtype=np.float32))
+    f = np.concatenate(vals)
+    f = f[~np.isnan(f)]
+    ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(orc.round_bf16(f), ref)
+    nan = orc.round_bf16(np.array([np.nan], dtype=np.float32))
+    assert np.isnan(orc.bf16_to_f32(nan))[0]
+
+
+@pytest.mark.parametrize("shape", [(5, 3, 3, 3, 3), (4, 64, 3, 3, 3), (3, 96, 1, 3, 3),
+                                   (2, 130, 1, 1, 1)])
+def test_pack_weight(orc, shape):
+    rng = np.random.default_rng(2)
+    w = rand_bf16(rng, shape)
+    p = orc.pack_weight(w)
+    Co, Ci, KT, KR, KS = shape
+    cp = -(-Ci // 64) * 64
+    ref = np.zeros((Co, KT, KR, KS, cp), dtype=np.uint16)
+    ref[..., :Ci] = np.transpose(w, (0, 2, 3, 4, 1))
+    np.testing.assert_array_equal(p, ref)
+
+
+# ---- epilogue -------------------------------------------------------------------------------
+
+def _parse_sparse(spec, C, default=0.0):
+    v = np.full(C, default, dtype=np.float32)
+    if spec == "-":
+        return None
+    for item in spec.split(","):
+        if item.startswith("all="):
+            v[:] = float(item[4:])
+        else:
+            k, val = item.split(":")
+            v[int(k)] = float(val)
+    return v
+
+
+def _golden_cases():
+    cases = []
+    with open(os.path.join(GOLDEN, "epilogue_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            cases.append([c.strip() for c in line.split("|")])
+    return cases
+
+
+@pytest.mark.parametrize("case", _golden_cases(), ids=lambda c: c[0])
+def test_epilogue_golden(orc, case):
+    name, C, flags_s, conv_s, bias_s, res_s, rb_s, gamma_s, field, exp_s = case
+    C = int(C)
+    names = {"BIAS": orc.BIAS, "RESIDUAL": orc.RESIDUAL, "RESIDUAL_BIAS": orc.RESIDUAL_BIAS,
+             "L2NORM": orc.L2NORM_SILU}
+    flags = 0
+    for f in flags_s.split(","):
+        flags |= names[f]
+    conv = _parse_sparse(conv_s, C)
+    conv = np.zeros(C, np.float32) if conv is None else conv
+    bias = _parse_sparse(bias_s, C)
+    res = _parse_sparse(res_s, C)
+    rb = _parse_sparse(rb_s, C)
+    gamma = _parse_sparse(gamma_s, C)
+    if flags & orc.BIAS and bias is None:
+        bias = np.zeros(C, np.float32)
+    out = orc.epilogue(orc.round_bf16(conv[None]), flags, bias,
+                       None if res is None else orc.round_bf16(res[None]), rb, gamma)
+    expect = _parse_sparse(exp_s, C)
+    expect = np.zeros(C, np.float32) if expect is None else expect
+    np.testing.assert_array_equal(orc.bf16_to_f32(out[field][0]), expect)
+
+
+def _ulp_dist(orc, a, b):
+    def ordinal(u):
+        i = u.astype(np.int32)
+        neg = (i & 0x8000) != 0
+        mag = i & 0x7FFF
+        return np.where(neg, -mag, mag)
+    return np.abs(ordinal(a) - ordinal(b))
+
+
+def test_norm_invariant_and_library(orc):
+    """||normalized||_2 ~= 1 within bf16 rounding; normalized and SiLU agree with
+    F.normalize / F.silu evaluated in float64 to within 1 bf16 ulp per step."""
+    rng = np.random.default_rng(21)
+    for C in (16, 32, 160, 320, 640):
+        M = 300
+        conv = rand_bf16(rng, (M, C))
+        bias = rng.standard_normal(C).astype(np.float32) * 0.1
+        gamma = orc.bf16_to_f32(rand_bf16(rng, (C,), 0.1)) + 1.0
+        res = rand_bf16(rng, (M, C))
+        flags = orc.BIAS | orc.RESIDUAL | orc.L2NORM_SILU
+        out = orc.epilogue(conv, flags, bias, res, None, gamma)
+        value = to_f64(orc, out["value"])
+        nrm = F.normalize(torch.from_numpy(value), dim=1, eps=1e-12).numpy()
+        n_bits = bf16_bits_from_f32(nrm.astype(np.float32))
+        norms = np.linalg.norm(orc.bf16_to_f32(n_bits).astype(np.float64), axis=1)
+        assert np.all(np.abs(norms - 1.0) <= 2.0 ** -8)
+        # activated from the library: silu(B(B(n * sqrt C) * gamma))
+        sc = orc.round_bf16((orc.bf16_to_f32(n_bits) * np.float32(np.sqrt(np.float32(C))))
+                            .astype(np.float32))
+        af = orc.round_bf16(orc.bf16_to_f32(sc) * gamma[None, :])
+        act_lib = bf16_bits_from_f32(
+            F.silu(torch.from_numpy(orc.bf16_to_f32(af).astype(np.float64))).numpy()
+            .astype(np.float32))
+        d = _ulp_dist(orc, out["act"], act_lib)
+        assert d.max() <= 2, d.max()
+        assert np.mean(d == 0) > 0.97
+
+
+def test_zero_row_and_silu_zero(orc):
+    C = 32
+    conv = np.zeros((3, C), dtype=np.uint16)
+    out = orc.epilogue(conv, orc.L2NORM_SILU, gamma=np.ones(C, np.float32))
+    assert np.all(out["act"] == 0)
+
+
+def test_l2norm_silu_standalone_matches_epilogue(orc):
+    """The standalone variant with input_bias equals the fused contract applied
+    to raw = conv ("main = B(raw + input_bias)")."""
+    rng = np.random.default_rng(31)
+    C = 64
+    raw = rand_bf16(rng, (50, C))
+    bias = rng.standard_normal(C).astype(np.float32) * 0.1
+    res = rand_bf16(rng, (50, C))
+    rb = rng.standard_normal(C).astype(np.float32) * 0.1
+    gamma = np.ones(C, np.float32)
+    y, v = orc.l2norm_silu(raw, gamma, bias, res, rb)
+    e = orc.epilogue(raw, orc.BIAS | orc.RESIDUAL | orc.RESIDUAL_BIAS | orc.L2NORM_SILU,
+                     bias, res, rb, gamma)
+    np.testing.assert_array_equal(y, e["act"])
+    np.testing.assert_array_equal(v, e["value"])
+    # without input_bias, main is raw itself
+    y2, v2 = orc.l2norm_silu(raw, gamma)
+    np.testing.assert_array_equal(v2, raw)
+
+
+def test_forward_small_workload_against_torch(orc):
+    """The seeded tiny workload through oracle.forward: conv equals the bf16
+    rounding of torch's fp64 conv3d."""
+    w = wl.tiny()
+    call = w.calls[0]
+    inp = wl.make_inputs("tiny", call)
+    xb = wl.bits(inp["x"])
+    wb = wl.bits(inp["w"])
+    out = orc.forward(xb, wl.NDHWC, wb, call.stride, call.pads, wl.NDHWC, orc.BIAS,
+                      bias=inp["bias"].numpy())
+    x64 = inp["x"].double().permute(0, 4, 1, 2, 3).numpy()
+    ref = torch_conv(x64, inp["w"].double().numpy(), call.stride, call.pads)
+    np.testing.assert_array_equal(out["conv"], bf16_bits_from_f32(ref.astype(np.float32)))
