@@ -1,0 +1,371 @@
+"""Benchmark: bf16 implicit-GEMM conv3d on one GB300 (per layer TFLOP/s and chain ms).
+
+Workload (one step = one pass of the whole chain): the Wan-like channel-constant
+chain of valid convolutions (pad applied outside) — x [1,96,6,354,642] with
+w [96,96,3,3,3]; x [1,384,3,46,82] with w [384,384,3,3,3]; rank-4 x [4,96,353,641]
+with w [96,96,3,3] — each run once with NCDHW input/output and once with NDHWC
+throughout.  Inputs are seeded synthetic tensors of those shapes.
+
+Prints one JSON line.  `value` is chain TFLOP/s (algorithmic FLOP of the six
+calls / device time of one chain), inputs resident in HBM, L2 flushed between
+steps.  `e2e` is the same metric with pinned host inputs copied in and outputs
+copied out inside the timed region.  `--impl reference` times the CPU oracle
+on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as wl  # noqa: E402
+
+WORKLOAD_NAME = "wan"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def chain_calls():
+    w = wl.wan()
+    out = []
+    for lay in (wl.NCDHW, wl.NDHWC):
+        for call in w.calls:
+            out.append((call, lay))
+    return out
+
+
+def workload_config(args, extra=None):
+    cfg = {"workload": "wan_chain: valid 3x3x3 96->96 [1,96,6,354,642], 384->384 "
+                       "[1,384,3,46,82], 3x3 96->96 [4,96,353,641]; each NCDHW->NCDHW and "
+                       "NDHWC->NDHWC",
+           "calls_per_step": 6, "l2": "flushed between steps (256 MiB write, untimed)",
+           "inputs": "seeded synthetic N(0,1) bf16, weights N(0,1/sqrt(fan_in))"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---- CPU oracle legs ------------------------------------------------------------------------
+
+def oracle_rate(target_s=12.0, max_points=None):
+    """Times the oracle on sampled output pixels of every chain call; returns
+    (TFLOP/s, cores, sample description)."""
+    import oracle
+    oracle.build()
+    cores = oracle.num_threads(0)
+    flops = 0.0
+    t_total = 0.0
+    samples = []
+    per_call = target_s / 3.0
+    for call in wl.wan().calls:
+        inp = wl.make_inputs("wan", call, wl.NDHWC)
+        xb, wb = wl.bits(inp["x"]), wl.bits(inp["w"])
+        Do, Ho, Wo = call.out_dims()
+        fpp = 2.0 * call.Cout * call.K  # FLOP per output pixel
+        rng = np.random.default_rng(1)
+        n = 64
+        spent = 0.0
+        while spent < per_call and (max_points is None or n <= max_points):
+            pts = np.stack([rng.integers(0, call.N, n), rng.integers(0, Do, n),
+                            rng.integers(0, Ho, n), rng.integers(0, Wo, n)], 1)
+            t0 = time.perf_counter()
+            oracle.conv3d_acc_points(xb, wl.NDHWC, wb, pts, call.stride, call.pads)
+            dt = time.perf_counter() - t0
+            spent += dt
+            t_total += dt
+            flops += fpp * n
+            samples.append(n)
+            n = min(n * 2, 1 << 16)
+    rate = flops / t_total / 1e12
+    desc = (f"oracle direct conv (fp64 accumulate) on {sum(samples)} sampled output pixels "
+            f"across the 3 chain shapes, {t_total:.1f} s")
+    return rate, cores, desc
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    budget = 8.0
+    rates = []
+    for _ in range(args.warmup):
+        oracle_rate(target_s=1.0)
+    t0 = time.perf_counter()
+    desc = ""
+    cores = 0
+    for _ in range(args.steps):
+        r, cores, desc = oracle_rate(target_s=budget)
+        rates.append(r)
+    elapsed = time.perf_counter() - t0
+    value = statistics.median(rates)
+    total_flop = sum(c.flops for c, _ in chain_calls())
+    line = {"impl": "reference", "metric": "bf16 conv3d TFLOP/s (chain)", "value": value,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total_flop / (value * 1e12) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(args),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": elapsed}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- GPU arm -------------------------------------------------------------------------------
+
+def run_gpu(args, rank, world):
+    import video_vae_convolution_gb300 as vvc
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+    calls = []
+    host = []
+    for call, lay in chain_calls():
+        inp = wl.make_inputs("wan", call, lay, lay)
+        x = inp["x"].to(dev)
+        wp = vvc.pack_weight(inp["w"].to(dev))
+        c = vvc.Conv3d(x, wp, call.Cout, call.kernel, call.stride, call.pads, lay, lay, 0)
+        calls.append((call, lay, c))
+        host.append(inp["x"].pin_memory())
+    torch.cuda.synchronize()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    total_flop = sum(call.flops for call, _, _ in calls)
+    launches_per_step = sum(c.launches for _, _, c in calls)
+
+    def chain(evs=None):
+        for i, (_, _, c) in enumerate(calls):
+            if evs is not None:
+                evs[i][0].record(stream)
+            rc = c.run(stream)
+            if rc != 0:
+                raise RuntimeError(f"conv3d_fwd failed: {rc}")
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        chain()
+    torch.cuda.synchronize()
+    assert vvc.device_status() == 0
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    per_call = [[] for _ in calls]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    step_ev = []
+    for _ in range(args.steps):
+        flush.zero_()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in calls]
+        chain(evs)
+        step_ev.append(evs)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    status = vvc.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+    step_ms = []
+    for evs in step_ev:
+        tot = 0.0
+        for i, (a, b) in enumerate(evs):
+            ms = a.elapsed_time(b)
+            per_call[i].append(ms)
+            tot += ms
+        step_ms.append(tot)
+    ms_step = statistics.mean(step_ms)
+    ms_step = max_over_ranks(ms_step, world)
+    value = world * total_flop / (ms_step * 1e-3) / 1e12
+
+    layers = []
+    for (call, lay, c), ts in zip(calls, per_call):
+        ms = statistics.median(ts)
+        tf = call.flops / (ms * 1e-3) / 1e12
+        layers.append({"name": call.name, "layout": "NCDHW" if lay == wl.NCDHW else "NDHWC",
+                       "ms": round(ms, 4), "tflops": round(tf, 1),
+                       "frac_bf16": round(tf / pk["bf16_tflops"], 3),
+                       "gbs": round(call.bytes() / (ms * 1e-3) / 1e9, 1),
+                       "launches": c.launches})
+    # dominant kernel: the 96->96 3-D call in NDHWC (one conv launch)
+    dom_i = next(i for i, (call, lay, c) in enumerate(calls)
+                 if call.name == "wan_96_3d" and lay == wl.NDHWC)
+    dom_call, _, dom_c = calls[dom_i]
+    dom_ms = statistics.mean(per_call[dom_i])
+    achieved = dom_call.flops / (dom_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
+                "traffic": None, "kernel": "vvc::conv_tc_kernel (wan_96_3d, NDHWC)",
+                "peak_source": pk["source"] + " burst bf16"}
+
+    # e2e: pinned host inputs -> device, chain, outputs -> pinned host
+    outs_host = [torch.empty(c.y.shape, dtype=torch.bfloat16).pin_memory() for _, _, c in calls]
+    h2d = sum(h.numel() * 2 for h in host)
+    d2h = sum(o.numel() * 2 for o in outs_host)
+    e2e_steps = max(1, min(args.steps, 5))
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for (call, lay, c), h in zip(calls, host):
+            c.x.copy_(h, non_blocking=True)
+        chain()
+        for (call, lay, c), o in zip(calls, outs_host):
+            o.copy_(c.y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    e2e_val = world * total_flop / (e2e_ms * 1e-3) / 1e12
+
+    line = {"metric": "bf16 conv3d TFLOP/s (chain)", "value": round(value, 2),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(args, {"parallelism": f"replicas x{world}"}),
+            "roofline": roofline, "clocks": clocks,
+            "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+            "gpu_launches": launches_per_step * args.steps,
+            "layers": layers, "wall_s": round(wall, 3)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r, cores, desc = oracle_rate(target_s=12.0)
+        line["cpu_baseline"] = {"value": r, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl != "reference" else args.warmup
+    rank, world = dist_init(args)
+    if args.impl == "reference":
+        rc = run_reference(args, rank, world)
+    else:
+        rc = run_gpu(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,210 @@
+/*
+ * conv3d.h — C ABI of the GB300 (sm_103a) video-VAE convolution library.
+ *
+ * The library computes the bf16 forward convolution of a video VAE layer as
+ * an implicit GEMM over channels-last activations, with an optional fused
+ * post-operation epilogue, and a standalone form of that epilogue.
+ *
+ * Sources (web pages, cited by title and section):
+ *  - ROCm/FlyDSL issue "[Feature]: conv3d_implicit — accept and emit NDHWC so
+ *    chained convs skip the layout round-trip", section "Ask": the op
+ *    conv3d_implicit(x, weight, bias, stride, padding, layout, out_layout) with
+ *    NCDHW or NDHWC input and output; comment "The call site is already a clean
+ *    drop-in": spatial reflect pad + temporal causal zero pad.
+ *  - ROCm/FlyDSL PR "[Flydsl] Add Qwen-Image VAE classic conv shapes to conv3d
+ *    tests", sections "T=1 degeneration" and "Downsample Conv2d": rank-4
+ *    (T=1) convolutions and the stride-2 downsample.
+ *  - cuDNN frontend doc "Fused Conv3D + Bias + Residual + RMSNorm + SiLU",
+ *    sections "Operation Contract" (epilogue arithmetic and its BF16 rounding
+ *    points), "Requirements" (16-byte alignment, no overlap), "Weight Packing"
+ *    (OITRS -> OTRSI, Ci padded to a multiple of 64), "Spatial Padding Variant"
+ *    (zero bottom row and right column), "Standalone Normalization and Padding
+ *    Variant" (post-operations without a convolution).
+ *
+ * Conventions for every entry point:
+ *  - Tensor pointers are caller-owned DEVICE memory of the current CUDA
+ *    device.  The library never allocates, never frees and never synchronises
+ *    the stream (except conv3d_get_device_status, which reads a status word).
+ *  - bf16 tensors are dense and contiguous in their declared layout, 16-byte
+ *    aligned.  fp32 vectors (bias, residual_bias, gamma) hold Cout values and
+ *    are 16-byte aligned.
+ *  - Outputs and workspace must not overlap any operand or each other.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *  - Every argument is validated before anything is launched; on a negative
+ *    return nothing was enqueued.  A CUDA launch error returns
+ *    CONV3D_ERR_CUDA.  A device-side wait that ran out of time records
+ *    CONV3D_ERR_DEVICE_TIMEOUT in a device status word, read with
+ *    conv3d_get_device_status.
+ *  - Rank-4 (N, C, H, W) tensors are passed as D = 1 with KT = 1.
+ */
+#ifndef VVC_CONV3D_H
+#define VVC_CONV3D_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* conv3d_stream_t; /* same type as cudaStream_t */
+
+/* ---- status codes ------------------------------------------------------------ */
+enum {
+  CONV3D_OK = 0,
+  CONV3D_ERR_INVALID_ARG = -1,   /* null pointer, bad shape or flag combination */
+  CONV3D_ERR_UNSUPPORTED = -2,   /* valid request outside what the kernels cover */
+  CONV3D_ERR_MISALIGNED = -3,    /* a tensor pointer is not 16-byte aligned */
+  CONV3D_ERR_OVERLAP = -4,       /* an output / workspace overlaps another buffer */
+  CONV3D_ERR_WORKSPACE = -5,     /* workspace missing or too small */
+  CONV3D_ERR_CUDA = -6,          /* a CUDA runtime / driver call failed */
+  CONV3D_ERR_DEVICE_TIMEOUT = -7 /* a kernel's bounded wait ran out (device word) */
+};
+
+/* ---- layouts and padding ------------------------------------------------------ */
+enum { CONV3D_NCDHW = 0, CONV3D_NDHWC = 1 };
+enum { CONV3D_PAD_ZERO = 0, CONV3D_PAD_REFLECT = 1 };
+
+/* Padding of one spatial dimension.  Zero: coordinates outside [0, L) read 0
+ * (a causal temporal pad is before = 2, after = 0).  Reflect: PyTorch 'reflect'
+ * (edge not repeated); needs before, after < L. */
+typedef struct {
+  int32_t before;
+  int32_t after;
+  int32_t mode;
+} conv3d_pad;
+
+/* ---- epilogue flags ([cuDNN page] "Operation Contract") --------------------------
+ * With acc the fp32 accumulator and B() the fp32 -> bf16 round to nearest even:
+ *   conv  = B(acc)
+ *   main  = B(conv + bias[c])                        if CONV3D_EPI_BIAS, else conv
+ *   skip  = residual, or B(residual + residual_bias[c]) with RESIDUAL_BIAS
+ *   value = B(main + skip)                           if CONV3D_EPI_RESIDUAL, else main
+ *   with CONV3D_EPI_L2NORM_SILU, over the full channel row of each pixel:
+ *     den = max(sqrt(sum_c value_c^2), 1e-12); normalized = B(value / den)
+ *     scaled = B(normalized * sqrt(Cout)); affine = B(scaled * gamma[c])
+ *     y = B(affine / (1 + exp(-affine)))
+ *   otherwise y = value.
+ * No reassociation: every B() above is applied. */
+enum {
+  CONV3D_EPI_BIAS = 1,
+  CONV3D_EPI_RESIDUAL = 2,
+  CONV3D_EPI_RESIDUAL_BIAS = 4,   /* requires RESIDUAL */
+  CONV3D_EPI_L2NORM_SILU = 8,     /* requires gamma */
+  CONV3D_EPI_SAVE_VALUE = 16,     /* also write value (pre-normalisation) to value_out */
+  CONV3D_EPI_OUT_PAD_BR = 32,     /* y gets a zero bottom row and right column:
+                                     y spatial extent (Ho + 1, Wo + 1); not with L2NORM */
+  CONV3D_EPI_DEBUG_STORE_CONV = 1 << 30 /* test aid: also write B(acc) to conv_out, NDHWC */
+};
+
+/* One convolution call.
+ *  x          input, bf16, `layout`: NCDHW [N, Cin, D, H, W] or NDHWC [N, D, H, W, Cin].
+ *  w_packed   weights packed by conv3d_pack_weight: [Cout][KT][KR][KS][Cin_pad64] bf16.
+ *  stride     (T, H, W) strides >= 1.
+ *  pad        (T, H, W) paddings.  Output extent per dimension:
+ *             (L + before + after - K) / stride + 1.
+ *  y          output, bf16, `out_layout`, [N, Cout, Do, Ho, Wo] or [N, Do, Ho, Wo, Cout]
+ *             (Ho + 1, Wo + 1 with CONV3D_EPI_OUT_PAD_BR).
+ *  bias, residual_bias, gamma   fp32 [Cout], as the flags require (else NULL).
+ *  residual   bf16, `out_layout`, unpadded output shape (with CONV3D_EPI_RESIDUAL).
+ *  value_out  bf16, `out_layout`, unpadded output shape (with CONV3D_EPI_SAVE_VALUE).
+ *  conv_out   bf16 NDHWC unpadded output shape (with CONV3D_EPI_DEBUG_STORE_CONV).
+ *  workspace  device scratch of at least conv3d_workspace_bytes() (may be NULL if 0). */
+typedef struct {
+  const void* x;
+  int32_t layout;
+  int32_t N, Cin, D, H, W;
+  const void* w_packed;
+  int32_t Cout, KT, KR, KS;
+  int32_t stride[3];
+  conv3d_pad pad[3];
+  void* y;
+  int32_t out_layout;
+  uint32_t epi;
+  const float* bias;
+  const void* residual;
+  const float* residual_bias;
+  const float* gamma;
+  void* value_out;
+  void* conv_out;
+  void* workspace;
+  size_t workspace_bytes;
+} conv3d_params;
+
+/* Optional plan overrides (tests and tuning).  0 (or -1 where noted) = automatic. */
+typedef struct {
+  int32_t tile_w;      /* output pixels per M-tile row (<= 128) */
+  int32_t tile_h;      /* output rows per M-tile (tile_w * tile_h <= 128) */
+  int32_t R;           /* M-tiles per CTA */
+  int32_t kc;          /* channels per K chunk: 16, 32 or 64 */
+  int32_t BN;          /* output channels per CTA (multiple of 16) */
+  int32_t halo;        /* -1 auto, 0 off, 1 on: one input-row halo serves all W taps */
+  int32_t stages;      /* shared-memory pipeline depth */
+  int32_t k_splits;    /* split of the reduction across CTAs (>= 1) */
+  int32_t desc_mode;   /* shared-memory descriptor base offset: 0 auto, 1 always zero,
+                          2 taken from the start address bits */
+  int32_t inject;      /* test aid: >0 makes the producer skip stage (inject-1) so a
+                          bounded wait runs out; the call then reports a timeout */
+  int32_t timeout_ms;  /* device wait limit (0 = default 4000 ms) */
+} conv3d_tuning;
+
+/* ---- weight packing ([cuDNN page] "Weight Packing") ------------------------------ */
+
+/* Bytes of the packed weight: Cout * KT * KR * KS * round_up(Cin, 64) * 2. */
+size_t conv3d_packed_weight_bytes(int32_t Cout, int32_t Cin, int32_t KT, int32_t KR,
+                                  int32_t KS);
+
+/* Packs checkpoint weights OITRS [Cout][Cin][KT][KR][KS] bf16 (device) into OTRSI
+ * [Cout][KT][KR][KS][Cin_pad64] bf16 (device), zero-filling channels Cin..Cin_pad64-1.
+ * Pack once; repack after the source weights change. */
+int conv3d_pack_weight(const void* w_oitrs, int32_t Cout, int32_t Cin, int32_t KT,
+                       int32_t KR, int32_t KS, void* w_packed, conv3d_stream_t stream);
+
+/* ---- convolution ---------------------------------------------------------------- */
+
+/* Scratch bytes conv3d_fwd needs for *p (0 for NDHWC inputs with Cin % 8 == 0 that
+ * need no split of the reduction).  Returns a status; *bytes is set on success. */
+int conv3d_workspace_bytes(const conv3d_params* p, size_t* bytes);
+int conv3d_workspace_bytes_ex(const conv3d_params* p, const conv3d_tuning* tuning,
+                              size_t* bytes);
+
+/* Enqueues the convolution and its epilogue on `stream`. */
+int conv3d_fwd(const conv3d_params* p, conv3d_stream_t stream);
+int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning,
+                  conv3d_stream_t stream);
+
+/* Number of kernel launches conv3d_fwd(_ex) enqueues for *p (for accounting). */
+int conv3d_launch_count(const conv3d_params* p, const conv3d_tuning* tuning);
+
+/* ---- standalone post-operations ([cuDNN page] "Standalone Normalization and
+ *      Padding Variant", contiguous output) ---------------------------------------
+ * x: bf16 [rows][C] (rows = N*T*H*W, channels last).  main = B(x + input_bias) when
+ * input_bias is non-NULL, else x; then the residual / L2-norm / SiLU steps of the
+ * epilogue contract.  y: bf16 [rows][C].  value_out (optional, bf16 [rows][C])
+ * receives the pre-normalisation value.  residual / residual_bias optional
+ * (residual_bias requires residual). */
+int l2norm_silu(const void* x, int64_t rows, int32_t C, const float* input_bias,
+                const void* residual, const float* residual_bias, const float* gamma,
+                void* y, void* value_out, conv3d_stream_t stream);
+
+/* ---- status ---------------------------------------------------------------------- */
+
+/* Synchronises `stream`, then reads and clears the device status word: *status
+ * is CONV3D_OK or CONV3D_ERR_DEVICE_TIMEOUT.  Returns CONV3D_ERR_CUDA if the copy
+ * fails. */
+int conv3d_get_device_status(int32_t* status, conv3d_stream_t stream);
+
+const char* conv3d_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int conv3d_version(void);
+
+/* sizeof() of the ABI structs, for bindings to check their mirrors:
+ * which = 0 conv3d_params, 1 conv3d_tuning, 2 conv3d_pad; 0 otherwise. */
+size_t conv3d_struct_size(int which);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VVC_CONV3D_H */

@@ -1,0 +1,150 @@
+"""GPU parity of the convolution library against the CPU oracle, through the C ABI.
+
+Small shapes are checked element by element on the whole output; they span
+several M-tiles, ragged W / H tails, every padding mode (zero, causal temporal,
+reflect spatial), strides 1 and 2, both layouts on both sides, narrow input and
+output channels, split reductions, and each plan variant (halo / direct, K
+chunk 16 / 32 / 64, tiles per CTA).  Tolerances are in tests/gpu_parity.py.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import video_vae_convolution_gb300 as vvc
+import workloads as wl
+from gpu_parity import GpuCall, check_conv, check_epilogue, full_reference, ulp_dist
+
+pytestmark = pytest.mark.gpu
+
+Z = wl.ZERO
+R = wl.REFLECT
+CR = ((2, 0, Z), (1, 1, R), (1, 1, R))     # causal T + reflect H, W
+P1 = ((1, 1, Z),) * 3
+P2D = ((0, 0, Z), (1, 1, Z), (1, 1, Z))
+VALID = ((0, 0, Z),) * 3
+
+
+def mk(name, N, Cin, D, H, W, Cout, kernel=(3, 3, 3), stride=(1, 1, 1), pads=P1, epi=0,
+       index=0, **kw):
+    return wl.ConvCall(name, N, Cin, D, H, W, Cout, kernel=kernel, stride=stride, pads=pads,
+                       epi=epi, index=index, **kw)
+
+
+def run_and_check(call, layout=wl.NDHWC, out_layout=wl.NDHWC, tuning=None, extra_epi=0):
+    inp = wl.make_inputs("test", call, layout, out_layout)
+    gc = GpuCall(call, inp, layout, out_layout, tuning=tuning, extra_epi=extra_epi)
+    acc = full_reference(gc)
+    check_conv(gc.conv, acc, call.name)
+    check_epilogue(gc)
+    return gc, acc
+
+
+def test_pack_weight_bit_exact():
+    for shape in [(32, 16, 3, 3, 3), (96, 3, 3, 3, 3), (3, 96, 1, 3, 3), (40, 130, 1, 1, 1)]:
+        w = wl.to_bf16(wl.normal(shape, 99))
+        got = vvc.pack_weight(w.cuda())
+        np.testing.assert_array_equal(wl.bits(got.cpu()), oracle.pack_weight(wl.bits(w)))
+
+
+BASE = mk("base", 1, 64, 3, 6, 150, 64, index=1)
+
+PLAN_VARIANTS = [
+    dict(halo=0),
+    dict(halo=1, desc_mode=1),
+    dict(halo=1, desc_mode=2),
+    dict(halo=0, kc=32),
+    dict(halo=0, kc=16),
+    dict(halo=1, kc=32, desc_mode=1),
+    dict(halo=1, kc=32, desc_mode=2),
+    dict(halo=1, kc=16, desc_mode=1),
+    dict(halo=1, kc=16, desc_mode=2),
+    dict(halo=0, R=2),
+    dict(halo=1, R=3, BN=32),
+    dict(halo=0, k_splits=3),
+    dict(halo=1, k_splits=2),
+    dict(halo=0, stages=2),
+]
+
+
+@pytest.mark.parametrize("tv", PLAN_VARIANTS, ids=lambda d: "-".join(f"{k}{v}" for k, v in d.items()))
+def test_plan_variants(tv):
+    tv = dict(tv)
+    tv.setdefault("k_splits", 1)
+    run_and_check(BASE, tuning=vvc.Tuning(**tv))
+
+
+SHAPES = [
+    mk("t1_2d_tiles_h", 2, 32, 1, 9, 40, 48, kernel=(1, 3, 3), pads=P2D, index=2),
+    mk("stride2_causal_reflect", 1, 32, 5, 11, 71, 32, stride=(2, 2, 2), pads=CR, index=3),
+    mk("reflect_causal_wide", 1, 16, 4, 7, 133, 32, pads=CR, index=4),
+    mk("narrow_cin3", 1, 3, 3, 10, 140, 96, pads=CR, index=5),
+    mk("narrow_cout3", 1, 96, 1, 12, 130, 3, kernel=(1, 3, 3), pads=P2D, index=6),
+    mk("pointwise", 2, 64, 2, 5, 37, 32, kernel=(1, 1, 1), pads=VALID, index=7),
+    mk("down2d", 1, 32, 1, 65, 65, 32, kernel=(1, 3, 3), stride=(1, 2, 2), pads=VALID,
+       zero_pad_br_input=True, index=8),
+    mk("valid3d_small_w", 1, 96, 4, 10, 21, 96, pads=VALID, index=9),
+    mk("stride_122", 1, 48, 3, 12, 260, 64, stride=(1, 2, 2), pads=CR, index=10),
+    mk("cout48_cin1024ish", 1, 256, 2, 6, 20, 48, pads=CR, index=11),
+]
+
+
+@pytest.mark.parametrize("call", SHAPES, ids=lambda c: c.name)
+def test_shapes(call):
+    run_and_check(call)
+
+
+@pytest.mark.parametrize("lay", [(wl.NCDHW, wl.NCDHW), (wl.NCDHW, wl.NDHWC), (wl.NDHWC, wl.NCDHW)])
+def test_layouts_parity_and_bit_identity(lay):
+    call = mk("layouts", 1, 40, 3, 7, 140, 32, pads=CR, epi=wl.EPI_BIAS, index=12)
+    gc, _ = run_and_check(call, lay[0], lay[1])
+    ref = GpuCall(call, wl.make_inputs("test", call, wl.NDHWC, wl.NDHWC))
+    # same plan, same MMA order: the four layout combinations are bit-identical
+    np.testing.assert_array_equal(oracle.from_layout(gc.y, lay[1]), ref.y)
+
+
+EPI_CASES = [
+    mk("epi_bias_res_rbias", 1, 32, 3, 6, 140, 64, pads=P1,
+       epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_RESIDUAL_BIAS, index=13),
+    mk("epi_norm160", 1, 32, 3, 6, 140, 160, pads=P1, epi=wl.EPI_BIAS | wl.EPI_L2NORM_SILU,
+       index=14),
+    mk("epi_norm320_res", 1, 64, 3, 5, 70, 320, pads=P1,
+       epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_L2NORM_SILU | wl.EPI_SAVE_VALUE, index=15),
+    mk("epi_pad_br", 1, 64, 4, 9, 140, 64, pads=VALID,
+       epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_RESIDUAL_BIAS | wl.EPI_OUT_PAD_BR, index=16),
+]
+
+
+@pytest.mark.parametrize("call", EPI_CASES, ids=lambda c: c.name)
+@pytest.mark.parametrize("out_layout", [wl.NDHWC, wl.NCDHW])
+def test_epilogues(call, out_layout):
+    run_and_check(call, wl.NDHWC, out_layout)
+
+
+def test_epilogue_split_k_matches():
+    call = mk("epi_split", 1, 64, 3, 5, 70, 160, pads=P1,
+              epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_L2NORM_SILU, index=17)
+    run_and_check(call, tuning=vvc.Tuning(k_splits=4))
+
+
+def test_tiny_workload_full():
+    for call in wl.tiny().calls:
+        run_and_check(call)
+
+
+def test_l2norm_silu_standalone():
+    rng = np.random.default_rng(5)
+    for C, rows in ((640, 1000), (160, 333), (24, 77)):
+        x = wl.to_bf16(torch.from_numpy(rng.standard_normal((rows, C)).astype(np.float32)))
+        res = wl.to_bf16(torch.from_numpy(rng.standard_normal((rows, C)).astype(np.float32)))
+        b = torch.from_numpy((rng.standard_normal(C) * 0.1).astype(np.float32))
+        rb = torch.from_numpy((rng.standard_normal(C) * 0.1).astype(np.float32))
+        g = wl.to_bf16(torch.from_numpy((1 + 0.1 * rng.standard_normal(C)).astype(np.float32))).float()
+        y, v = vvc.l2norm_silu(x.cuda(), g.cuda(), b.cuda(), res.cuda(), rb.cuda(), save_value=True)
+        ry, rv = oracle.l2norm_silu(wl.bits(x), g.numpy(), b.numpy(), wl.bits(res), rb.numpy())
+        assert ulp_dist(wl.bits(y.cpu()), ry).max() <= 3
+        assert ulp_dist(wl.bits(v.cpu()), rv).max() <= 1
+        y2 = vvc.l2norm_silu(x.cuda(), g.cuda())
+        ry2, _ = oracle.l2norm_silu(wl.bits(x), g.numpy())
+        assert ulp_dist(wl.bits(y2.cpu()), ry2).max() <= 3

@@ -1,0 +1,130 @@
+"""Host-side checks of the CUDA library that need no GPU: it builds, loads,
+exports every function include/conv3d.h declares, its ABI structs match the
+binding, and argument validation rejects bad calls before launching anything.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import video_vae_convolution_gb300 as vvc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "conv3d.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while", "sizeof")))
+
+
+def test_library_loads_and_exports_header():
+    lib = vvc._lib()
+    declared = header_functions()
+    assert len(declared) >= 10
+    for name in declared:
+        assert hasattr(lib, name), f"{name} declared in conv3d.h but not exported"
+    assert sorted(declared) == sorted(vvc.EXPORTS)
+    assert lib.conv3d_version() >= 100
+    assert lib.conv3d_status_string(vvc.ERR_OVERLAP) == b"output or workspace overlaps another buffer"
+
+
+def test_packed_weight_bytes():
+    lib = vvc._lib()
+    assert lib.conv3d_packed_weight_bytes(96, 96, 3, 3, 3) == 96 * 27 * 128 * 2
+    assert lib.conv3d_packed_weight_bytes(128, 3, 3, 3, 3) == 128 * 27 * 64 * 2
+    assert lib.conv3d_packed_weight_bytes(0, 3, 3, 3, 3) == 0
+
+
+def _params(**kw):
+    p = vvc.Params()
+    p.x, p.w_packed, p.y = 0x100000, 0x200000, 0x10000000
+    p.layout = p.out_layout = vvc.NDHWC
+    p.N, p.Cin, p.D, p.H, p.W = 1, 16, 4, 12, 12
+    p.Cout, p.KT, p.KR, p.KS = 32, 3, 3, 3
+    for i in range(3):
+        p.stride[i] = 1
+        p.pad[i].before = p.pad[i].after = 1
+        p.pad[i].mode = vvc.PAD_ZERO
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def fwd(p, t=None):
+    return vvc._lib().conv3d_fwd_ex(ctypes.byref(p), None if t is None else ctypes.byref(t), None)
+
+
+def test_validation_rejects_before_launch():
+    assert fwd(_params(Cin=0)) == vvc.ERR_INVALID_ARG
+    assert fwd(_params(layout=7)) == vvc.ERR_INVALID_ARG
+    assert fwd(_params(x=None)) == vvc.ERR_INVALID_ARG
+    p = _params()
+    p.stride[1] = 0
+    assert fwd(p) == vvc.ERR_INVALID_ARG
+    p = _params(epi=vvc.EPI_RESIDUAL_BIAS, residual_bias=0x300000)
+    assert fwd(p) == vvc.ERR_INVALID_ARG                     # residual_bias needs residual
+    p = _params(epi=vvc.EPI_L2NORM_SILU)
+    assert fwd(p) == vvc.ERR_INVALID_ARG                     # gamma missing
+    p = _params(epi=vvc.EPI_L2NORM_SILU | vvc.EPI_OUT_PAD_BR, gamma=0x300000)
+    assert fwd(p) == vvc.ERR_INVALID_ARG                     # pad variant stops at value
+    p = _params(W=2)
+    p.pad[2].before = p.pad[2].after = 0
+    assert fwd(p) == vvc.ERR_INVALID_ARG                     # output extent < 1
+    p = _params()
+    p.pad[1].mode = vvc.PAD_REFLECT
+    p.pad[1].before = 12
+    assert fwd(p) == vvc.ERR_INVALID_ARG                     # reflect pad >= extent
+    p = _params()
+    p.pad[0].mode = vvc.PAD_REFLECT
+    assert fwd(p) == vvc.ERR_UNSUPPORTED                     # no reflect along T
+    p = _params(epi=vvc.EPI_L2NORM_SILU, gamma=0x300000, Cout=640)
+    assert fwd(p) == vvc.ERR_UNSUPPORTED
+
+
+def test_alignment_overlap_workspace():
+    one = vvc.Tuning(k_splits=1)
+    assert fwd(_params(x=0x100008), one) == vvc.ERR_MISALIGNED
+    assert fwd(_params(y=0x100000), one) == vvc.ERR_OVERLAP   # y on top of x
+    p = _params(epi=vvc.EPI_SAVE_VALUE, value_out=0x10000010)
+    assert fwd(p, one) == vvc.ERR_OVERLAP                     # value_out inside y
+    p = _params(layout=vvc.NCDHW)                             # NCDHW input needs staging
+    assert fwd(p, one) == vvc.ERR_WORKSPACE
+    n = ctypes.c_size_t(0)
+    assert vvc._lib().conv3d_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == vvc.OK
+    assert n.value >= 1 * 16 * 4 * 12 * 12 * 2
+    p.workspace, p.workspace_bytes = 0x100000, n.value         # workspace overlapping x
+    assert fwd(p) == vvc.ERR_OVERLAP
+    p.workspace, p.workspace_bytes = 0x40000000, n.value - 16  # too small
+    assert fwd(p) == vvc.ERR_WORKSPACE
+
+
+def test_workspace_and_launch_plan():
+    lib = vvc._lib()
+    p = _params()
+    n = ctypes.c_size_t(1)
+    assert lib.conv3d_workspace_bytes(ctypes.byref(p), ctypes.byref(n)) == vvc.OK
+    t = vvc.Tuning(k_splits=3)
+    assert lib.conv3d_workspace_bytes_ex(ctypes.byref(p), ctypes.byref(t), ctypes.byref(n)) == 0
+    Do, Ho, Wo = 4, 12, 12
+    assert n.value >= 3 * Do * Ho * Wo * 32 * 4
+    assert lib.conv3d_launch_count(ctypes.byref(p), ctypes.byref(t)) == 2   # conv + reduce
+    assert lib.conv3d_launch_count(ctypes.byref(_params(Cin=3)), None) >= 2  # staging
+    assert lib.conv3d_launch_count(ctypes.byref(_params(Cin=64, Cout=64)),
+                                   ctypes.byref(vvc.Tuning(k_splits=1))) == 1
+
+
+def test_l2norm_validation():
+    lib = vvc._lib()
+    assert lib.l2norm_silu(None, 10, 16, None, None, None, 0x1000, 0x2000, None, None) == \
+        vvc.ERR_INVALID_ARG
+    assert lib.l2norm_silu(0x1000, 10, 16, None, None, 0x3000, 0x4000, 0x5000, None, None) == \
+        vvc.ERR_INVALID_ARG
+    assert lib.l2norm_silu(0x1000, 10, 16, None, None, None, 0x4000, 0x1010, None, None) == \
+        vvc.ERR_OVERLAP
+    assert lib.l2norm_silu(0x1002, 10, 16, None, None, None, 0x4000, 0x8000, None, None) == \
+        vvc.ERR_MISALIGNED

@@ -1,0 +1,306 @@
+"""GB300 (sm_103a) video-VAE convolution: thin Python binding of the C ABI.
+
+Everything here is argument marshalling: tensors are allocated with torch (device
+memory and streams only) and every step of the computation runs in the CUDA
+library ``libvvc_conv3d.so`` (see ``include/conv3d.h``).  There is no fallback:
+if the library cannot be built or loaded, the calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+NCDHW = 0
+NDHWC = 1
+PAD_ZERO = 0
+PAD_REFLECT = 1
+
+EPI_BIAS = 1
+EPI_RESIDUAL = 2
+EPI_RESIDUAL_BIAS = 4
+EPI_L2NORM_SILU = 8
+EPI_SAVE_VALUE = 16
+EPI_OUT_PAD_BR = 32
+EPI_DEBUG_STORE_CONV = 1 << 30
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_MISALIGNED = -3
+ERR_OVERLAP = -4
+ERR_WORKSPACE = -5
+ERR_CUDA = -6
+ERR_DEVICE_TIMEOUT = -7
+
+# Every function the C header declares (checked by the tests against include/conv3d.h).
+EXPORTS = (
+    "conv3d_packed_weight_bytes", "conv3d_pack_weight", "conv3d_workspace_bytes",
+    "conv3d_workspace_bytes_ex", "conv3d_fwd", "conv3d_fwd_ex", "conv3d_launch_count",
+    "l2norm_silu", "conv3d_get_device_status", "conv3d_status_string", "conv3d_version",
+    "conv3d_struct_size",
+)
+
+
+class Conv3dError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        msg = _lib().conv3d_status_string(status).decode() if _LIB is not None else str(status)
+        super().__init__(f"{what}: {msg} ({status})" if what else f"{msg} ({status})")
+
+
+class Pad(ctypes.Structure):
+    _fields_ = [("before", ctypes.c_int32), ("after", ctypes.c_int32), ("mode", ctypes.c_int32)]
+
+
+class Params(ctypes.Structure):
+    _fields_ = [
+        ("x", ctypes.c_void_p), ("layout", ctypes.c_int32),
+        ("N", ctypes.c_int32), ("Cin", ctypes.c_int32), ("D", ctypes.c_int32),
+        ("H", ctypes.c_int32), ("W", ctypes.c_int32),
+        ("w_packed", ctypes.c_void_p),
+        ("Cout", ctypes.c_int32), ("KT", ctypes.c_int32), ("KR", ctypes.c_int32),
+        ("KS", ctypes.c_int32),
+        ("stride", ctypes.c_int32 * 3),
+        ("pad", Pad * 3),
+        ("y", ctypes.c_void_p), ("out_layout", ctypes.c_int32), ("epi", ctypes.c_uint32),
+        ("bias", ctypes.c_void_p), ("residual", ctypes.c_void_p),
+        ("residual_bias", ctypes.c_void_p), ("gamma", ctypes.c_void_p),
+        ("value_out", ctypes.c_void_p), ("conv_out", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+class Tuning(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "tile_w", "tile_h", "R", "kc", "BN", "halo", "stages", "k_splits", "desc_mode",
+        "inject", "timeout_ms")]
+
+    def __init__(self, **kw):
+        super().__init__()
+        self.halo = -1
+        for k, v in kw.items():
+            setattr(self, k, int(v))
+
+
+_LIB = None
+_lock = threading.Lock()
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        with _lock:
+            if _LIB is None:
+                path = _build.LIB_PATH
+                if not _build.up_to_date():
+                    path = _build.build()
+                lib = ctypes.CDLL(path)
+                P = ctypes.POINTER(Params)
+                T = ctypes.POINTER(Tuning)
+                vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+                lib.conv3d_packed_weight_bytes.argtypes = [i32] * 5
+                lib.conv3d_packed_weight_bytes.restype = sz
+                lib.conv3d_pack_weight.argtypes = [vp] + [i32] * 5 + [vp, vp]
+                lib.conv3d_pack_weight.restype = ctypes.c_int
+                lib.conv3d_workspace_bytes.argtypes = [P, ctypes.POINTER(sz)]
+                lib.conv3d_workspace_bytes.restype = ctypes.c_int
+                lib.conv3d_workspace_bytes_ex.argtypes = [P, T, ctypes.POINTER(sz)]
+                lib.conv3d_workspace_bytes_ex.restype = ctypes.c_int
+                lib.conv3d_fwd.argtypes = [P, vp]
+                lib.conv3d_fwd.restype = ctypes.c_int
+                lib.conv3d_fwd_ex.argtypes = [P, T, vp]
+                lib.conv3d_fwd_ex.restype = ctypes.c_int
+                lib.conv3d_launch_count.argtypes = [P, T]
+                lib.conv3d_launch_count.restype = ctypes.c_int
+                lib.l2norm_silu.argtypes = [vp, i64, i32, vp, vp, vp, vp, vp, vp, vp]
+                lib.l2norm_silu.restype = ctypes.c_int
+                lib.conv3d_get_device_status.argtypes = [ctypes.POINTER(i32), vp]
+                lib.conv3d_get_device_status.restype = ctypes.c_int
+                lib.conv3d_status_string.argtypes = [ctypes.c_int]
+                lib.conv3d_status_string.restype = ctypes.c_char_p
+                lib.conv3d_version.argtypes = []
+                lib.conv3d_version.restype = ctypes.c_int
+                lib.conv3d_struct_size.argtypes = [ctypes.c_int]
+                lib.conv3d_struct_size.restype = sz
+                for which, st in ((0, Params), (1, Tuning), (2, Pad)):
+                    if lib.conv3d_struct_size(which) != ctypes.sizeof(st):
+                        raise RuntimeError(f"ABI struct mismatch for {st.__name__}")
+                _LIB = lib
+    return _LIB
+
+
+def library_path() -> str:
+    _lib()
+    return _build.LIB_PATH
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise Conv3dError(rc, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# ---- weights -------------------------------------------------------------------------------
+
+def packed_weight_shape(Cout, Cin, KT, KR, KS):
+    return (Cout, KT, KR, KS, (Cin + 63) // 64 * 64)
+
+
+def pack_weight(w: torch.Tensor, stream=None) -> torch.Tensor:
+    """OITRS (or OIRS, read as KT = 1) bf16 CUDA weights -> packed OTRSI tensor."""
+    if w.dim() == 4:
+        w = w.unsqueeze(2)
+    assert w.dim() == 5 and w.dtype == torch.bfloat16 and w.is_cuda
+    w = w.contiguous()
+    Cout, Cin, KT, KR, KS = w.shape
+    out = torch.empty(packed_weight_shape(Cout, Cin, KT, KR, KS), dtype=torch.bfloat16,
+                      device=w.device)
+    _check(_lib().conv3d_pack_weight(_ptr(w), Cout, Cin, KT, KR, KS, _ptr(out), _stream(stream)),
+           "conv3d_pack_weight")
+    return out
+
+
+# ---- convolution -----------------------------------------------------------------------------
+
+def out_dims(D, H, W, kernel, stride, pads):
+    L = (D, H, W)
+    return tuple((L[i] + pads[i][0] + pads[i][1] - kernel[i]) // stride[i] + 1 for i in range(3))
+
+
+def _dims(x: torch.Tensor, layout: int):
+    if x.dim() == 4:  # rank-4 NCHW / NHWC: D = 1
+        if layout == NCDHW:
+            N, C, H, W = x.shape
+        else:
+            N, H, W, C = x.shape
+        return N, C, 1, H, W
+    if layout == NCDHW:
+        N, C, D, H, W = x.shape
+    else:
+        N, D, H, W, C = x.shape
+    return N, C, D, H, W
+
+
+def out_shape(N, Cout, Do, Ho, Wo, layout, pad_br=False):
+    if pad_br:
+        Ho, Wo = Ho + 1, Wo + 1
+    return (N, Cout, Do, Ho, Wo) if layout == NCDHW else (N, Do, Ho, Wo, Cout)
+
+
+class Conv3d:
+    """One prepared convolution call: builds the C parameter block once so that
+    ``run()`` is a single C call (cheap enough for timing loops and CUDA graphs).
+
+    x: bf16 CUDA tensor in `layout` (5-D, or 4-D with D = 1).  w_packed from
+    pack_weight.  pads: ((before, after, mode) for T, H, W).  Outputs are allocated
+    here unless given; the workspace is allocated here (torch) unless given.
+    """
+
+    def __init__(self, x, w_packed, Cout, kernel, stride=(1, 1, 1),
+                 pads=((0, 0, PAD_ZERO),) * 3, layout=NDHWC, out_layout=NDHWC, epi=0,
+                 bias=None, residual=None, residual_bias=None, gamma=None, y=None,
+                 value_out=None, conv_out=None, workspace=None, tuning: Optional[Tuning] = None):
+        N, C, D, H, W = _dims(x, layout)
+        KT, KR, KS = kernel
+        Do, Ho, Wo = out_dims(D, H, W, kernel, stride, pads)
+        dev = x.device
+        self.dims = (N, C, D, H, W)
+        self.out_dims = (Do, Ho, Wo)
+        pad_br = bool(epi & EPI_OUT_PAD_BR)
+        if y is None:
+            y = torch.empty(out_shape(N, Cout, Do, Ho, Wo, out_layout, pad_br),
+                            dtype=torch.bfloat16, device=dev)
+        if epi & EPI_SAVE_VALUE and value_out is None:
+            value_out = torch.empty(out_shape(N, Cout, Do, Ho, Wo, out_layout),
+                                    dtype=torch.bfloat16, device=dev)
+        if epi & EPI_DEBUG_STORE_CONV and conv_out is None:
+            conv_out = torch.empty((N, Do, Ho, Wo, Cout), dtype=torch.bfloat16, device=dev)
+        p = Params()
+        p.x = x.data_ptr()
+        p.layout = layout
+        p.N, p.Cin, p.D, p.H, p.W = N, C, D, H, W
+        p.w_packed = w_packed.data_ptr()
+        p.Cout, p.KT, p.KR, p.KS = Cout, KT, KR, KS
+        for i in range(3):
+            p.stride[i] = stride[i]
+            p.pad[i].before, p.pad[i].after, p.pad[i].mode = pads[i]
+        p.y = y.data_ptr()
+        p.out_layout = out_layout
+        p.epi = epi
+        p.bias = None if bias is None else bias.data_ptr()
+        p.residual = None if residual is None else residual.data_ptr()
+        p.residual_bias = None if residual_bias is None else residual_bias.data_ptr()
+        p.gamma = None if gamma is None else gamma.data_ptr()
+        p.value_out = None if value_out is None else value_out.data_ptr()
+        p.conv_out = None if conv_out is None else conv_out.data_ptr()
+        self.tuning = tuning
+        tp = ctypes.byref(tuning) if tuning is not None else None
+        nbytes = ctypes.c_size_t(0)
+        _check(_lib().conv3d_workspace_bytes_ex(ctypes.byref(p), tp, ctypes.byref(nbytes)),
+               "conv3d_workspace_bytes")
+        self.workspace_bytes = nbytes.value
+        if workspace is None and nbytes.value > 0:
+            workspace = torch.empty(nbytes.value, dtype=torch.uint8, device=dev)
+        p.workspace = None if workspace is None else workspace.data_ptr()
+        p.workspace_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+        self.params = p
+        # keep every buffer alive as long as the call object
+        self.x, self.w_packed, self.y = x, w_packed, y
+        self.value_out, self.conv_out, self.workspace = value_out, conv_out, workspace
+        self.bias, self.residual, self.residual_bias, self.gamma = bias, residual, residual_bias, gamma
+        self.launches = _lib().conv3d_launch_count(ctypes.byref(p), tp)
+
+    def run(self, stream=None) -> int:
+        tp = ctypes.byref(self.tuning) if self.tuning is not None else None
+        return _lib().conv3d_fwd_ex(ctypes.byref(self.params), tp, _stream(stream))
+
+    def __call__(self, stream=None):
+        _check(self.run(stream), "conv3d_fwd")
+        return self.y
+
+
+def conv3d(x, w_packed, Cout, kernel, **kw):
+    """Runs one convolution; returns y (and fills value_out / conv_out if asked)."""
+    c = Conv3d(x, w_packed, Cout, kernel, **kw)
+    c()
+    if kw.get("epi", 0) & (EPI_SAVE_VALUE | EPI_DEBUG_STORE_CONV):
+        return {"y": c.y, "value": c.value_out, "conv": c.conv_out}
+    return c.y
+
+
+def l2norm_silu(x: torch.Tensor, gamma: torch.Tensor, input_bias=None, residual=None,
+                residual_bias=None, save_value=False, y=None, stream=None):
+    """Standalone post-operations on channels-last bf16 x [..., C]; returns y
+    (and the pre-normalisation value when save_value)."""
+    C = x.shape[-1]
+    rows = x.numel() // C
+    if y is None:
+        y = torch.empty_like(x)
+    value = torch.empty_like(x) if save_value else None
+    _check(_lib().l2norm_silu(_ptr(x), rows, C, _ptr(input_bias), _ptr(residual),
+                              _ptr(residual_bias), _ptr(gamma), _ptr(y), _ptr(value),
+                              _stream(stream)), "l2norm_silu")
+    return (y, value) if save_value else y
+
+
+def device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device status word."""
+    v = ctypes.c_int32(0)
+    _check(_lib().conv3d_get_device_status(ctypes.byref(v), _stream(stream)),
+           "conv3d_get_device_status")
+    return v.value

@@ -1,0 +1,594 @@
+// C ABI of the convolution library: argument validation, the launch plan
+// (input staging, tile shape, pipeline depth, split of the reduction), TMA
+// tensor-map encoding and kernel dispatch.  See include/conv3d.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+
+#include "../../include/conv3d.h"
+#include "internal.h"
+
+namespace vvc {
+cudaError_t launch_conv_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const ConvTCParams& p,
+                           dim3 grid, size_t smem_bytes, cudaStream_t stream);
+cudaError_t conv_status_read_clear(int* status, cudaStream_t stream);
+cudaError_t launch_pack_weight(const void* w, void* out, int Co, int Ci, int taps,
+                               cudaStream_t s);
+cudaError_t launch_stage_input(const void* x, int layout, int N, int C, int Cp, long long S,
+                               void* out, cudaStream_t s);
+cudaError_t launch_splitk_epilogue(const float* partial, int splits, long long M,
+                                   const EpiParams& e, cudaStream_t s);
+cudaError_t launch_l2norm_silu(const void* x, long long rows, const EpiParams& e,
+                               cudaStream_t s);
+}  // namespace vvc
+
+namespace {
+
+using vvc::ConvTCParams;
+using vvc::EpiParams;
+
+constexpr size_t kMaxSmem = 232448;  // sm_100 / sm_103 opt-in dynamic shared memory per block
+constexpr int kDefaultSMs = 148;
+
+int num_sms() {
+  static int cached = 0;
+  if (cached) return cached;
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
+    cached = n;
+  } else {
+    (void)cudaGetLastError();
+    cached = kDefaultSMs;
+  }
+  return cached;
+}
+
+inline long long round_up(long long a, long long b) { return (a + b - 1) / b * b; }
+inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
+
+struct Plan {
+  int Do = 0, Ho = 0, Wo = 0;
+  bool stage = false;
+  int Cst = 0;
+  size_t stage_off = 0, stage_bytes = 0;
+  size_t partial_off = 0, partial_bytes = 0;
+  size_t ws_bytes = 0;
+  ConvTCParams kp{};
+  dim3 grid;
+  size_t smem = 0;
+  int launches = 0;
+};
+
+struct Span {
+  uintptr_t lo, hi;
+};
+
+bool overlaps(const Span& a, const Span& b) {
+  return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo;
+}
+
+int out_extent(int L, int b, int a, int K, int s) {
+  const long long num = (long long)L + b + a - K;
+  if (num < 0) return -1;
+  return static_cast<int>(num / s + 1);
+}
+
+// Geometry and flag validation; no CUDA calls.
+int validate_shape(const conv3d_params* p, int* Do, int* Ho, int* Wo) {
+  if (!p) return CONV3D_ERR_INVALID_ARG;
+  if (p->layout != CONV3D_NCDHW && p->layout != CONV3D_NDHWC) return CONV3D_ERR_INVALID_ARG;
+  if (p->out_layout != CONV3D_NCDHW && p->out_layout != CONV3D_NDHWC)
+    return CONV3D_ERR_INVALID_ARG;
+  if (p->N < 1 || p->Cin < 1 || p->D < 1 || p->H < 1 || p->W < 1 || p->Cout < 1)
+    return CONV3D_ERR_INVALID_ARG;
+  if (p->KT < 1 || p->KR < 1 || p->KS < 1) return CONV3D_ERR_INVALID_ARG;
+  for (int i = 0; i < 3; ++i) {
+    if (p->stride[i] < 1) return CONV3D_ERR_INVALID_ARG;
+    if (p->pad[i].before < 0 || p->pad[i].after < 0) return CONV3D_ERR_INVALID_ARG;
+    if (p->pad[i].mode != CONV3D_PAD_ZERO && p->pad[i].mode != CONV3D_PAD_REFLECT)
+      return CONV3D_ERR_INVALID_ARG;
+  }
+  const int L[3] = {p->D, p->H, p->W};
+  const int K[3] = {p->KT, p->KR, p->KS};
+  int o[3];
+  for (int i = 0; i < 3; ++i) {
+    if (p->pad[i].mode == CONV3D_PAD_REFLECT &&
+        (p->pad[i].before >= L[i] || p->pad[i].after >= L[i]))
+      return CONV3D_ERR_INVALID_ARG;
+    o[i] = out_extent(L[i], p->pad[i].before, p->pad[i].after, K[i], p->stride[i]);
+    if (o[i] < 1) return CONV3D_ERR_INVALID_ARG;
+  }
+  const unsigned e = p->epi;
+  const unsigned known = CONV3D_EPI_BIAS | CONV3D_EPI_RESIDUAL | CONV3D_EPI_RESIDUAL_BIAS |
+                         CONV3D_EPI_L2NORM_SILU | CONV3D_EPI_SAVE_VALUE |
+                         CONV3D_EPI_OUT_PAD_BR | CONV3D_EPI_DEBUG_STORE_CONV;
+  if (e & ~known) return CONV3D_ERR_INVALID_ARG;
+  if ((e & CONV3D_EPI_RESIDUAL_BIAS) && !(e & CONV3D_EPI_RESIDUAL)) return CONV3D_ERR_INVALID_ARG;
+  if ((e & CONV3D_EPI_OUT_PAD_BR) && (e & CONV3D_EPI_L2NORM_SILU)) return CONV3D_ERR_INVALID_ARG;
+  if (!p->x || !p->w_packed || !p->y) return CONV3D_ERR_INVALID_ARG;
+  if ((e & CONV3D_EPI_BIAS) && !p->bias) return CONV3D_ERR_INVALID_ARG;
+  if ((e & CONV3D_EPI_RESIDUAL) && !p->residual) return CONV3D_ERR_INVALID_ARG;
+  if ((e & CONV3D_EPI_RESIDUAL_BIAS) && !p->residual_bias) return CONV3D_ERR_INVALID_ARG;
+  if ((e & CONV3D_EPI_L2NORM_SILU) && !p->gamma) return CONV3D_ERR_INVALID_ARG;
+  if ((e & CONV3D_EPI_SAVE_VALUE) && !p->value_out) return CONV3D_ERR_INVALID_ARG;
+  if ((e & CONV3D_EPI_DEBUG_STORE_CONV) && !p->conv_out) return CONV3D_ERR_INVALID_ARG;
+  // element counts must stay addressable with 32-bit TMA coordinates
+  if ((long long)p->KT * p->KR * p->KS * round_up(p->Cin, 64) > 0x7fffffffLL)
+    return CONV3D_ERR_UNSUPPORTED;
+  *Do = o[0];
+  *Ho = o[1];
+  *Wo = o[2];
+  return CONV3D_OK;
+}
+
+// Covered by the kernels (beyond plain validity).
+int check_supported(const conv3d_params* p) {
+  if (p->pad[0].mode == CONV3D_PAD_REFLECT && (p->pad[0].before || p->pad[0].after))
+    return CONV3D_ERR_UNSUPPORTED;  // reflect along T: not used by the VAE paths
+  if (p->pad[2].mode == CONV3D_PAD_REFLECT) {
+    if (p->pad[2].before > 1 || p->pad[2].after > 1) return CONV3D_ERR_UNSUPPORTED;
+    if (p->stride[2] > 2) return CONV3D_ERR_UNSUPPORTED;
+    if (p->W < 3) return CONV3D_ERR_UNSUPPORTED;
+  }
+  if (p->KS > 8 || p->KR > 64 || p->KT > 64) return CONV3D_ERR_UNSUPPORTED;
+  if ((p->epi & CONV3D_EPI_L2NORM_SILU) && p->Cout > 512) return CONV3D_ERR_UNSUPPORTED;
+  if (p->stride[2] > 8) return CONV3D_ERR_UNSUPPORTED;
+  return CONV3D_OK;
+}
+
+int make_plan(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
+  int rc = validate_shape(p, &pl->Do, &pl->Ho, &pl->Wo);
+  if (rc) return rc;
+  rc = check_supported(p);
+  if (rc) return rc;
+  conv3d_tuning t{};
+  if (tu) t = *tu;
+  const int Do = pl->Do, Ho = pl->Ho, Wo = pl->Wo;
+  const int st = p->stride[0], sh = p->stride[1], sw = p->stride[2];
+  const bool norm = (p->epi & CONV3D_EPI_L2NORM_SILU) != 0;
+
+  // ---- input staging ----
+  pl->stage = (p->layout == CONV3D_NCDHW) || (p->Cin % 8 != 0);
+  pl->Cst = static_cast<int>(round_up(p->Cin, 8));
+  size_t off = 0;
+  if (pl->stage) {
+    pl->stage_off = off;
+    pl->stage_bytes = (size_t)p->N * p->D * p->H * p->W * pl->Cst * 2;
+    off = static_cast<size_t>(round_up(off + pl->stage_bytes, 256));
+  }
+
+  ConvTCParams& k = pl->kp;
+  std::memset(&k, 0, sizeof(k));
+  // ---- channel chunk ----
+  int kc = t.kc;
+  if (kc == 0) kc = (pl->Cst % 64 == 0) ? 64 : (pl->Cst % 32 == 0) ? 32 : 16;
+  if (kc != 16 && kc != 32 && kc != 64) return CONV3D_ERR_INVALID_ARG;
+  k.kc = kc;
+  k.row_bytes = kc * 2;
+  k.swz = (kc == 64) ? 2 : (kc == 32) ? 4 : 6;
+  k.n_chunks = static_cast<int>(cdiv(p->Cin, kc));
+
+  // ---- N tiling ----
+  int BN, n_sub, sub_n;
+  if (norm) {
+    BN = static_cast<int>(round_up(p->Cout, 16));
+    n_sub = static_cast<int>(cdiv(BN, 256));
+    sub_n = static_cast<int>(round_up(cdiv(BN, n_sub), 16));
+    BN = n_sub * sub_n;
+    if (BN > 512) return CONV3D_ERR_UNSUPPORTED;
+  } else if (t.BN > 0) {
+    if (t.BN % 16 || t.BN > 256) return CONV3D_ERR_INVALID_ARG;
+    BN = t.BN;
+    n_sub = 1;
+    sub_n = BN;
+  } else {
+    const int nt = static_cast<int>(cdiv(p->Cout, 256));
+    BN = static_cast<int>(round_up(cdiv(p->Cout, nt), 16));
+    n_sub = 1;
+    sub_n = BN;
+  }
+  const int n_tiles = static_cast<int>(cdiv(p->Cout, BN));
+  k.BN = BN;
+  k.n_sub = n_sub;
+  k.sub_n = sub_n;
+  k.acc_stride = static_cast<int>(round_up(BN, 32));
+
+  // ---- M tile ----
+  int tile_w = t.tile_w, tile_h = t.tile_h;
+  if (tile_w <= 0) {
+    if (Wo >= 128) {
+      tile_w = 128;
+      tile_h = 1;
+    } else {
+      tile_w = static_cast<int>(round_up(Wo, 8));
+      if (tile_h <= 0) tile_h = std::max(1, std::min(128 / tile_w, Ho));
+    }
+  }
+  if (tile_h <= 0) tile_h = 1;
+  while (tile_w * sw > 256) tile_w -= 8;
+  if (tile_w < 1 || tile_w > 128 || tile_w * tile_h > 128) return CONV3D_ERR_INVALID_ARG;
+  if (tile_h > 1 && tile_w % 8) return CONV3D_ERR_INVALID_ARG;
+  bool halo = (sw == 1 && tile_h == 1 && p->KS > 1);
+  if (t.halo == 0) halo = false;
+  if (t.halo == 1) {
+    if (sw != 1 || tile_h != 1) return CONV3D_ERR_INVALID_ARG;
+    halo = true;
+  }
+  k.tile_w = tile_w;
+  k.tile_h = tile_h;
+  k.halo = halo ? 1 : 0;
+  k.box_w = halo ? tile_w + p->KS - 1 : tile_w;
+  k.pitch_rows = static_cast<int>(round_up(k.box_w, 8));
+  if (tile_h > 1) k.pitch_rows = tile_w;  // rows of one M-tile must be contiguous
+  k.a_tile_rows = tile_h * k.pitch_rows;
+  k.taps_per_stage = halo ? p->KS : 1;
+  k.stages_total = p->KT * p->KR * (halo ? 1 : p->KS) * k.n_chunks;
+
+  const int tiles_w = static_cast<int>(cdiv(Wo, tile_w));
+  const int sms = num_sms();
+  // ---- R (M-tiles per CTA) and pipeline depth ----
+  int Rmax = std::max(1, std::min(4, 512 / k.acc_stride));
+  if (t.R > 0) Rmax = t.R;
+  int R = Rmax;
+  size_t a_stage = 0, b_stage = 0;
+  int stages = 0;
+  for (; R >= 1; --R) {
+    if (R * k.acc_stride > 512) continue;
+    const long long groups_h = cdiv(Ho, (long long)R * tile_h);
+    const long long ctas = (long long)tiles_w * groups_h * Do * p->N * n_tiles;
+    if (t.R == 0 && R > 1 && ctas < 2LL * sms) continue;
+    const long long a_rows = (long long)(R - 1) * k.a_tile_rows +
+                             std::max<long long>(k.a_tile_rows, 128 + (halo ? p->KS - 1 : 0));
+    a_stage = static_cast<size_t>(round_up(round_up(a_rows, 8) * k.row_bytes, 1024));
+    b_stage = static_cast<size_t>(round_up((long long)k.taps_per_stage * BN * k.row_bytes, 1024));
+    const size_t avail = kMaxSmem - 1024 - 256;
+    stages = static_cast<int>(std::min<size_t>(8, avail / (a_stage + b_stage)));
+    if (t.stages > 0) stages = std::min(stages, t.stages);
+    if (stages >= 2) break;
+  }
+  if (R < 1 || stages < 2) return CONV3D_ERR_UNSUPPORTED;
+  k.R = R;
+  k.stages = stages;
+  k.a_stage_bytes = static_cast<uint32_t>(a_stage);
+  k.b_stage_bytes = static_cast<uint32_t>(b_stage);
+  k.bar_off = static_cast<uint32_t>((a_stage + b_stage) * stages);
+  int cols = 32;
+  while (cols < R * k.acc_stride) cols *= 2;
+  k.tmem_cols = cols;
+  k.tiles_w = tiles_w;
+  k.groups_h = static_cast<int>(cdiv(Ho, (long long)R * tile_h));
+  k.tx_bytes = static_cast<uint32_t>((long long)R * tile_h * k.box_w * k.row_bytes +
+                                     (long long)k.taps_per_stage * n_sub * sub_n * k.row_bytes);
+
+  // ---- split of the reduction ----
+  const long long m_groups = (long long)tiles_w * k.groups_h * Do * p->N;
+  const long long ctas = m_groups * n_tiles;
+  int splits = t.k_splits;
+  if (splits <= 0) {
+    splits = 1;
+    if (ctas < sms) {
+      splits = static_cast<int>(std::max<long long>(1, (sms + ctas / 2) / ctas));
+      splits = std::min(splits, std::max(1, k.stages_total / 4));
+      splits = std::min(splits, 16);
+    }
+  }
+  splits = std::max(1, std::min(splits, k.stages_total));
+  int per = static_cast<int>(cdiv(k.stages_total, splits));
+  splits = static_cast<int>(cdiv(k.stages_total, per));
+  k.k_splits = splits;
+  k.stages_per_split = per;
+  k.M_total = (long long)p->N * Do * Ho * Wo;
+  if (splits > 1) {
+    pl->partial_off = off;
+    pl->partial_bytes = (size_t)splits * (size_t)k.M_total * p->Cout * 4;
+    off = static_cast<size_t>(round_up(off + pl->partial_bytes, 256));
+  }
+  pl->ws_bytes = off;
+  if (m_groups > 0x7fffffffLL || n_tiles > 65535 || splits > 65535) return CONV3D_ERR_UNSUPPORTED;
+  pl->grid = dim3(static_cast<unsigned>(m_groups), static_cast<unsigned>(n_tiles),
+                  static_cast<unsigned>(splits));
+  pl->smem = 1024 + k.bar_off + 8 * (3 * stages + 2) + 16;
+  pl->launches = (pl->stage ? 1 : 0) + 1 + (splits > 1 ? 1 : 0);
+
+  // ---- geometry ----
+  k.C = pl->Cst;
+  k.D = p->D;
+  k.H = p->H;
+  k.W = p->W;
+  k.KT = p->KT;
+  k.KR = p->KR;
+  k.KS = p->KS;
+  k.st = st;
+  k.sh = sh;
+  k.sw = sw;
+  k.pt = p->pad[0].before;
+  k.ph = p->pad[1].before;
+  k.pw = p->pad[2].before;
+  k.reflect_h = (p->pad[1].mode == CONV3D_PAD_REFLECT && (p->pad[1].before || p->pad[1].after));
+  k.reflect_w = (p->pad[2].mode == CONV3D_PAD_REFLECT && (p->pad[2].before || p->pad[2].after));
+  k.cp64 = static_cast<int>(round_up(p->Cin, 64));
+  k.desc_mode = t.desc_mode > 0 ? t.desc_mode - 1 : 0;  // swizzle follows absolute address bits
+  k.inject = t.inject;
+  k.timeout_ns = (unsigned long long)(t.timeout_ms > 0 ? t.timeout_ms : 4000) * 1000000ULL;
+
+  EpiParams& e = k.epi;
+  e.y = p->y;
+  e.out_layout = p->out_layout;
+  e.N = p->N;
+  e.Cout = p->Cout;
+  e.Do = Do;
+  e.Ho = Ho;
+  e.Wo = Wo;
+  e.flags = p->epi;
+  e.bias = p->bias;
+  e.residual = static_cast<const uint16_t*>(p->residual);
+  e.rbias = p->residual_bias;
+  e.gamma = p->gamma;
+  e.value_out = static_cast<uint16_t*>(p->value_out);
+  e.conv_out = static_cast<uint16_t*>(p->conv_out);
+  e.sqrt_c = std::sqrt(static_cast<float>(p->Cout));
+  return CONV3D_OK;
+}
+
+int check_pointers(const conv3d_params* p, const Plan& pl) {
+  auto mis = [](const void* q) { return q && (reinterpret_cast<uintptr_t>(q) & 15u); };
+  if (mis(p->x) || mis(p->w_packed) || mis(p->y) || mis(p->residual) || mis(p->value_out) ||
+      mis(p->conv_out) || mis(p->bias) || mis(p->residual_bias) || mis(p->gamma) ||
+      (pl.ws_bytes && mis(p->workspace)))
+    return CONV3D_ERR_MISALIGNED;
+  if (pl.ws_bytes && (!p->workspace || p->workspace_bytes < pl.ws_bytes))
+    return CONV3D_ERR_WORKSPACE;
+  const bool padbr = (p->epi & CONV3D_EPI_OUT_PAD_BR) != 0;
+  const size_t out_elems = (size_t)p->N * p->Cout * pl.Do * pl.Ho * pl.Wo;
+  const size_t y_elems =
+      (size_t)p->N * p->Cout * pl.Do * (pl.Ho + (padbr ? 1 : 0)) * (pl.Wo + (padbr ? 1 : 0));
+  auto span = [](const void* q, size_t bytes) {
+    Span s;
+    s.lo = reinterpret_cast<uintptr_t>(q);
+    s.hi = q ? s.lo + bytes : s.lo;
+    return s;
+  };
+  const Span in[] = {
+      span(p->x, (size_t)p->N * p->Cin * p->D * p->H * p->W * 2),
+      span(p->w_packed, conv3d_packed_weight_bytes(p->Cout, p->Cin, p->KT, p->KR, p->KS)),
+      span((p->epi & CONV3D_EPI_RESIDUAL) ? p->residual : nullptr, out_elems * 2),
+      span((p->epi & CONV3D_EPI_BIAS) ? p->bias : nullptr, (size_t)p->Cout * 4),
+      span((p->epi & CONV3D_EPI_RESIDUAL_BIAS) ? p->residual_bias : nullptr, (size_t)p->Cout * 4),
+      span((p->epi & CONV3D_EPI_L2NORM_SILU) ? p->gamma : nullptr, (size_t)p->Cout * 4),
+  };
+  const Span out[] = {
+      span(p->y, y_elems * 2),
+      span((p->epi & CONV3D_EPI_SAVE_VALUE) ? p->value_out : nullptr, out_elems * 2),
+      span((p->epi & CONV3D_EPI_DEBUG_STORE_CONV) ? p->conv_out : nullptr, out_elems * 2),
+      span(pl.ws_bytes ? p->workspace : nullptr, pl.ws_bytes),
+  };
+  for (size_t i = 0; i < sizeof(out) / sizeof(out[0]); ++i) {
+    for (size_t j = 0; j < sizeof(in) / sizeof(in[0]); ++j)
+      if (overlaps(out[i], in[j])) return CONV3D_ERR_OVERLAP;
+    for (size_t j = i + 1; j < sizeof(out) / sizeof(out[0]); ++j)
+      if (overlaps(out[i], out[j])) return CONV3D_ERR_OVERLAP;
+  }
+  return CONV3D_OK;
+}
+
+// ---- TMA descriptors ----------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+CUtensorMapSwizzle swizzle_of(int kc) {
+  return kc == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                  : (kc == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
+int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtensorMap* tmA,
+                CUtensorMap* tmB) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return CONV3D_ERR_CUDA;
+  const ConvTCParams& k = pl.kp;
+  const cuuint64_t C = static_cast<cuuint64_t>(pl.Cst);
+  cuuint64_t gdimA[5] = {C, (cuuint64_t)p->W, (cuuint64_t)p->H, (cuuint64_t)p->D,
+                         (cuuint64_t)p->N};
+  cuuint64_t gstrA[4] = {C * 2, C * 2 * p->W, C * 2 * p->W * p->H, C * 2 * p->W * p->H * p->D};
+  const int es_w = k.halo ? 1 : k.sw;
+  cuuint32_t boxA[5] = {(cuuint32_t)k.kc,
+                        (cuuint32_t)(k.halo ? k.box_w : k.tile_w * k.sw), 1, 1, 1};
+  cuuint32_t esA[5] = {1, (cuuint32_t)es_w, 1, 1, 1};
+  CUresult r = enc(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(xin), gdimA, gstrA,
+                   boxA, esA, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(k.kc),
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
+  const cuuint64_t Ktot = (cuuint64_t)p->KT * p->KR * p->KS * k.cp64;
+  cuuint64_t gdimB[2] = {Ktot, (cuuint64_t)p->Cout};
+  cuuint64_t gstrB[1] = {Ktot * 2};
+  cuuint32_t boxB[2] = {(cuuint32_t)k.kc, (cuuint32_t)k.sub_n};
+  cuuint32_t esB[2] = {1, 1};
+  r = enc(tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p->w_packed), gdimB, gstrB,
+          boxB, esB, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(k.kc),
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
+  return CONV3D_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t conv3d_packed_weight_bytes(int32_t Cout, int32_t Cin, int32_t KT, int32_t KR,
+                                  int32_t KS) {
+  if (Cout < 1 || Cin < 1 || KT < 1 || KR < 1 || KS < 1) return 0;
+  return (size_t)Cout * KT * KR * KS * (size_t)round_up(Cin, 64) * 2;
+}
+
+int conv3d_pack_weight(const void* w_oitrs, int32_t Cout, int32_t Cin, int32_t KT, int32_t KR,
+                       int32_t KS, void* w_packed, conv3d_stream_t stream) {
+  if (!w_oitrs || !w_packed) return CONV3D_ERR_INVALID_ARG;
+  if (Cout < 1 || Cin < 1 || KT < 1 || KR < 1 || KS < 1) return CONV3D_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(w_oitrs) & 15u) || (reinterpret_cast<uintptr_t>(w_packed) & 15u))
+    return CONV3D_ERR_MISALIGNED;
+  const size_t in_bytes = (size_t)Cout * Cin * KT * KR * KS * 2;
+  const size_t out_bytes = conv3d_packed_weight_bytes(Cout, Cin, KT, KR, KS);
+  Span a{reinterpret_cast<uintptr_t>(w_oitrs), reinterpret_cast<uintptr_t>(w_oitrs) + in_bytes};
+  Span b{reinterpret_cast<uintptr_t>(w_packed), reinterpret_cast<uintptr_t>(w_packed) + out_bytes};
+  if (overlaps(a, b)) return CONV3D_ERR_OVERLAP;
+  cudaError_t err = vvc::launch_pack_weight(w_oitrs, w_packed, Cout, Cin, KT * KR * KS,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? CONV3D_OK : CONV3D_ERR_CUDA;
+}
+
+int conv3d_workspace_bytes_ex(const conv3d_params* p, const conv3d_tuning* tuning,
+                              size_t* bytes) {
+  if (!bytes) return CONV3D_ERR_INVALID_ARG;
+  Plan pl;
+  const int rc = make_plan(p, tuning, &pl);
+  if (rc) return rc;
+  *bytes = pl.ws_bytes;
+  return CONV3D_OK;
+}
+
+int conv3d_workspace_bytes(const conv3d_params* p, size_t* bytes) {
+  return conv3d_workspace_bytes_ex(p, nullptr, bytes);
+}
+
+int conv3d_launch_count(const conv3d_params* p, const conv3d_tuning* tuning) {
+  Plan pl;
+  const int rc = make_plan(p, tuning, &pl);
+  if (rc) return rc;
+  return pl.launches;
+}
+
+int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_stream_t stream) {
+  Plan pl;
+  int rc = make_plan(p, tuning, &pl);
+  if (rc) return rc;
+  rc = check_pointers(p, pl);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const void* xin = p->x;
+  uint8_t* ws = static_cast<uint8_t*>(p->workspace);
+  if (pl.stage) {
+    void* dst = ws + pl.stage_off;
+    if (vvc::launch_stage_input(p->x, p->layout, p->N, p->Cin, pl.Cst,
+                                (long long)p->D * p->H * p->W, dst, s) != cudaSuccess)
+      return CONV3D_ERR_CUDA;
+    xin = dst;
+  }
+  CUtensorMap tmA, tmB;
+  rc = encode_maps(p, pl, xin, &tmA, &tmB);
+  if (rc) return rc;
+  ConvTCParams kp = pl.kp;
+  if (kp.k_splits > 1) kp.partial = reinterpret_cast<float*>(ws + pl.partial_off);
+  if (vvc::launch_conv_tc(tmA, tmB, kp, pl.grid, pl.smem, s) != cudaSuccess)
+    return CONV3D_ERR_CUDA;
+  if (kp.k_splits > 1) {
+    if (vvc::launch_splitk_epilogue(kp.partial, kp.k_splits, kp.M_total, kp.epi, s) !=
+        cudaSuccess)
+      return CONV3D_ERR_CUDA;
+  }
+  return CONV3D_OK;
+}
+
+int conv3d_fwd(const conv3d_params* p, conv3d_stream_t stream) {
+  return conv3d_fwd_ex(p, nullptr, stream);
+}
+
+int l2norm_silu(const void* x, int64_t rows, int32_t C, const float* input_bias,
+                const void* residual, const float* residual_bias, const float* gamma, void* y,
+                void* value_out, conv3d_stream_t stream) {
+  if (!x || !y || !gamma || rows < 1 || C < 1) return CONV3D_ERR_INVALID_ARG;
+  if (rows > 0x7fffffffLL) return CONV3D_ERR_UNSUPPORTED;
+  if (residual_bias && !residual) return CONV3D_ERR_INVALID_ARG;
+  auto mis = [](const void* q) { return q && (reinterpret_cast<uintptr_t>(q) & 15u); };
+  if (mis(x) || mis(y) || mis(input_bias) || mis(residual) || mis(residual_bias) || mis(gamma) ||
+      mis(value_out))
+    return CONV3D_ERR_MISALIGNED;
+  const size_t tb = (size_t)rows * C * 2;
+  auto span = [](const void* q, size_t bytes) {
+    Span s;
+    s.lo = reinterpret_cast<uintptr_t>(q);
+    s.hi = q ? s.lo + bytes : s.lo;
+    return s;
+  };
+  const Span in[] = {span(x, tb), span(input_bias, (size_t)C * 4), span(residual, tb),
+                     span(residual_bias, (size_t)C * 4), span(gamma, (size_t)C * 4)};
+  const Span out[] = {span(y, tb), span(value_out, tb)};
+  for (const Span& o : out)
+    for (const Span& i : in)
+      if (overlaps(o, i)) return CONV3D_ERR_OVERLAP;
+  if (overlaps(out[0], out[1])) return CONV3D_ERR_OVERLAP;
+  EpiParams e{};
+  e.y = y;
+  e.out_layout = vvc::LAYOUT_NDHWC;
+  e.N = 1;
+  e.Cout = C;
+  e.Do = 1;
+  e.Ho = 1;
+  e.Wo = static_cast<int>(rows);
+  e.flags = vvc::EPI_L2NORM_SILU | (input_bias ? vvc::EPI_BIAS : 0u) |
+            (residual ? vvc::EPI_RESIDUAL : 0u) | (residual_bias ? vvc::EPI_RESIDUAL_BIAS : 0u) |
+            (value_out ? vvc::EPI_SAVE_VALUE : 0u);
+  e.bias = input_bias;
+  e.residual = static_cast<const uint16_t*>(residual);
+  e.rbias = residual_bias;
+  e.gamma = gamma;
+  e.value_out = static_cast<uint16_t*>(value_out);
+  e.sqrt_c = std::sqrt(static_cast<float>(C));
+  cudaError_t err = vvc::launch_l2norm_silu(x, rows, e, reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? CONV3D_OK : CONV3D_ERR_CUDA;
+}
+
+int conv3d_get_device_status(int32_t* status, conv3d_stream_t stream) {
+  if (!status) return CONV3D_ERR_INVALID_ARG;
+  int v = 0;
+  if (vvc::conv_status_read_clear(&v, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CONV3D_ERR_CUDA;
+  *status = v;
+  return CONV3D_OK;
+}
+
+const char* conv3d_status_string(int status) {
+  switch (status) {
+    case CONV3D_OK: return "ok";
+    case CONV3D_ERR_INVALID_ARG: return "invalid argument";
+    case CONV3D_ERR_UNSUPPORTED: return "unsupported configuration";
+    case CONV3D_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+    case CONV3D_ERR_OVERLAP: return "output or workspace overlaps another buffer";
+    case CONV3D_ERR_WORKSPACE: return "workspace missing or too small";
+    case CONV3D_ERR_CUDA: return "CUDA error";
+    case CONV3D_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int conv3d_version(void) { return 100; }
+
+}  // extern "C"
+
+extern "C" size_t conv3d_struct_size(int which) {
+  switch (which) {
+    case 0: return sizeof(conv3d_params);
+    case 1: return sizeof(conv3d_tuning);
+    case 2: return sizeof(conv3d_pad);
+    default: return 0;
+  }
+}

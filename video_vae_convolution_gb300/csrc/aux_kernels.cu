@@ -1,0 +1,180 @@
+// Memory-bound companions of the tensor-core convolution:
+//  - weight pack OITRS -> OTRSI with Cin padded to 64 (cuDNN frontend doc
+//    "Fused Conv3D + Bias + Residual + RMSNorm + SiLU", "Weight Packing");
+//  - input staging into channels-last (NCDHW -> NDHWC transpose, or channel
+//    padding to a multiple of 8 so TMA strides stay 16-byte multiples);
+//  - the deterministic split-K reduction + epilogue (ROCm/FlyDSL issue
+//    "[Feature]: conv3d_implicit — ...", maintainer comment: the split-K path
+//    materialises an NDHWC-flat (npq, k) buffer then reduces);
+//  - the standalone post-operations (cuDNN doc, "Standalone Normalization and
+//    Padding Variant", contiguous output).
+#include <cuda_runtime.h>
+
+#include "epilogue.cuh"
+#include "internal.h"
+
+namespace vvc {
+
+// ---- weight pack -------------------------------------------------------------------
+__global__ void pack_weight_kernel(const uint16_t* __restrict__ w, uint16_t* __restrict__ out,
+                                   int Co, int Ci, int taps, int cp, long long total) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int ci = static_cast<int>(i % cp);
+    const long long rest = i / cp;
+    const int tap = static_cast<int>(rest % taps);
+    const long long co = rest / taps;
+    out[i] = (ci < Ci) ? w[(co * Ci + ci) * taps + tap] : uint16_t(0);
+  }
+}
+
+cudaError_t launch_pack_weight(const void* w, void* out, int Co, int Ci, int taps,
+                               cudaStream_t s) {
+  const int cp = (Ci + 63) / 64 * 64;
+  const long long total = (long long)Co * taps * cp;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  pack_weight_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(
+      static_cast<const uint16_t*>(w), static_cast<uint16_t*>(out), Co, Ci, taps, cp, total);
+  return cudaGetLastError();
+}
+
+// ---- input staging --------------------------------------------------------------------
+// NCDHW [N][C][S] (S = D*H*W) -> NDHWC [N][S][Cp], channels Cin..Cp-1 zero.
+// 32 x 32 tiles through shared memory: reads coalesced along S, writes along C.
+__global__ void ncdhw_to_ndhwc_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ out,
+                                      int C, int Cp, long long S) {
+  __shared__ uint16_t tile[32][33];
+  const int n = blockIdx.z;
+  const long long s0 = (long long)blockIdx.x * 32;
+  const int c0 = blockIdx.y * 32;
+  const uint16_t* xn = x + (long long)n * C * S;
+  uint16_t* on = out + (long long)n * Cp * S;
+  for (int k = threadIdx.y; k < 32; k += blockDim.y) {
+    const int c = c0 + k;
+    const long long s = s0 + threadIdx.x;
+    tile[k][threadIdx.x] = (c < C && s < S) ? xn[(long long)c * S + s] : uint16_t(0);
+  }
+  __syncthreads();
+  for (int k = threadIdx.y; k < 32; k += blockDim.y) {
+    const long long s = s0 + k;
+    const int c = c0 + threadIdx.x;
+    if (s < S && c < Cp) on[s * Cp + c] = tile[threadIdx.x][k];
+  }
+}
+
+// NDHWC [P][C] -> [P][Cp] with zero channels Cin..Cp-1.
+__global__ void pad_channels_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ out,
+                                    int C, int Cp, long long P) {
+  const long long total = P * Cp;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = static_cast<int>(i % Cp);
+    const long long p = i / Cp;
+    out[i] = (c < C) ? x[p * C + c] : uint16_t(0);
+  }
+}
+
+cudaError_t launch_stage_input(const void* x, int layout, int N, int C, int Cp, long long S,
+                               void* out, cudaStream_t s) {
+  if (layout == LAYOUT_NCDHW) {
+    dim3 grid(static_cast<unsigned>((S + 31) / 32), static_cast<unsigned>((Cp + 31) / 32),
+              static_cast<unsigned>(N));
+    dim3 block(32, 8);
+    ncdhw_to_ndhwc_kernel<<<grid, block, 0, s>>>(static_cast<const uint16_t*>(x),
+                                                 static_cast<uint16_t*>(out), C, Cp, S);
+  } else {
+    const long long total = (long long)N * S * Cp;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 152 * 64) blocks = 152 * 64;
+    pad_channels_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(
+        static_cast<const uint16_t*>(x), static_cast<uint16_t*>(out), C, Cp, (long long)N * S);
+  }
+  return cudaGetLastError();
+}
+
+// ---- split-K reduction + epilogue ----------------------------------------------------------
+// partial: [splits][M][Cout] fp32, NDHWC-flat pixels.  One thread per pixel, the
+// splits summed in index order (deterministic).
+__global__ void splitk_epilogue_kernel(const float* __restrict__ partial, int splits,
+                                       long long M, EpiParams e) {
+  const long long pix = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  Pixel px;
+  px.valid = pix < M;
+  const long long pp = px.valid ? pix : 0;
+  px.w = static_cast<int>(pp % e.Wo);
+  long long rest = pp / e.Wo;
+  px.h = static_cast<int>(rest % e.Ho);
+  rest /= e.Ho;
+  px.d = static_cast<int>(rest % e.Do);
+  px.n = static_cast<int>(rest / e.Do);
+  const bool vec = (e.Cout % 4) == 0;
+  auto load = [&](int c_rel, float(&v)[16]) {
+    const int c = c_rel;
+    const int cnt = min(16, e.Cout - c);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+    if (!px.valid) return;
+    for (int s = 0; s < splits; ++s) {
+      const float* src = partial + ((long long)s * M + pp) * e.Cout + c;
+      if (vec && cnt == 16) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 q = __ldg(reinterpret_cast<const float4*>(src) + k);
+          v[4 * k] += q.x;
+          v[4 * k + 1] += q.y;
+          v[4 * k + 2] += q.z;
+          v[4 * k + 3] += q.w;
+        }
+      } else {
+        for (int i = 0; i < cnt; ++i) v[i] += __ldg(src + i);
+      }
+    }
+  };
+  epilogue_pixel(e, px, 0, e.Cout, load);
+}
+
+cudaError_t launch_splitk_epilogue(const float* partial, int splits, long long M,
+                                   const EpiParams& e, cudaStream_t s) {
+  const int threads = 128;
+  const long long blocks = (M + threads - 1) / threads;
+  splitk_epilogue_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(partial, splits, M, e);
+  return cudaGetLastError();
+}
+
+// ---- standalone post-operations ------------------------------------------------------------
+// x: [rows][C] bf16.  One thread per row; the epilogue addressing sees the rows as
+// an NDHWC tensor of extent (1, 1, 1, rows, C).
+__global__ void l2norm_silu_kernel(const uint16_t* __restrict__ x, long long rows, EpiParams e) {
+  const long long row = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  Pixel px;
+  px.valid = row < rows;
+  px.n = 0;
+  px.d = 0;
+  px.h = 0;
+  px.w = static_cast<int>(px.valid ? row : 0);
+  const int C = e.Cout;
+  auto load = [&](int c_rel, float(&v)[16]) {
+    const int cnt = min(16, C - c_rel);
+    if (!px.valid) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+      return;
+    }
+    load_chunk(x, LAYOUT_NDHWC, C, 1, 1, e.Wo, 0, 0, 0, px.w, c_rel, cnt, v);
+  };
+  epilogue_pixel(e, px, 0, C, load);
+}
+
+cudaError_t launch_l2norm_silu(const void* x, long long rows, const EpiParams& e,
+                               cudaStream_t s) {
+  const int threads = 128;
+  const long long blocks = (rows + threads - 1) / threads;
+  l2norm_silu_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+      static_cast<const uint16_t*>(x), rows, e);
+  return cudaGetLastError();
+}
+
+}  // namespace vvc

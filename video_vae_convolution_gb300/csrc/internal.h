@@ -1,0 +1,70 @@
+// Host/device parameter blocks shared by the launcher (api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+
+namespace vvc {
+
+enum : unsigned {
+  EPI_BIAS = 1u,
+  EPI_RESIDUAL = 2u,
+  EPI_RESIDUAL_BIAS = 4u,
+  EPI_L2NORM_SILU = 8u,
+  EPI_SAVE_VALUE = 16u,
+  EPI_OUT_PAD_BR = 32u,
+  EPI_DEBUG_STORE_CONV = 1u << 30,
+};
+
+enum : int { LAYOUT_NCDHW = 0, LAYOUT_NDHWC = 1 };
+
+// Where and how the epilogue writes one output pixel's channel row.
+struct EpiParams {
+  void* y;                 // bf16 output, out_layout, (Ho+1, Wo+1) with OUT_PAD_BR
+  int out_layout;
+  int N, Cout, Do, Ho, Wo;
+  unsigned flags;
+  const float* bias;       // [Cout] (BIAS)
+  const uint16_t* residual;  // bf16, out_layout, unpadded (RESIDUAL)
+  const float* rbias;      // [Cout] (RESIDUAL_BIAS)
+  const float* gamma;      // [Cout] (L2NORM_SILU)
+  uint16_t* value_out;     // bf16, out_layout, unpadded (SAVE_VALUE)
+  uint16_t* conv_out;      // bf16 NDHWC unpadded (DEBUG_STORE_CONV)
+  float sqrt_c;            // sqrtf((float)Cout)
+};
+
+// Implicit-GEMM convolution on tcgen05 (one CTA = R M-tiles x BN output channels).
+struct ConvTCParams {
+  EpiParams epi;
+  int C;                   // channels of the NDHWC tensor the A tensor map reads
+  int D, H, W;
+  int KT, KR, KS;
+  int st, sh, sw;
+  int pt, ph, pw;          // leading pads (zero via TMA bounds, or reflect)
+  int reflect_h, reflect_w;
+  int tile_w, tile_h, R;   // M-tile = tile_h rows x tile_w pixels; R tiles per CTA
+  int kc, n_chunks;        // channels per K chunk, chunks per tap
+  int halo;                // 1: a stage holds one input-row halo for all KS taps
+  int box_w;               // A box width in loaded elements
+  int pitch_rows;          // shared-memory rows per A box (box_w rounded to 8)
+  int a_tile_rows;         // rows between consecutive M-tiles in a stage
+  int row_bytes;           // kc * 2
+  int swz;                 // descriptor layout code (2 = 128B, 4 = 64B, 6 = 32B)
+  int BN, n_sub, sub_n;    // CTA N = n_sub MMAs of sub_n columns
+  int acc_stride;          // TMEM columns between M-tile accumulators
+  int tmem_cols;
+  int stages;
+  uint32_t a_stage_bytes, b_stage_bytes, bar_off;
+  uint32_t tx_bytes;       // bytes one stage's loads deliver
+  int taps_per_stage;
+  int stages_total;
+  int k_splits, stages_per_split;
+  int tiles_w, groups_h;
+  int cp64;                // channel pitch of the packed weight
+  int desc_mode;           // 1: descriptor base offset from address bits
+  int inject;              // test aid (see conv3d_tuning.inject)
+  unsigned long long timeout_ns;
+  float* partial;          // [k_splits][M][Cout] fp32 when k_splits > 1
+  long long M_total;
+};
+
+}  // namespace vvc

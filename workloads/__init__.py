@@ -46,7 +46,7 @@ EPI_L2NORM_SILU = 8
 EPI_SAVE_VALUE = 16
 EPI_OUT_PAD_BR = 32
 
-WORKLOAD_IDS = {"tiny": 1, "wan": 2, "ladder": 3, "fused160": 4, "t1": 5}
+WORKLOAD_IDS = {"tiny": 1, "wan": 2, "ladder": 3, "fused160": 4, "t1": 5, "test": 9}
 
 
 @dataclass
