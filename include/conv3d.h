@@ -141,8 +141,7 @@ typedef struct {
   int32_t halo;        /* -1 auto, 0 off, 1 on: one input-row halo serves all W taps */
   int32_t stages;      /* shared-memory pipeline depth */
   int32_t k_splits;    /* split of the reduction across CTAs (>= 1) */
-  int32_t desc_mode;   /* shared-memory descriptor base offset: 0 auto, 1 always zero,
-                          2 taken from the start address bits */
+  int32_t reserved0;   /* must be 0 */
   int32_t inject;      /* test aid: >0 makes the producer skip stage (inject-1) so a
                           bounded wait runs out; the call then reports a timeout */
   int32_t timeout_ms;  /* device wait limit (0 = default 4000 ms) */

@@ -52,14 +52,11 @@ BASE = mk("base", 1, 64, 3, 6, 150, 64, index=1)
 
 PLAN_VARIANTS = [
     dict(halo=0),
-    dict(halo=1, desc_mode=1),
-    dict(halo=1, desc_mode=2),
+    dict(halo=1),
     dict(halo=0, kc=32),
     dict(halo=0, kc=16),
-    dict(halo=1, kc=32, desc_mode=1),
-    dict(halo=1, kc=32, desc_mode=2),
-    dict(halo=1, kc=16, desc_mode=1),
-    dict(halo=1, kc=16, desc_mode=2),
+    dict(halo=1, kc=32),
+    dict(halo=1, kc=16),
     dict(halo=0, R=2),
     dict(halo=1, R=3, BN=32),
     dict(halo=0, k_splits=3),

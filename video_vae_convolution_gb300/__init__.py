@@ -79,7 +79,7 @@ class Params(ctypes.Structure):
 
 class Tuning(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
-        "tile_w", "tile_h", "R", "kc", "BN", "halo", "stages", "k_splits", "desc_mode",
+        "tile_w", "tile_h", "R", "kc", "BN", "halo", "stages", "k_splits", "reserved0",
         "inject", "timeout_ms")]
 
     def __init__(self, **kw):

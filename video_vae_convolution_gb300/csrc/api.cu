@@ -313,7 +313,6 @@ int make_plan(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
   k.reflect_h = (p->pad[1].mode == CONV3D_PAD_REFLECT && (p->pad[1].before || p->pad[1].after));
   k.reflect_w = (p->pad[2].mode == CONV3D_PAD_REFLECT && (p->pad[2].before || p->pad[2].after));
   k.cp64 = static_cast<int>(round_up(p->Cin, 64));
-  k.desc_mode = t.desc_mode > 0 ? t.desc_mode - 1 : 0;  // swizzle follows absolute address bits
   k.inject = t.inject;
   k.timeout_ns = (unsigned long long)(t.timeout_ms > 0 ? t.timeout_ms : 4000) * 1000000ULL;
 

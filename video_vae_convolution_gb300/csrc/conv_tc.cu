@@ -54,12 +54,6 @@ __device__ __forceinline__ uint32_t swizzle_off(uint32_t off, int swz) {
   return off ^ (((off >> 7) & mask) << 4);
 }
 
-__device__ __forceinline__ uint32_t desc_base_offset(uint32_t addr, int swz, int mode) {
-  if (mode != 1) return 0u;
-  const uint32_t mask = (swz == 2) ? 7u : (swz == 4) ? 3u : 1u;
-  return (addr >> 7) & mask;
-}
-
 __device__ __forceinline__ bool wait_no_abort(uint32_t bar, uint32_t parity,
                                               unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -220,14 +214,14 @@ __global__ void __launch_bounds__(256, 1)
             for (int kk = 0; kk < p.kc / 16; ++kk) {
               const uint32_t a_addr =
                   a_stage + static_cast<uint32_t>(a_row * p.row_bytes + kk * 32);
-              const uint64_t adesc =
-                  sdesc(a_addr, 16u, sbo, p.swz, desc_base_offset(a_addr, p.swz, p.desc_mode));
+              // The swizzle follows absolute shared-memory address bits, so a view
+              // shifted by whole rows (the halo taps) keeps base offset 0.
+              const uint64_t adesc = sdesc(a_addr, 16u, sbo, p.swz, 0u);
               for (int u = 0; u < p.n_sub; ++u) {
                 const uint32_t b_addr =
                     b_stage +
                     static_cast<uint32_t>((tl * p.BN + u * p.sub_n) * p.row_bytes + kk * 32);
-                const uint64_t bdesc =
-                    sdesc(b_addr, 16u, sbo, p.swz, desc_base_offset(b_addr, p.swz, p.desc_mode));
+                const uint64_t bdesc = sdesc(b_addr, 16u, sbo, p.swz, 0u);
                 const uint32_t d = tmem_base + static_cast<uint32_t>(j * p.acc_stride +
                                                                      u * p.sub_n);
                 const uint32_t acc = (first_stage && tl == 0 && kk == 0) ? 0u : 1u;

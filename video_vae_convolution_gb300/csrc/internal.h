@@ -60,7 +60,6 @@ struct ConvTCParams {
   int k_splits, stages_per_split;
   int tiles_w, groups_h;
   int cp64;                // channel pitch of the packed weight
-  int desc_mode;           // 1: descriptor base offset from address bits
   int inject;              // test aid (see conv3d_tuning.inject)
   unsigned long long timeout_ns;
   float* partial;          // [k_splits][M][Cout] fp32 when k_splits > 1
