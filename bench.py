@@ -65,7 +65,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -188,10 +188,11 @@ def oracle_rate(target_s=12.0, max_points=None):
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
-    budget = 8.0
+    # bounded: the whole run stays within about two minutes of CPU time
+    budget = max(1.0, min(8.0, 120.0 / max(1, args.steps + args.warmup)))
     rates = []
     for _ in range(args.warmup):
-        oracle_rate(target_s=1.0)
+        oracle_rate(target_s=min(1.0, budget))
     t0 = time.perf_counter()
     desc = ""
     cores = 0
@@ -347,15 +348,64 @@ def run_gpu(args, rank, world):
     return 0
 
 
+def run_case(args):
+    """One call of a workload, timed alone (for profiling and tuning)."""
+    import video_vae_convolution_gb300 as vvc
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    work = wl.all_workloads()[args.workload]
+    call = next(c for c in work.calls if c.name == args.case)
+    lay = wl.NCDHW if args.layout == "ncdhw" else wl.NDHWC
+    inp = wl.make_inputs(args.workload, call, lay, lay)
+    g = lambda k: None if inp[k] is None else inp[k].to(dev)
+    tun = None
+    if args.tune:
+        tun = vvc.Tuning(**{k: int(v) for k, v in (kv.split("=") for kv in args.tune.split(","))})
+    wp = vvc.pack_weight(inp["w"].to(dev))
+    c = vvc.Conv3d(inp["x"].to(dev), wp, call.Cout, call.kernel, call.stride, call.pads, lay, lay,
+                   call.epi, bias=g("bias"), residual=g("residual"),
+                   residual_bias=g("residual_bias"), gamma=g("gamma"), tuning=tun)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        c(stream)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        c(stream)
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    assert vvc.device_status() == 0
+    ms = statistics.median(ts)
+    print(json.dumps({"case": call.name, "layout": args.layout, "ms": round(ms, 4),
+                      "tflops": round(call.flops / (ms * 1e-3) / 1e12, 1),
+                      "gbs": round(call.bytes() / (ms * 1e-3) / 1e9, 1),
+                      "launches": c.launches, "tune": args.tune}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--workload", default="wan")
+    ap.add_argument("--case", default=None, help="time one call of --workload alone")
+    ap.add_argument("--layout", default="ndhwc", choices=["ndhwc", "ncdhw"])
+    ap.add_argument("--tune", default="", help="plan overrides, e.g. R=2,kc=32")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl != "reference" else args.warmup
+    if args.case:
+        return run_case(args)
     rank, world = dist_init(args)
     if args.impl == "reference":
         rc = run_reference(args, rank, world)

@@ -138,10 +138,11 @@ typedef struct {
   int32_t R;           /* M-tiles per CTA */
   int32_t kc;          /* channels per K chunk: 16, 32 or 64 */
   int32_t BN;          /* output channels per CTA (multiple of 16) */
-  int32_t halo;        /* -1 auto, 0 off, 1 on: one input-row halo serves all W taps */
+  int32_t halo;        /* 0 auto, 1 on, 2 off: one input-row halo serves all W taps */
   int32_t stages;      /* shared-memory pipeline depth */
   int32_t k_splits;    /* split of the reduction across CTAs (>= 1) */
-  int32_t reserved0;   /* must be 0 */
+  int32_t kernel;      /* 0 auto, 1 pixel-major tiles (M = pixels), 2 channel-major tiles
+                          (M = output channels, N = up to 256 pixels) */
   int32_t inject;      /* test aid: >0 makes the producer skip stage (inject-1) so a
                           bounded wait runs out; the call then reports a timeout */
   int32_t timeout_ms;  /* device wait limit (0 = default 4000 ms) */

@@ -50,18 +50,30 @@ def test_pack_weight_bit_exact():
 
 BASE = mk("base", 1, 64, 3, 6, 150, 64, index=1)
 
+# tuning: kernel 1 = pixel-major tiles, 2 = channel-major tiles; halo 1 on, 2 off
 PLAN_VARIANTS = [
-    dict(halo=0),
-    dict(halo=1),
-    dict(halo=0, kc=32),
-    dict(halo=0, kc=16),
-    dict(halo=1, kc=32),
-    dict(halo=1, kc=16),
-    dict(halo=0, R=2),
-    dict(halo=1, R=3, BN=32),
-    dict(halo=0, k_splits=3),
-    dict(halo=1, k_splits=2),
-    dict(halo=0, stages=2),
+    dict(kernel=2),
+    dict(kernel=2, halo=1),
+    dict(kernel=2, halo=2),
+    dict(kernel=2, kc=32),
+    dict(kernel=2, kc=16),
+    dict(kernel=2, kc=32, halo=1),
+    dict(kernel=2, tile_w=64, tile_h=3),
+    dict(kernel=2, tile_w=128, halo=1),
+    dict(kernel=2, k_splits=3),
+    dict(kernel=2, halo=1, k_splits=2),
+    dict(kernel=2, stages=2),
+    dict(kernel=1, halo=2),
+    dict(kernel=1, halo=1),
+    dict(kernel=1, halo=2, kc=32),
+    dict(kernel=1, halo=2, kc=16),
+    dict(kernel=1, halo=1, kc=32),
+    dict(kernel=1, halo=1, kc=16),
+    dict(kernel=1, halo=2, R=2),
+    dict(kernel=1, halo=1, R=3, BN=32),
+    dict(kernel=1, halo=2, k_splits=3),
+    dict(kernel=1, halo=1, k_splits=2),
+    dict(kernel=1, halo=2, stages=2),
 ]
 
 
@@ -73,6 +85,9 @@ def test_plan_variants(tv):
 
 
 SHAPES = [
+    mk("wide_halo_two_boxes", 1, 64, 2, 4, 250, 128, index=18),
+    mk("cout200_two_channel_tiles", 1, 64, 2, 5, 90, 200, pads=CR, index=19),
+    mk("wide_640_tiles", 1, 64, 3, 3, 642, 96, pads=VALID, index=20),
     mk("t1_2d_tiles_h", 2, 32, 1, 9, 40, 48, kernel=(1, 3, 3), pads=P2D, index=2),
     mk("stride2_causal_reflect", 1, 32, 5, 11, 71, 32, stride=(2, 2, 2), pads=CR, index=3),
     mk("reflect_causal_wide", 1, 16, 4, 7, 133, 32, pads=CR, index=4),

@@ -79,12 +79,11 @@ class Params(ctypes.Structure):
 
 class Tuning(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
-        "tile_w", "tile_h", "R", "kc", "BN", "halo", "stages", "k_splits", "reserved0",
+        "tile_w", "tile_h", "R", "kc", "BN", "halo", "stages", "k_splits", "kernel",
         "inject", "timeout_ms")]
 
     def __init__(self, **kw):
         super().__init__()
-        self.halo = -1
         for k, v in kw.items():
             setattr(self, k, int(v))
 

@@ -10,13 +10,17 @@
 #include <cstdlib>
 #include <cstring>
 
-#include "../../include/conv3d.h"
+#include "conv3d.h"
 #include "internal.h"
 
 namespace vvc {
 cudaError_t launch_conv_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const ConvTCParams& p,
                            dim3 grid, size_t smem_bytes, cudaStream_t stream);
+cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
+                           const ConvCMParams& p, int grid, size_t smem_bytes,
+                           cudaStream_t stream);
 cudaError_t conv_status_read_clear(int* status, cudaStream_t stream);
+cudaError_t conv_cm_status_read_clear(int* status);
 cudaError_t launch_pack_weight(const void* w, void* out, int Co, int Ci, int taps,
                                cudaStream_t s);
 cudaError_t launch_stage_input(const void* x, int layout, int N, int C, int Cp, long long S,
@@ -29,6 +33,7 @@ cudaError_t launch_l2norm_silu(const void* x, long long rows, const EpiParams& e
 
 namespace {
 
+using vvc::ConvCMParams;
 using vvc::ConvTCParams;
 using vvc::EpiParams;
 
@@ -59,7 +64,9 @@ struct Plan {
   size_t stage_off = 0, stage_bytes = 0;
   size_t partial_off = 0, partial_bytes = 0;
   size_t ws_bytes = 0;
+  bool cm = false;          // channel-major kernel (conv_cm) instead of pixel-major (conv_tc)
   ConvTCParams kp{};
+  ConvCMParams cp{};
   dim3 grid;
   size_t smem = 0;
   int launches = 0;
@@ -142,27 +149,159 @@ int check_supported(const conv3d_params* p) {
   return CONV3D_OK;
 }
 
-int make_plan(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
-  int rc = validate_shape(p, &pl->Do, &pl->Ho, &pl->Wo);
-  if (rc) return rc;
-  rc = check_supported(p);
-  if (rc) return rc;
-  conv3d_tuning t{};
-  if (tu) t = *tu;
+// Epilogue parameters common to both kernels.
+void fill_epi(const conv3d_params* p, const Plan& pl, EpiParams* e) {
+  e->y = p->y;
+  e->out_layout = p->out_layout;
+  e->N = p->N;
+  e->Cout = p->Cout;
+  e->Do = pl.Do;
+  e->Ho = pl.Ho;
+  e->Wo = pl.Wo;
+  e->flags = p->epi;
+  e->bias = p->bias;
+  e->residual = static_cast<const uint16_t*>(p->residual);
+  e->rbias = p->residual_bias;
+  e->gamma = p->gamma;
+  e->value_out = static_cast<uint16_t*>(p->value_out);
+  e->conv_out = static_cast<uint16_t*>(p->conv_out);
+  e->sqrt_c = std::sqrt(static_cast<float>(p->Cout));
+}
+
+// Split of the reduction so that small layers still fill the GPU.
+int choose_splits(const conv3d_tuning& t, long long tiles, int stages_total, int sms, int* per) {
+  int splits = t.k_splits;
+  if (splits <= 0) {
+    splits = 1;
+    if (tiles < sms) {
+      splits = static_cast<int>(std::max<long long>(1, (sms + tiles / 2) / tiles));
+      splits = std::min(splits, std::max(1, stages_total / 4));
+      splits = std::min(splits, 16);
+    }
+  }
+  splits = std::max(1, std::min(splits, stages_total));
+  *per = static_cast<int>(cdiv(stages_total, splits));
+  return static_cast<int>(cdiv(stages_total, *per));
+}
+
+// Channel-major plan: M = 128 output channels, N = up to 256 output pixels.
+int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off) {
+  ConvCMParams& k = pl->cp;
+  std::memset(&k, 0, sizeof(k));
+  const int Do = pl->Do, Ho = pl->Ho, Wo = pl->Wo;
+  const int sw = p->stride[2];
+  int kc = t.kc;
+  if (kc == 0) kc = (pl->Cst > 32) ? 64 : (pl->Cst > 16 ? 32 : 16);
+  if (kc != 16 && kc != 32 && kc != 64) return CONV3D_ERR_INVALID_ARG;
+  k.kc = kc;
+  k.row_bytes = kc * 2;
+  k.n_chunks = static_cast<int>(cdiv(p->Cin, kc));
+  // pixel tile
+  bool halo;
+  int tw, rh;
+  if (t.tile_w > 0) {
+    tw = t.tile_w;
+    rh = t.tile_h > 0 ? t.tile_h : 1;
+    halo = (t.halo == 1) || (t.halo == 0 && sw == 1 && rh == 1 && p->KS > 1);
+  } else if (sw == 1 && p->KS > 1 && Wo >= 176 && t.halo != 2) {
+    const int nt = static_cast<int>(cdiv(Wo, 256));
+    tw = static_cast<int>(round_up(cdiv(Wo, nt), 16));
+    if (tw > 256) tw = 256;
+    rh = 1;
+    halo = true;
+  } else {
+    const int maxw = std::min(256, 256 / sw);
+    tw = static_cast<int>(std::min<long long>(round_up(Wo, 8), maxw / 8 * 8));
+    rh = std::max(1, std::min(256 / tw, Ho));
+    halo = (t.halo == 1) && sw == 1 && rh == 1;
+  }
+  if (halo && (sw != 1 || rh != 1)) return CONV3D_ERR_INVALID_ARG;
+  if (tw < 1 || rh < 1 || tw * rh > 256 || tw * sw > 256) return CONV3D_ERR_INVALID_ARG;
+  if (rh > 1 && tw % 8) return CONV3D_ERR_INVALID_ARG;
+  k.tw = tw;
+  k.rh = rh;
+  k.halo = halo ? 1 : 0;
+  k.N = static_cast<int>(round_up((long long)tw * rh, 16));
+  if (halo) {
+    const int run = tw + p->KS - 1;
+    k.nbox = static_cast<int>(cdiv(run, 256));
+    k.box_w = k.nbox == 1 ? run : static_cast<int>(round_up(cdiv(run, k.nbox), 8));
+    k.box_pitch = k.nbox == 1 ? static_cast<int>(round_up(run, 8)) : k.box_w;
+  } else {
+    k.nbox = rh;
+    k.box_w = tw;
+    k.box_pitch = tw;
+  }
+  k.taps_per_stage = halo ? p->KS : 1;
+  k.stages_total = p->KT * p->KR * (halo ? 1 : p->KS) * k.n_chunks;
+  const long long act_rows = std::max<long long>((long long)k.nbox * k.box_pitch,
+                                                 k.N + (halo ? p->KS - 1 : 0));
+  k.act_bytes = static_cast<uint32_t>(round_up(round_up(act_rows, 8) * k.row_bytes, 1024));
+  const uint32_t wgt_bytes = static_cast<uint32_t>(k.taps_per_stage * 128 * k.row_bytes);
+  k.stage_bytes = k.act_bytes + wgt_bytes;
+  constexpr size_t kEpiStage = 4 * 32 * 33 * 4;  // per-warp transpose blocks
+  int stages = static_cast<int>(
+      std::min<size_t>(8, (kMaxSmem - 1024 - 256 - kEpiStage) / k.stage_bytes));
+  if (t.stages > 0) stages = std::min(stages, t.stages);
+  if (stages < 2) return CONV3D_ERR_UNSUPPORTED;
+  k.stages = stages;
+  k.bar_off = k.stage_bytes * stages;
+  k.tx_bytes = static_cast<uint32_t>((long long)k.nbox * k.box_w * k.row_bytes) + wgt_bytes;
+  k.tiles_w = static_cast<int>(cdiv(Wo, tw));
+  k.tiles_h = static_cast<int>(cdiv(Ho, rh));
+  k.tiles_c = static_cast<int>(cdiv(p->Cout, 128));
+  const long long tiles = (long long)k.tiles_w * k.tiles_h * Do * p->N * k.tiles_c;
+  const int sms = num_sms();
+  int per = 0;
+  const int splits = choose_splits(t, tiles, k.stages_total, sms, &per);
+  k.k_splits = splits;
+  k.stages_per_split = per;
+  if (tiles * splits > 0x7fffffffLL) return CONV3D_ERR_UNSUPPORTED;
+  k.num_tiles = static_cast<int>(tiles * splits);
+  k.acc_cols = static_cast<int>(round_up(k.N, 32));
+  k.nbuf = (2 * k.acc_cols <= 512) ? 2 : 1;
+  int cols = 32;
+  while (cols < k.nbuf * k.acc_cols) cols *= 2;
+  k.tmem_cols = cols;
+  k.M_total = (long long)p->N * Do * Ho * Wo;
+  if (splits > 1) {
+    pl->partial_off = off;
+    pl->partial_bytes = (size_t)splits * (size_t)k.M_total * p->Cout * 4;
+    off = static_cast<size_t>(round_up(off + pl->partial_bytes, 256));
+  }
+  pl->ws_bytes = off;
+  pl->grid = dim3(static_cast<unsigned>(std::min<long long>(k.num_tiles, sms)), 1, 1);
+  k.epi_off = k.bar_off + 256;
+  pl->smem = 1024 + k.epi_off + kEpiStage;
+  pl->launches = (pl->stage ? 1 : 0) + 1 + (splits > 1 ? 1 : 0);
+  k.C = pl->Cst;
+  k.D = p->D;
+  k.H = p->H;
+  k.W = p->W;
+  k.KT = p->KT;
+  k.KR = p->KR;
+  k.KS = p->KS;
+  k.st = p->stride[0];
+  k.sh = p->stride[1];
+  k.sw = sw;
+  k.pt = p->pad[0].before;
+  k.ph = p->pad[1].before;
+  k.pw = p->pad[2].before;
+  k.reflect_h = (p->pad[1].mode == CONV3D_PAD_REFLECT && (p->pad[1].before || p->pad[1].after));
+  k.reflect_w = (p->pad[2].mode == CONV3D_PAD_REFLECT && (p->pad[2].before || p->pad[2].after));
+  k.cp64 = static_cast<int>(round_up(p->Cin, 64));
+  k.inject = t.inject;
+  k.timeout_ns = (unsigned long long)(t.timeout_ms > 0 ? t.timeout_ms : 4000) * 1000000ULL;
+  fill_epi(p, *pl, &k.epi);
+  return CONV3D_OK;
+}
+
+// Pixel-major plan: M = 128 output pixels per tile, N = output channels.  Used
+// for the fused L2-norm epilogue, which needs a pixel's whole channel row.
+int plan_pm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off) {
   const int Do = pl->Do, Ho = pl->Ho, Wo = pl->Wo;
   const int st = p->stride[0], sh = p->stride[1], sw = p->stride[2];
   const bool norm = (p->epi & CONV3D_EPI_L2NORM_SILU) != 0;
-
-  // ---- input staging ----
-  pl->stage = (p->layout == CONV3D_NCDHW) || (p->Cin % 8 != 0);
-  pl->Cst = static_cast<int>(round_up(p->Cin, 8));
-  size_t off = 0;
-  if (pl->stage) {
-    pl->stage_off = off;
-    pl->stage_bytes = (size_t)p->N * p->D * p->H * p->W * pl->Cst * 2;
-    off = static_cast<size_t>(round_up(off + pl->stage_bytes, 256));
-  }
-
   ConvTCParams& k = pl->kp;
   std::memset(&k, 0, sizeof(k));
   // ---- channel chunk ----
@@ -215,7 +354,7 @@ int make_plan(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
   if (tile_w < 1 || tile_w > 128 || tile_w * tile_h > 128) return CONV3D_ERR_INVALID_ARG;
   if (tile_h > 1 && tile_w % 8) return CONV3D_ERR_INVALID_ARG;
   bool halo = (sw == 1 && tile_h == 1 && p->KS > 1);
-  if (t.halo == 0) halo = false;
+  if (t.halo == 2) halo = false;
   if (t.halo == 1) {
     if (sw != 1 || tile_h != 1) return CONV3D_ERR_INVALID_ARG;
     halo = true;
@@ -251,6 +390,18 @@ int make_plan(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
     stages = static_cast<int>(std::min<size_t>(8, avail / (a_stage + b_stage)));
     if (t.stages > 0) stages = std::min(stages, t.stages);
     if (stages >= 2) break;
+    if (R == 1 && halo && t.halo != 1) {
+      // the KS weight boxes of a halo stage do not fit twice: load one tap per stage
+      halo = false;
+      k.halo = 0;
+      k.box_w = tile_w;
+      k.pitch_rows = static_cast<int>(round_up(k.box_w, 8));
+      if (tile_h > 1) k.pitch_rows = tile_w;
+      k.a_tile_rows = tile_h * k.pitch_rows;
+      k.taps_per_stage = 1;
+      k.stages_total = p->KT * p->KR * p->KS * k.n_chunks;
+      R = Rmax + 1;  // retry every R without the halo
+    }
   }
   if (R < 1 || stages < 2) return CONV3D_ERR_UNSUPPORTED;
   k.R = R;
@@ -316,23 +467,35 @@ int make_plan(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
   k.inject = t.inject;
   k.timeout_ns = (unsigned long long)(t.timeout_ms > 0 ? t.timeout_ms : 4000) * 1000000ULL;
 
-  EpiParams& e = k.epi;
-  e.y = p->y;
-  e.out_layout = p->out_layout;
-  e.N = p->N;
-  e.Cout = p->Cout;
-  e.Do = Do;
-  e.Ho = Ho;
-  e.Wo = Wo;
-  e.flags = p->epi;
-  e.bias = p->bias;
-  e.residual = static_cast<const uint16_t*>(p->residual);
-  e.rbias = p->residual_bias;
-  e.gamma = p->gamma;
-  e.value_out = static_cast<uint16_t*>(p->value_out);
-  e.conv_out = static_cast<uint16_t*>(p->conv_out);
-  e.sqrt_c = std::sqrt(static_cast<float>(p->Cout));
+  fill_epi(p, *pl, &k.epi);
   return CONV3D_OK;
+}
+
+int make_plan(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
+  int rc = validate_shape(p, &pl->Do, &pl->Ho, &pl->Wo);
+  if (rc) return rc;
+  rc = check_supported(p);
+  if (rc) return rc;
+  conv3d_tuning t{};
+  if (tu) t = *tu;
+  // input staging: NCDHW input, or channels not a multiple of 8 (TMA strides)
+  pl->stage = (p->layout == CONV3D_NCDHW) || (p->Cin % 8 != 0);
+  pl->Cst = static_cast<int>(round_up(p->Cin, 8));
+  size_t off = 0;
+  if (pl->stage) {
+    pl->stage_off = off;
+    pl->stage_bytes = (size_t)p->N * p->D * p->H * p->W * pl->Cst * 2;
+    off = static_cast<size_t>(round_up(off + pl->stage_bytes, 256));
+  }
+  const bool norm = (p->epi & CONV3D_EPI_L2NORM_SILU) != 0;
+  bool cm = !norm;
+  if (t.kernel == 1) cm = false;
+  if (t.kernel == 2) {
+    if (norm) return CONV3D_ERR_UNSUPPORTED;
+    cm = true;
+  }
+  pl->cm = cm;
+  return cm ? plan_cm(p, t, pl, off) : plan_pm(p, t, pl, off);
 }
 
 int check_pointers(const conv3d_params* p, const Plan& pl) {
@@ -404,26 +567,42 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
                 CUtensorMap* tmB) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return CONV3D_ERR_CUDA;
-  const ConvTCParams& k = pl.kp;
+  int kc, act_box, es_w, wgt_rows, cp64;
+  if (pl.cm) {
+    const ConvCMParams& k = pl.cp;
+    kc = k.kc;
+    act_box = k.halo ? k.box_w : k.box_w * k.sw;
+    es_w = k.halo ? 1 : k.sw;
+    wgt_rows = 128;
+    cp64 = k.cp64;
+  } else {
+    const ConvTCParams& k = pl.kp;
+    kc = k.kc;
+    act_box = k.halo ? k.box_w : k.tile_w * k.sw;
+    es_w = k.halo ? 1 : k.sw;
+    wgt_rows = k.sub_n;
+    cp64 = k.cp64;
+  }
+  // activations: NDHWC bf16, dims (C, W, H, D, N); one box = kc channels x a run of
+  // input pixels along W (element stride = the W stride of the convolution)
   const cuuint64_t C = static_cast<cuuint64_t>(pl.Cst);
   cuuint64_t gdimA[5] = {C, (cuuint64_t)p->W, (cuuint64_t)p->H, (cuuint64_t)p->D,
                          (cuuint64_t)p->N};
   cuuint64_t gstrA[4] = {C * 2, C * 2 * p->W, C * 2 * p->W * p->H, C * 2 * p->W * p->H * p->D};
-  const int es_w = k.halo ? 1 : k.sw;
-  cuuint32_t boxA[5] = {(cuuint32_t)k.kc,
-                        (cuuint32_t)(k.halo ? k.box_w : k.tile_w * k.sw), 1, 1, 1};
+  cuuint32_t boxA[5] = {(cuuint32_t)kc, (cuuint32_t)act_box, 1, 1, 1};
   cuuint32_t esA[5] = {1, (cuuint32_t)es_w, 1, 1, 1};
   CUresult r = enc(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(xin), gdimA, gstrA,
-                   boxA, esA, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(k.kc),
+                   boxA, esA, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kc),
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
-  const cuuint64_t Ktot = (cuuint64_t)p->KT * p->KR * p->KS * k.cp64;
+  // packed weights [Cout][taps * cp64]: one box = kc channels x wgt_rows output channels
+  const cuuint64_t Ktot = (cuuint64_t)p->KT * p->KR * p->KS * cp64;
   cuuint64_t gdimB[2] = {Ktot, (cuuint64_t)p->Cout};
   cuuint64_t gstrB[1] = {Ktot * 2};
-  cuuint32_t boxB[2] = {(cuuint32_t)k.kc, (cuuint32_t)k.sub_n};
+  cuuint32_t boxB[2] = {(cuuint32_t)kc, (cuuint32_t)wgt_rows};
   cuuint32_t esB[2] = {1, 1};
   r = enc(tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p->w_packed), gdimB, gstrB,
-          boxB, esB, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(k.kc),
+          boxB, esB, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kc),
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
   return CONV3D_OK;
@@ -495,15 +674,25 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
   CUtensorMap tmA, tmB;
   rc = encode_maps(p, pl, xin, &tmA, &tmB);
   if (rc) return rc;
-  ConvTCParams kp = pl.kp;
-  if (kp.k_splits > 1) kp.partial = reinterpret_cast<float*>(ws + pl.partial_off);
-  if (vvc::launch_conv_tc(tmA, tmB, kp, pl.grid, pl.smem, s) != cudaSuccess)
-    return CONV3D_ERR_CUDA;
-  if (kp.k_splits > 1) {
-    if (vvc::launch_splitk_epilogue(kp.partial, kp.k_splits, kp.M_total, kp.epi, s) !=
+  float* partial = reinterpret_cast<float*>(ws + pl.partial_off);
+  if (pl.cm) {
+    ConvCMParams kp = pl.cp;
+    if (kp.k_splits > 1) kp.partial = partial;
+    if (vvc::launch_conv_cm(tmA, tmB, kp, static_cast<int>(pl.grid.x), pl.smem, s) !=
         cudaSuccess)
       return CONV3D_ERR_CUDA;
+    if (kp.k_splits > 1 &&
+        vvc::launch_splitk_epilogue(partial, kp.k_splits, kp.M_total, kp.epi, s) != cudaSuccess)
+      return CONV3D_ERR_CUDA;
+    return CONV3D_OK;
   }
+  ConvTCParams kp = pl.kp;
+  if (kp.k_splits > 1) kp.partial = partial;
+  if (vvc::launch_conv_tc(tmA, tmB, kp, pl.grid, pl.smem, s) != cudaSuccess)
+    return CONV3D_ERR_CUDA;
+  if (kp.k_splits > 1 &&
+      vvc::launch_splitk_epilogue(partial, kp.k_splits, kp.M_total, kp.epi, s) != cudaSuccess)
+    return CONV3D_ERR_CUDA;
   return CONV3D_OK;
 }
 
@@ -558,10 +747,11 @@ int l2norm_silu(const void* x, int64_t rows, int32_t C, const float* input_bias,
 
 int conv3d_get_device_status(int32_t* status, conv3d_stream_t stream) {
   if (!status) return CONV3D_ERR_INVALID_ARG;
-  int v = 0;
+  int v = 0, w = 0;
   if (vvc::conv_status_read_clear(&v, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return CONV3D_ERR_CUDA;
-  *status = v;
+  if (vvc::conv_cm_status_read_clear(&w) != cudaSuccess) return CONV3D_ERR_CUDA;
+  *status = v ? v : w;
   return CONV3D_OK;
 }
 

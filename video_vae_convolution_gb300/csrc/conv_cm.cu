@@ -1,0 +1,414 @@
+// Channel-major implicit-GEMM bf16 convolution on the sm_103a tensor cores.
+//
+// Same GEMM as conv_tc.cu (ROCm/FlyDSL issue "[Feature]: conv3d_implicit —
+// accept and emit NDHWC ...": output pixels x output channels x (taps *
+// input channels)), but with the operands swapped so that every MMA is as wide
+// as the hardware allows: the accumulator is D[channel][pixel] in TMEM, each
+// tcgen05.mma is M = 128 output channels (packed weights, cuDNN frontend doc
+// "Fused Conv3D + Bias + Residual + RMSNorm + SiLU", "Weight Packing") by
+// N = up to 256 output pixels (activations) by K = 16.  On sm_103a an MMA costs
+// about the same issue time for any N up to ~192, so a 256-pixel N keeps the
+// tensor pipe busy even when the layer has only 96 or 128 output channels.
+//
+// Persistent CTAs walk a static list of tiles (128 channels x one pixel tile,
+// times a slice of the reduction when it is split).  A pixel tile is either one
+// run of up to 256 output pixels of one output row (halo mode, stride 1 along W:
+// one TMA run of tw + KS - 1 input pixels serves all KS taps as shifted views)
+// or rh rows of tw pixels (direct mode: one TMA box per row and tap, element
+// stride = conv stride).  Channel chunks are 64 wide (128-byte swizzled rows).
+// The accumulator is double buffered in TMEM so the epilogue of one tile runs
+// under the MMAs of the next.
+//
+// Warp roles (256 threads): 0 TMA producer, 1 MMA issuer + TMEM owner,
+// 2 reflect-W patcher, 4..7 epilogue (thread = output channel, loops over the
+// tile's pixels; stores are coalesced across channels for NDHWC output).
+// Waits are bounded; a time-out records CONV3D_ERR_DEVICE_TIMEOUT.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "epilogue.cuh"
+#include "epilogue_cm.cuh"
+#include "internal.h"
+#include "kernel_common.cuh"
+#include "ptx.cuh"
+
+namespace vvc {
+
+__device__ int g_conv_cm_status = 0;
+
+namespace {
+
+constexpr int kWarpProducer = 0;
+constexpr int kWarpMMA = 1;
+constexpr int kWarpPatch = 2;
+constexpr int kWarpEpi0 = 4;
+
+struct TileCoord {
+  int ct, split, twi, thi, od, nb;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const ConvCMParams& p, int tile) {
+  TileCoord c;
+  c.ct = tile % p.tiles_c;
+  tile /= p.tiles_c;
+  c.split = tile % p.k_splits;
+  tile /= p.k_splits;
+  c.twi = tile % p.tiles_w;
+  tile /= p.tiles_w;
+  c.thi = tile % p.tiles_h;
+  tile /= p.tiles_h;
+  c.od = tile % p.epi.Do;
+  c.nb = tile / p.epi.Do;
+  return c;
+}
+
+struct StageCoord {
+  int t, r, sblk, ch;
+};
+
+__device__ __forceinline__ StageCoord decode_stage(const ConvCMParams& p, int it) {
+  StageCoord c;
+  c.ch = it % p.n_chunks;
+  int rest = it / p.n_chunks;
+  if (p.halo) {
+    c.sblk = 0;
+  } else {
+    c.sblk = rest % p.KS;
+    rest /= p.KS;
+  }
+  c.r = rest % p.KR;
+  c.t = rest / p.KR;
+  return c;
+}
+
+__device__ __forceinline__ void stage_range(const ConvCMParams& p, int split, int& b, int& e) {
+  b = split * p.stages_per_split;
+  e = min(p.stages_total, b + p.stages_per_split);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(256, 1)
+    conv_cm_kernel(const __grid_constant__ CUtensorMap tmAct,
+                   const __grid_constant__ CUtensorMap tmWgt,
+                   const __grid_constant__ ConvCMParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int S = p.stages;
+  const uint32_t bars = sbase + p.bar_off;
+  auto full_bar = [&](int s) { return bars + 8u * s; };
+  auto empty_bar = [&](int s) { return bars + 8u * (S + s); };
+  auto ready_bar = [&](int s) { return bars + 8u * (2 * S + s); };
+  auto accf_bar = [&](int b) { return bars + 8u * (3 * S + b); };
+  auto acce_bar = [&](int b) { return bars + 8u * (3 * S + 2 + b); };
+  const uint32_t drain_bar = bars + 8u * (3 * S + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.bar_off + 8 * (3 * S + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int swz = swz_code_for_rowbytes(p.row_bytes);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+      mbar_init(ready_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 4);  // one arrive per epilogue warp
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmAct);
+    tma_prefetch_desc(&tmWgt);
+  }
+  if (warp == kWarpMMA) {
+    tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(p.tmem_cols));
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const unsigned long long lim = p.timeout_ns;
+
+  if (warp == kWarpProducer) {
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0;
+      long long k_global = 0;   // stage counter across tiles
+      long long k_skip = -1;    // stage left unissued by the test aid
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const TileCoord tc = decode_tile(p, tile);
+        const int w0 = tc.twi * p.tw, h0 = tc.thi * p.rh, c0 = tc.ct * 128;
+        int it_b, it_e;
+        stage_range(p, tc.split, it_b, it_e);
+        for (int it = it_b; it < it_e; ++it) {
+          if (!mbar_wait(empty_bar(slot), phase ^ 1u, abort_flag, lim)) {
+            ok = false;
+            break;
+          }
+          const StageCoord sc = decode_stage(p, it);
+          const bool skip = (p.inject > 0 && k_global == p.inject - 1);
+          if (!skip) {
+            const uint32_t full = full_bar(slot);
+            mbar_arrive_expect_tx(full, p.tx_bytes);
+            const uint32_t act = sbase + p.stage_bytes * slot;
+            const uint32_t wgt = act + p.act_bytes;
+            const int d_in = tc.od * p.st + sc.t - p.pt;
+            if (p.halo) {
+              const int ho = h0;
+              int h_in = ho * p.sh + sc.r - p.ph;
+              if (p.reflect_h && ho < p.epi.Ho) h_in = reflect_coord(h_in, p.H);
+              const int w_start = w0 - p.pw;
+              for (int b = 0; b < p.nbox; ++b)
+                tma_load_5d(act + static_cast<uint32_t>(b * p.box_pitch * p.row_bytes), &tmAct,
+                            full, sc.ch * p.kc, w_start + b * p.box_w, h_in, d_in, tc.nb);
+            } else {
+              const int w_start = w0 * p.sw + sc.sblk - p.pw;
+              for (int i = 0; i < p.rh; ++i) {
+                const int ho = h0 + i;
+                int h_in = ho * p.sh + sc.r - p.ph;
+                if (p.reflect_h && ho < p.epi.Ho) h_in = reflect_coord(h_in, p.H);
+                tma_load_5d(act + static_cast<uint32_t>(i * p.box_pitch * p.row_bytes), &tmAct,
+                            full, sc.ch * p.kc, w_start, h_in, d_in, tc.nb);
+              }
+            }
+            for (int tl = 0; tl < p.taps_per_stage; ++tl) {
+              const int s = p.halo ? tl : sc.sblk;
+              const int tap = (sc.t * p.KR + sc.r) * p.KS + s;
+              tma_load_2d(wgt + static_cast<uint32_t>(tl * 128 * p.row_bytes), &tmWgt, full,
+                          tap * p.cp64 + sc.ch * p.kc, c0);
+            }
+          } else {
+            k_skip = k_global;
+          }
+          ++k_global;
+          if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Let every issued copy land before the CTA can exit: in each slot, wait
+      // for the phase of the last stage issued into it.
+      for (int s = 0; s < S; ++s) {
+        long long k_last = k_global - 1 - ((k_global - 1 - s) % S + S) % S;
+        if (k_last == k_skip) k_last -= S;
+        if (k_last >= 0)
+          wait_no_abort(full_bar(s), static_cast<uint32_t>((k_last / S) & 1), lim);
+      }
+    }
+  } else if (warp == kWarpMMA) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128, p.N);
+      const uint32_t sbo = 8u * static_cast<uint32_t>(p.row_bytes);
+      // The high descriptor word (stride, version, swizzle) is fixed; operand
+      // views differ only in the start-address field (16-byte units).  The
+      // swizzle follows absolute address bits, so row-shifted halo views keep
+      // base offset 0.
+      const uint32_t desc_hi = static_cast<uint32_t>(sdesc(0u, 16u, sbo, swz, 0u) >> 32);
+      const uint32_t desc_lo0 = static_cast<uint32_t>(sdesc(0u, 16u, sbo, swz, 0u));
+      const uint32_t w_tap_step = static_cast<uint32_t>(128 * p.row_bytes) >> 4;
+      const uint32_t a_tap_step = p.halo ? (static_cast<uint32_t>(p.row_bytes) >> 4) : 0u;
+      const int kk_n = p.kc / 16;
+      int slot = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int local = 0;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+        const TileCoord tc = decode_tile(p, tile);
+        const int buf = (p.nbuf == 2) ? (local & 1) : 0;
+        const int use = (p.nbuf == 2) ? (local >> 1) : local;
+        if (!mbar_wait(acce_bar(buf), static_cast<uint32_t>(use & 1) ^ 1u, abort_flag, lim)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + static_cast<uint32_t>(buf * p.acc_cols);
+        int it_b, it_e;
+        stage_range(p, tc.split, it_b, it_e);
+        uint32_t acc = 0u;
+        for (int it = it_b; it < it_e; ++it) {
+          const uint32_t bar = p.reflect_w ? ready_bar(slot) : full_bar(slot);
+          if (!mbar_wait(bar, phase, abort_flag, lim)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t act = sbase + p.stage_bytes * slot;
+          const uint32_t b_lo = desc_lo0 + (act >> 4);
+          const uint32_t a_lo = desc_lo0 + ((act + p.act_bytes) >> 4);
+          for (int tl = 0; tl < p.taps_per_stage; ++tl) {
+            const uint32_t a_t = a_lo + tl * w_tap_step;
+            const uint32_t b_t = b_lo + tl * a_tap_step;
+            for (int kk = 0; kk < kk_n; ++kk) {
+              const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (a_t + 2u * kk);
+              const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (b_t + 2u * kk);
+              mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+              acc = 1u;
+            }
+          }
+          mma_commit(empty_bar(slot));
+          if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(accf_bar(buf));
+      }
+      mma_commit(drain_bar);
+      wait_no_abort(drain_bar, 0u, lim);
+    }
+  } else if (warp == kWarpPatch) {
+    if (p.reflect_w) {
+      // Reflect padding along W (pad 1): element w = -1 takes x[1] and w = W takes
+      // x[W - 2]; TMA filled both with zeros.
+      int slot = 0;
+      uint32_t phase = 0;
+      const int es = p.halo ? 1 : p.sw;
+      const int step = 2 / es;
+      const int runs = p.halo ? 1 : p.rh;
+      const int run_len = p.halo ? p.nbox * p.box_w : p.box_w;
+      const int run_pitch = p.halo ? 0 : p.box_pitch;
+      const int chunks = p.row_bytes / 16;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const TileCoord tc = decode_tile(p, tile);
+        const int w0 = tc.twi * p.tw;
+        int it_b, it_e;
+        stage_range(p, tc.split, it_b, it_e);
+        for (int it = it_b; it < it_e; ++it) {
+          if (!mbar_wait(full_bar(slot), phase, abort_flag, lim)) {
+            ok = false;
+            break;
+          }
+          const StageCoord sc = decode_stage(p, it);
+          const int w_start = p.halo ? (w0 - p.pw) : (w0 * p.sw + sc.sblk - p.pw);
+          int e_left = -1, e_right = -1;
+          if (w_start <= -1 && ((-1 - w_start) % es) == 0) {
+            const int e = (-1 - w_start) / es;
+            if (e + step < run_len) e_left = e;
+          }
+          if (p.W - w_start >= 0 && ((p.W - w_start) % es) == 0) {
+            const int e = (p.W - w_start) / es;
+            if (e < run_len && e - step >= 0) e_right = e;
+          }
+          uint8_t* act = smem + p.stage_bytes * slot;
+          const int work = runs * 2 * chunks;
+          for (int wi = lane; wi < work; wi += 32) {
+            const int ck = wi % chunks;
+            const int side = (wi / chunks) & 1;
+            const int k = wi / (2 * chunks);
+            const int e = side ? e_right : e_left;
+            if (e < 0) continue;
+            const int src = side ? e - step : e + step;
+            copy_swizzled_row(act, k * run_pitch + src, k * run_pitch + e, p.row_bytes, ck, swz);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ready_bar(slot));
+          if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp >= kWarpEpi0) {
+    const int q = warp & 3;
+    // Everything the epilogue reads per element is copied into registers first.
+    CmEpi E;
+    E.flags = p.epi.flags;
+    E.Cout = p.epi.Cout;
+    E.Do = p.epi.Do;
+    E.Ho = p.epi.Ho;
+    E.Wo = p.epi.Wo;
+    E.pad = (E.flags & EPI_OUT_PAD_BR) != 0;
+    E.Hy = E.Ho + (E.pad ? 1 : 0);
+    E.Wy = E.Wo + (E.pad ? 1 : 0);
+    E.ndhwc = (p.epi.out_layout == LAYOUT_NDHWC);
+    E.split = p.k_splits > 1;
+    E.y = static_cast<uint16_t*>(p.epi.y);
+    E.res = p.epi.residual;
+    E.val = p.epi.value_out;
+    E.conv = p.epi.conv_out;
+    E.part = p.partial;
+    E.bias = p.epi.bias;
+    E.rbias = p.epi.rbias;
+    E.M_total = p.M_total;
+    float(*stage)[33] = reinterpret_cast<float(*)[33]>(smem + p.epi_off + q * (32 * 33 * 4));
+    const int nbuf = p.nbuf, acc_cols = p.acc_cols, Ncols = p.N;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
+      const TileCoord tc = decode_tile(p, tile);
+      const int buf = (nbuf == 2) ? (local & 1) : 0;
+      const int use = (nbuf == 2) ? (local >> 1) : local;
+      if (!mbar_wait(accf_bar(buf), static_cast<uint32_t>(use & 1), abort_flag, lim)) break;
+      tc_fence_after();
+      CmTile t;
+      t.nb = tc.nb;
+      t.od = tc.od;
+      t.split = tc.split;
+      t.w0 = tc.twi * p.tw;
+      t.h0 = tc.thi * p.rh;
+      t.tw = p.tw;
+      t.npix = p.rh * p.tw;
+      const int cw = tc.ct * 128 + q * 32;  // first channel of this warp's TMEM lanes
+      const bool warp_live = cw < E.Cout;
+      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                          static_cast<uint32_t>(buf * acc_cols);
+      for (int j0 = 0; j0 < Ncols; j0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tb + static_cast<uint32_t>(j0), r);
+        tmem_ld_wait();
+        if (warp_live) cm_block(E, t, stage, lane, cw, j0, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce_bar(buf));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, static_cast<uint32_t>(p.tmem_cols));
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicExch(&g_conv_cm_status, -7);
+}
+
+cudaError_t conv_cm_status_read_clear(int* status) {
+  int v = 0;
+  cudaError_t err = cudaMemcpyFromSymbol(&v, g_conv_cm_status, sizeof(int));
+  if (err != cudaSuccess) return err;
+  *status = v;
+  const int zero = 0;
+  return cudaMemcpyToSymbol(g_conv_cm_status, &zero, sizeof(int));
+}
+
+cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
+                           const ConvCMParams& p, int grid, size_t smem_bytes,
+                           cudaStream_t stream) {
+  static size_t configured = 0;
+  if (smem_bytes > configured) {
+    cudaError_t err = cudaFuncSetAttribute(conv_cm_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem_bytes));
+    if (err != cudaSuccess) return err;
+    configured = smem_bytes;
+  }
+  conv_cm_kernel<<<grid, 256, smem_bytes, stream>>>(tmAct, tmWgt, p);
+  return cudaGetLastError();
+}
+
+}  // namespace vvc

@@ -28,6 +28,7 @@
 
 #include "epilogue.cuh"
 #include "internal.h"
+#include "kernel_common.cuh"
 #include "ptx.cuh"
 
 namespace vvc {
@@ -40,29 +41,6 @@ constexpr int kWarpProducer = 0;
 constexpr int kWarpMMA = 1;
 constexpr int kWarpPatch = 2;
 constexpr int kWarpEpi0 = 4;
-
-__device__ __forceinline__ int reflect_coord(int i, int L) {
-  if (i < 0) i = -i;
-  if (i >= L) i = 2 * (L - 1) - i;
-  return i;
-}
-
-// Byte address swizzle of the TMA/UMMA 128B / 64B / 32B patterns, relative to a
-// base aligned to the pattern period.
-__device__ __forceinline__ uint32_t swizzle_off(uint32_t off, int swz) {
-  const uint32_t mask = (swz == 2) ? 7u : (swz == 4) ? 3u : 1u;
-  return off ^ (((off >> 7) & mask) << 4);
-}
-
-__device__ __forceinline__ bool wait_no_abort(uint32_t bar, uint32_t parity,
-                                              unsigned long long limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
-}
 
 struct StageCoord {
   int t, r, sblk, ch;
@@ -146,8 +124,7 @@ __global__ void __launch_bounds__(256, 1)
     if (lane == 0) {
       int slot = 0;
       uint32_t phase = 0;
-      int last_k[8];
-      for (int s = 0; s < 8; ++s) last_k[s] = -1;
+      int k_skip = -1;  // stage left unissued by the test aid
       for (int it = it_begin; it < it_end; ++it) {
         if (!mbar_wait(bars + 8u * (S + slot), phase ^ 1u, abort_flag, lim)) break;
         const StageCoord sc = decode_stage(p, it);
@@ -179,22 +156,39 @@ __global__ void __launch_bounds__(256, 1)
               tma_load_2d(dst, &tmB, full, tap * p.cp64 + sc.ch * p.kc, n0 + u * p.sub_n);
             }
           }
-          last_k[slot] = it - it_begin;
+        } else {
+          k_skip = it - it_begin;
         }
         if (++slot == S) {
           slot = 0;
           phase ^= 1u;
         }
       }
-      // Let every issued copy land before the CTA can exit.
-      for (int s = 0; s < S; ++s)
-        if (last_k[s] >= 0)
-          wait_no_abort(bars + 8u * s, static_cast<uint32_t>((last_k[s] / S) & 1), lim);
+      // Let every issued copy land before the CTA can exit: in each slot, wait
+      // for the phase of the last stage issued into it.
+      const int n_it = it_end - it_begin;
+      for (int s = 0; s < S; ++s) {
+        int k_last = n_it - 1 - ((n_it - 1 - s) % S + S) % S;
+        if (k_last == k_skip) k_last -= S;
+        if (k_last >= 0)
+          wait_no_abort(bars + 8u * s, static_cast<uint32_t>((k_last / S) & 1), lim);
+      }
     }
   } else if (warp == kWarpMMA) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(128, p.sub_n);
       const uint32_t sbo = 8u * static_cast<uint32_t>(p.row_bytes);
+      // Descriptors are built once: the high word (stride, version, swizzle) is
+      // fixed, and every operand view is the low word plus an offset in 16-byte
+      // units.  The swizzle follows absolute shared-memory address bits, so a
+      // view shifted by whole rows (the halo taps) keeps base offset 0.
+      const uint32_t desc_hi = static_cast<uint32_t>(sdesc(0u, 16u, sbo, p.swz, 0u) >> 32);
+      const uint32_t desc_lo0 = static_cast<uint32_t>(sdesc(0u, 16u, sbo, p.swz, 0u));
+      const uint32_t a_tile_step = static_cast<uint32_t>(p.a_tile_rows * p.row_bytes) >> 4;
+      const uint32_t a_tap_step = p.halo ? (static_cast<uint32_t>(p.row_bytes) >> 4) : 0u;
+      const uint32_t b_tap_step = static_cast<uint32_t>(p.BN * p.row_bytes) >> 4;
+      const uint32_t b_sub_step = static_cast<uint32_t>(p.sub_n * p.row_bytes) >> 4;
+      const int kk_n = p.kc / 16;
       int slot = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -205,29 +199,27 @@ __global__ void __launch_bounds__(256, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t a_stage = a_base + p.a_stage_bytes * slot;
-        const uint32_t b_stage = b_base + p.b_stage_bytes * slot;
-        const bool first_stage = (it == it_begin);
+        const uint32_t a_lo = desc_lo0 + ((a_base + p.a_stage_bytes * slot) >> 4);
+        const uint32_t b_lo = desc_lo0 + ((b_base + p.b_stage_bytes * slot) >> 4);
+        uint32_t acc = (it == it_begin) ? 0u : 1u;
         for (int tl = 0; tl < p.taps_per_stage; ++tl) {
-          for (int j = 0; j < p.R; ++j) {
-            const int a_row = j * p.a_tile_rows + (p.halo ? tl : 0);
-            for (int kk = 0; kk < p.kc / 16; ++kk) {
-              const uint32_t a_addr =
-                  a_stage + static_cast<uint32_t>(a_row * p.row_bytes + kk * 32);
-              // The swizzle follows absolute shared-memory address bits, so a view
-              // shifted by whole rows (the halo taps) keeps base offset 0.
-              const uint64_t adesc = sdesc(a_addr, 16u, sbo, p.swz, 0u);
+          const uint32_t a_tl = a_lo + tl * a_tap_step;
+          const uint32_t b_tl = b_lo + tl * b_tap_step;
+          for (int kk = 0; kk < kk_n; ++kk) {
+            uint32_t d = tmem_base;
+            uint32_t a_j = a_tl + 2u * kk;  // 32 bytes per K = 16 step
+            for (int j = 0; j < p.R; ++j) {
+              const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | a_j;
+              uint32_t b_u = b_tl + 2u * kk;
               for (int u = 0; u < p.n_sub; ++u) {
-                const uint32_t b_addr =
-                    b_stage +
-                    static_cast<uint32_t>((tl * p.BN + u * p.sub_n) * p.row_bytes + kk * 32);
-                const uint64_t bdesc = sdesc(b_addr, 16u, sbo, p.swz, 0u);
-                const uint32_t d = tmem_base + static_cast<uint32_t>(j * p.acc_stride +
-                                                                     u * p.sub_n);
-                const uint32_t acc = (first_stage && tl == 0 && kk == 0) ? 0u : 1u;
-                mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+                const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | b_u;
+                mma_bf16_ss(d + static_cast<uint32_t>(u * p.sub_n), adesc, bdesc, idesc, acc);
+                b_u += b_sub_step;
               }
+              a_j += a_tile_step;
+              d += static_cast<uint32_t>(p.acc_stride);
             }
+            acc = 1u;
           }
         }
         mma_commit(bars + 8u * (S + slot));  // frees the slot once these MMAs finish

@@ -1,0 +1,244 @@
+// Epilogue of the channel-major convolution kernel: the post-operation contract
+// of the cuDNN frontend doc "Fused Conv3D + Bias + Residual + RMSNorm + SiLU"
+// (section "Operation Contract", bias / residual / residual-bias part; every
+// B() is an explicit round-to-nearest-even fp32 -> bf16 conversion), applied to
+// a 32-channel x 32-pixel block of the accumulator.
+//
+// A warp loads its block from TMEM (thread = channel, registers = pixels),
+// stages it in shared memory, and then each thread handles units of 8 values
+// that are contiguous in the output: 8 channels of one pixel for NDHWC output
+// (16-byte loads and stores, coalesced across the warp) or 8 pixels of one
+// channel for NCDHW output.
+#pragma once
+
+#include <cstdint>
+
+#include "epilogue.cuh"
+#include "internal.h"
+
+namespace vvc {
+
+struct CmEpi {
+  unsigned flags;
+  int Cout, Do, Ho, Wo, Hy, Wy;
+  bool ndhwc, pad, split;
+  uint16_t* y;
+  const uint16_t* res;
+  uint16_t* val;
+  uint16_t* conv;
+  float* part;
+  const float* bias;
+  const float* rbias;
+  long long M_total;
+};
+
+struct CmTile {
+  int nb, od, split;
+  int w0, h0, tw, npix;
+};
+
+__device__ __forceinline__ void cm_pixel(const CmTile& t, int n, int& h, int& w) {
+  const int i = n / t.tw;
+  h = t.h0 + i;
+  w = t.w0 + (n - i * t.tw);
+}
+
+__device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
+  uint4 u;
+  u.x = v[0] | (uint32_t(v[1]) << 16);
+  u.y = v[2] | (uint32_t(v[3]) << 16);
+  u.z = v[4] | (uint32_t(v[5]) << 16);
+  u.w = v[6] | (uint32_t(v[7]) << 16);
+  return u;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// 8 channels [c0, c0 + cnt) of one pixel, NDHWC addressing.
+__device__ __forceinline__ void cm_unit_ndhwc(const CmEpi& E, const CmTile& t, int n, int c0,
+                                              int cnt, const float (&a)[8]) {
+  int h, w;
+  cm_pixel(t, n, h, w);
+  if (n >= t.npix || h >= E.Ho || w >= E.Wo || cnt <= 0) return;
+  const long long nd = (long long)t.nb * E.Do + t.od;
+  const long long pix = (nd * E.Ho + h) * E.Wo + w;
+  const bool vec = (cnt == 8) && ((E.Cout & 7) == 0);
+  if (E.split) {
+    float* dst = E.part + ((long long)t.split * E.M_total + pix) * E.Cout + c0;
+    if (vec) {
+      reinterpret_cast<float4*>(dst)[0] = make_float4(a[0], a[1], a[2], a[3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(a[4], a[5], a[6], a[7]);
+    } else {
+      for (int e = 0; e < cnt; ++e) dst[e] = a[e];
+    }
+    return;
+  }
+  uint16_t cb[8];
+  float v[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    cb[e] = bf16_bits(a[e]);
+    v[e] = bf16_val(cb[e]);
+  }
+  if (E.flags & EPI_BIAS) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (e < cnt) v[e] = round_bf16(__fadd_rn(v[e], __ldg(E.bias + c0 + e)));
+  }
+  const long long ou = pix * E.Cout + c0;
+  if (E.flags & EPI_RESIDUAL) {
+    float sk[8];
+    if (vec) {
+      unpack8(__ldg(reinterpret_cast<const uint4*>(E.res + ou)), sk);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sk[e] = (e < cnt) ? bf16_val(E.res[ou + e]) : 0.0f;
+    }
+    if (E.flags & EPI_RESIDUAL_BIAS) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (e < cnt) sk[e] = round_bf16(__fadd_rn(sk[e], __ldg(E.rbias + c0 + e)));
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = round_bf16(__fadd_rn(v[e], sk[e]));
+  }
+  uint16_t vb[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) vb[e] = bf16_bits(v[e]);
+  const long long yo = ((nd * E.Hy + h) * E.Wy + w) * E.Cout + c0;
+  if (vec) {
+    const uint4 pv = pack8(vb);
+    reinterpret_cast<uint4*>(E.y + yo)[0] = pv;
+    if (E.flags & EPI_SAVE_VALUE) reinterpret_cast<uint4*>(E.val + ou)[0] = pv;
+    if (E.flags & EPI_DEBUG_STORE_CONV) reinterpret_cast<uint4*>(E.conv + ou)[0] = pack8(cb);
+    if (E.pad) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      const long long sw_ = E.Cout, sh_ = (long long)E.Wy * E.Cout;
+      if (w == E.Wo - 1) reinterpret_cast<uint4*>(E.y + yo + sw_)[0] = z;
+      if (h == E.Ho - 1) reinterpret_cast<uint4*>(E.y + yo + sh_)[0] = z;
+      if (w == E.Wo - 1 && h == E.Ho - 1) reinterpret_cast<uint4*>(E.y + yo + sh_ + sw_)[0] = z;
+    }
+  } else {
+    for (int e = 0; e < cnt; ++e) {
+      E.y[yo + e] = vb[e];
+      if (E.flags & EPI_SAVE_VALUE) E.val[ou + e] = vb[e];
+      if (E.flags & EPI_DEBUG_STORE_CONV) E.conv[ou + e] = cb[e];
+      if (E.pad) {
+        const long long sw_ = E.Cout, sh_ = (long long)E.Wy * E.Cout;
+        if (w == E.Wo - 1) E.y[yo + e + sw_] = 0;
+        if (h == E.Ho - 1) E.y[yo + e + sh_] = 0;
+        if (w == E.Wo - 1 && h == E.Ho - 1) E.y[yo + e + sh_ + sw_] = 0;
+      }
+    }
+  }
+}
+
+// 8 consecutive tile pixels [n0, n0 + 8) of one channel c, NCDHW addressing.
+__device__ __forceinline__ void cm_unit_ncdhw(const CmEpi& E, const CmTile& t, int n0, int c,
+                                              const float (&a)[8]) {
+  if (c >= E.Cout) return;
+  const float bias_c = (E.flags & EPI_BIAS) ? __ldg(E.bias + c) : 0.0f;
+  const float rb_c = (E.flags & EPI_RESIDUAL_BIAS) ? __ldg(E.rbias + c) : 0.0f;
+  const long long ncd = ((long long)t.nb * E.Cout + c) * E.Do + t.od;
+  const long long nd = (long long)t.nb * E.Do + t.od;
+  int h0, w0;
+  cm_pixel(t, n0, h0, w0);
+  // fast path: 8 pixels of one output row, all valid, 16-byte aligned
+  const bool vec = (n0 + 8 <= t.npix) && (w0 + 8 <= E.Wo) && (h0 < E.Ho) &&
+                   ((t.tw - (n0 % t.tw)) >= 8) && ((w0 & 7) == 0) && ((E.Wo & 7) == 0) &&
+                   !E.split && !(E.flags & EPI_DEBUG_STORE_CONV) && !E.pad;
+  if (vec) {
+    const long long ou = ncd * ((long long)E.Ho * E.Wo) + (long long)h0 * E.Wo + w0;
+    float v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      v[e] = round_bf16(a[e]);
+      if (E.flags & EPI_BIAS) v[e] = round_bf16(__fadd_rn(v[e], bias_c));
+    }
+    if (E.flags & EPI_RESIDUAL) {
+      float sk[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(E.res + ou)), sk);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (E.flags & EPI_RESIDUAL_BIAS) sk[e] = round_bf16(__fadd_rn(sk[e], rb_c));
+        v[e] = round_bf16(__fadd_rn(v[e], sk[e]));
+      }
+    }
+    uint16_t vb[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vb[e] = bf16_bits(v[e]);
+    const uint4 pv = pack8(vb);
+    reinterpret_cast<uint4*>(E.y + ou)[0] = pv;  // Hy == Ho, Wy == Wo without the pad
+    if (E.flags & EPI_SAVE_VALUE) reinterpret_cast<uint4*>(E.val + ou)[0] = pv;
+    return;
+  }
+  for (int e = 0; e < 8; ++e) {
+    int h, w;
+    cm_pixel(t, n0 + e, h, w);
+    if (n0 + e >= t.npix || h >= E.Ho || w >= E.Wo) continue;
+    const long long pix = (nd * E.Ho + h) * E.Wo + w;
+    if (E.split) {
+      E.part[((long long)t.split * E.M_total + pix) * E.Cout + c] = a[e];
+      continue;
+    }
+    const uint16_t cb = bf16_bits(a[e]);
+    float v = bf16_val(cb);
+    if (E.flags & EPI_BIAS) v = round_bf16(__fadd_rn(v, bias_c));
+    const long long ou = ncd * ((long long)E.Ho * E.Wo) + (long long)h * E.Wo + w;
+    if (E.flags & EPI_RESIDUAL) {
+      float sk = bf16_val(E.res[ou]);
+      if (E.flags & EPI_RESIDUAL_BIAS) sk = round_bf16(__fadd_rn(sk, rb_c));
+      v = round_bf16(__fadd_rn(v, sk));
+    }
+    const uint16_t vb = bf16_bits(v);
+    if (E.flags & EPI_DEBUG_STORE_CONV) E.conv[pix * E.Cout + c] = cb;
+    if (E.flags & EPI_SAVE_VALUE) E.val[ou] = vb;
+    const long long yo = ncd * ((long long)E.Hy * E.Wy) + (long long)h * E.Wy + w;
+    E.y[yo] = vb;
+    if (E.pad) {
+      if (w == E.Wo - 1) E.y[yo + 1] = 0;
+      if (h == E.Ho - 1) E.y[yo + E.Wy] = 0;
+      if (w == E.Wo - 1 && h == E.Ho - 1) E.y[yo + E.Wy + 1] = 0;
+    }
+  }
+}
+
+// One 32-channel x 32-pixel block: r[j] = accumulator of this lane's channel for
+// tile pixel j0 + j.  `stage` is this warp's [32][33] fp32 shared buffer.
+__device__ __forceinline__ void cm_block(const CmEpi& E, const CmTile& t, float (*stage)[33],
+                                         int lane, int cw, int j0, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) stage[j][lane] = __uint_as_float(r[j]);
+  __syncwarp();
+  if (E.ndhwc || E.split) {
+    // unit = (pixel, 8-channel group): lanes 4k..4k+3 share a pixel
+    const int g = lane & 3;
+    const int c0 = cw + 8 * g;
+    const int cnt = min(8, E.Cout - c0);
+    for (int k = 0; k < 4; ++k) {
+      const int pl = 8 * k + (lane >> 2);
+      float a[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a[e] = stage[pl][8 * g + e];
+      cm_unit_ndhwc(E, t, j0 + pl, c0, cnt, a);
+    }
+  } else {
+    // unit = (channel = lane, 8 consecutive pixels)
+    for (int k = 0; k < 4; ++k) {
+      float a[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a[e] = stage[8 * k + e][lane];
+      cm_unit_ncdhw(E, t, j0 + 8 * k, cw + lane, a);
+    }
+  }
+  __syncwarp();
+}
+
+}  // namespace vvc

@@ -66,4 +66,36 @@ struct ConvTCParams {
   long long M_total;
 };
 
+// Channel-major implicit GEMM (persistent): D[channel][pixel] in TMEM, MMA
+// M = 128 output channels, N = up to 256 output pixels of one tile.
+struct ConvCMParams {
+  EpiParams epi;
+  int C;                   // channels of the NDHWC tensor the activation map reads
+  int D, H, W;
+  int KT, KR, KS;
+  int st, sh, sw;
+  int pt, ph, pw;
+  int reflect_h, reflect_w;
+  int tw, rh;              // pixel tile: rh output rows x tw output pixels
+  int halo;                // 1: one run of tw + KS - 1 input pixels serves all KS taps
+  int nbox;                // activation boxes per stage (halo: 1..2, direct: rh)
+  int box_w;               // loaded elements per activation box
+  int box_pitch;           // shared-memory rows between activation boxes
+  int N;                   // MMA N = round_up(rh * tw, 16)
+  int kc, n_chunks, row_bytes;
+  int taps_per_stage;
+  int stages;
+  uint32_t act_bytes, stage_bytes, bar_off, tx_bytes;
+  uint32_t epi_off;        // 4 x [32][33] fp32 epilogue staging blocks
+  int stages_total, k_splits, stages_per_split;
+  int tiles_w, tiles_h, tiles_c;  // pixel tiles along W / H, 128-channel tiles
+  int num_tiles;
+  int acc_cols, nbuf, tmem_cols;
+  int cp64;
+  int inject;
+  unsigned long long timeout_ns;
+  float* partial;          // [k_splits][M][Cout] fp32 when k_splits > 1
+  long long M_total;
+};
+
 }  // namespace vvc
