@@ -88,6 +88,8 @@ SHAPES = [
     mk("wide_halo_two_boxes", 1, 64, 2, 4, 250, 128, index=18),
     mk("cout200_two_channel_tiles", 1, 64, 2, 5, 90, 200, pads=CR, index=19),
     mk("wide_640_tiles", 1, 64, 3, 3, 642, 96, pads=VALID, index=20),
+    mk("flat_h_zero_pad", 1, 64, 3, 7, 50, 64, pads=((2, 0, Z), (1, 1, Z), (0, 0, Z)), index=21),
+    mk("flat_small_w_384", 1, 384, 3, 9, 22, 384, pads=VALID, index=22),
     mk("t1_2d_tiles_h", 2, 32, 1, 9, 40, 48, kernel=(1, 3, 3), pads=P2D, index=2),
     mk("stride2_causal_reflect", 1, 32, 5, 11, 71, 32, stride=(2, 2, 2), pads=CR, index=3),
     mk("reflect_causal_wide", 1, 16, 4, 7, 133, 32, pads=CR, index=4),

@@ -197,9 +197,20 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.row_bytes = kc * 2;
   k.n_chunks = static_cast<int>(cdiv(p->Cin, kc));
   // pixel tile
-  bool halo;
+  bool halo, flat = false;
   int tw, rh;
-  if (t.tile_w > 0) {
+  const bool flat_ok = sw == 1 && p->stride[1] == 1 && p->pad[2].before == 0 &&
+                       p->pad[2].after == 0 &&
+                       (p->pad[1].mode == CONV3D_PAD_ZERO ||
+                        (p->pad[1].before == 0 && p->pad[1].after == 0));
+  const long long q_total = (long long)(Ho - 1) * p->W + Wo;  // flattened output range
+  if (t.tile_w <= 0 && t.halo != 2 && flat_ok && q_total < 0x7fffff00LL) {
+    // flattened H*W: a tile is 256 consecutive positions with row pitch W
+    flat = true;
+    halo = true;
+    rh = 1;
+    tw = static_cast<int>(std::min<long long>(256, round_up(q_total, 16)));
+  } else if (t.tile_w > 0) {
     tw = t.tile_w;
     rh = t.tile_h > 0 ? t.tile_h : 1;
     halo = (t.halo == 1) || (t.halo == 0 && sw == 1 && rh == 1 && p->KS > 1);
@@ -221,6 +232,7 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.tw = tw;
   k.rh = rh;
   k.halo = halo ? 1 : 0;
+  k.flat = flat ? 1 : 0;
   k.N = static_cast<int>(round_up((long long)tw * rh, 16));
   if (halo) {
     const int run = tw + p->KS - 1;
@@ -247,8 +259,8 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.stages = stages;
   k.bar_off = k.stage_bytes * stages;
   k.tx_bytes = static_cast<uint32_t>((long long)k.nbox * k.box_w * k.row_bytes) + wgt_bytes;
-  k.tiles_w = static_cast<int>(cdiv(Wo, tw));
-  k.tiles_h = static_cast<int>(cdiv(Ho, rh));
+  k.tiles_w = static_cast<int>(flat ? cdiv(q_total, tw) : cdiv(Wo, tw));
+  k.tiles_h = static_cast<int>(flat ? 1 : cdiv(Ho, rh));
   k.tiles_c = static_cast<int>(cdiv(p->Cout, 128));
   const long long tiles = (long long)k.tiles_w * k.tiles_h * Do * p->N * k.tiles_c;
   const int sms = num_sms();
@@ -568,8 +580,10 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
   EncodeTiledFn enc = encode_fn();
   if (!enc) return CONV3D_ERR_CUDA;
   int kc, act_box, es_w, wgt_rows, cp64;
+  bool flat = false;
   if (pl.cm) {
     const ConvCMParams& k = pl.cp;
+    flat = k.flat != 0;
     kc = k.kc;
     act_box = k.halo ? k.box_w : k.box_w * k.sw;
     es_w = k.halo ? 1 : k.sw;
@@ -591,8 +605,18 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
   cuuint64_t gstrA[4] = {C * 2, C * 2 * p->W, C * 2 * p->W * p->H, C * 2 * p->W * p->H * p->D};
   cuuint32_t boxA[5] = {(cuuint32_t)kc, (cuuint32_t)act_box, 1, 1, 1};
   cuuint32_t esA[5] = {1, (cuuint32_t)es_w, 1, 1, 1};
-  CUresult r = enc(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(xin), gdimA, gstrA,
-                   boxA, esA, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kc),
+  cuuint32_t rankA = 5;
+  if (flat) {
+    // H and W merged into one dimension of H*W positions (dims C, H*W, D, N)
+    gdimA[1] = (cuuint64_t)p->H * p->W;
+    gdimA[2] = (cuuint64_t)p->D;
+    gdimA[3] = (cuuint64_t)p->N;
+    gstrA[1] = gstrA[2];
+    gstrA[2] = gstrA[3];
+    rankA = 4;
+  }
+  CUresult r = enc(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rankA, const_cast<void*>(xin), gdimA,
+                   gstrA, boxA, esA, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kc),
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
   // packed weights [Cout][taps * cp64]: one box = kc channels x wgt_rows output channels

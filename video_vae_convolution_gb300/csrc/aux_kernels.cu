@@ -43,25 +43,40 @@ cudaError_t launch_pack_weight(const void* w, void* out, int Co, int Ci, int tap
 
 // ---- input staging --------------------------------------------------------------------
 // NCDHW [N][C][S] (S = D*H*W) -> NDHWC [N][S][Cp], channels Cin..Cp-1 zero.
-// 32 x 32 tiles through shared memory: reads coalesced along S, writes along C.
-__global__ void ncdhw_to_ndhwc_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ out,
-                                      int C, int Cp, long long S) {
-  __shared__ uint16_t tile[32][33];
+// A block moves 32 channels x 256 positions through shared memory: each channel
+// row is read as 512 contiguous bytes, and each position's 32 channels are
+// written as four 16-byte stores by four neighbouring lanes.
+__global__ void __launch_bounds__(256) ncdhw_to_ndhwc_kernel(const uint16_t* __restrict__ x,
+                                                             uint16_t* __restrict__ out, int C,
+                                                             int Cp, long long S) {
+  __shared__ uint16_t tile[32][256 + 2];  // odd word pitch: conflict-free column reads
   const int n = blockIdx.z;
-  const long long s0 = (long long)blockIdx.x * 32;
+  const long long s0 = (long long)blockIdx.x * 256;
   const int c0 = blockIdx.y * 32;
   const uint16_t* xn = x + (long long)n * C * S;
   uint16_t* on = out + (long long)n * Cp * S;
-  for (int k = threadIdx.y; k < 32; k += blockDim.y) {
+  const int tid = threadIdx.x;
+  const long long s = s0 + tid;
+  for (int k = 0; k < 32; ++k) {
     const int c = c0 + k;
-    const long long s = s0 + threadIdx.x;
-    tile[k][threadIdx.x] = (c < C && s < S) ? xn[(long long)c * S + s] : uint16_t(0);
+    tile[k][tid] = (c < C && s < S) ? xn[(long long)c * S + s] : uint16_t(0);
   }
   __syncthreads();
-  for (int k = threadIdx.y; k < 32; k += blockDim.y) {
-    const long long s = s0 + k;
-    const int c = c0 + threadIdx.x;
-    if (s < S && c < Cp) on[s * Cp + c] = tile[threadIdx.x][k];
+  const int nch = min(32, Cp - c0);     // channels of this block present in the output
+  const int groups = (nch + 7) / 8;     // 16-byte groups per position (Cp % 8 == 0)
+  for (int u = tid; u < 256 * 4; u += 256) {
+    const int pl = u >> 2, g = u & 3;
+    const long long sp = s0 + pl;
+    if (g >= groups || sp >= S) continue;
+    uint16_t v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = tile[8 * g + e][pl];
+    uint4 q;
+    q.x = v[0] | (uint32_t(v[1]) << 16);
+    q.y = v[2] | (uint32_t(v[3]) << 16);
+    q.z = v[4] | (uint32_t(v[5]) << 16);
+    q.w = v[6] | (uint32_t(v[7]) << 16);
+    *reinterpret_cast<uint4*>(on + sp * Cp + c0 + 8 * g) = q;
   }
 }
 
@@ -80,11 +95,10 @@ __global__ void pad_channels_kernel(const uint16_t* __restrict__ x, uint16_t* __
 cudaError_t launch_stage_input(const void* x, int layout, int N, int C, int Cp, long long S,
                                void* out, cudaStream_t s) {
   if (layout == LAYOUT_NCDHW) {
-    dim3 grid(static_cast<unsigned>((S + 31) / 32), static_cast<unsigned>((Cp + 31) / 32),
+    dim3 grid(static_cast<unsigned>((S + 255) / 256), static_cast<unsigned>((Cp + 31) / 32),
               static_cast<unsigned>(N));
-    dim3 block(32, 8);
-    ncdhw_to_ndhwc_kernel<<<grid, block, 0, s>>>(static_cast<const uint16_t*>(x),
-                                                 static_cast<uint16_t*>(out), C, Cp, S);
+    ncdhw_to_ndhwc_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x),
+                                               static_cast<uint16_t*>(out), C, Cp, S);
   } else {
     const long long total = (long long)N * S * Cp;
     long long blocks = (total + 255) / 256;
@@ -136,9 +150,61 @@ __global__ void splitk_epilogue_kernel(const float* __restrict__ partial, int sp
   epilogue_pixel(e, px, 0, e.Cout, load);
 }
 
+// Same reduction when the epilogue is per element (no L2 norm): one thread per
+// (pixel, 16-channel chunk), so small layers still spread over every SM; adjacent
+// threads read and write adjacent 64-byte chunks of a pixel row.
+__global__ void splitk_epilogue_chunk_kernel(const float* __restrict__ partial, int splits,
+                                             long long M, EpiParams e) {
+  const int chunks = (e.Cout + 15) / 16;
+  const long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  Pixel px;
+  px.valid = u < M * chunks;
+  const long long uu = px.valid ? u : 0;
+  const long long pp = uu / chunks;
+  const int c0 = static_cast<int>(uu - pp * chunks) * 16;
+  px.w = static_cast<int>(pp % e.Wo);
+  long long rest = pp / e.Wo;
+  px.h = static_cast<int>(rest % e.Ho);
+  rest /= e.Ho;
+  px.d = static_cast<int>(rest % e.Do);
+  px.n = static_cast<int>(rest / e.Do);
+  const int cnt = min(16, e.Cout - c0);
+  const bool vec = (e.Cout % 4) == 0 && cnt == 16;
+  auto load = [&](int c_rel, float(&v)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+    if (!px.valid) return;
+    for (int s = 0; s < splits; ++s) {
+      const float* src = partial + ((long long)s * M + pp) * e.Cout + c0 + c_rel;
+      if (vec) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 q = __ldg(reinterpret_cast<const float4*>(src) + k);
+          v[4 * k] += q.x;
+          v[4 * k + 1] += q.y;
+          v[4 * k + 2] += q.z;
+          v[4 * k + 3] += q.w;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (i < cnt) v[i] += __ldg(src + i);
+      }
+    }
+  };
+  epilogue_pixel(e, px, c0, c0 + cnt, load);
+}
+
 cudaError_t launch_splitk_epilogue(const float* partial, int splits, long long M,
                                    const EpiParams& e, cudaStream_t s) {
   const int threads = 128;
+  if (!(e.flags & EPI_L2NORM_SILU)) {
+    const long long units = M * ((e.Cout + 15) / 16);
+    const long long blocks = (units + threads - 1) / threads;
+    splitk_epilogue_chunk_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(partial,
+                                                                                   splits, M, e);
+    return cudaGetLastError();
+  }
   const long long blocks = (M + threads - 1) / threads;
   splitk_epilogue_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(partial, splits, M, e);
   return cudaGetLastError();

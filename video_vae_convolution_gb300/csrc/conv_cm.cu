@@ -162,7 +162,13 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t act = sbase + p.stage_bytes * slot;
             const uint32_t wgt = act + p.act_bytes;
             const int d_in = tc.od * p.st + sc.t - p.pt;
-            if (p.halo) {
+            if (p.flat) {
+              // flattened (H*W) positions: output q reads input q + (r - ph) * W + s
+              const int q_start = w0 + (sc.r - p.ph) * p.W;
+              for (int b = 0; b < p.nbox; ++b)
+                tma_load_4d(act + static_cast<uint32_t>(b * p.box_pitch * p.row_bytes), &tmAct,
+                            full, sc.ch * p.kc, q_start + b * p.box_w, d_in, tc.nb);
+            } else if (p.halo) {
               const int ho = h0;
               int h_in = ho * p.sh + sc.r - p.ph;
               if (p.reflect_h && ho < p.epi.Ho) h_in = reflect_coord(h_in, p.H);
@@ -361,6 +367,8 @@ __global__ void __launch_bounds__(256, 1)
       t.h0 = tc.thi * p.rh;
       t.tw = p.tw;
       t.npix = p.rh * p.tw;
+      t.flat = p.flat;
+      t.pitch = p.W;
       const int cw = tc.ct * 128 + q * 32;  // first channel of this warp's TMEM lanes
       const bool warp_live = cw < E.Cout;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +

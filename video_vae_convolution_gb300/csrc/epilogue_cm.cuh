@@ -35,12 +35,26 @@ struct CmEpi {
 struct CmTile {
   int nb, od, split;
   int w0, h0, tw, npix;
+  int flat, pitch;  // flat: tile pixel n is flattened position w0 + n with row pitch `pitch`
 };
 
+// Output coordinates of tile pixel n (possibly outside [0, Ho) x [0, Wo)).
 __device__ __forceinline__ void cm_pixel(const CmTile& t, int n, int& h, int& w) {
-  const int i = n / t.tw;
-  h = t.h0 + i;
-  w = t.w0 + (n - i * t.tw);
+  if (t.flat) {
+    const int q = t.w0 + n;
+    h = q / t.pitch;
+    w = q - h * t.pitch;
+  } else {
+    const int i = n / t.tw;
+    h = t.h0 + i;
+    w = t.w0 + (n - i * t.tw);
+  }
+}
+
+// Whether tile pixels [n, n + len) lie on one output row at consecutive w.
+__device__ __forceinline__ bool cm_same_row(const CmTile& t, int n, int len) {
+  if (t.flat) return ((t.w0 + n) % t.pitch) + len <= t.pitch;
+  return (n % t.tw) + len <= t.tw;
 }
 
 __device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
@@ -152,7 +166,7 @@ __device__ __forceinline__ void cm_unit_ncdhw(const CmEpi& E, const CmTile& t, i
   cm_pixel(t, n0, h0, w0);
   // fast path: 8 pixels of one output row, all valid, 16-byte aligned
   const bool vec = (n0 + 8 <= t.npix) && (w0 + 8 <= E.Wo) && (h0 < E.Ho) &&
-                   ((t.tw - (n0 % t.tw)) >= 8) && ((w0 & 7) == 0) && ((E.Wo & 7) == 0) &&
+                   cm_same_row(t, n0, 8) && ((w0 & 7) == 0) && ((E.Wo & 7) == 0) &&
                    !E.split && !(E.flags & EPI_DEBUG_STORE_CONV) && !E.pad;
   if (vec) {
     const long long ou = ncd * ((long long)E.Ho * E.Wo) + (long long)h0 * E.Wo + w0;
@@ -230,12 +244,53 @@ __device__ __forceinline__ void cm_block(const CmEpi& E, const CmTile& t, float 
       cm_unit_ndhwc(E, t, j0 + pl, c0, cnt, a);
     }
   } else {
-    // unit = (channel = lane, 8 consecutive pixels)
-    for (int k = 0; k < 4; ++k) {
-      float a[8];
+    int h0, w0;
+    cm_pixel(t, j0, h0, w0);
+    const bool row_aligned = cm_same_row(t, j0, 32) && (w0 & 7) == 0 && (E.Wo & 7) == 0;
+    if (row_aligned) {
+      // unit = (channel = lane, 8 consecutive pixels): 16-byte stores
+      for (int k = 0; k < 4; ++k) {
+        float a[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) a[e] = stage[8 * k + e][lane];
-      cm_unit_ncdhw(E, t, j0 + 8 * k, cw + lane, a);
+        for (int e = 0; e < 8; ++e) a[e] = stage[8 * k + e][lane];
+        cm_unit_ncdhw(E, t, j0 + 8 * k, cw + lane, a);
+      }
+    } else {
+      // lane = pixel: for each channel, the warp writes 32 consecutive pixels
+      const int n = j0 + lane;
+      int h, w;
+      cm_pixel(t, n, h, w);
+      const bool pv = n < t.npix && h < E.Ho && w < E.Wo;
+      const long long plane_o = (long long)E.Ho * E.Wo, plane_y = (long long)E.Hy * E.Wy;
+      const long long pix = (((long long)t.nb * E.Do + t.od) * E.Ho + h) * E.Wo + w;
+      const int cend = min(32, E.Cout - cw);
+      for (int cc = 0; cc < cend; ++cc) {
+        const int c = cw + cc;
+        const float a = stage[lane][cc];
+        if (!pv) continue;
+        const float bias_c = (E.flags & EPI_BIAS) ? __ldg(E.bias + c) : 0.0f;
+        const uint16_t cb = bf16_bits(a);
+        float v = bf16_val(cb);
+        if (E.flags & EPI_BIAS) v = round_bf16(__fadd_rn(v, bias_c));
+        const long long ncd = ((long long)t.nb * E.Cout + c) * E.Do + t.od;
+        const long long ou = ncd * plane_o + (long long)h * E.Wo + w;
+        if (E.flags & EPI_RESIDUAL) {
+          float sk = bf16_val(E.res[ou]);
+          if (E.flags & EPI_RESIDUAL_BIAS)
+            sk = round_bf16(__fadd_rn(sk, __ldg(E.rbias + c)));
+          v = round_bf16(__fadd_rn(v, sk));
+        }
+        const uint16_t vb = bf16_bits(v);
+        if (E.flags & EPI_DEBUG_STORE_CONV) E.conv[pix * E.Cout + c] = cb;
+        if (E.flags & EPI_SAVE_VALUE) E.val[ou] = vb;
+        const long long yo = ncd * plane_y + (long long)h * E.Wy + w;
+        E.y[yo] = vb;
+        if (E.pad) {
+          if (w == E.Wo - 1) E.y[yo + 1] = 0;
+          if (h == E.Ho - 1) E.y[yo + E.Wy] = 0;
+          if (w == E.Wo - 1 && h == E.Ho - 1) E.y[yo + E.Wy + 1] = 0;
+        }
+      }
     }
   }
   __syncwarp();

@@ -78,6 +78,9 @@ struct ConvCMParams {
   int reflect_h, reflect_w;
   int tw, rh;              // pixel tile: rh output rows x tw output pixels
   int halo;                // 1: one run of tw + KS - 1 input pixels serves all KS taps
+  int flat;                // 1 (with halo): H and W merged; a tile is tw consecutive
+                           // positions of the flattened plane, row pitch W (needs
+                           // stride 1, no W padding, zero H padding)
   int nbox;                // activation boxes per stage (halo: 1..2, direct: rh)
   int box_w;               // loaded elements per activation box
   int box_pitch;           // shared-memory rows between activation boxes
