@@ -251,7 +251,7 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.act_bytes = static_cast<uint32_t>(round_up(round_up(act_rows, 8) * k.row_bytes, 1024));
   const uint32_t wgt_bytes = static_cast<uint32_t>(k.taps_per_stage * 128 * k.row_bytes);
   k.stage_bytes = k.act_bytes + wgt_bytes;
-  constexpr size_t kEpiStage = 4 * 32 * 33 * 4;  // per-warp transpose blocks
+  constexpr size_t kEpiStage = 8 * 32 * 33 * 4;  // per-warp transpose blocks
   int stages = static_cast<int>(
       std::min<size_t>(8, (kMaxSmem - 1024 - 256 - kEpiStage) / k.stage_bytes));
   if (t.stages > 0) stages = std::min(stages, t.stages);

@@ -19,9 +19,10 @@
 // The accumulator is double buffered in TMEM so the epilogue of one tile runs
 // under the MMAs of the next.
 //
-// Warp roles (256 threads): 0 TMA producer, 1 MMA issuer + TMEM owner,
-// 2 reflect-W patcher, 4..7 epilogue (thread = output channel, loops over the
-// tile's pixels; stores are coalesced across channels for NDHWC output).
+// Warp roles (384 threads): 0 TMA producer, 1 MMA issuer + TMEM owner,
+// 2 reflect-W patcher, 4..11 epilogue in two warpgroups that take alternate
+// 32-pixel column blocks (a warp reads the TMEM lane quarter warp % 4: thread =
+// output channel; stores are coalesced across channels for NDHWC output).
 // Waits are bounded; a time-out records CONV3D_ERR_DEVICE_TIMEOUT.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -88,7 +89,7 @@ __device__ __forceinline__ void stage_range(const ConvCMParams& p, int split, in
 
 }  // namespace
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     conv_cm_kernel(const __grid_constant__ CUtensorMap tmAct,
                    const __grid_constant__ CUtensorMap tmWgt,
                    const __grid_constant__ ConvCMParams p) {
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 4);  // one arrive per epilogue warp
+      mbar_init(acce_bar(b), 8);  // one arrive per epilogue warp
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -223,7 +224,6 @@ __global__ void __launch_bounds__(256, 1)
       const uint32_t desc_lo0 = static_cast<uint32_t>(sdesc(0u, 16u, sbo, swz, 0u));
       const uint32_t w_tap_step = static_cast<uint32_t>(128 * p.row_bytes) >> 4;
       const uint32_t a_tap_step = p.halo ? (static_cast<uint32_t>(p.row_bytes) >> 4) : 0u;
-      const int kk_n = p.kc / 16;
       int slot = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -248,6 +248,9 @@ __global__ void __launch_bounds__(256, 1)
             break;
           }
           tc_fence_after();
+          // K steps of 16 channels that hold real channels: the rest of a
+          // chunk beyond C is zero-filled by TMA and contributes nothing.
+          const int kk_n = (min(p.kc, p.C - (it % p.n_chunks) * p.kc) + 15) / 16;
           const uint32_t act = sbase + p.stage_bytes * slot;
           const uint32_t b_lo = desc_lo0 + (act >> 4);
           const uint32_t a_lo = desc_lo0 + ((act + p.act_bytes) >> 4);
@@ -329,7 +332,8 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
   } else if (warp >= kWarpEpi0) {
-    const int q = warp & 3;
+    const int q = warp & 3;              // TMEM lane quarter
+    const int grp = (warp - kWarpEpi0) >> 2;  // epilogue warpgroup: alternate 32-column chunks
     // Everything the epilogue reads per element is copied into registers first.
     CmEpi E;
     E.flags = p.epi.flags;
@@ -350,7 +354,8 @@ __global__ void __launch_bounds__(256, 1)
     E.bias = p.epi.bias;
     E.rbias = p.epi.rbias;
     E.M_total = p.M_total;
-    float(*stage)[33] = reinterpret_cast<float(*)[33]>(smem + p.epi_off + q * (32 * 33 * 4));
+    float(*stage)[33] =
+        reinterpret_cast<float(*)[33]>(smem + p.epi_off + (warp - kWarpEpi0) * (32 * 33 * 4));
     const int nbuf = p.nbuf, acc_cols = p.acc_cols, Ncols = p.N;
     int local = 0;
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
@@ -373,7 +378,7 @@ __global__ void __launch_bounds__(256, 1)
       const bool warp_live = cw < E.Cout;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                           static_cast<uint32_t>(buf * acc_cols);
-      for (int j0 = 0; j0 < Ncols; j0 += 32) {
+      for (int j0 = 32 * grp; j0 < Ncols; j0 += 64) {
         uint32_t r[32];
         tmem_ld32(tb + static_cast<uint32_t>(j0), r);
         tmem_ld_wait();
@@ -415,7 +420,7 @@ cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
     if (err != cudaSuccess) return err;
     configured = smem_bytes;
   }
-  conv_cm_kernel<<<grid, 256, smem_bytes, stream>>>(tmAct, tmWgt, p);
+  conv_cm_kernel<<<grid, 384, smem_bytes, stream>>>(tmAct, tmWgt, p);
   return cudaGetLastError();
 }
 

@@ -188,7 +188,6 @@ __global__ void __launch_bounds__(256, 1)
       const uint32_t a_tap_step = p.halo ? (static_cast<uint32_t>(p.row_bytes) >> 4) : 0u;
       const uint32_t b_tap_step = static_cast<uint32_t>(p.BN * p.row_bytes) >> 4;
       const uint32_t b_sub_step = static_cast<uint32_t>(p.sub_n * p.row_bytes) >> 4;
-      const int kk_n = p.kc / 16;
       int slot = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -199,6 +198,9 @@ __global__ void __launch_bounds__(256, 1)
           break;
         }
         tc_fence_after();
+        // K steps of 16 channels that hold real channels: the rest of a chunk
+        // beyond C is zero-filled by TMA and contributes nothing.
+        const int kk_n = (min(p.kc, p.C - (it % p.n_chunks) * p.kc) + 15) / 16;
         const uint32_t a_lo = desc_lo0 + ((a_base + p.a_stage_bytes * slot) >> 4);
         const uint32_t b_lo = desc_lo0 + ((b_base + p.b_stage_bytes * slot) >> 4);
         uint32_t acc = (it == it_begin) ? 0u : 1u;

@@ -264,31 +264,51 @@ __device__ __forceinline__ void cm_block(const CmEpi& E, const CmTile& t, float 
       const long long plane_o = (long long)E.Ho * E.Wo, plane_y = (long long)E.Hy * E.Wy;
       const long long pix = (((long long)t.nb * E.Do + t.od) * E.Ho + h) * E.Wo + w;
       const int cend = min(32, E.Cout - cw);
-      for (int cc = 0; cc < cend; ++cc) {
-        const int c = cw + cc;
-        const float a = stage[lane][cc];
-        if (!pv) continue;
-        const float bias_c = (E.flags & EPI_BIAS) ? __ldg(E.bias + c) : 0.0f;
-        const uint16_t cb = bf16_bits(a);
-        float v = bf16_val(cb);
-        if (E.flags & EPI_BIAS) v = round_bf16(__fadd_rn(v, bias_c));
-        const long long ncd = ((long long)t.nb * E.Cout + c) * E.Do + t.od;
-        const long long ou = ncd * plane_o + (long long)h * E.Wo + w;
-        if (E.flags & EPI_RESIDUAL) {
-          float sk = bf16_val(E.res[ou]);
-          if (E.flags & EPI_RESIDUAL_BIAS)
-            sk = round_bf16(__fadd_rn(sk, __ldg(E.rbias + c)));
-          v = round_bf16(__fadd_rn(v, sk));
+      // 8 channels per step: eight independent chains per lane keep the single
+      // epilogue warp of each scheduler busy.
+      const long long ou0 = ((long long)t.nb * E.Cout + cw) * E.Do * plane_o +
+                            (long long)t.od * plane_o + (long long)h * E.Wo + w;
+      const long long yo0 = ((long long)t.nb * E.Cout + cw) * E.Do * plane_y +
+                            (long long)t.od * plane_y + (long long)h * E.Wy + w;
+      const long long cstep_o = (long long)E.Do * plane_o, cstep_y = (long long)E.Do * plane_y;
+      for (int cc0 = 0; cc0 < cend; cc0 += 8) {
+        float v[8];
+        uint16_t cb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          cb[e] = bf16_bits(stage[lane][cc0 + e]);
+          v[e] = bf16_val(cb[e]);
         }
-        const uint16_t vb = bf16_bits(v);
-        if (E.flags & EPI_DEBUG_STORE_CONV) E.conv[pix * E.Cout + c] = cb;
-        if (E.flags & EPI_SAVE_VALUE) E.val[ou] = vb;
-        const long long yo = ncd * plane_y + (long long)h * E.Wy + w;
-        E.y[yo] = vb;
-        if (E.pad) {
-          if (w == E.Wo - 1) E.y[yo + 1] = 0;
-          if (h == E.Ho - 1) E.y[yo + E.Wy] = 0;
-          if (w == E.Wo - 1 && h == E.Ho - 1) E.y[yo + E.Wy + 1] = 0;
+        if (!pv) continue;
+        if (E.flags & EPI_BIAS) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (cc0 + e < cend) v[e] = round_bf16(__fadd_rn(v[e], __ldg(E.bias + cw + cc0 + e)));
+        }
+        if (E.flags & EPI_RESIDUAL) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            if (cc0 + e >= cend) continue;
+            float sk = bf16_val(E.res[ou0 + (cc0 + e) * cstep_o]);
+            if (E.flags & EPI_RESIDUAL_BIAS)
+              sk = round_bf16(__fadd_rn(sk, __ldg(E.rbias + cw + cc0 + e)));
+            v[e] = round_bf16(__fadd_rn(v[e], sk));
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (cc0 + e >= cend) continue;
+          const uint16_t vb = bf16_bits(v[e]);
+          const long long ou = ou0 + (cc0 + e) * cstep_o;
+          const long long yo = yo0 + (cc0 + e) * cstep_y;
+          if (E.flags & EPI_DEBUG_STORE_CONV) E.conv[pix * E.Cout + cw + cc0 + e] = cb[e];
+          if (E.flags & EPI_SAVE_VALUE) E.val[ou] = vb;
+          E.y[yo] = vb;
+          if (E.pad) {
+            if (w == E.Wo - 1) E.y[yo + 1] = 0;
+            if (h == E.Ho - 1) E.y[yo + E.Wy] = 0;
+            if (w == E.Wo - 1 && h == E.Ho - 1) E.y[yo + E.Wy + 1] = 0;
+          }
         }
       }
     }
