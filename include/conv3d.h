@@ -58,7 +58,9 @@ enum {
   CONV3D_ERR_OVERLAP = -4,       /* an output / workspace overlaps another buffer */
   CONV3D_ERR_WORKSPACE = -5,     /* workspace missing or too small */
   CONV3D_ERR_CUDA = -6,          /* a CUDA runtime / driver call failed */
-  CONV3D_ERR_DEVICE_TIMEOUT = -7 /* a kernel's bounded wait ran out (device word) */
+  CONV3D_ERR_DEVICE_TIMEOUT = -7, /* a kernel's bounded wait ran out (device word) */
+  CONV3D_ERR_SCRATCH_LIMIT = -8   /* conv3d_fwd_static_scratch: the call needs more scratch
+                                     than the library's static 16 MiB buffer */
 };
 
 /* ---- layouts and padding ------------------------------------------------------ */
@@ -172,6 +174,27 @@ int conv3d_workspace_bytes_ex(const conv3d_params* p, const conv3d_tuning* tunin
 int conv3d_fwd(const conv3d_params* p, conv3d_stream_t stream);
 int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning,
                   conv3d_stream_t stream);
+
+/* Allocation-free variant of conv3d_fwd (no counterpart on the source pages).
+ * For callers that cannot allocate device memory when they run a convolution
+ * (they only hold buffers handed to them, or allocation is forbidden in their
+ * latency-critical or timed region): the scratch conv3d_fwd would take from
+ * p->workspace (input staging copy, split-reduction partial sums) comes from a
+ * static device array of 16 MiB that the library module holds on every GPU it
+ * is loaded on, until the process exits.  p->workspace is ignored; inputs and
+ * outputs are the caller's as for conv3d_fwd.
+ *  - Calls whose conv3d_workspace_bytes() exceeds 16 MiB return
+ *    CONV3D_ERR_SCRATCH_LIMIT and launch nothing.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture on the device.
+ *  - All calls share the one array per device and it keeps the last call's
+ *    contents; every byte a call reads is written earlier in the same call, so
+ *    nothing needs clearing.  Calls that can run at the same time on the GPU
+ *    (different streams, or several host threads) race on the array: serialise
+ *    them on one stream.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+int conv3d_fwd_static_scratch(const conv3d_params* p, conv3d_stream_t stream);
 
 /* Number of kernel launches conv3d_fwd(_ex) enqueues for *p (for accounting). */
 int conv3d_launch_count(const conv3d_params* p, const conv3d_tuning* tuning);

@@ -38,13 +38,14 @@ ERR_OVERLAP = -4
 ERR_WORKSPACE = -5
 ERR_CUDA = -6
 ERR_DEVICE_TIMEOUT = -7
+ERR_SCRATCH_LIMIT = -8
 
 # Every function the C header declares (checked by the tests against include/conv3d.h).
 EXPORTS = (
     "conv3d_packed_weight_bytes", "conv3d_pack_weight", "conv3d_workspace_bytes",
     "conv3d_workspace_bytes_ex", "conv3d_fwd", "conv3d_fwd_ex", "conv3d_launch_count",
     "l2norm_silu", "conv3d_get_device_status", "conv3d_status_string", "conv3d_version",
-    "conv3d_struct_size",
+    "conv3d_struct_size", "conv3d_fwd_static_scratch",
 )
 
 
@@ -116,6 +117,8 @@ def _lib():
                 lib.conv3d_fwd.restype = ctypes.c_int
                 lib.conv3d_fwd_ex.argtypes = [P, T, vp]
                 lib.conv3d_fwd_ex.restype = ctypes.c_int
+                lib.conv3d_fwd_static_scratch.argtypes = [P, vp]
+                lib.conv3d_fwd_static_scratch.restype = ctypes.c_int
                 lib.conv3d_launch_count.argtypes = [P, T]
                 lib.conv3d_launch_count.restype = ctypes.c_int
                 lib.l2norm_silu.argtypes = [vp, i64, i32, vp, vp, vp, vp, vp, vp, vp]

@@ -789,6 +789,8 @@ const char* conv3d_status_string(int status) {
     case CONV3D_ERR_WORKSPACE: return "workspace missing or too small";
     case CONV3D_ERR_CUDA: return "CUDA error";
     case CONV3D_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case CONV3D_ERR_SCRATCH_LIMIT:
+      return "call needs more scratch than the allocation-free entry point holds (16 MiB)";
     default: return "unknown status";
   }
 }
@@ -804,4 +806,60 @@ extern "C" size_t conv3d_struct_size(int which) {
     case 2: return sizeof(conv3d_pad);
     default: return 0;
   }
+}
+
+// ---- allocation-free variant of conv3d_fwd -----------------------------------------
+//
+// Some callers cannot allocate device memory at the point where they run a
+// convolution: code that only receives pre-allocated tensors from a host
+// framework, allocators that forbid allocation inside a timed or latency-critical
+// region, or embedders whose memory is fully reserved up front.  For them the
+// scratch that conv3d_fwd takes from the caller's workspace (the channels-last
+// staging copy of the input and the split-reduction partial sums) lives instead
+// in one file-scope device array that the CUDA module holds from load until exit.
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB per device
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+// Device address of g_static_scratch, resolved once per device.  In host code the
+// array's name is only a host-side stand-in, so the address must come from
+// cudaGetSymbolAddress with that device current.
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+
+int static_scratch_for_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return CONV3D_ERR_CUDA;
+  void* ptr = __atomic_load_n(&g_scratch_addr[dev], __ATOMIC_ACQUIRE);
+  if (!ptr) {
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr)
+      return CONV3D_ERR_CUDA;
+    __atomic_store_n(&g_scratch_addr[dev], ptr, __ATOMIC_RELEASE);
+  }
+  *out = ptr;
+  return CONV3D_OK;
+}
+
+}  // namespace
+
+extern "C" int conv3d_fwd_static_scratch(const conv3d_params* p, conv3d_stream_t stream) {
+  if (!p) return CONV3D_ERR_INVALID_ARG;
+  Plan pl;
+  int rc = make_plan(p, nullptr, &pl);
+  if (rc) return rc;
+  if (pl.ws_bytes > kStaticScratchBytes) return CONV3D_ERR_SCRATCH_LIMIT;
+  conv3d_params q = *p;
+  if (pl.ws_bytes > 0) {
+    void* scratch = nullptr;
+    rc = static_scratch_for_current_device(&scratch);
+    if (rc) return rc;
+    q.workspace = scratch;
+    q.workspace_bytes = kStaticScratchBytes;
+  }
+  // Nothing in the scratch needs to start at zero: the staging copy and every
+  // partial sum are written before they are read within the same call.
+  return conv3d_fwd(&q, stream);
 }
