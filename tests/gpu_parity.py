@@ -134,6 +134,7 @@ def full_reference(gc: GpuCall, x_bits_ncdhw_or_ndhwc=None):
 def sample_points(N, Do, Ho, Wo, k, seed=0, tile_w=128):
     """Border, tile-boundary and random output pixels (n, d, h, w)."""
     rng = np.random.default_rng(seed)
+    k = min(k, N * Do * Ho * Wo)
     pts = set()
     ws = sorted({0, 1, Wo - 2, Wo - 1} | {min(Wo - 1, max(0, t + o))
                                           for t in range(0, Wo, tile_w) for o in (-1, 0)})
