@@ -147,7 +147,8 @@ typedef struct {
                           (M = output channels, N = up to 256 pixels) */
   int32_t inject;      /* test aid: >0 makes the producer skip stage (inject-1) so a
                           bounded wait runs out; the call then reports a timeout */
-  int32_t timeout_ms;  /* device wait limit (0 = default 4000 ms) */
+  int32_t timeout_ms;  /* device wait limit (0 = default: 4000 ms, or the environment
+                          variable CONV3D_TIMEOUT_MS when set) */
 } conv3d_tuning;
 
 /* ---- weight packing ([cuDNN page] "Weight Packing") ------------------------------ */

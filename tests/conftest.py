@@ -18,3 +18,8 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+# Device waits give up after 0.5 s in tests (default 4 s): a kernel whose
+# pipeline bookkeeping is wrong fails its test quickly instead of stalling.
+os.environ.setdefault("CONV3D_TIMEOUT_MS", "500")

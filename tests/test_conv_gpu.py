@@ -60,6 +60,8 @@ PLAN_VARIANTS = [
     dict(kernel=2, kc=32, halo=1),
     dict(kernel=2, tile_w=64, tile_h=3),
     dict(kernel=2, tile_w=128, halo=1),
+    dict(kernel=2, tile_w=48, tile_h=3, halo=1),
+    dict(kernel=2, tile_w=30, tile_h=4, halo=1),
     dict(kernel=2, k_splits=3),
     dict(kernel=2, halo=1, k_splits=2),
     dict(kernel=2, stages=2),
@@ -90,6 +92,9 @@ SHAPES = [
     mk("wide_640_tiles", 1, 64, 3, 3, 642, 96, pads=VALID, index=20),
     mk("flat_h_zero_pad", 1, 64, 3, 7, 50, 64, pads=((2, 0, Z), (1, 1, Z), (0, 0, Z)), index=21),
     mk("flat_small_w_384", 1, 384, 3, 9, 22, 384, pads=VALID, index=22),
+    mk("strip_reflect_small_w", 1, 64, 3, 12, 20, 128, pads=CR, index=23),
+    mk("strip_reflect_128", 1, 128, 2, 6, 128, 96, pads=CR, index=24),
+    mk("strip_zero_pad_odd", 2, 32, 2, 7, 37, 64, pads=P1, index=25),
     mk("t1_2d_tiles_h", 2, 32, 1, 9, 40, 48, kernel=(1, 3, 3), pads=P2D, index=2),
     mk("stride2_causal_reflect", 1, 32, 5, 11, 71, 32, stride=(2, 2, 2), pads=CR, index=3),
     mk("reflect_causal_wide", 1, 16, 4, 7, 133, 32, pads=CR, index=4),

@@ -55,6 +55,18 @@ int num_sms() {
 }
 
 inline long long round_up(long long a, long long b) { return (a + b - 1) / b * b; }
+
+// Limit of every device-side wait: 4 s, or CONV3D_TIMEOUT_MS from the environment
+// (read once; lets a test run fail fast).
+int default_timeout_ms() {
+  static int ms = -1;
+  if (ms < 0) {
+    const char* e = std::getenv("CONV3D_TIMEOUT_MS");
+    const int v = e ? std::atoi(e) : 0;
+    ms = (v > 0) ? v : 4000;
+  }
+  return ms;
+}
 inline long long cdiv(long long a, long long b) { return (a + b - 1) / b; }
 
 struct Plan {
@@ -213,40 +225,84 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   } else if (t.tile_w > 0) {
     tw = t.tile_w;
     rh = t.tile_h > 0 ? t.tile_h : 1;
-    halo = (t.halo == 1) || (t.halo == 0 && sw == 1 && rh == 1 && p->KS > 1);
-  } else if (sw == 1 && p->KS > 1 && Wo >= 176 && t.halo != 2) {
-    const int nt = static_cast<int>(cdiv(Wo, 256));
-    tw = static_cast<int>(round_up(cdiv(Wo, nt), 16));
-    if (tw > 256) tw = 256;
+    halo = (t.halo == 1) || (t.halo == 0 && sw == 1 && p->KS > 1 &&
+                             rh * (tw + p->KS - 1) <= 256 + p->KS - 1);
+  } else if (sw == 1 && p->KS > 1 && t.halo != 2) {
+    // Strip tiles: rh output rows of tw pixels; each row's run of tw + KS - 1
+    // input pixels sits run_pitch rows after the previous one, so one MMA of
+    // N = (rh - 1) * pitch + tw rows covers the tile for every W tap.  The split
+    // of the width (nt pieces) and of the rows is chosen to minimise MMA issue
+    // time: an MMA costs about as much for N up to ~208 as for N = 208.
+    long long best = -1;
+    tw = 0;
     rh = 1;
+    for (int nt = 1; nt <= 16; ++nt) {
+      const int ctw = static_cast<int>(cdiv(Wo, nt));
+      const int run = ctw + p->KS - 1;
+      int crh, cN;
+      if (run > 256) {
+        if (ctw > 256) continue;
+        crh = 1;
+        cN = static_cast<int>(round_up(ctw, 16));
+      } else {
+        const int pitch = static_cast<int>(round_up(run, 8));  // runs stay 1024-byte aligned
+        const int rmax = std::max(1, std::min((256 - ctw) / pitch + 1, Ho));
+        const int nth = static_cast<int>(cdiv(Ho, rmax));
+        crh = static_cast<int>(cdiv(Ho, nth));
+        cN = static_cast<int>(round_up((long long)(crh - 1) * pitch + ctw, 16));
+        if (cN > 256) continue;
+      }
+      const long long cost = (long long)std::max(cN, 208) * nt * cdiv(Ho, crh);
+      if (best < 0 || cost < best) {
+        best = cost;
+        tw = ctw;
+        rh = crh;
+      }
+    }
+    if (best < 0) return CONV3D_ERR_UNSUPPORTED;
     halo = true;
   } else {
     const int maxw = std::min(256, 256 / sw);
     tw = static_cast<int>(std::min<long long>(round_up(Wo, 8), maxw / 8 * 8));
     rh = std::max(1, std::min(256 / tw, Ho));
-    halo = (t.halo == 1) && sw == 1 && rh == 1;
+    halo = false;
   }
-  if (halo && (sw != 1 || rh != 1)) return CONV3D_ERR_INVALID_ARG;
-  if (tw < 1 || rh < 1 || tw * rh > 256 || tw * sw > 256) return CONV3D_ERR_INVALID_ARG;
-  if (rh > 1 && tw % 8) return CONV3D_ERR_INVALID_ARG;
+  if (halo && sw != 1) return CONV3D_ERR_INVALID_ARG;
+  if (tw < 1 || rh < 1 || tw * sw > 256) return CONV3D_ERR_INVALID_ARG;
   k.tw = tw;
   k.rh = rh;
   k.halo = halo ? 1 : 0;
   k.flat = flat ? 1 : 0;
-  k.N = static_cast<int>(round_up((long long)tw * rh, 16));
-  if (halo) {
+  if (flat) {
+    k.nbox = static_cast<int>(cdiv(tw + p->KS - 1, 256));
+    k.box_w = k.nbox == 1 ? tw + p->KS - 1
+                          : static_cast<int>(round_up(cdiv(tw + p->KS - 1, k.nbox), 8));
+    k.run_pitch = k.nbox * k.box_w;
+    k.N = static_cast<int>(round_up(tw, 16));
+  } else if (halo) {
     const int run = tw + p->KS - 1;
-    k.nbox = static_cast<int>(cdiv(run, 256));
-    k.box_w = k.nbox == 1 ? run : static_cast<int>(round_up(cdiv(run, k.nbox), 8));
-    k.box_pitch = k.nbox == 1 ? static_cast<int>(round_up(run, 8)) : k.box_w;
+    if (run > 256) {
+      if (rh != 1) return CONV3D_ERR_INVALID_ARG;
+      k.nbox = 2;
+      k.box_w = static_cast<int>(round_up(cdiv(run, 2), 8));
+    } else {
+      k.nbox = 1;
+      k.box_w = run;
+    }
+    // runs start on 8-row (swizzle-period) boundaries
+    k.run_pitch = static_cast<int>(round_up((long long)k.nbox * k.box_w, 8));
+    k.N = static_cast<int>(round_up((long long)(rh - 1) * k.run_pitch + tw, 16));
   } else {
-    k.nbox = rh;
+    if (rh > 1 && tw % 8) return CONV3D_ERR_INVALID_ARG;
+    k.nbox = 1;
     k.box_w = tw;
-    k.box_pitch = tw;
+    k.run_pitch = tw;
+    k.N = static_cast<int>(round_up((long long)tw * rh, 16));
   }
+  if (k.N > 256) return CONV3D_ERR_INVALID_ARG;
   k.taps_per_stage = halo ? p->KS : 1;
   k.stages_total = p->KT * p->KR * (halo ? 1 : p->KS) * k.n_chunks;
-  const long long act_rows = std::max<long long>((long long)k.nbox * k.box_pitch,
+  const long long act_rows = std::max<long long>((long long)k.rh * k.run_pitch,
                                                  k.N + (halo ? p->KS - 1 : 0));
   k.act_bytes = static_cast<uint32_t>(round_up(round_up(act_rows, 8) * k.row_bytes, 1024));
   const uint32_t wgt_bytes = static_cast<uint32_t>(k.taps_per_stage * 128 * k.row_bytes);
@@ -258,7 +314,29 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   if (stages < 2) return CONV3D_ERR_UNSUPPORTED;
   k.stages = stages;
   k.bar_off = k.stage_bytes * stages;
-  k.tx_bytes = static_cast<uint32_t>((long long)k.nbox * k.box_w * k.row_bytes) + wgt_bytes;
+  // Only the rows of real output channels are loaded: out-of-bounds box rows
+  // still cost transfer bandwidth.  The MMA reads all 128 rows; the rows past
+  // Cout hold stale data and only reach accumulator lanes that are never stored.
+  k.wgt_rows = static_cast<int>(std::min<long long>(128, round_up(p->Cout, 8)));
+  {
+    // Bytes one stage's copies deliver, counted the way the producer issues them:
+    // per output row of the tile (one run for flat tiles) nbox boxes of box_w
+    // pixels, then one weight box per tap.  A wrong count leaves the stage's
+    // barrier incomplete or completes it early, so the plan is refused when the
+    // closed form and the walk disagree.
+    const int runs = flat ? 1 : k.rh;
+    long long walked = 0;
+    for (int i = 0; i < runs; ++i)
+      for (int b = 0; b < k.nbox; ++b) walked += (long long)k.box_w * k.row_bytes;
+    for (int tl = 0; tl < k.taps_per_stage; ++tl) walked += (long long)k.wgt_rows * k.row_bytes;
+    const long long closed = (long long)runs * k.nbox * k.box_w * k.row_bytes +
+                             (long long)k.taps_per_stage * k.wgt_rows * k.row_bytes;
+    if (walked != closed || closed >= (1LL << 20)) return CONV3D_ERR_UNSUPPORTED;
+    k.tx_bytes = static_cast<uint32_t>(closed);
+    // every loaded row must land inside the stage's activation / weight regions
+    if ((long long)((runs - 1) * k.run_pitch + k.nbox * k.box_w) * k.row_bytes > k.act_bytes)
+      return CONV3D_ERR_UNSUPPORTED;
+  }
   k.tiles_w = static_cast<int>(flat ? cdiv(q_total, tw) : cdiv(Wo, tw));
   k.tiles_h = static_cast<int>(flat ? 1 : cdiv(Ho, rh));
   k.tiles_c = static_cast<int>(cdiv(p->Cout, 128));
@@ -303,7 +381,8 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.reflect_w = (p->pad[2].mode == CONV3D_PAD_REFLECT && (p->pad[2].before || p->pad[2].after));
   k.cp64 = static_cast<int>(round_up(p->Cin, 64));
   k.inject = t.inject;
-  k.timeout_ns = (unsigned long long)(t.timeout_ms > 0 ? t.timeout_ms : 4000) * 1000000ULL;
+  k.timeout_ns = (unsigned long long)(t.timeout_ms > 0 ? t.timeout_ms : default_timeout_ms()) *
+                 1000000ULL;
   fill_epi(p, *pl, &k.epi);
   return CONV3D_OK;
 }
@@ -477,7 +556,8 @@ int plan_pm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.reflect_w = (p->pad[2].mode == CONV3D_PAD_REFLECT && (p->pad[2].before || p->pad[2].after));
   k.cp64 = static_cast<int>(round_up(p->Cin, 64));
   k.inject = t.inject;
-  k.timeout_ns = (unsigned long long)(t.timeout_ms > 0 ? t.timeout_ms : 4000) * 1000000ULL;
+  k.timeout_ns = (unsigned long long)(t.timeout_ms > 0 ? t.timeout_ms : default_timeout_ms()) *
+                 1000000ULL;
 
   fill_epi(p, *pl, &k.epi);
   return CONV3D_OK;
@@ -587,7 +667,7 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
     kc = k.kc;
     act_box = k.halo ? k.box_w : k.box_w * k.sw;
     es_w = k.halo ? 1 : k.sw;
-    wgt_rows = 128;
+    wgt_rows = k.wgt_rows;
     cp64 = k.cp64;
   } else {
     const ConvTCParams& k = pl.kp;

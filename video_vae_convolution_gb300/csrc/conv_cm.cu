@@ -167,24 +167,21 @@ __global__ void __launch_bounds__(384, 1)
               // flattened (H*W) positions: output q reads input q + (r - ph) * W + s
               const int q_start = w0 + (sc.r - p.ph) * p.W;
               for (int b = 0; b < p.nbox; ++b)
-                tma_load_4d(act + static_cast<uint32_t>(b * p.box_pitch * p.row_bytes), &tmAct,
+                tma_load_4d(act + static_cast<uint32_t>(b * p.box_w * p.row_bytes), &tmAct,
                             full, sc.ch * p.kc, q_start + b * p.box_w, d_in, tc.nb);
-            } else if (p.halo) {
-              const int ho = h0;
-              int h_in = ho * p.sh + sc.r - p.ph;
-              if (p.reflect_h && ho < p.epi.Ho) h_in = reflect_coord(h_in, p.H);
-              const int w_start = w0 - p.pw;
-              for (int b = 0; b < p.nbox; ++b)
-                tma_load_5d(act + static_cast<uint32_t>(b * p.box_pitch * p.row_bytes), &tmAct,
-                            full, sc.ch * p.kc, w_start + b * p.box_w, h_in, d_in, tc.nb);
             } else {
-              const int w_start = w0 * p.sw + sc.sblk - p.pw;
+              // one run per output row of the tile, run_pitch rows apart: halo runs
+              // of tw + KS - 1 pixels (all KS taps), or tw pixels at one tap
+              const int w_start = p.halo ? (w0 - p.pw) : (w0 * p.sw + sc.sblk - p.pw);
               for (int i = 0; i < p.rh; ++i) {
                 const int ho = h0 + i;
                 int h_in = ho * p.sh + sc.r - p.ph;
                 if (p.reflect_h && ho < p.epi.Ho) h_in = reflect_coord(h_in, p.H);
-                tma_load_5d(act + static_cast<uint32_t>(i * p.box_pitch * p.row_bytes), &tmAct,
-                            full, sc.ch * p.kc, w_start, h_in, d_in, tc.nb);
+                for (int b = 0; b < p.nbox; ++b)
+                  tma_load_5d(act + static_cast<uint32_t>((i * p.run_pitch + b * p.box_w) *
+                                                          p.row_bytes),
+                              &tmAct, full, sc.ch * p.kc, w_start + b * p.box_w, h_in, d_in,
+                              tc.nb);
               }
             }
             for (int tl = 0; tl < p.taps_per_stage; ++tl) {
@@ -284,9 +281,9 @@ __global__ void __launch_bounds__(384, 1)
       uint32_t phase = 0;
       const int es = p.halo ? 1 : p.sw;
       const int step = 2 / es;
-      const int runs = p.halo ? 1 : p.rh;
-      const int run_len = p.halo ? p.nbox * p.box_w : p.box_w;
-      const int run_pitch = p.halo ? 0 : p.box_pitch;
+      const int runs = p.rh;
+      const int run_len = p.nbox * p.box_w;
+      const int run_pitch = p.run_pitch;
       const int chunks = p.row_bytes / 16;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
@@ -371,9 +368,9 @@ __global__ void __launch_bounds__(384, 1)
       t.w0 = tc.twi * p.tw;
       t.h0 = tc.thi * p.rh;
       t.tw = p.tw;
-      t.npix = p.rh * p.tw;
       t.flat = p.flat;
-      t.pitch = p.W;
+      t.pitch = p.flat ? p.W : p.run_pitch;
+      t.npix = p.flat ? p.tw : p.rh * p.run_pitch;
       const int cw = tc.ct * 128 + q * 32;  // first channel of this warp's TMEM lanes
       const bool warp_live = cw < E.Cout;
       const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +

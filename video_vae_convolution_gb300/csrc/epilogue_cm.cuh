@@ -35,26 +35,32 @@ struct CmEpi {
 struct CmTile {
   int nb, od, split;
   int w0, h0, tw, npix;
-  int flat, pitch;  // flat: tile pixel n is flattened position w0 + n with row pitch `pitch`
+  // flat: tile pixel n is flattened position w0 + n of the plane (row pitch `pitch` = W);
+  // otherwise pixel n is output row h0 + n / pitch, column w0 + n % pitch, and only
+  // columns n % pitch < tw belong to the tile (the rest are halo rows of a run)
+  int flat, pitch;
 };
 
-// Output coordinates of tile pixel n (possibly outside [0, Ho) x [0, Wo)).
-__device__ __forceinline__ void cm_pixel(const CmTile& t, int n, int& h, int& w) {
+// Output coordinates of tile pixel n; false when n is not one of the tile's pixels.
+// The caller still checks h < Ho and w < Wo.
+__device__ __forceinline__ bool cm_pixel(const CmTile& t, int n, int& h, int& w) {
   if (t.flat) {
     const int q = t.w0 + n;
     h = q / t.pitch;
     w = q - h * t.pitch;
-  } else {
-    const int i = n / t.tw;
-    h = t.h0 + i;
-    w = t.w0 + (n - i * t.tw);
+    return true;
   }
+  const int i = n / t.pitch;
+  const int j = n - i * t.pitch;
+  h = t.h0 + i;
+  w = t.w0 + j;
+  return j < t.tw;
 }
 
 // Whether tile pixels [n, n + len) lie on one output row at consecutive w.
 __device__ __forceinline__ bool cm_same_row(const CmTile& t, int n, int len) {
   if (t.flat) return ((t.w0 + n) % t.pitch) + len <= t.pitch;
-  return (n % t.tw) + len <= t.tw;
+  return (n % t.pitch) + len <= t.tw;
 }
 
 __device__ __forceinline__ uint4 pack8(const uint16_t (&v)[8]) {
@@ -79,8 +85,8 @@ __device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
 __device__ __forceinline__ void cm_unit_ndhwc(const CmEpi& E, const CmTile& t, int n, int c0,
                                               int cnt, const float (&a)[8]) {
   int h, w;
-  cm_pixel(t, n, h, w);
-  if (n >= t.npix || h >= E.Ho || w >= E.Wo || cnt <= 0) return;
+  const bool in_tile = cm_pixel(t, n, h, w);
+  if (!in_tile || n >= t.npix || h >= E.Ho || w >= E.Wo || cnt <= 0) return;
   const long long nd = (long long)t.nb * E.Do + t.od;
   const long long pix = (nd * E.Ho + h) * E.Wo + w;
   const bool vec = (cnt == 8) && ((E.Cout & 7) == 0);
@@ -195,8 +201,8 @@ __device__ __forceinline__ void cm_unit_ncdhw(const CmEpi& E, const CmTile& t, i
   }
   for (int e = 0; e < 8; ++e) {
     int h, w;
-    cm_pixel(t, n0 + e, h, w);
-    if (n0 + e >= t.npix || h >= E.Ho || w >= E.Wo) continue;
+    const bool in_tile = cm_pixel(t, n0 + e, h, w);
+    if (!in_tile || n0 + e >= t.npix || h >= E.Ho || w >= E.Wo) continue;
     const long long pix = (nd * E.Ho + h) * E.Wo + w;
     if (E.split) {
       E.part[((long long)t.split * E.M_total + pix) * E.Cout + c] = a[e];
@@ -259,8 +265,8 @@ __device__ __forceinline__ void cm_block(const CmEpi& E, const CmTile& t, float 
       // lane = pixel: for each channel, the warp writes 32 consecutive pixels
       const int n = j0 + lane;
       int h, w;
-      cm_pixel(t, n, h, w);
-      const bool pv = n < t.npix && h < E.Ho && w < E.Wo;
+      const bool in_tile = cm_pixel(t, n, h, w);
+      const bool pv = in_tile && n < t.npix && h < E.Ho && w < E.Wo;
       const long long plane_o = (long long)E.Ho * E.Wo, plane_y = (long long)E.Hy * E.Wy;
       const long long pix = (((long long)t.nb * E.Do + t.od) * E.Ho + h) * E.Wo + w;
       const int cend = min(32, E.Cout - cw);

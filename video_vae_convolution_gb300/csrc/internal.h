@@ -83,13 +83,15 @@ struct ConvCMParams {
                            // stride 1, no W padding, zero H padding)
   int nbox;                // activation boxes per stage (halo: 1..2, direct: rh)
   int box_w;               // loaded elements per activation box
-  int box_pitch;           // shared-memory rows between activation boxes
+  int run_pitch;           // shared-memory rows between the runs of consecutive output
+                           // rows (also the tile's pixel pitch: valid columns are < tw)
   int N;                   // MMA N = round_up(rh * tw, 16)
   int kc, n_chunks, row_bytes;
   int taps_per_stage;
   int stages;
   uint32_t act_bytes, stage_bytes, bar_off, tx_bytes;
-  uint32_t epi_off;        // 4 x [32][33] fp32 epilogue staging blocks
+  uint32_t epi_off;        // per-warp [32][33] fp32 epilogue staging blocks
+  int wgt_rows;            // weight box rows loaded per tap (<= 128; the MMA reads 128)
   int stages_total, k_splits, stages_per_split;
   int tiles_w, tiles_h, tiles_c;  // pixel tiles along W / H, 128-channel tiles
   int num_tiles;
