@@ -141,6 +141,36 @@ def test_epilogues(call, out_layout):
     run_and_check(call, wl.NDHWC, out_layout)
 
 
+# Fused L2 norm in the channel-major kernel (all channel tiles of a pixel tile on
+# one CTA): flat, strip and direct pixel tiles; 1..4 channel tiles with a partial
+# last tile; Cout not a multiple of 8; residual, residual bias and the saved value.
+NORM_CM_CASES = [
+    mk("norm_cm160_flat", 1, 32, 3, 7, 50, 160, pads=((2, 0, Z), (1, 1, Z), (0, 0, Z)),
+       epi=wl.EPI_BIAS | wl.EPI_L2NORM_SILU, index=26),
+    mk("norm_cm320_strip_res", 1, 64, 3, 5, 70, 320, pads=CR,
+       epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_RESIDUAL_BIAS | wl.EPI_L2NORM_SILU |
+       wl.EPI_SAVE_VALUE, index=27),
+    mk("norm_cm200_direct_s2", 1, 32, 3, 9, 41, 200, stride=(1, 2, 2), pads=CR,
+       epi=wl.EPI_BIAS | wl.EPI_L2NORM_SILU | wl.EPI_SAVE_VALUE, index=28),
+    mk("norm_cm36_odd", 2, 24, 2, 5, 33, 36, pads=P1, epi=wl.EPI_RESIDUAL | wl.EPI_L2NORM_SILU,
+       index=29),
+    mk("norm_cm512_wide", 1, 64, 2, 3, 300, 512, pads=CR, epi=wl.EPI_BIAS | wl.EPI_L2NORM_SILU,
+       index=30),
+]
+
+
+@pytest.mark.parametrize("call", NORM_CM_CASES, ids=lambda c: c.name)
+@pytest.mark.parametrize("out_layout", [wl.NDHWC, wl.NCDHW])
+def test_norm_channel_major(call, out_layout):
+    run_and_check(call, wl.NDHWC, out_layout, tuning=vvc.Tuning(kernel=2, k_splits=1))
+
+
+@pytest.mark.parametrize("call", [c for c in EPI_CASES if c.epi & wl.EPI_L2NORM_SILU],
+                         ids=lambda c: c.name)
+def test_norm_pixel_major(call):
+    run_and_check(call, wl.NDHWC, wl.NDHWC, tuning=vvc.Tuning(kernel=1))
+
+
 def test_epilogue_split_k_matches():
     call = mk("epi_split", 1, 64, 3, 5, 70, 160, pads=P1,
               epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_L2NORM_SILU, index=17)

@@ -17,8 +17,8 @@ namespace vvc {
 cudaError_t launch_conv_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const ConvTCParams& p,
                            dim3 grid, size_t smem_bytes, cudaStream_t stream);
 cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
-                           const ConvCMParams& p, int grid, size_t smem_bytes,
-                           cudaStream_t stream);
+                           const CUtensorMap& tmWgtLast, const ConvCMParams& p, int grid,
+                           size_t smem_bytes, cudaStream_t stream);
 cudaError_t conv_status_read_clear(int* status, cudaStream_t stream);
 cudaError_t conv_cm_status_read_clear(int* status);
 cudaError_t launch_pack_weight(const void* w, void* out, int Co, int Ci, int taps,
@@ -75,6 +75,7 @@ struct Plan {
   int Cst = 0;
   size_t stage_off = 0, stage_bytes = 0;
   size_t partial_off = 0, partial_bytes = 0;
+  size_t vscratch_off = 0, vscratch_bytes = 0;
   size_t ws_bytes = 0;
   bool cm = false;          // channel-major kernel (conv_cm) instead of pixel-major (conv_tc)
   ConvTCParams kp{};
@@ -308,8 +309,12 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   const uint32_t wgt_bytes = static_cast<uint32_t>(k.taps_per_stage * 128 * k.row_bytes);
   k.stage_bytes = k.act_bytes + wgt_bytes;
   constexpr size_t kEpiStage = 8 * 32 * 33 * 4;  // per-warp transpose blocks
-  int stages = static_cast<int>(
-      std::min<size_t>(8, (kMaxSmem - 1024 - 256 - kEpiStage) / k.stage_bytes));
+  k.tiles_c = static_cast<int>(cdiv(p->Cout, 128));
+  // fused L2 norm: den[N] in shared memory
+  const bool norm = (p->epi & CONV3D_EPI_L2NORM_SILU) != 0;
+  const size_t norm_bytes = norm ? (size_t)k.N * 4 : 0;
+  int stages = static_cast<int>(std::min<size_t>(
+      8, (kMaxSmem - 1024 - 256 - kEpiStage - norm_bytes) / k.stage_bytes));
   if (t.stages > 0) stages = std::min(stages, t.stages);
   if (stages < 2) return CONV3D_ERR_UNSUPPORTED;
   k.stages = stages;
@@ -318,6 +323,7 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   // still cost transfer bandwidth.  The MMA reads all 128 rows; the rows past
   // Cout hold stale data and only reach accumulator lanes that are never stored.
   k.wgt_rows = static_cast<int>(std::min<long long>(128, round_up(p->Cout, 8)));
+  k.wgt_rows_last = static_cast<int>(round_up(p->Cout - 128LL * (cdiv(p->Cout, 128) - 1), 8));
   {
     // Bytes one stage's copies deliver, counted the way the producer issues them:
     // per output row of the tile (one run for flat tiles) nbox boxes of box_w
@@ -328,26 +334,39 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
     long long walked = 0;
     for (int i = 0; i < runs; ++i)
       for (int b = 0; b < k.nbox; ++b) walked += (long long)k.box_w * k.row_bytes;
-    for (int tl = 0; tl < k.taps_per_stage; ++tl) walked += (long long)k.wgt_rows * k.row_bytes;
-    const long long closed = (long long)runs * k.nbox * k.box_w * k.row_bytes +
-                             (long long)k.taps_per_stage * k.wgt_rows * k.row_bytes;
-    if (walked != closed || closed >= (1LL << 20)) return CONV3D_ERR_UNSUPPORTED;
+    long long walked_last = walked;
+    for (int tl = 0; tl < k.taps_per_stage; ++tl) {
+      walked += (long long)k.wgt_rows * k.row_bytes;
+      walked_last += (long long)k.wgt_rows_last * k.row_bytes;
+    }
+    const long long act_part = (long long)runs * k.nbox * k.box_w * k.row_bytes;
+    const long long closed = act_part + (long long)k.taps_per_stage * k.wgt_rows * k.row_bytes;
+    const long long closed_last =
+        act_part + (long long)k.taps_per_stage * k.wgt_rows_last * k.row_bytes;
+    if (walked != closed || walked_last != closed_last || closed >= (1LL << 20) ||
+        closed_last >= (1LL << 20) || k.wgt_rows_last < 8 || k.wgt_rows_last > 128)
+      return CONV3D_ERR_UNSUPPORTED;
     k.tx_bytes = static_cast<uint32_t>(closed);
+    k.tx_bytes_last = static_cast<uint32_t>(closed_last);
     // every loaded row must land inside the stage's activation / weight regions
     if ((long long)((runs - 1) * k.run_pitch + k.nbox * k.box_w) * k.row_bytes > k.act_bytes)
       return CONV3D_ERR_UNSUPPORTED;
   }
   k.tiles_w = static_cast<int>(flat ? cdiv(q_total, tw) : cdiv(Wo, tw));
   k.tiles_h = static_cast<int>(flat ? 1 : cdiv(Ho, rh));
-  k.tiles_c = static_cast<int>(cdiv(p->Cout, 128));
   const long long tiles = (long long)k.tiles_w * k.tiles_h * Do * p->N * k.tiles_c;
   const int sms = num_sms();
   int per = 0;
-  const int splits = choose_splits(t, tiles, k.stages_total, sms, &per);
+  // with the fused norm the channel tiles of a pixel tile share a CTA, so the
+  // parallelism that decides the split is the number of pixel tiles
+  const long long par = norm ? tiles / k.tiles_c : tiles;
+  const int splits = choose_splits(t, par, k.stages_total, sms, &per);
   k.k_splits = splits;
   k.stages_per_split = per;
   if (tiles * splits > 0x7fffffffLL) return CONV3D_ERR_UNSUPPORTED;
   k.num_tiles = static_cast<int>(tiles * splits);
+  k.norm = (norm && splits == 1) ? 1 : 0;
+  k.tpu = k.norm ? k.tiles_c : 1;
   k.acc_cols = static_cast<int>(round_up(k.N, 32));
   k.nbuf = (2 * k.acc_cols <= 512) ? 2 : 1;
   int cols = 32;
@@ -359,10 +378,18 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
     pl->partial_bytes = (size_t)splits * (size_t)k.M_total * p->Cout * 4;
     off = static_cast<size_t>(round_up(off + pl->partial_bytes, 256));
   }
+  const int grid = static_cast<int>(std::min<long long>(k.num_tiles / k.tpu, sms));
+  if (k.norm) {
+    k.norm_cs = static_cast<int>(round_up(p->Cout, 8));
+    pl->vscratch_off = off;
+    pl->vscratch_bytes = (size_t)grid * k.N * k.norm_cs * 2;
+    off = static_cast<size_t>(round_up(off + pl->vscratch_bytes, 256));
+  }
   pl->ws_bytes = off;
-  pl->grid = dim3(static_cast<unsigned>(std::min<long long>(k.num_tiles, sms)), 1, 1);
+  pl->grid = dim3(static_cast<unsigned>(grid), 1, 1);
   k.epi_off = k.bar_off + 256;
-  pl->smem = 1024 + k.epi_off + kEpiStage;
+  k.norm_off = static_cast<uint32_t>(k.epi_off + kEpiStage);
+  pl->smem = 1024 + k.norm_off + norm_bytes;
   pl->launches = (pl->stage ? 1 : 0) + 1 + (splits > 1 ? 1 : 0);
   k.C = pl->Cst;
   k.D = p->D;
@@ -387,8 +414,9 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   return CONV3D_OK;
 }
 
-// Pixel-major plan: M = 128 output pixels per tile, N = output channels.  Used
-// for the fused L2-norm epilogue, which needs a pixel's whole channel row.
+// Pixel-major plan: M = 128 output pixels per tile, N = output channels (a tile
+// holds a pixel's whole channel row).  Used when no channel-major plan fits, or
+// on request (conv3d_tuning.kernel = 1).
 int plan_pm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off) {
   const int Do = pl->Do, Ho = pl->Ho, Wo = pl->Wo;
   const int st = p->stride[0], sh = p->stride[1], sw = p->stride[2];
@@ -579,15 +607,18 @@ int make_plan(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
     pl->stage_bytes = (size_t)p->N * p->D * p->H * p->W * pl->Cst * 2;
     off = static_cast<size_t>(round_up(off + pl->stage_bytes, 256));
   }
-  const bool norm = (p->epi & CONV3D_EPI_L2NORM_SILU) != 0;
-  bool cm = !norm;
-  if (t.kernel == 1) cm = false;
-  if (t.kernel == 2) {
-    if (norm) return CONV3D_ERR_UNSUPPORTED;
-    cm = true;
+  if (t.kernel == 1) {
+    pl->cm = false;
+    return plan_pm(p, t, pl, off);
   }
-  pl->cm = cm;
-  return cm ? plan_cm(p, t, pl, off) : plan_pm(p, t, pl, off);
+  const Plan before = *pl;
+  pl->cm = true;
+  rc = plan_cm(p, t, pl, off);
+  if (rc != CONV3D_ERR_UNSUPPORTED || t.kernel == 2) return rc;
+  // no channel-major plan for this shape: pixel-major tiles
+  *pl = before;
+  pl->cm = false;
+  return plan_pm(p, t, pl, off);
 }
 
 int check_pointers(const conv3d_params* p, const Plan& pl) {
@@ -656,10 +687,10 @@ CUtensorMapSwizzle swizzle_of(int kc) {
 }
 
 int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtensorMap* tmA,
-                CUtensorMap* tmB) {
+                CUtensorMap* tmB, CUtensorMap* tmBLast) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return CONV3D_ERR_CUDA;
-  int kc, act_box, es_w, wgt_rows, cp64;
+  int kc, act_box, es_w, wgt_rows, wgt_rows_last, cp64;
   bool flat = false;
   if (pl.cm) {
     const ConvCMParams& k = pl.cp;
@@ -668,6 +699,7 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
     act_box = k.halo ? k.box_w : k.box_w * k.sw;
     es_w = k.halo ? 1 : k.sw;
     wgt_rows = k.wgt_rows;
+    wgt_rows_last = k.wgt_rows_last;
     cp64 = k.cp64;
   } else {
     const ConvTCParams& k = pl.kp;
@@ -675,6 +707,7 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
     act_box = k.halo ? k.box_w : k.tile_w * k.sw;
     es_w = k.halo ? 1 : k.sw;
     wgt_rows = k.sub_n;
+    wgt_rows_last = k.sub_n;
     cp64 = k.cp64;
   }
   // activations: NDHWC bf16, dims (C, W, H, D, N); one box = kc channels x a run of
@@ -707,6 +740,16 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
   cuuint32_t esB[2] = {1, 1};
   r = enc(tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p->w_packed), gdimB, gstrB,
           boxB, esB, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kc),
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
+  // the last 128-channel tile: a box of its real rows only
+  if (wgt_rows_last == wgt_rows) {
+    *tmBLast = *tmB;
+    return CONV3D_OK;
+  }
+  cuuint32_t boxL[2] = {(cuuint32_t)kc, (cuuint32_t)wgt_rows_last};
+  r = enc(tmBLast, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p->w_packed), gdimB,
+          gstrB, boxL, esB, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kc),
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
   return CONV3D_OK;
@@ -775,14 +818,15 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
       return CONV3D_ERR_CUDA;
     xin = dst;
   }
-  CUtensorMap tmA, tmB;
-  rc = encode_maps(p, pl, xin, &tmA, &tmB);
+  CUtensorMap tmA, tmB, tmBLast;
+  rc = encode_maps(p, pl, xin, &tmA, &tmB, &tmBLast);
   if (rc) return rc;
   float* partial = reinterpret_cast<float*>(ws + pl.partial_off);
   if (pl.cm) {
     ConvCMParams kp = pl.cp;
     if (kp.k_splits > 1) kp.partial = partial;
-    if (vvc::launch_conv_cm(tmA, tmB, kp, static_cast<int>(pl.grid.x), pl.smem, s) !=
+    if (kp.norm) kp.vscratch = reinterpret_cast<uint16_t*>(ws + pl.vscratch_off);
+    if (vvc::launch_conv_cm(tmA, tmB, tmBLast, kp, static_cast<int>(pl.grid.x), pl.smem, s) !=
         cudaSuccess)
       return CONV3D_ERR_CUDA;
     if (kp.k_splits > 1 &&
@@ -930,6 +974,15 @@ extern "C" int conv3d_fwd_static_scratch(const conv3d_params* p, conv3d_stream_t
   Plan pl;
   int rc = make_plan(p, nullptr, &pl);
   if (rc) return rc;
+  conv3d_tuning tu{};
+  const conv3d_tuning* tp = nullptr;
+  if (pl.ws_bytes > kStaticScratchBytes && pl.cm && pl.cp.norm) {
+    // the fused-norm value rows do not fit: pixel-major tiles need none
+    tu.kernel = 1;
+    tp = &tu;
+    rc = make_plan(p, tp, &pl);
+    if (rc) return rc;
+  }
   if (pl.ws_bytes > kStaticScratchBytes) return CONV3D_ERR_SCRATCH_LIMIT;
   conv3d_params q = *p;
   if (pl.ws_bytes > 0) {
@@ -939,7 +992,8 @@ extern "C" int conv3d_fwd_static_scratch(const conv3d_params* p, conv3d_stream_t
     q.workspace = scratch;
     q.workspace_bytes = kStaticScratchBytes;
   }
-  // Nothing in the scratch needs to start at zero: the staging copy and every
-  // partial sum are written before they are read within the same call.
-  return conv3d_fwd(&q, stream);
+  // Nothing in the scratch needs to start at zero: the staging copy, every
+  // partial sum and the fused-norm value rows are written before they are read
+  // within the same call.
+  return conv3d_fwd_ex(&q, tp, stream);
 }

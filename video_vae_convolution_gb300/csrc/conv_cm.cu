@@ -87,11 +87,20 @@ __device__ __forceinline__ void stage_range(const ConvCMParams& p, int split, in
   e = min(p.stages_total, b + p.stages_per_split);
 }
 
+// The CTA's l-th tile, or -1 past its last.  CTAs take units of tpu consecutive
+// tiles round-robin (tpu > 1 keeps the channel tiles of a pixel tile together).
+__device__ __forceinline__ int cta_tile(const ConvCMParams& p, int l) {
+  const int u = l / p.tpu;
+  const long long t = ((long long)blockIdx.x + (long long)u * gridDim.x) * p.tpu + (l - u * p.tpu);
+  return t < p.num_tiles ? static_cast<int>(t) : -1;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(384, 1)
     conv_cm_kernel(const __grid_constant__ CUtensorMap tmAct,
                    const __grid_constant__ CUtensorMap tmWgt,
+                   const __grid_constant__ CUtensorMap tmWgtLast,
                    const __grid_constant__ ConvCMParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -127,6 +136,7 @@ __global__ void __launch_bounds__(384, 1)
     fence_mbar_init();
     tma_prefetch_desc(&tmAct);
     tma_prefetch_desc(&tmWgt);
+    tma_prefetch_desc(&tmWgtLast);
   }
   if (warp == kWarpMMA) {
     tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(p.tmem_cols));
@@ -145,9 +155,15 @@ __global__ void __launch_bounds__(384, 1)
       long long k_global = 0;   // stage counter across tiles
       long long k_skip = -1;    // stage left unissued by the test aid
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int l = 0; ok; ++l) {
+        const int tile = cta_tile(p, l);
+        if (tile < 0) break;
         const TileCoord tc = decode_tile(p, tile);
         const int w0 = tc.twi * p.tw, h0 = tc.thi * p.rh, c0 = tc.ct * 128;
+        // the last channel tile loads only its real weight rows, through its own map
+        const bool last_ct = tc.ct == p.tiles_c - 1;
+        const CUtensorMap* wmap = last_ct ? &tmWgtLast : &tmWgt;
+        const uint32_t tx = last_ct ? p.tx_bytes_last : p.tx_bytes;
         int it_b, it_e;
         stage_range(p, tc.split, it_b, it_e);
         for (int it = it_b; it < it_e; ++it) {
@@ -159,7 +175,7 @@ __global__ void __launch_bounds__(384, 1)
           const bool skip = (p.inject > 0 && k_global == p.inject - 1);
           if (!skip) {
             const uint32_t full = full_bar(slot);
-            mbar_arrive_expect_tx(full, p.tx_bytes);
+            mbar_arrive_expect_tx(full, tx);
             const uint32_t act = sbase + p.stage_bytes * slot;
             const uint32_t wgt = act + p.act_bytes;
             const int d_in = tc.od * p.st + sc.t - p.pt;
@@ -187,7 +203,7 @@ __global__ void __launch_bounds__(384, 1)
             for (int tl = 0; tl < p.taps_per_stage; ++tl) {
               const int s = p.halo ? tl : sc.sblk;
               const int tap = (sc.t * p.KR + sc.r) * p.KS + s;
-              tma_load_2d(wgt + static_cast<uint32_t>(tl * 128 * p.row_bytes), &tmWgt, full,
+              tma_load_2d(wgt + static_cast<uint32_t>(tl * 128 * p.row_bytes), wmap, full,
                           tap * p.cp64 + sc.ch * p.kc, c0);
             }
           } else {
@@ -224,8 +240,9 @@ __global__ void __launch_bounds__(384, 1)
       int slot = 0;
       uint32_t phase = 0;
       bool ok = true;
-      int local = 0;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x, ++local) {
+      for (int local = 0; ok; ++local) {
+        const int tile = cta_tile(p, local);
+        if (tile < 0) break;
         const TileCoord tc = decode_tile(p, tile);
         const int buf = (p.nbuf == 2) ? (local & 1) : 0;
         const int use = (p.nbuf == 2) ? (local >> 1) : local;
@@ -286,7 +303,9 @@ __global__ void __launch_bounds__(384, 1)
       const int run_pitch = p.run_pitch;
       const int chunks = p.row_bytes / 16;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int l = 0; ok; ++l) {
+        const int tile = cta_tile(p, l);
+        if (tile < 0) break;
         const TileCoord tc = decode_tile(p, tile);
         const int w0 = tc.twi * p.tw;
         int it_b, it_e;
@@ -350,17 +369,13 @@ __global__ void __launch_bounds__(384, 1)
     E.part = p.partial;
     E.bias = p.epi.bias;
     E.rbias = p.epi.rbias;
+    E.gamma = p.epi.gamma;
+    E.sqrt_c = p.epi.sqrt_c;
     E.M_total = p.M_total;
     float(*stage)[33] =
         reinterpret_cast<float(*)[33]>(smem + p.epi_off + (warp - kWarpEpi0) * (32 * 33 * 4));
     const int nbuf = p.nbuf, acc_cols = p.acc_cols, Ncols = p.N;
-    int local = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++local) {
-      const TileCoord tc = decode_tile(p, tile);
-      const int buf = (nbuf == 2) ? (local & 1) : 0;
-      const int use = (nbuf == 2) ? (local >> 1) : local;
-      if (!mbar_wait(accf_bar(buf), static_cast<uint32_t>(use & 1), abort_flag, lim)) break;
-      tc_fence_after();
+    auto tile_view = [&](const TileCoord& tc) {
       CmTile t;
       t.nb = tc.nb;
       t.od = tc.od;
@@ -371,19 +386,84 @@ __global__ void __launch_bounds__(384, 1)
       t.flat = p.flat;
       t.pitch = p.flat ? p.W : p.run_pitch;
       t.npix = p.flat ? p.tw : p.rh * p.run_pitch;
-      const int cw = tc.ct * 128 + q * 32;  // first channel of this warp's TMEM lanes
-      const bool warp_live = cw < E.Cout;
-      const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                          static_cast<uint32_t>(buf * acc_cols);
-      for (int j0 = 32 * grp; j0 < Ncols; j0 += 64) {
-        uint32_t r[32];
-        tmem_ld32(tb + static_cast<uint32_t>(j0), r);
-        tmem_ld_wait();
-        if (warp_live) cm_block(E, t, stage, lane, cw, j0, r);
+      return t;
+    };
+    if (!p.norm) {
+      for (int local = 0;; ++local) {
+        const int tile = cta_tile(p, local);
+        if (tile < 0) break;
+        const TileCoord tc = decode_tile(p, tile);
+        const int buf = (nbuf == 2) ? (local & 1) : 0;
+        const int use = (nbuf == 2) ? (local >> 1) : local;
+        if (!mbar_wait(accf_bar(buf), static_cast<uint32_t>(use & 1), abort_flag, lim)) break;
+        tc_fence_after();
+        const CmTile t = tile_view(tc);
+        const int cw = tc.ct * 128 + q * 32;  // first channel of this warp's TMEM lanes
+        const bool warp_live = cw < E.Cout;
+        const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                            static_cast<uint32_t>(buf * acc_cols);
+        for (int j0 = 32 * grp; j0 < Ncols; j0 += 64) {
+          uint32_t r[32];
+          tmem_ld32(tb + static_cast<uint32_t>(j0), r);
+          tmem_ld_wait();
+          if (warp_live) cm_block(E, t, stage, lane, cw, j0, r);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar(buf));
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce_bar(buf));
+    } else {
+      // Fused L2 norm: pass 1 per channel tile, pass 2 once per pixel tile.  Every
+      // epilogue warp runs the same sequence of named barriers: after a failed wait
+      // a warp skips the work but keeps taking part, so no barrier is left short.
+      const int tid = threadIdx.x - kWarpEpi0 * 32;
+      const int Cs = p.norm_cs;
+      float* den = reinterpret_cast<float*>(smem + p.norm_off);  // [N]
+      uint16_t* scr = p.vscratch + (long long)blockIdx.x * Ncols * Cs;
+      bool ok = true;
+      int local = 0;
+      for (int l0 = 0;; l0 += p.tpu) {
+        const int tile0 = cta_tile(p, l0);
+        if (tile0 < 0) break;
+        const CmTile t = tile_view(decode_tile(p, tile0));
+        for (int ct = 0; ct < p.tiles_c; ++ct, ++local) {
+          const int buf = (nbuf == 2) ? (local & 1) : 0;
+          const int use = (nbuf == 2) ? (local >> 1) : local;
+          if (ok && !mbar_wait(accf_bar(buf), static_cast<uint32_t>(use & 1), abort_flag, lim))
+            ok = false;
+          if (!ok) continue;
+          tc_fence_after();
+          const int cw = ct * 128 + q * 32;
+          const bool warp_live = cw < E.Cout;
+          const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                              static_cast<uint32_t>(buf * acc_cols);
+          for (int j0 = 32 * grp; j0 < Ncols; j0 += 64) {
+            uint32_t r[32];
+            tmem_ld32(tb + static_cast<uint32_t>(j0), r);
+            tmem_ld_wait();
+            if (warp_live) cm_norm_pass1(E, t, stage, lane, cw, j0, r, scr, Cs);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acce_bar(buf));
+        }
+        named_bar_sync(1, 256);
+        if (ok) {
+          for (int n = tid; n < Ncols; n += 256) {
+            int h, w;
+            const bool pv = cm_pixel(t, n, h, w) && n < t.npix && h < E.Ho && w < E.Wo;
+            den[n] = pv ? cm_norm_den(E, scr + (long long)n * Cs) : 1.0f;
+          }
+        }
+        named_bar_sync(1, 256);
+        if (ok) {
+          if (E.ndhwc)
+            cm_norm_pass2_ndhwc(E, t, tid, 256, Ncols, scr, Cs, den);
+          else
+            cm_norm_pass2_ncdhw(E, t, stage, lane, warp - kWarpEpi0, 8, Ncols, scr, Cs, den);
+        }
+        named_bar_sync(1, 256);
+      }
     }
   }
 
@@ -407,8 +487,8 @@ cudaError_t conv_cm_status_read_clear(int* status) {
 }
 
 cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
-                           const ConvCMParams& p, int grid, size_t smem_bytes,
-                           cudaStream_t stream) {
+                           const CUtensorMap& tmWgtLast, const ConvCMParams& p, int grid,
+                           size_t smem_bytes, cudaStream_t stream) {
   static size_t configured = 0;
   if (smem_bytes > configured) {
     cudaError_t err = cudaFuncSetAttribute(conv_cm_kernel,
@@ -417,7 +497,7 @@ cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
     if (err != cudaSuccess) return err;
     configured = smem_bytes;
   }
-  conv_cm_kernel<<<grid, 384, smem_bytes, stream>>>(tmAct, tmWgt, p);
+  conv_cm_kernel<<<grid, 384, smem_bytes, stream>>>(tmAct, tmWgt, tmWgtLast, p);
   return cudaGetLastError();
 }
 

@@ -136,16 +136,26 @@ __device__ __forceinline__ void epi_value16(const EpiParams& e, const Pixel& px,
 
 // value -> activated: normalized = B(value / den); scaled = B(normalized * sqrt(C));
 // affine = B(scaled * gamma); activated = B(affine / (1 + exp(-affine))).
+__device__ __forceinline__ float norm_silu1(float v, float den, float sqrt_c, float g) {
+  const float nrm = round_bf16(__fdiv_rn(v, den));
+  const float sc = round_bf16(__fmul_rn(nrm, sqrt_c));
+  const float af = round_bf16(__fmul_rn(sc, g));
+  const float ex = expf(-af);
+  return round_bf16(__fdiv_rn(af, __fadd_rn(1.0f, ex)));
+}
+
+// den = max(sqrt(sum of squares), 1e-12)
+__device__ __forceinline__ float norm_den(float ss) {
+  const float den = __fsqrt_rn(ss);
+  return (den > 1e-12f) ? den : 1e-12f;
+}
+
 __device__ __forceinline__ void epi_norm_silu16(const EpiParams& e, int c, int cnt, float den,
                                                 float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const float g = (i < cnt) ? __ldg(e.gamma + c + i) : 0.0f;
-    const float nrm = round_bf16(__fdiv_rn(v[i], den));
-    const float sc = round_bf16(__fmul_rn(nrm, e.sqrt_c));
-    const float af = round_bf16(__fmul_rn(sc, g));
-    const float ex = expf(-af);
-    v[i] = round_bf16(__fdiv_rn(af, __fadd_rn(1.0f, ex)));
+    v[i] = norm_silu1(v[i], den, e.sqrt_c, g);
   }
 }
 
@@ -194,8 +204,7 @@ __device__ __forceinline__ void epilogue_pixel(const EpiParams& e, const Pixel& 
       for (int i = 0; i < 16; ++i)
         if (i < cnt) ss = __fadd_rn(ss, __fmul_rn(v[i], v[i]));
     }
-    den = __fsqrt_rn(ss);
-    if (!(den > 1e-12f)) den = 1e-12f;
+    den = norm_den(ss);
   }
   for (int c = cb; c < ce; c += 16) {
     const int cnt = min(16, ce - c);

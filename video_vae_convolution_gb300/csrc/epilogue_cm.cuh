@@ -29,6 +29,8 @@ struct CmEpi {
   float* part;
   const float* bias;
   const float* rbias;
+  const float* gamma;
+  float sqrt_c;
   long long M_total;
 };
 
@@ -320,6 +322,202 @@ __device__ __forceinline__ void cm_block(const CmEpi& E, const CmTile& t, float 
     }
   }
   __syncwarp();
+}
+
+// ---- fused L2 norm over the channel row ---------------------------------------------
+//
+// The norm needs every output channel of a pixel, while a tile holds 128 of them.
+// All channel tiles of one pixel tile therefore run on the same CTA, one after
+// the other.  Pass 1 (once per channel tile) turns the accumulators into values
+// and keeps them as bf16 in the CTA's scratch rows (row n = tile pixel n, Cs =
+// Cout rounded up to 8 channels; the rows are rewritten for every pixel tile, so
+// they stay in L2).  After the last channel tile one thread per pixel sums
+// value^2 over the row serially in channel order (as the contract's fp32 sum;
+// the square of a bf16 value is exact in fp32), and pass 2 normalizes, scales,
+// applies gamma and SiLU, and stores y.
+
+// Residual element offset of (pixel (h, w) of the tile's plane, channel c).
+__device__ __forceinline__ long long cm_res_offset(const CmEpi& E, const CmTile& t, int h, int w,
+                                                   int c) {
+  if (E.ndhwc)
+    return ((((long long)t.nb * E.Do + t.od) * E.Ho + h) * E.Wo + w) * E.Cout + c;
+  return (((long long)t.nb * E.Cout + c) * E.Do + t.od) * ((long long)E.Ho * E.Wo) +
+         (long long)h * E.Wo + w;
+}
+
+// Pass 1 for one 32-channel x 32-pixel block (r[j] = accumulator of this lane's
+// channel cw + lane at tile pixel j0 + j).
+__device__ __forceinline__ void cm_norm_pass1(const CmEpi& E, const CmTile& t, float (*stage)[33],
+                                              int lane, int cw, int j0, const uint32_t (&r)[32],
+                                              uint16_t* scr, int Cs) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) stage[j][lane] = __uint_as_float(r[j]);
+  __syncwarp();
+  const int g = lane & 3;
+  const int c0 = cw + 8 * g;
+  const int cnt = min(8, E.Cout - c0);
+  const bool vec = (cnt == 8) && ((E.Cout & 7) == 0) && E.ndhwc;
+  for (int k = 0; k < 4; ++k) {
+    const int pl = 8 * k + (lane >> 2);
+    const int n = j0 + pl;
+    int h, w;
+    const bool in_tile = cm_pixel(t, n, h, w);
+    const bool pv = in_tile && n < t.npix && h < E.Ho && w < E.Wo && cnt > 0;
+    if (pv) {
+      uint16_t cb[8], vb[8];
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        cb[e] = bf16_bits(stage[pl][8 * g + e]);
+        v[e] = bf16_val(cb[e]);
+      }
+      if (E.flags & EPI_BIAS) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (e < cnt) v[e] = round_bf16(__fadd_rn(v[e], __ldg(E.bias + c0 + e)));
+      }
+      if (E.flags & EPI_RESIDUAL) {
+        const long long ro = cm_res_offset(E, t, h, w, c0);
+        float sk[8];
+        if (vec) {
+          unpack8(__ldg(reinterpret_cast<const uint4*>(E.res + ro)), sk);
+        } else {
+          const long long cstep = E.ndhwc ? 1 : (long long)E.Do * E.Ho * E.Wo;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) sk[e] = (e < cnt) ? bf16_val(E.res[ro + e * cstep]) : 0.0f;
+        }
+        if (E.flags & EPI_RESIDUAL_BIAS) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (e < cnt) sk[e] = round_bf16(__fadd_rn(sk[e], __ldg(E.rbias + c0 + e)));
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = round_bf16(__fadd_rn(v[e], sk[e]));
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) vb[e] = (e < cnt) ? bf16_bits(v[e]) : uint16_t(0);
+      *reinterpret_cast<uint4*>(scr + (long long)n * Cs + c0) = pack8(vb);
+      if (E.flags & EPI_DEBUG_STORE_CONV) {
+        const long long pix = (((long long)t.nb * E.Do + t.od) * E.Ho + h) * E.Wo + w;
+        for (int e = 0; e < cnt; ++e) E.conv[pix * E.Cout + c0 + e] = cb[e];
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// den of tile pixel n from its scratch row: serial fp32 sum in channel order.
+__device__ __forceinline__ float cm_norm_den(const CmEpi& E, const uint16_t* row) {
+  float ss = 0.0f;
+  const int full = E.Cout & ~7;
+#pragma unroll 2
+  for (int c = 0; c < full; c += 8) {
+    float v[8];
+    unpack8(*reinterpret_cast<const uint4*>(row + c), v);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = __fadd_rn(ss, __fmul_rn(v[e], v[e]));
+  }
+  for (int c = full; c < E.Cout; ++c) {
+    const float v = bf16_val(row[c]);
+    ss = __fadd_rn(ss, __fmul_rn(v, v));
+  }
+  return norm_den(ss);
+}
+
+// Pass 2, NDHWC output: units of (tile pixel, 8 channels) over the 256 epilogue
+// threads; consecutive threads take consecutive channel groups of a pixel.
+__device__ __forceinline__ void cm_norm_pass2_ndhwc(const CmEpi& E, const CmTile& t, int tid,
+                                                    int nthreads, int N, const uint16_t* scr,
+                                                    int Cs, const float* den) {
+  const int G = Cs / 8;
+  const int units = N * G;
+  const long long nd = (long long)t.nb * E.Do + t.od;
+  const bool vec = (E.Cout & 7) == 0;
+  for (int u = tid; u < units; u += nthreads) {
+    const int n = u / G;
+    const int c0 = 8 * (u - n * G);
+    int h, w;
+    const bool in_tile = cm_pixel(t, n, h, w);
+    if (!in_tile || n >= t.npix || h >= E.Ho || w >= E.Wo) continue;
+    const int cnt = min(8, E.Cout - c0);
+    const uint4 raw = *reinterpret_cast<const uint4*>(scr + (long long)n * Cs + c0);
+    float v[8];
+    unpack8(raw, v);
+    const long long o = ((nd * E.Ho + h) * E.Wo + w) * E.Cout + c0;
+    const float dn = den[n];
+    uint16_t yb[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float gm = (e < cnt) ? __ldg(E.gamma + c0 + e) : 0.0f;
+      yb[e] = bf16_bits(norm_silu1(v[e], dn, E.sqrt_c, gm));
+    }
+    if (vec) {
+      if (E.flags & EPI_SAVE_VALUE) reinterpret_cast<uint4*>(E.val + o)[0] = raw;
+      reinterpret_cast<uint4*>(E.y + o)[0] = pack8(yb);
+    } else {
+      const uint32_t rw[4] = {raw.x, raw.y, raw.z, raw.w};
+      for (int e = 0; e < cnt; ++e) {
+        if (E.flags & EPI_SAVE_VALUE)
+          E.val[o + e] = static_cast<uint16_t>((rw[e >> 1] >> (16 * (e & 1))) & 0xFFFFu);
+        E.y[o + e] = yb[e];
+      }
+    }
+  }
+}
+
+// Pass 2, NCDHW output: 32-pixel x 32-channel blocks per warp, transposed in the
+// warp's staging block so that each store covers consecutive pixels of a channel.
+__device__ __forceinline__ void cm_norm_pass2_ncdhw(const CmEpi& E, const CmTile& t,
+                                                    float (*stage)[33], int lane, int warp_e,
+                                                    int nwarps, int N, const uint16_t* scr,
+                                                    int Cs, const float* den) {
+  const int nbn = (N + 31) / 32, nbc = (E.Cout + 31) / 32;
+  const long long plane = (long long)E.Ho * E.Wo;
+  const long long cstep = (long long)E.Do * plane;
+  const int g = lane & 3;
+  for (int blk = warp_e; blk < nbn * nbc; blk += nwarps) {
+    const int bn = blk / nbc;
+    const int n0 = 32 * bn, c0 = 32 * (blk - bn * nbc);
+    const int cg = c0 + 8 * g;
+    for (int k = 0; k < 4; ++k) {
+      const int pl = 8 * k + (lane >> 2);
+      const int n = n0 + pl;
+      float y8[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y8[e] = 0.0f;
+      if (n < N && cg < E.Cout) {
+        const int cnt = min(8, E.Cout - cg);
+        const uint4 raw = *reinterpret_cast<const uint4*>(scr + (long long)n * Cs + cg);
+        float v[8];
+        unpack8(raw, v);
+        const float dn = den[n];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float gm = (e < cnt) ? __ldg(E.gamma + cg + e) : 0.0f;
+          y8[e] = norm_silu1(v[e], dn, E.sqrt_c, gm);
+        }
+        int h, w;
+        const bool in_tile = cm_pixel(t, n, h, w);
+        if ((E.flags & EPI_SAVE_VALUE) && in_tile && n < t.npix && h < E.Ho && w < E.Wo) {
+          const long long o = cm_res_offset(E, t, h, w, cg);
+          for (int e = 0; e < cnt; ++e) E.val[o + e * cstep] = bf16_bits(v[e]);
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) stage[pl][8 * g + e] = y8[e];
+    }
+    __syncwarp();
+    // lane = pixel n0 + lane: for each channel the warp stores 32 consecutive pixels
+    const int n = n0 + lane;
+    int h, w;
+    const bool in_tile = cm_pixel(t, n, h, w);
+    if (n < N && in_tile && n < t.npix && h < E.Ho && w < E.Wo) {
+      const long long o = cm_res_offset(E, t, h, w, c0);
+      const int cend = min(32, E.Cout - c0);
+      for (int c = 0; c < cend; ++c) E.y[o + c * cstep] = bf16_bits(stage[lane][c]);
+    }
+    __syncwarp();
+  }
 }
 
 }  // namespace vvc

@@ -92,6 +92,8 @@ struct ConvCMParams {
   uint32_t act_bytes, stage_bytes, bar_off, tx_bytes;
   uint32_t epi_off;        // per-warp [32][33] fp32 epilogue staging blocks
   int wgt_rows;            // weight box rows loaded per tap (<= 128; the MMA reads 128)
+  int wgt_rows_last;       // the same for the last 128-channel tile (its own tensor map)
+  uint32_t tx_bytes_last;  // bytes one stage of the last channel tile delivers
   int stages_total, k_splits, stages_per_split;
   int tiles_w, tiles_h, tiles_c;  // pixel tiles along W / H, 128-channel tiles
   int num_tiles;
@@ -101,6 +103,12 @@ struct ConvCMParams {
   unsigned long long timeout_ns;
   float* partial;          // [k_splits][M][Cout] fp32 when k_splits > 1
   long long M_total;
+  // fused L2 norm (k_splits == 1): the tiles_c channel tiles of a pixel tile run on
+  // one CTA (tpu consecutive tiles per unit; tpu = 1 otherwise)
+  int norm, tpu;
+  uint32_t norm_off;       // shared den[N] (fp32) of the current pixel tile
+  int norm_cs;             // channels per scratch row: Cout rounded up to 8
+  uint16_t* vscratch;      // [grid][N][norm_cs] bf16 values, one slice per CTA
 };
 
 }  // namespace vvc

@@ -68,6 +68,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Barrier among `count` threads (a multiple of 32) on hardware barrier `id` (1..15).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---- proxy fences ------------------------------------------------------------------
 // Makes generic-proxy shared-memory writes visible to the async proxy (TMA/MMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
