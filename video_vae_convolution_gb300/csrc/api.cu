@@ -348,6 +348,7 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
       return CONV3D_ERR_UNSUPPORTED;
     k.tx_bytes = static_cast<uint32_t>(closed);
     k.tx_bytes_last = static_cast<uint32_t>(closed_last);
+    k.act_tx = static_cast<uint32_t>(act_part);
     // every loaded row must land inside the stage's activation / weight regions
     if ((long long)((runs - 1) * k.run_pitch + k.nbox * k.box_w) * k.row_bytes > k.act_bytes)
       return CONV3D_ERR_UNSUPPORTED;

@@ -42,6 +42,7 @@ namespace {
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMMA = 1;
 constexpr int kWarpPatch = 2;
+constexpr int kWarpWgt = 3;
 constexpr int kWarpEpi0 = 4;
 
 struct TileCoord {
@@ -80,6 +81,20 @@ __device__ __forceinline__ StageCoord decode_stage(const ConvCMParams& p, int it
   c.r = rest % p.KR;
   c.t = rest / p.KR;
   return c;
+}
+
+// Stage after c, in the order decode_stage numbers them (no divisions: the
+// issuing threads sit on the load-latency path).
+__device__ __forceinline__ void next_stage(const ConvCMParams& p, StageCoord& c) {
+  if (++c.ch < p.n_chunks) return;
+  c.ch = 0;
+  if (!p.halo) {
+    if (++c.sblk < p.KS) return;
+    c.sblk = 0;
+  }
+  if (++c.r < p.KR) return;
+  c.r = 0;
+  ++c.t;
 }
 
 __device__ __forceinline__ void stage_range(const ConvCMParams& p, int split, int& b, int& e) {
@@ -123,7 +138,7 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 2);  // activation and weight producers
       mbar_init(empty_bar(s), 1);
       mbar_init(ready_bar(s), 1);
     }
@@ -148,7 +163,10 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem_base = *tmem_slot;
   const unsigned long long lim = p.timeout_ns;
 
-  if (warp == kWarpProducer) {
+  if (warp == kWarpProducer || warp == kWarpWgt) {
+    // Two producers issue each stage in parallel, each after its own wait on the
+    // slot: warp 0 the activation runs, warp 3 the weight boxes.
+    const bool act_role = warp == kWarpProducer;
     if (lane == 0) {
       int slot = 0;
       uint32_t phase = 0;
@@ -163,15 +181,16 @@ __global__ void __launch_bounds__(384, 1)
         // the last channel tile loads only its real weight rows, through its own map
         const bool last_ct = tc.ct == p.tiles_c - 1;
         const CUtensorMap* wmap = last_ct ? &tmWgtLast : &tmWgt;
-        const uint32_t tx = last_ct ? p.tx_bytes_last : p.tx_bytes;
+        const uint32_t tx = act_role ? p.act_tx
+                                     : (last_ct ? p.tx_bytes_last : p.tx_bytes) - p.act_tx;
         int it_b, it_e;
         stage_range(p, tc.split, it_b, it_e);
-        for (int it = it_b; it < it_e; ++it) {
+        StageCoord sc = decode_stage(p, it_b);
+        for (int it = it_b; it < it_e; ++it, next_stage(p, sc)) {
           if (!mbar_wait(empty_bar(slot), phase ^ 1u, abort_flag, lim)) {
             ok = false;
             break;
           }
-          const StageCoord sc = decode_stage(p, it);
           const bool skip = (p.inject > 0 && k_global == p.inject - 1);
           if (!skip) {
             const uint32_t full = full_bar(slot);
@@ -179,7 +198,14 @@ __global__ void __launch_bounds__(384, 1)
             const uint32_t act = sbase + p.stage_bytes * slot;
             const uint32_t wgt = act + p.act_bytes;
             const int d_in = tc.od * p.st + sc.t - p.pt;
-            if (p.flat) {
+            if (!act_role) {
+              for (int tl = 0; tl < p.taps_per_stage; ++tl) {
+                const int s = p.halo ? tl : sc.sblk;
+                const int tap = (sc.t * p.KR + sc.r) * p.KS + s;
+                tma_load_2d(wgt + static_cast<uint32_t>(tl * 128 * p.row_bytes), wmap, full,
+                            tap * p.cp64 + sc.ch * p.kc, c0);
+              }
+            } else if (p.flat) {
               // flattened (H*W) positions: output q reads input q + (r - ph) * W + s
               const int q_start = w0 + (sc.r - p.ph) * p.W;
               for (int b = 0; b < p.nbox; ++b)
@@ -199,12 +225,6 @@ __global__ void __launch_bounds__(384, 1)
                               &tmAct, full, sc.ch * p.kc, w_start + b * p.box_w, h_in, d_in,
                               tc.nb);
               }
-            }
-            for (int tl = 0; tl < p.taps_per_stage; ++tl) {
-              const int s = p.halo ? tl : sc.sblk;
-              const int tap = (sc.t * p.KR + sc.r) * p.KS + s;
-              tma_load_2d(wgt + static_cast<uint32_t>(tl * 128 * p.row_bytes), wmap, full,
-                          tap * p.cp64 + sc.ch * p.kc, c0);
             }
           } else {
             k_skip = k_global;
@@ -255,7 +275,8 @@ __global__ void __launch_bounds__(384, 1)
         int it_b, it_e;
         stage_range(p, tc.split, it_b, it_e);
         uint32_t acc = 0u;
-        for (int it = it_b; it < it_e; ++it) {
+        int ch = it_b % p.n_chunks;
+        for (int it = it_b; it < it_e; ++it, ch = (ch + 1 == p.n_chunks) ? 0 : ch + 1) {
           const uint32_t bar = p.reflect_w ? ready_bar(slot) : full_bar(slot);
           if (!mbar_wait(bar, phase, abort_flag, lim)) {
             ok = false;
@@ -264,7 +285,7 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
           // K steps of 16 channels that hold real channels: the rest of a
           // chunk beyond C is zero-filled by TMA and contributes nothing.
-          const int kk_n = (min(p.kc, p.C - (it % p.n_chunks) * p.kc) + 15) / 16;
+          const int kk_n = (min(p.kc, p.C - ch * p.kc) + 15) / 16;
           const uint32_t act = sbase + p.stage_bytes * slot;
           const uint32_t b_lo = desc_lo0 + (act >> 4);
           const uint32_t a_lo = desc_lo0 + ((act + p.act_bytes) >> 4);
@@ -310,12 +331,12 @@ __global__ void __launch_bounds__(384, 1)
         const int w0 = tc.twi * p.tw;
         int it_b, it_e;
         stage_range(p, tc.split, it_b, it_e);
-        for (int it = it_b; it < it_e; ++it) {
+        StageCoord sc = decode_stage(p, it_b);
+        for (int it = it_b; it < it_e; ++it, next_stage(p, sc)) {
           if (!mbar_wait(full_bar(slot), phase, abort_flag, lim)) {
             ok = false;
             break;
           }
-          const StageCoord sc = decode_stage(p, it);
           const int w_start = p.halo ? (w0 - p.pw) : (w0 * p.sw + sc.sblk - p.pw);
           int e_left = -1, e_right = -1;
           if (w_start <= -1 && ((-1 - w_start) % es) == 0) {

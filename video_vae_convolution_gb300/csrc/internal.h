@@ -94,6 +94,7 @@ struct ConvCMParams {
   int wgt_rows;            // weight box rows loaded per tap (<= 128; the MMA reads 128)
   int wgt_rows_last;       // the same for the last 128-channel tile (its own tensor map)
   uint32_t tx_bytes_last;  // bytes one stage of the last channel tile delivers
+  uint32_t act_tx;         // activation bytes of one stage (part of both totals)
   int stages_total, k_splits, stages_per_split;
   int tiles_w, tiles_h, tiles_c;  // pixel tiles along W / H, 128-channel tiles
   int num_tiles;
