@@ -308,7 +308,7 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.act_bytes = static_cast<uint32_t>(round_up(round_up(act_rows, 8) * k.row_bytes, 1024));
   const uint32_t wgt_bytes = static_cast<uint32_t>(k.taps_per_stage * 128 * k.row_bytes);
   k.stage_bytes = k.act_bytes + wgt_bytes;
-  constexpr size_t kEpiStage = 8 * 32 * 33 * 4;  // per-warp transpose blocks
+  constexpr size_t kEpiStage = 8 * 32 * 36 * 4;  // per-warp transpose blocks (kStageFloats)
   k.tiles_c = static_cast<int>(cdiv(p->Cout, 128));
   // fused L2 norm: den[N] in shared memory
   const bool norm = (p->epi & CONV3D_EPI_L2NORM_SILU) != 0;

@@ -393,8 +393,7 @@ __global__ void __launch_bounds__(384, 1)
     E.gamma = p.epi.gamma;
     E.sqrt_c = p.epi.sqrt_c;
     E.M_total = p.M_total;
-    float(*stage)[33] =
-        reinterpret_cast<float(*)[33]>(smem + p.epi_off + (warp - kWarpEpi0) * (32 * 33 * 4));
+    float* st = reinterpret_cast<float*>(smem + p.epi_off) + (warp - kWarpEpi0) * kStageFloats;
     const int nbuf = p.nbuf, acc_cols = p.acc_cols, Ncols = p.N;
     auto tile_view = [&](const TileCoord& tc) {
       CmTile t;
@@ -407,6 +406,10 @@ __global__ void __launch_bounds__(384, 1)
       t.flat = p.flat;
       t.pitch = p.flat ? p.W : p.run_pitch;
       t.npix = p.flat ? p.tw : p.rh * p.run_pitch;
+      t.q0 = p.flat ? t.w0 : 0;
+      t.hoff = p.flat ? 0 : t.h0;
+      t.woff = p.flat ? 0 : t.w0;
+      t.jlim = p.flat ? p.W : p.tw;
       return t;
     };
     if (!p.norm) {
@@ -421,13 +424,14 @@ __global__ void __launch_bounds__(384, 1)
         const CmTile t = tile_view(tc);
         const int cw = tc.ct * 128 + q * 32;  // first channel of this warp's TMEM lanes
         const bool warp_live = cw < E.Cout;
+        const CmChan ch = cm_chan(E, cw, lane);
         const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                             static_cast<uint32_t>(buf * acc_cols);
         for (int j0 = 32 * grp; j0 < Ncols; j0 += 64) {
           uint32_t r[32];
           tmem_ld32(tb + static_cast<uint32_t>(j0), r);
           tmem_ld_wait();
-          if (warp_live) cm_block(E, t, stage, lane, cw, j0, r);
+          if (warp_live) cm_block(E, t, st, lane, cw, j0, r, ch);
         }
         tc_fence_before();
         __syncwarp();
@@ -456,13 +460,14 @@ __global__ void __launch_bounds__(384, 1)
           tc_fence_after();
           const int cw = ct * 128 + q * 32;
           const bool warp_live = cw < E.Cout;
+          const CmChan ch = cm_chan(E, cw, lane);
           const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(buf * acc_cols);
           for (int j0 = 32 * grp; j0 < Ncols; j0 += 64) {
             uint32_t r[32];
             tmem_ld32(tb + static_cast<uint32_t>(j0), r);
             tmem_ld_wait();
-            if (warp_live) cm_norm_pass1(E, t, stage, lane, cw, j0, r, scr, Cs);
+            if (warp_live) cm_norm_pass1(E, t, st, lane, j0, r, scr, Cs, ch);
           }
           tc_fence_before();
           __syncwarp();
@@ -481,7 +486,7 @@ __global__ void __launch_bounds__(384, 1)
           if (E.ndhwc)
             cm_norm_pass2_ndhwc(E, t, tid, 256, Ncols, scr, Cs, den);
           else
-            cm_norm_pass2_ncdhw(E, t, stage, lane, warp - kWarpEpi0, 8, Ncols, scr, Cs, den);
+            cm_norm_pass2_ncdhw(E, t, st, lane, warp - kWarpEpi0, 8, Ncols, scr, Cs, den);
         }
         named_bar_sync(1, 256);
       }

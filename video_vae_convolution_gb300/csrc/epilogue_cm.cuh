@@ -9,6 +9,11 @@
 // that are contiguous in the output: 8 channels of one pixel for NDHWC output
 // (16-byte loads and stores, coalesced across the warp) or 8 pixels of one
 // channel for NCDHW output.
+//
+// Layers with little reduction work per output element (narrow input, 96
+// channels) are bound by this code, so the per-unit work is kept short: one
+// division per block for the pixel positions, the thread's bias values held in
+// registers for the whole tile, 16-byte shared-memory reads.
 #pragma once
 
 #include <cstdint>
@@ -41,7 +46,77 @@ struct CmTile {
   // otherwise pixel n is output row h0 + n / pitch, column w0 + n % pitch, and only
   // columns n % pitch < tw belong to the tile (the rest are halo rows of a run)
   int flat, pitch;
+  // the same as a row/column split of q = q0 + n by pitch: output row hoff + q / pitch,
+  // column woff + q % pitch, in the tile while the column index is below jlim
+  int q0, hoff, woff, jlim;
 };
+
+// Per-warp staging block: 32 rows (pixels) of 32 channels, fp32.  Rows are
+// kStageVec floats apart where a thread reads 8 channels of a pixel as two
+// 16-byte words, kStageScalar floats apart where threads read along a row.
+constexpr int kStageVec = 36;
+constexpr int kStageScalar = 33;
+constexpr int kStageFloats = 32 * kStageVec;  // per warp
+
+// The 8 output channels [c0, c0 + cnt) of one epilogue thread in the NDHWC units
+// (lanes 4k + g share a pixel; g = lane & 3), with their bias and residual bias.
+struct CmChan {
+  int c0, cnt;
+  float b[8], rb[8];
+};
+
+__device__ __forceinline__ CmChan cm_chan(const CmEpi& E, int cw, int lane) {
+  CmChan c;
+  c.c0 = cw + 8 * (lane & 3);
+  c.cnt = min(8, E.Cout - c.c0);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const bool in = e < c.cnt;
+    c.b[e] = ((E.flags & EPI_BIAS) && in) ? __ldg(E.bias + c.c0 + e) : 0.0f;
+    c.rb[e] = ((E.flags & EPI_RESIDUAL_BIAS) && in) ? __ldg(E.rbias + c.c0 + e) : 0.0f;
+  }
+  return c;
+}
+
+// Row / column of tile pixel j0 + pl from the block origin (ib, jb) of pixel j0;
+// true when the pixel belongs to the tile and lies inside the output.
+__device__ __forceinline__ bool cm_unit_pos(const CmEpi& E, const CmTile& t, int ib, int jb,
+                                            int j0, int pl, int& h, int& w) {
+  int i = ib, j = jb + pl;
+  while (j >= t.pitch) {
+    j -= t.pitch;
+    ++i;
+  }
+  h = t.hoff + i;
+  w = t.woff + j;
+  return j < t.jlim && j0 + pl < t.npix && h < E.Ho && w < E.Wo;
+}
+
+// value = B(B(B(acc) + bias) + B(res + rbias)) for the 8 channels of a unit;
+// conv bits kept for the debug store.  `res_at(e)` gives the residual element.
+template <class Res>
+__device__ __forceinline__ void cm_value8(const CmEpi& E, const CmChan& ch, const float (&a)[8],
+                                          uint16_t (&cb)[8], float (&v)[8], Res&& res8) {
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    cb[e] = bf16_bits(a[e]);
+    v[e] = bf16_val(cb[e]);
+  }
+  if (E.flags & EPI_BIAS) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = round_bf16(__fadd_rn(v[e], ch.b[e]));
+  }
+  if (E.flags & EPI_RESIDUAL) {
+    float sk[8];
+    res8(sk);
+    if (E.flags & EPI_RESIDUAL_BIAS) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sk[e] = round_bf16(__fadd_rn(sk[e], ch.rb[e]));
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = round_bf16(__fadd_rn(v[e], sk[e]));
+  }
+}
 
 // Output coordinates of tile pixel n; false when n is not one of the tile's pixels.
 // The caller still checks h < Ho and w < Wo.
@@ -83,80 +158,80 @@ __device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
   }
 }
 
-// 8 channels [c0, c0 + cnt) of one pixel, NDHWC addressing.
-__device__ __forceinline__ void cm_unit_ndhwc(const CmEpi& E, const CmTile& t, int n, int c0,
-                                              int cnt, const float (&a)[8]) {
-  int h, w;
-  const bool in_tile = cm_pixel(t, n, h, w);
-  if (!in_tile || n >= t.npix || h >= E.Ho || w >= E.Wo || cnt <= 0) return;
+// NDHWC output (or split partial sums) for one 32-channel x 32-pixel block staged
+// at st (rows kStageVec apart): unit = (pixel, the thread's 8 channels).
+__device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, const float* st,
+                                               int lane, const CmChan& ch, int j0) {
+  const int q = t.q0 + j0;
+  const int ib = q / t.pitch;
+  const int jb = q - ib * t.pitch;
   const long long nd = (long long)t.nb * E.Do + t.od;
-  const long long pix = (nd * E.Ho + h) * E.Wo + w;
-  const bool vec = (cnt == 8) && ((E.Cout & 7) == 0);
-  if (E.split) {
-    float* dst = E.part + ((long long)t.split * E.M_total + pix) * E.Cout + c0;
+  const bool vec = (ch.cnt == 8) && ((E.Cout & 7) == 0);
+  const int g = lane & 3;
+  for (int k = 0; k < 4; ++k) {
+    const int pl = 8 * k + (lane >> 2);
+    int h, w;
+    if (ch.cnt <= 0 || !cm_unit_pos(E, t, ib, jb, j0, pl, h, w)) continue;
+    float a[8];
+    {
+      const float4 lo = *reinterpret_cast<const float4*>(st + pl * kStageVec + 8 * g);
+      const float4 hi = *reinterpret_cast<const float4*>(st + pl * kStageVec + 8 * g + 4);
+      a[0] = lo.x; a[1] = lo.y; a[2] = lo.z; a[3] = lo.w;
+      a[4] = hi.x; a[5] = hi.y; a[6] = hi.z; a[7] = hi.w;
+    }
+    const long long pix = (nd * E.Ho + h) * E.Wo + w;
+    if (E.split) {
+      float* dst = E.part + ((long long)t.split * E.M_total + pix) * E.Cout + ch.c0;
+      if (vec) {
+        reinterpret_cast<float4*>(dst)[0] = make_float4(a[0], a[1], a[2], a[3]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(a[4], a[5], a[6], a[7]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (e < ch.cnt) dst[e] = a[e];
+      }
+      continue;
+    }
+    const long long ou = pix * E.Cout + ch.c0;
+    uint16_t cb[8];
+    float v[8];
+    cm_value8(E, ch, a, cb, v, [&](float (&sk)[8]) {
+      if (vec) {
+        unpack8(__ldg(reinterpret_cast<const uint4*>(E.res + ou)), sk);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sk[e] = (e < ch.cnt) ? bf16_val(E.res[ou + e]) : 0.0f;
+      }
+    });
+    uint16_t vb[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vb[e] = bf16_bits(v[e]);
+    const long long yo = ((nd * E.Hy + h) * E.Wy + w) * E.Cout + ch.c0;
     if (vec) {
-      reinterpret_cast<float4*>(dst)[0] = make_float4(a[0], a[1], a[2], a[3]);
-      reinterpret_cast<float4*>(dst)[1] = make_float4(a[4], a[5], a[6], a[7]);
-    } else {
-      for (int e = 0; e < cnt; ++e) dst[e] = a[e];
-    }
-    return;
-  }
-  uint16_t cb[8];
-  float v[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    cb[e] = bf16_bits(a[e]);
-    v[e] = bf16_val(cb[e]);
-  }
-  if (E.flags & EPI_BIAS) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e)
-      if (e < cnt) v[e] = round_bf16(__fadd_rn(v[e], __ldg(E.bias + c0 + e)));
-  }
-  const long long ou = pix * E.Cout + c0;
-  if (E.flags & EPI_RESIDUAL) {
-    float sk[8];
-    if (vec) {
-      unpack8(__ldg(reinterpret_cast<const uint4*>(E.res + ou)), sk);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sk[e] = (e < cnt) ? bf16_val(E.res[ou + e]) : 0.0f;
-    }
-    if (E.flags & EPI_RESIDUAL_BIAS) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (e < cnt) sk[e] = round_bf16(__fadd_rn(sk[e], __ldg(E.rbias + c0 + e)));
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = round_bf16(__fadd_rn(v[e], sk[e]));
-  }
-  uint16_t vb[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) vb[e] = bf16_bits(v[e]);
-  const long long yo = ((nd * E.Hy + h) * E.Wy + w) * E.Cout + c0;
-  if (vec) {
-    const uint4 pv = pack8(vb);
-    reinterpret_cast<uint4*>(E.y + yo)[0] = pv;
-    if (E.flags & EPI_SAVE_VALUE) reinterpret_cast<uint4*>(E.val + ou)[0] = pv;
-    if (E.flags & EPI_DEBUG_STORE_CONV) reinterpret_cast<uint4*>(E.conv + ou)[0] = pack8(cb);
-    if (E.pad) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      const long long sw_ = E.Cout, sh_ = (long long)E.Wy * E.Cout;
-      if (w == E.Wo - 1) reinterpret_cast<uint4*>(E.y + yo + sw_)[0] = z;
-      if (h == E.Ho - 1) reinterpret_cast<uint4*>(E.y + yo + sh_)[0] = z;
-      if (w == E.Wo - 1 && h == E.Ho - 1) reinterpret_cast<uint4*>(E.y + yo + sh_ + sw_)[0] = z;
-    }
-  } else {
-    for (int e = 0; e < cnt; ++e) {
-      E.y[yo + e] = vb[e];
-      if (E.flags & EPI_SAVE_VALUE) E.val[ou + e] = vb[e];
-      if (E.flags & EPI_DEBUG_STORE_CONV) E.conv[ou + e] = cb[e];
+      const uint4 pv = pack8(vb);
+      reinterpret_cast<uint4*>(E.y + yo)[0] = pv;
+      if (E.flags & EPI_SAVE_VALUE) reinterpret_cast<uint4*>(E.val + ou)[0] = pv;
+      if (E.flags & EPI_DEBUG_STORE_CONV) reinterpret_cast<uint4*>(E.conv + ou)[0] = pack8(cb);
       if (E.pad) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
         const long long sw_ = E.Cout, sh_ = (long long)E.Wy * E.Cout;
-        if (w == E.Wo - 1) E.y[yo + e + sw_] = 0;
-        if (h == E.Ho - 1) E.y[yo + e + sh_] = 0;
-        if (w == E.Wo - 1 && h == E.Ho - 1) E.y[yo + e + sh_ + sw_] = 0;
+        if (w == E.Wo - 1) reinterpret_cast<uint4*>(E.y + yo + sw_)[0] = z;
+        if (h == E.Ho - 1) reinterpret_cast<uint4*>(E.y + yo + sh_)[0] = z;
+        if (w == E.Wo - 1 && h == E.Ho - 1) reinterpret_cast<uint4*>(E.y + yo + sh_ + sw_)[0] = z;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (e >= ch.cnt) continue;
+        E.y[yo + e] = vb[e];
+        if (E.flags & EPI_SAVE_VALUE) E.val[ou + e] = vb[e];
+        if (E.flags & EPI_DEBUG_STORE_CONV) E.conv[ou + e] = cb[e];
+        if (E.pad) {
+          const long long sw_ = E.Cout, sh_ = (long long)E.Wy * E.Cout;
+          if (w == E.Wo - 1) E.y[yo + e + sw_] = 0;
+          if (h == E.Ho - 1) E.y[yo + e + sh_] = 0;
+          if (w == E.Wo - 1 && h == E.Ho - 1) E.y[yo + e + sh_ + sw_] = 0;
+        }
       }
     }
   }
@@ -233,25 +308,20 @@ __device__ __forceinline__ void cm_unit_ncdhw(const CmEpi& E, const CmTile& t, i
 }
 
 // One 32-channel x 32-pixel block: r[j] = accumulator of this lane's channel for
-// tile pixel j0 + j.  `stage` is this warp's [32][33] fp32 shared buffer.
-__device__ __forceinline__ void cm_block(const CmEpi& E, const CmTile& t, float (*stage)[33],
-                                         int lane, int cw, int j0, const uint32_t (&r)[32]) {
-#pragma unroll
-  for (int j = 0; j < 32; ++j) stage[j][lane] = __uint_as_float(r[j]);
-  __syncwarp();
+// tile pixel j0 + j.  `st` is this warp's staging block (kStageFloats floats).
+__device__ __forceinline__ void cm_block(const CmEpi& E, const CmTile& t, float* st, int lane,
+                                         int cw, int j0, const uint32_t (&r)[32],
+                                         const CmChan& ch) {
   if (E.ndhwc || E.split) {
-    // unit = (pixel, 8-channel group): lanes 4k..4k+3 share a pixel
-    const int g = lane & 3;
-    const int c0 = cw + 8 * g;
-    const int cnt = min(8, E.Cout - c0);
-    for (int k = 0; k < 4; ++k) {
-      const int pl = 8 * k + (lane >> 2);
-      float a[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) a[e] = stage[pl][8 * g + e];
-      cm_unit_ndhwc(E, t, j0 + pl, c0, cnt, a);
-    }
+    for (int j = 0; j < 32; ++j) st[j * kStageVec + lane] = __uint_as_float(r[j]);
+    __syncwarp();
+    cm_block_ndhwc(E, t, st, lane, ch, j0);
   } else {
+    float(*stage)[kStageScalar] = reinterpret_cast<float(*)[kStageScalar]>(st);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) stage[j][lane] = __uint_as_float(r[j]);
+    __syncwarp();
     int h0, w0;
     cm_pixel(t, j0, h0, w0);
     const bool row_aligned = cm_same_row(t, j0, 32) && (w0 & 7) == 0 && (E.Wo & 7) == 0;
@@ -347,60 +417,49 @@ __device__ __forceinline__ long long cm_res_offset(const CmEpi& E, const CmTile&
 
 // Pass 1 for one 32-channel x 32-pixel block (r[j] = accumulator of this lane's
 // channel cw + lane at tile pixel j0 + j).
-__device__ __forceinline__ void cm_norm_pass1(const CmEpi& E, const CmTile& t, float (*stage)[33],
-                                              int lane, int cw, int j0, const uint32_t (&r)[32],
-                                              uint16_t* scr, int Cs) {
+__device__ __forceinline__ void cm_norm_pass1(const CmEpi& E, const CmTile& t, float* st, int lane,
+                                              int j0, const uint32_t (&r)[32], uint16_t* scr,
+                                              int Cs, const CmChan& ch) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) stage[j][lane] = __uint_as_float(r[j]);
+  for (int j = 0; j < 32; ++j) st[j * kStageVec + lane] = __uint_as_float(r[j]);
   __syncwarp();
+  const int q = t.q0 + j0;
+  const int ib = q / t.pitch;
+  const int jb = q - ib * t.pitch;
   const int g = lane & 3;
-  const int c0 = cw + 8 * g;
-  const int cnt = min(8, E.Cout - c0);
-  const bool vec = (cnt == 8) && ((E.Cout & 7) == 0) && E.ndhwc;
+  const bool vec = (ch.cnt == 8) && ((E.Cout & 7) == 0) && E.ndhwc;
+  const long long cstep = E.ndhwc ? 1 : (long long)E.Do * E.Ho * E.Wo;
   for (int k = 0; k < 4; ++k) {
     const int pl = 8 * k + (lane >> 2);
     const int n = j0 + pl;
     int h, w;
-    const bool in_tile = cm_pixel(t, n, h, w);
-    const bool pv = in_tile && n < t.npix && h < E.Ho && w < E.Wo && cnt > 0;
-    if (pv) {
-      uint16_t cb[8], vb[8];
-      float v[8];
+    if (ch.cnt <= 0 || !cm_unit_pos(E, t, ib, jb, j0, pl, h, w)) continue;
+    float a[8];
+    {
+      const float4 lo = *reinterpret_cast<const float4*>(st + pl * kStageVec + 8 * g);
+      const float4 hi = *reinterpret_cast<const float4*>(st + pl * kStageVec + 8 * g + 4);
+      a[0] = lo.x; a[1] = lo.y; a[2] = lo.z; a[3] = lo.w;
+      a[4] = hi.x; a[5] = hi.y; a[6] = hi.z; a[7] = hi.w;
+    }
+    uint16_t cb[8], vb[8];
+    float v[8];
+    cm_value8(E, ch, a, cb, v, [&](float (&sk)[8]) {
+      const long long ro = cm_res_offset(E, t, h, w, ch.c0);
+      if (vec) {
+        unpack8(__ldg(reinterpret_cast<const uint4*>(E.res + ro)), sk);
+      } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        cb[e] = bf16_bits(stage[pl][8 * g + e]);
-        v[e] = bf16_val(cb[e]);
+        for (int e = 0; e < 8; ++e) sk[e] = (e < ch.cnt) ? bf16_val(E.res[ro + e * cstep]) : 0.0f;
       }
-      if (E.flags & EPI_BIAS) {
+    });
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (e < cnt) v[e] = round_bf16(__fadd_rn(v[e], __ldg(E.bias + c0 + e)));
-      }
-      if (E.flags & EPI_RESIDUAL) {
-        const long long ro = cm_res_offset(E, t, h, w, c0);
-        float sk[8];
-        if (vec) {
-          unpack8(__ldg(reinterpret_cast<const uint4*>(E.res + ro)), sk);
-        } else {
-          const long long cstep = E.ndhwc ? 1 : (long long)E.Do * E.Ho * E.Wo;
+    for (int e = 0; e < 8; ++e) vb[e] = (e < ch.cnt) ? bf16_bits(v[e]) : uint16_t(0);
+    *reinterpret_cast<uint4*>(scr + (long long)n * Cs + ch.c0) = pack8(vb);
+    if (E.flags & EPI_DEBUG_STORE_CONV) {
+      const long long pix = (((long long)t.nb * E.Do + t.od) * E.Ho + h) * E.Wo + w;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) sk[e] = (e < cnt) ? bf16_val(E.res[ro + e * cstep]) : 0.0f;
-        }
-        if (E.flags & EPI_RESIDUAL_BIAS) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (e < cnt) sk[e] = round_bf16(__fadd_rn(sk[e], __ldg(E.rbias + c0 + e)));
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = round_bf16(__fadd_rn(v[e], sk[e]));
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) vb[e] = (e < cnt) ? bf16_bits(v[e]) : uint16_t(0);
-      *reinterpret_cast<uint4*>(scr + (long long)n * Cs + c0) = pack8(vb);
-      if (E.flags & EPI_DEBUG_STORE_CONV) {
-        const long long pix = (((long long)t.nb * E.Do + t.od) * E.Ho + h) * E.Wo + w;
-        for (int e = 0; e < cnt; ++e) E.conv[pix * E.Cout + c0 + e] = cb[e];
-      }
+      for (int e = 0; e < 8; ++e)
+        if (e < ch.cnt) E.conv[pix * E.Cout + ch.c0 + e] = cb[e];
     }
   }
   __syncwarp();
@@ -467,10 +526,11 @@ __device__ __forceinline__ void cm_norm_pass2_ndhwc(const CmEpi& E, const CmTile
 
 // Pass 2, NCDHW output: 32-pixel x 32-channel blocks per warp, transposed in the
 // warp's staging block so that each store covers consecutive pixels of a channel.
-__device__ __forceinline__ void cm_norm_pass2_ncdhw(const CmEpi& E, const CmTile& t,
-                                                    float (*stage)[33], int lane, int warp_e,
-                                                    int nwarps, int N, const uint16_t* scr,
-                                                    int Cs, const float* den) {
+__device__ __forceinline__ void cm_norm_pass2_ncdhw(const CmEpi& E, const CmTile& t, float* st,
+                                                    int lane, int warp_e, int nwarps, int N,
+                                                    const uint16_t* scr, int Cs,
+                                                    const float* den) {
+  float(*stage)[kStageScalar] = reinterpret_cast<float(*)[kStageScalar]>(st);
   const int nbn = (N + 31) / 32, nbc = (E.Cout + 31) / 32;
   const long long plane = (long long)E.Ho * E.Wo;
   const long long cstep = (long long)E.Do * plane;
