@@ -39,6 +39,8 @@ using vvc::EpiParams;
 
 constexpr size_t kMaxSmem = 232448;  // sm_100 / sm_103 opt-in dynamic shared memory per block
 constexpr int kDefaultSMs = 148;
+// Per-warp epilogue staging block of the channel-major kernel (kStageFloats fp32).
+constexpr size_t kEpiWarpBytes = 32 * 36 * 4;
 
 int num_sms() {
   static int cached = 0;
@@ -308,13 +310,24 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.act_bytes = static_cast<uint32_t>(round_up(round_up(act_rows, 8) * k.row_bytes, 1024));
   const uint32_t wgt_bytes = static_cast<uint32_t>(k.taps_per_stage * 128 * k.row_bytes);
   k.stage_bytes = k.act_bytes + wgt_bytes;
-  constexpr size_t kEpiStage = 8 * 32 * 36 * 4;  // per-warp transpose blocks (kStageFloats)
   k.tiles_c = static_cast<int>(cdiv(p->Cout, 128));
   // fused L2 norm: den[N] in shared memory
   const bool norm = (p->epi & CONV3D_EPI_L2NORM_SILU) != 0;
   const size_t norm_bytes = norm ? (size_t)k.N * 4 : 0;
-  int stages = static_cast<int>(std::min<size_t>(
-      8, (kMaxSmem - 1024 - 256 - kEpiStage - norm_bytes) / k.stage_bytes));
+  // Epilogue warpgroups: three hide the latency of the per-element work better
+  // (layers with little reduction per output element are bound by it), two leave
+  // room for one more pipeline stage.  Three unless that costs a stage on a layer
+  // with a long reduction.
+  auto stages_for = [&](int groups) {
+    const size_t epi = (size_t)groups * 4 * kEpiWarpBytes;
+    return static_cast<int>(std::min<size_t>(
+        8, (kMaxSmem - 1024 - 256 - epi - norm_bytes) / k.stage_bytes));
+  };
+  const long long k_total = (long long)p->KT * p->KR * p->KS * p->Cin;
+  const int epi_groups = (stages_for(3) >= stages_for(2) || k_total <= 1152) ? 3 : 2;
+  k.epi_groups = epi_groups;
+  const size_t kEpiStage = (size_t)epi_groups * 4 * kEpiWarpBytes;
+  int stages = stages_for(epi_groups);
   if (t.stages > 0) stages = std::min(stages, t.stages);
   if (stages < 2) return CONV3D_ERR_UNSUPPORTED;
   k.stages = stages;

@@ -19,9 +19,9 @@
 // The accumulator is double buffered in TMEM so the epilogue of one tile runs
 // under the MMAs of the next.
 //
-// Warp roles (384 threads): 0 TMA producer, 1 MMA issuer + TMEM owner,
-// 2 reflect-W patcher, 4..11 epilogue in two warpgroups that take alternate
-// 32-pixel column blocks (a warp reads the TMEM lane quarter warp % 4: thread =
+// Warp roles (128 + 128 G threads): 0 activation producer, 1 MMA issuer + TMEM
+// owner, 2 reflect-W patcher, 3 weight producer, 4.. epilogue in G warpgroups
+// (G = 2 or 3) that take every G-th 32-pixel column block (a warp reads the TMEM lane quarter warp % 4: thread =
 // output channel; stores are coalesced across channels for NDHWC output).
 // Waits are bounded; a time-out records CONV3D_ERR_DEVICE_TIMEOUT.
 #include <cuda.h>
@@ -44,6 +44,7 @@ constexpr int kWarpMMA = 1;
 constexpr int kWarpPatch = 2;
 constexpr int kWarpWgt = 3;
 constexpr int kWarpEpi0 = 4;
+constexpr int kMaxThreads = 512;  // 4 role warps + up to 3 epilogue warpgroups
 
 struct TileCoord {
   int ct, split, twi, thi, od, nb;
@@ -112,7 +113,7 @@ __device__ __forceinline__ int cta_tile(const ConvCMParams& p, int l) {
 
 }  // namespace
 
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(kMaxThreads, 1)
     conv_cm_kernel(const __grid_constant__ CUtensorMap tmAct,
                    const __grid_constant__ CUtensorMap tmWgt,
                    const __grid_constant__ CUtensorMap tmWgtLast,
@@ -144,7 +145,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 8);  // one arrive per epilogue warp
+      mbar_init(acce_bar(b), 4 * p.epi_groups);  // one arrive per epilogue warp
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -370,7 +371,9 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp >= kWarpEpi0) {
     const int q = warp & 3;              // TMEM lane quarter
-    const int grp = (warp - kWarpEpi0) >> 2;  // epilogue warpgroup: alternate 32-column chunks
+    const int grp = (warp - kWarpEpi0) >> 2;  // epilogue warpgroup: every G-th 32-column chunk
+    const int G = p.epi_groups;
+    const int nepi = 128 * G;  // epilogue threads
     // Everything the epilogue reads per element is copied into registers first.
     CmEpi E;
     E.flags = p.epi.flags;
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(384, 1)
         const CmChan ch = cm_chan(E, cw, lane);
         const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                             static_cast<uint32_t>(buf * acc_cols);
-        for (int j0 = 32 * grp; j0 < Ncols; j0 += 64) {
+        for (int j0 = 32 * grp; j0 < Ncols; j0 += 32 * G) {
           uint32_t r[32];
           tmem_ld32(tb + static_cast<uint32_t>(j0), r);
           tmem_ld_wait();
@@ -463,7 +466,7 @@ __global__ void __launch_bounds__(384, 1)
           const CmChan ch = cm_chan(E, cw, lane);
           const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                               static_cast<uint32_t>(buf * acc_cols);
-          for (int j0 = 32 * grp; j0 < Ncols; j0 += 64) {
+          for (int j0 = 32 * grp; j0 < Ncols; j0 += 32 * G) {
             uint32_t r[32];
             tmem_ld32(tb + static_cast<uint32_t>(j0), r);
             tmem_ld_wait();
@@ -473,22 +476,22 @@ __global__ void __launch_bounds__(384, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(acce_bar(buf));
         }
-        named_bar_sync(1, 256);
+        named_bar_sync(1, nepi);
         if (ok) {
-          for (int n = tid; n < Ncols; n += 256) {
+          for (int n = tid; n < Ncols; n += nepi) {
             int h, w;
             const bool pv = cm_pixel(t, n, h, w) && n < t.npix && h < E.Ho && w < E.Wo;
             den[n] = pv ? cm_norm_den(E, scr + (long long)n * Cs) : 1.0f;
           }
         }
-        named_bar_sync(1, 256);
+        named_bar_sync(1, nepi);
         if (ok) {
           if (E.ndhwc)
-            cm_norm_pass2_ndhwc(E, t, tid, 256, Ncols, scr, Cs, den);
+            cm_norm_pass2_ndhwc(E, t, tid, nepi, Ncols, scr, Cs, den);
           else
-            cm_norm_pass2_ncdhw(E, t, st, lane, warp - kWarpEpi0, 8, Ncols, scr, Cs, den);
+            cm_norm_pass2_ncdhw(E, t, st, lane, warp - kWarpEpi0, 4 * G, Ncols, scr, Cs, den);
         }
-        named_bar_sync(1, 256);
+        named_bar_sync(1, nepi);
       }
     }
   }
@@ -523,7 +526,8 @@ cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
     if (err != cudaSuccess) return err;
     configured = smem_bytes;
   }
-  conv_cm_kernel<<<grid, 384, smem_bytes, stream>>>(tmAct, tmWgt, tmWgtLast, p);
+  conv_cm_kernel<<<grid, 128 + 128 * p.epi_groups, smem_bytes, stream>>>(tmAct, tmWgt,
+                                                                        tmWgtLast, p);
   return cudaGetLastError();
 }
 

@@ -107,6 +107,7 @@ struct ConvCMParams {
   // fused L2 norm (k_splits == 1): the tiles_c channel tiles of a pixel tile run on
   // one CTA (tpu consecutive tiles per unit; tpu = 1 otherwise)
   int norm, tpu;
+  int epi_groups;          // epilogue warpgroups (2 or 3): block = 128 + 128 * epi_groups
   uint32_t norm_off;       // shared den[N] (fp32) of the current pixel tile
   int norm_cs;             // channels per scratch row: Cout rounded up to 8
   uint16_t* vscratch;      // [grid][N][norm_cs] bf16 values, one slice per CTA
