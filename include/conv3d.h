@@ -149,6 +149,9 @@ typedef struct {
                           bounded wait runs out; the call then reports a timeout */
   int32_t timeout_ms;  /* device wait limit (0 = default: 4000 ms, or the environment
                           variable CONV3D_TIMEOUT_MS when set) */
+  int32_t im2col;      /* 0 auto, 1 on, 2 off: for Cin * KR * KS <= 64 (Cin < 8) gather
+                          the spatial taps into a staged tensor first and run a
+                          (KT, 1, 1) convolution over it */
 } conv3d_tuning;
 
 /* ---- weight packing ([cuDNN page] "Weight Packing") ------------------------------ */
@@ -165,8 +168,10 @@ int conv3d_pack_weight(const void* w_oitrs, int32_t Cout, int32_t Cin, int32_t K
 
 /* ---- convolution ---------------------------------------------------------------- */
 
-/* Scratch bytes conv3d_fwd needs for *p (0 for NDHWC inputs with Cin % 8 == 0 that
- * need no split of the reduction).  Returns a status; *bytes is set on success. */
+/* Scratch bytes conv3d_fwd needs for *p: the staged input (NCDHW input, Cin not a
+ * multiple of 8, or the spatial im2col of a narrow input with its repacked weights),
+ * split-reduction partial sums, and the bf16 value rows of the fused L2 norm.  0 when
+ * none of these applies.  Returns a status; *bytes is set on success. */
 int conv3d_workspace_bytes(const conv3d_params* p, size_t* bytes);
 int conv3d_workspace_bytes_ex(const conv3d_params* p, const conv3d_tuning* tuning,
                               size_t* bytes);

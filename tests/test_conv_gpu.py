@@ -171,6 +171,25 @@ def test_norm_pixel_major(call):
     run_and_check(call, wl.NDHWC, wl.NDHWC, tuning=vvc.Tuning(kernel=1))
 
 
+# Narrow inputs (Cin < 8, Cin * KR * KS <= 64): the spatial taps are gathered by the
+# staging kernel and the convolution runs as (KT, 1, 1) over the gathered channels.
+IM2COL_CASES = [
+    mk("im2col_cin3_causal_reflect", 1, 3, 4, 9, 70, 96, pads=CR, index=31),
+    mk("im2col_cin1_zero_bias", 2, 1, 3, 7, 33, 32, pads=P1, epi=wl.EPI_BIAS, index=32),
+    mk("im2col_cin5_t1", 1, 5, 1, 17, 40, 48, kernel=(1, 3, 3), pads=P2D, index=33),
+    mk("im2col_cin7_stride2", 1, 7, 3, 13, 29, 64, stride=(1, 2, 2), pads=CR, index=34),
+    mk("im2col_cin3_valid_norm", 1, 3, 3, 8, 30, 160, pads=VALID,
+       epi=wl.EPI_BIAS | wl.EPI_L2NORM_SILU, index=35),
+]
+
+
+@pytest.mark.parametrize("call", IM2COL_CASES, ids=lambda c: c.name)
+@pytest.mark.parametrize("layout", [wl.NDHWC, wl.NCDHW])
+def test_im2col_narrow_input(call, layout):
+    gc, _ = run_and_check(call, layout, wl.NDHWC)
+    assert gc.c.launches >= 2  # the gather runs before the convolution
+
+
 def test_epilogue_split_k_matches():
     call = mk("epi_split", 1, 64, 3, 5, 70, 160, pads=P1,
               epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_L2NORM_SILU, index=17)

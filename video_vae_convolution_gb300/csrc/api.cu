@@ -25,6 +25,10 @@ cudaError_t launch_pack_weight(const void* w, void* out, int Co, int Ci, int tap
                                cudaStream_t s);
 cudaError_t launch_stage_input(const void* x, int layout, int N, int C, int Cp, long long S,
                                void* out, cudaStream_t s);
+cudaError_t launch_im2col_hw(const void* x, int layout, int N, int C, int D, int H, int W, int Ho,
+                             int Wo, int KT, int KR, int KS, int sh, int sw, int ph, int pw,
+                             int reflect_h, int reflect_w, int Ck, void* out, const void* wp,
+                             int Cout, void* wr, cudaStream_t s);
 cudaError_t launch_splitk_epilogue(const float* partial, int splits, long long M,
                                    const EpiParams& e, cudaStream_t s);
 cudaError_t launch_l2norm_silu(const void* x, long long rows, const EpiParams& e,
@@ -79,6 +83,12 @@ struct Plan {
   size_t partial_off = 0, partial_bytes = 0;
   size_t vscratch_off = 0, vscratch_bytes = 0;
   size_t ws_bytes = 0;
+  // narrow input: the staging kernel gathers the spatial taps (im2col) and the
+  // convolution runs as (KT, 1, 1) over Ck channels with repacked weights
+  bool im2col = false;
+  int Ck = 0;
+  size_t wr_off = 0, wr_bytes = 0;
+  conv3d_params q{};
   bool cm = false;          // channel-major kernel (conv_cm) instead of pixel-major (conv_tc)
   ConvTCParams kp{};
   ConvCMParams cp{};
@@ -612,10 +622,43 @@ int make_plan(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
   if (rc) return rc;
   conv3d_tuning t{};
   if (tu) t = *tu;
+  size_t off = 0;
+  const int krs = p->KR * p->KS;
+  if (t.im2col != 2 && krs > 1 && p->Cin < 8 && (long long)krs * p->Cin <= 64 &&
+      pl->Ho <= 65535 && (long long)p->N * p->D <= 65535) {
+    // narrow input: gather the KR x KS spatial taps of every output pixel
+    pl->im2col = true;
+    pl->stage = true;
+    pl->Ck = static_cast<int>(round_up((long long)krs * p->Cin, 16));
+    pl->Cst = pl->Ck;
+    pl->stage_off = 0;
+    pl->stage_bytes = (size_t)p->N * p->D * pl->Ho * pl->Wo * pl->Ck * 2;
+    off = static_cast<size_t>(round_up(pl->stage_bytes, 256));
+    pl->wr_off = off;
+    pl->wr_bytes = (size_t)p->Cout * p->KT * round_up(pl->Ck, 64) * 2;
+    off = static_cast<size_t>(round_up(off + pl->wr_bytes, 256));
+    conv3d_params q = *p;
+    q.layout = CONV3D_NDHWC;
+    q.Cin = pl->Ck;
+    q.H = pl->Ho;
+    q.W = pl->Wo;
+    q.KR = q.KS = 1;
+    q.stride[1] = q.stride[2] = 1;
+    for (int i = 1; i < 3; ++i) {
+      q.pad[i].before = q.pad[i].after = 0;
+      q.pad[i].mode = CONV3D_PAD_ZERO;
+    }
+    pl->q = q;
+    if (t.kernel == 1) {
+      pl->cm = false;
+      return plan_pm(&pl->q, t, pl, off);
+    }
+    pl->cm = true;
+    return plan_cm(&pl->q, t, pl, off);
+  }
   // input staging: NCDHW input, or channels not a multiple of 8 (TMA strides)
   pl->stage = (p->layout == CONV3D_NCDHW) || (p->Cin % 8 != 0);
   pl->Cst = static_cast<int>(round_up(p->Cin, 8));
-  size_t off = 0;
   if (pl->stage) {
     pl->stage_off = off;
     pl->stage_bytes = (size_t)p->N * p->D * p->H * p->W * pl->Cst * 2;
@@ -825,7 +868,24 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const void* xin = p->x;
   uint8_t* ws = static_cast<uint8_t*>(p->workspace);
-  if (pl.stage) {
+  const conv3d_params* pm = p;  // the convolution the tensor maps describe
+  conv3d_params q;
+  if (pl.im2col) {
+    void* dst = ws + pl.stage_off;
+    void* wr = ws + pl.wr_off;
+    const int rh = (p->pad[1].mode == CONV3D_PAD_REFLECT && (p->pad[1].before || p->pad[1].after));
+    const int rw = (p->pad[2].mode == CONV3D_PAD_REFLECT && (p->pad[2].before || p->pad[2].after));
+    if (vvc::launch_im2col_hw(p->x, p->layout, p->N, p->Cin, p->D, p->H, p->W, pl.Ho, pl.Wo,
+                              p->KT, p->KR, p->KS, p->stride[1], p->stride[2], p->pad[1].before,
+                              p->pad[2].before, rh, rw, pl.Ck, dst, p->w_packed, p->Cout, wr,
+                              s) != cudaSuccess)
+      return CONV3D_ERR_CUDA;
+    q = pl.q;
+    q.x = dst;
+    q.w_packed = wr;
+    pm = &q;
+    xin = dst;
+  } else if (pl.stage) {
     void* dst = ws + pl.stage_off;
     if (vvc::launch_stage_input(p->x, p->layout, p->N, p->Cin, pl.Cst,
                                 (long long)p->D * p->H * p->W, dst, s) != cudaSuccess)
@@ -833,7 +893,7 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
     xin = dst;
   }
   CUtensorMap tmA, tmB, tmBLast;
-  rc = encode_maps(p, pl, xin, &tmA, &tmB, &tmBLast);
+  rc = encode_maps(pm, pl, xin, &tmA, &tmB, &tmBLast);
   if (rc) return rc;
   float* partial = reinterpret_cast<float*>(ws + pl.partial_off);
   if (pl.cm) {

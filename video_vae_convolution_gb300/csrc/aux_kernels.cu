@@ -41,6 +41,132 @@ cudaError_t launch_pack_weight(const void* w, void* out, int Co, int Ci, int tap
   return cudaGetLastError();
 }
 
+// ---- spatial im2col staging for narrow inputs ------------------------------------------
+// For a layer with few input channels (Cin * KR * KS <= 64) the spatial taps are
+// gathered once: out[n][d][ho][wo][(r * KS + s) * C + c] = x[n, c, d, ho*sh + r - ph,
+// wo*sw + s - pw] (zero or reflect padding; channels past KR*KS*C are zero), so the
+// convolution that follows is (KT, 1, 1) over Ck channels, and its weights are
+// repacked to match: wr[co][t][(r * KS + s) * C + c] = wp[co][(t*KR + r)*KS + s][c].
+// The last `wblocks` blocks of the grid do the weight repack.
+struct Im2colArgs {
+  const uint16_t* x;
+  int layout;                 // LAYOUT_NCDHW / LAYOUT_NDHWC
+  int N, C, D, H, W, Ho, Wo;
+  int KT, KR, KS, sh, sw, ph, pw, reflect_h, reflect_w;
+  int Ck;                     // staged channels (multiple of 8)
+  uint16_t* out;
+  const uint16_t* wp;         // packed weights [Cout][KT*KR*KS][cp]
+  int Cout, cp;               // cp = round_up(C, 64)
+  int cp2;                    // round_up(Ck, 64): channel pitch of the repacked weights
+  uint16_t* wr;               // [Cout][KT][cp2]
+  long long units;            // N * D * Ho * Wo * (Ck / 8)
+  int iblocks;                // blocks doing the gather
+};
+
+__device__ __forceinline__ int pad_index(int i, int L, bool reflect) {
+  if (reflect) {
+    if (i < 0) i = -i;
+    if (i >= L) i = 2 * (L - 1) - i;
+  }
+  return i;  // out of [0, L) means zero padding
+}
+
+// Grid: x = 256-pixel pieces of an output row, y = output row ho, z = n * D + d;
+// blockIdx.x past the row pieces (x >= xblocks) repacks the weights.
+__global__ void __launch_bounds__(256) im2col_hw_kernel(const Im2colArgs a) {
+  const int xblocks = (a.Wo + 255) / 256;
+  if (static_cast<int>(blockIdx.x) >= xblocks) {
+    if (blockIdx.y != 0 || blockIdx.z != 0) return;
+    // weight repack
+    const long long total = (long long)a.Cout * a.KT * a.cp2;
+    const int krs = a.KR * a.KS * a.C;
+    const int nb = gridDim.x - xblocks;
+    for (long long i = (long long)(blockIdx.x - xblocks) * blockDim.x + threadIdx.x; i < total;
+         i += (long long)nb * blockDim.x) {
+      const int kk = static_cast<int>(i % a.cp2);
+      const long long rest = i / a.cp2;
+      const int t = static_cast<int>(rest % a.KT);
+      const long long co = rest / a.KT;
+      uint16_t v = 0;
+      if (kk < krs) {
+        const int rs = kk / a.C, c = kk - rs * a.C;
+        const int tap = t * a.KR * a.KS + rs;
+        v = a.wp[(co * a.KT * a.KR * a.KS + tap) * a.cp + c];
+      }
+      a.wr[i] = v;
+    }
+    return;
+  }
+  const int wo = blockIdx.x * 256 + threadIdx.x;
+  if (wo >= a.Wo) return;
+  const int ho = blockIdx.y;
+  const int nd = blockIdx.z;
+  const int n = nd / a.D, d = nd - n * a.D;
+  const long long plane = (long long)a.H * a.W;
+  const long long cstride = (a.layout == LAYOUT_NDHWC) ? 1 : (long long)a.D * plane;
+  const long long base = (a.layout == LAYOUT_NDHWC)
+                             ? ((long long)n * a.D + d) * plane * a.C
+                             : ((long long)n * a.C * a.D + d) * plane;
+  const int pix_stride = (a.layout == LAYOUT_NDHWC) ? a.C : 1;
+  uint4* dst = reinterpret_cast<uint4*>(a.out) +
+               ((((long long)nd * a.Ho + ho) * a.Wo + wo) * (a.Ck / 8));
+  // values are appended 16 bits at a time to (lo, hi); every 8 form one 16-byte store
+  unsigned long long lo = 0, hi = 0;
+  int ne = 0, g = 0;
+  for (int r = 0; r < a.KR; ++r) {
+    const int h = pad_index(ho * a.sh + r - a.ph, a.H, a.reflect_h);
+    for (int s = 0; s < a.KS; ++s) {
+      const int w = pad_index(wo * a.sw + s - a.pw, a.W, a.reflect_w);
+      const bool in = h >= 0 && h < a.H && w >= 0 && w < a.W;
+      const long long pos = base + ((long long)h * a.W + w) * pix_stride;
+      for (int c = 0; c < a.C; ++c) {
+        const unsigned long long val = in ? __ldg(a.x + pos + c * cstride) : 0u;
+        if (ne < 4)
+          lo |= val << (16 * ne);
+        else
+          hi |= val << (16 * (ne - 4));
+        if (++ne == 8) {
+          dst[g++] = make_uint4(static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32),
+                                static_cast<uint32_t>(hi), static_cast<uint32_t>(hi >> 32));
+          lo = hi = 0;
+          ne = 0;
+        }
+      }
+    }
+  }
+  // the rest of the Ck channels are zero
+  for (; g < a.Ck / 8; ++g) {
+    dst[g] = make_uint4(static_cast<uint32_t>(lo), static_cast<uint32_t>(lo >> 32),
+                        static_cast<uint32_t>(hi), static_cast<uint32_t>(hi >> 32));
+    lo = hi = 0;
+  }
+}
+
+cudaError_t launch_im2col_hw(const void* x, int layout, int N, int C, int D, int H, int W, int Ho,
+                             int Wo, int KT, int KR, int KS, int sh, int sw, int ph, int pw,
+                             int reflect_h, int reflect_w, int Ck, void* out, const void* wp,
+                             int Cout, void* wr, cudaStream_t s) {
+  Im2colArgs a;
+  a.x = static_cast<const uint16_t*>(x);
+  a.layout = layout;
+  a.N = N; a.C = C; a.D = D; a.H = H; a.W = W; a.Ho = Ho; a.Wo = Wo;
+  a.KT = KT; a.KR = KR; a.KS = KS; a.sh = sh; a.sw = sw; a.ph = ph; a.pw = pw;
+  a.reflect_h = reflect_h; a.reflect_w = reflect_w;
+  a.Ck = Ck;
+  a.out = static_cast<uint16_t*>(out);
+  a.wp = static_cast<const uint16_t*>(wp);
+  a.Cout = Cout;
+  a.cp = (C + 63) / 64 * 64;
+  a.cp2 = (Ck + 63) / 64 * 64;
+  a.wr = static_cast<uint16_t*>(wr);
+  a.units = (long long)N * D * Ho * Wo * (Ck / 8);
+  const int xblocks = (Wo + 255) / 256;
+  a.iblocks = xblocks;
+  const int wblocks = 8;
+  im2col_hw_kernel<<<dim3(xblocks + wblocks, Ho, N * D), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 // ---- input staging --------------------------------------------------------------------
 // NCDHW [N][C][S] (S = D*H*W) -> NDHWC [N][S][Cp], channels Cin..Cp-1 zero.
 // A block moves 32 channels x 256 positions through shared memory: each channel

@@ -158,6 +158,14 @@ __device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8]) {
   }
 }
 
+// Two fp32 values -> packed bf16x2 (round to nearest even; lo in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ float bf16x2_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16x2_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
 // NDHWC output (or split partial sums) for one 32-channel x 32-pixel block staged
 // at st (rows kStageVec apart): unit = (pixel, the thread's 8 channels).
 __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, const float* st,
@@ -168,6 +176,59 @@ __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, 
   const long long nd = (long long)t.nb * E.Do + t.od;
   const bool vec = (ch.cnt == 8) && ((E.Cout & 7) == 0);
   const int g = lane & 3;
+  // Fast path: the block's 32 pixels are consecutive pixels of one output row, all
+  // inside the output, and the thread's 8 channels are a full 16-byte group.  One
+  // base address per block; values converted two at a time.
+  if (vec && !E.split && !E.pad && jb + 31 < t.jlim && jb + 31 < t.pitch && j0 + 31 < t.npix &&
+      t.hoff + ib < E.Ho && t.woff + jb + 31 < E.Wo) {
+    const long long o0 =
+        ((nd * E.Ho + t.hoff + ib) * E.Wo + t.woff + jb + (lane >> 2)) * E.Cout + ch.c0;
+    const long long step = 8LL * E.Cout;  // the thread's next pixel is 8 pixels on
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int pl = 8 * k + (lane >> 2);
+      const long long o = o0 + k * step;
+      const float4 lo = *reinterpret_cast<const float4*>(st + pl * kStageVec + 8 * g);
+      const float4 hi = *reinterpret_cast<const float4*>(st + pl * kStageVec + 8 * g + 4);
+      uint4 cb;  // B(conv)
+      cb.x = pack_bf16x2(lo.x, lo.y);
+      cb.y = pack_bf16x2(lo.z, lo.w);
+      cb.z = pack_bf16x2(hi.x, hi.y);
+      cb.w = pack_bf16x2(hi.z, hi.w);
+      uint4 v = cb;
+      if (E.flags & EPI_BIAS) {
+        v.x = pack_bf16x2(__fadd_rn(bf16x2_lo(v.x), ch.b[0]), __fadd_rn(bf16x2_hi(v.x), ch.b[1]));
+        v.y = pack_bf16x2(__fadd_rn(bf16x2_lo(v.y), ch.b[2]), __fadd_rn(bf16x2_hi(v.y), ch.b[3]));
+        v.z = pack_bf16x2(__fadd_rn(bf16x2_lo(v.z), ch.b[4]), __fadd_rn(bf16x2_hi(v.z), ch.b[5]));
+        v.w = pack_bf16x2(__fadd_rn(bf16x2_lo(v.w), ch.b[6]), __fadd_rn(bf16x2_hi(v.w), ch.b[7]));
+      }
+      if (E.flags & EPI_RESIDUAL) {
+        uint4 sk = __ldg(reinterpret_cast<const uint4*>(E.res + o));
+        if (E.flags & EPI_RESIDUAL_BIAS) {
+          sk.x = pack_bf16x2(__fadd_rn(bf16x2_lo(sk.x), ch.rb[0]),
+                             __fadd_rn(bf16x2_hi(sk.x), ch.rb[1]));
+          sk.y = pack_bf16x2(__fadd_rn(bf16x2_lo(sk.y), ch.rb[2]),
+                             __fadd_rn(bf16x2_hi(sk.y), ch.rb[3]));
+          sk.z = pack_bf16x2(__fadd_rn(bf16x2_lo(sk.z), ch.rb[4]),
+                             __fadd_rn(bf16x2_hi(sk.z), ch.rb[5]));
+          sk.w = pack_bf16x2(__fadd_rn(bf16x2_lo(sk.w), ch.rb[6]),
+                             __fadd_rn(bf16x2_hi(sk.w), ch.rb[7]));
+        }
+        v.x = pack_bf16x2(__fadd_rn(bf16x2_lo(v.x), bf16x2_lo(sk.x)),
+                          __fadd_rn(bf16x2_hi(v.x), bf16x2_hi(sk.x)));
+        v.y = pack_bf16x2(__fadd_rn(bf16x2_lo(v.y), bf16x2_lo(sk.y)),
+                          __fadd_rn(bf16x2_hi(v.y), bf16x2_hi(sk.y)));
+        v.z = pack_bf16x2(__fadd_rn(bf16x2_lo(v.z), bf16x2_lo(sk.z)),
+                          __fadd_rn(bf16x2_hi(v.z), bf16x2_hi(sk.z)));
+        v.w = pack_bf16x2(__fadd_rn(bf16x2_lo(v.w), bf16x2_lo(sk.w)),
+                          __fadd_rn(bf16x2_hi(v.w), bf16x2_hi(sk.w)));
+      }
+      *reinterpret_cast<uint4*>(E.y + o) = v;
+      if (E.flags & EPI_SAVE_VALUE) *reinterpret_cast<uint4*>(E.val + o) = v;
+      if (E.flags & EPI_DEBUG_STORE_CONV) *reinterpret_cast<uint4*>(E.conv + o) = cb;
+    }
+    return;
+  }
   for (int k = 0; k < 4; ++k) {
     const int pl = 8 * k + (lane >> 2);
     int h, w;
