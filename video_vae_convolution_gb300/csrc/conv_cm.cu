@@ -50,18 +50,22 @@ struct TileCoord {
   int ct, split, twi, thi, od, nb;
 };
 
+// Tile index, fastest first: channel tile, split, output depth, W tile, H tile,
+// batch.  CTAs run consecutive tiles at the same time, so with the output depth
+// next to the channel tile they share input rows across all output depths while
+// those rows are still in L2 (the 3-D layers read their input from HBM about once).
 __device__ __forceinline__ TileCoord decode_tile(const ConvCMParams& p, int tile) {
   TileCoord c;
   c.ct = tile % p.tiles_c;
   tile /= p.tiles_c;
   c.split = tile % p.k_splits;
   tile /= p.k_splits;
+  c.od = tile % p.epi.Do;
+  tile /= p.epi.Do;
   c.twi = tile % p.tiles_w;
   tile /= p.tiles_w;
   c.thi = tile % p.tiles_h;
-  tile /= p.tiles_h;
-  c.od = tile % p.epi.Do;
-  c.nb = tile / p.epi.Do;
+  c.nb = tile / p.tiles_h;
   return c;
 }
 
