@@ -193,15 +193,28 @@ void fill_epi(const conv3d_params* p, const Plan& pl, EpiParams* e) {
   e->sqrt_c = std::sqrt(static_cast<float>(p->Cout));
 }
 
-// Split of the reduction so that small layers still fill the GPU.
+// Split of the reduction so that small layers still fill the GPU.  Each split
+// adds work items (tiles x splits, run by persistent CTAs in waves of `sms`) and
+// partial sums to reduce; the cost counted is waves x (stages per item + a fixed
+// pipeline fill) + a small charge per split for the reduction pass.
 int choose_splits(const conv3d_tuning& t, long long tiles, int stages_total, int sms, int* per) {
   int splits = t.k_splits;
   if (splits <= 0) {
     splits = 1;
-    if (tiles < sms) {
-      splits = static_cast<int>(std::max<long long>(1, (sms + tiles / 2) / tiles));
-      splits = std::min(splits, std::max(1, stages_total / 4));
-      splits = std::min(splits, 16);
+    if (tiles < 2LL * sms) {
+      double best = -1.0;
+      const int smax = std::min(16, std::max(1, stages_total / 4));
+      for (int s = 1; s <= smax; ++s) {
+        const int p = static_cast<int>(cdiv(stages_total, s));
+        const int se = static_cast<int>(cdiv(stages_total, p));
+        if (se != s) continue;  // the same split as a smaller s
+        const long long waves = cdiv(tiles * se, sms);
+        const double cost = (double)waves * (p + 4) + (se > 1 ? 0.5 * se : 0.0);
+        if (best < 0 || cost < best - 1e-9) {
+          best = cost;
+          splits = se;
+        }
+      }
     }
   }
   splits = std::max(1, std::min(splits, stages_total));
