@@ -41,7 +41,7 @@ L2_FLUSH_BYTES = 256 << 20
 # sources: a changed kernel reports null until it is captured again.
 KERNEL_SOURCES = ["conv_cm.cu", "epilogue_cm.cuh", "epilogue.cuh", "kernel_common.cuh",
                   "ptx.cuh", "internal.h"]
-NCU_TRAFFIC = {"65a97ea2c70cd239": 522032640 + 152374528}
+NCU_TRAFFIC = {"fa21ee721957a9fc": 262686208 + 140327680}
 
 
 def kernel_source_hash():
@@ -81,9 +81,12 @@ class ClockSampler:
     def __init__(self, index=0):
         self.index = index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (perf_counter time, csv line)
+        self.t0 = self.t1 = None
 
     def start(self):
+        """Starts nvidia-smi and waits (up to 3 s) for its first sample, so that the
+        timed region that follows is sampled from its beginning."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
@@ -91,12 +94,21 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.perf_counter() + 3.0
+            while not self.lines and time.perf_counter() < deadline:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def begin(self):
+        self.t0 = time.perf_counter()
+
+    def end(self):
+        self.t1 = time.perf_counter()
 
     def stop(self):
         if self.proc is None:
@@ -108,7 +120,13 @@ class ClockSampler:
             self.proc.kill()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        # samples taken inside the timed region (the last one before it when none is)
+        lines = [ln for t, ln in self.lines
+                 if self.t0 is None or (self.t0 <= t <= (self.t1 or t))]
+        if not lines and self.lines:
+            before = [ln for t, ln in self.lines if self.t0 is None or t <= self.t0]
+            lines = before[-1:] or [self.lines[0][1]]
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -283,6 +301,7 @@ def run_gpu(args, rank, world):
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
+    sampler.begin()
     step_ev = []
     for _ in range(args.steps):
         flush.zero_()
@@ -293,6 +312,7 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
+    sampler.end()
     clocks = sampler.stop()
     status = vvc.device_status()
     if status != 0:
@@ -421,7 +441,7 @@ def main():
     ap.add_argument("--layout", default="ndhwc", choices=["ndhwc", "ncdhw"])
     ap.add_argument("--tune", default="", help="plan overrides, e.g. R=2,kc=32")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
