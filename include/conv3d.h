@@ -143,8 +143,10 @@ typedef struct {
   int32_t halo;        /* 0 auto, 1 on, 2 off: one input-row halo serves all W taps */
   int32_t stages;      /* shared-memory pipeline depth */
   int32_t k_splits;    /* split of the reduction across CTAs (>= 1) */
-  int32_t kernel;      /* 0 auto, 1 pixel-major tiles (M = pixels), 2 channel-major tiles
-                          (M = output channels, N = up to 256 pixels) */
+  int32_t kernel;      /* 0 auto, 1 pixel-major kernel (M = pixels), 2 persistent kernel in
+                          channel-major mode (M = 128 output channels, N = up to 256
+                          pixels), 3 persistent kernel in pixel-major mode (M = 128 pixels
+                          per half of the tile, N = Cout <= 128) */
   int32_t inject;      /* test aid: >0 makes the producer skip stage (inject-1) so a
                           bounded wait runs out; the call then reports a timeout */
   int32_t timeout_ms;  /* device wait limit (0 = default: 4000 ms, or the environment

@@ -50,7 +50,8 @@ def test_pack_weight_bit_exact():
 
 BASE = mk("base", 1, 64, 3, 6, 150, 64, index=1)
 
-# tuning: kernel 1 = pixel-major tiles, 2 = channel-major tiles; halo 1 on, 2 off
+# tuning: kernel 1 = pixel-major kernel, 2 = channel-major mode, 3 = pixel-major mode of
+# the persistent kernel; halo 1 on, 2 off
 PLAN_VARIANTS = [
     dict(kernel=2),
     dict(kernel=2, halo=1),
@@ -65,6 +66,15 @@ PLAN_VARIANTS = [
     dict(kernel=2, k_splits=3),
     dict(kernel=2, halo=1, k_splits=2),
     dict(kernel=2, stages=2),
+    dict(kernel=3),
+    dict(kernel=3, halo=1),
+    dict(kernel=3, halo=2),
+    dict(kernel=3, kc=32),
+    dict(kernel=3, kc=16),
+    dict(kernel=3, tile_w=64, tile_h=3),
+    dict(kernel=3, tile_w=48, tile_h=3, halo=1),
+    dict(kernel=3, k_splits=3),
+    dict(kernel=3, stages=2),
     dict(kernel=1, halo=2),
     dict(kernel=1, halo=1),
     dict(kernel=1, halo=2, kc=32),
@@ -123,6 +133,22 @@ def test_layouts_parity_and_bit_identity(lay):
     np.testing.assert_array_equal(oracle.from_layout(gc.y, lay[1]), ref.y)
 
 
+# NCDHW output written from registers by row segments at every alignment (odd Wo:
+# rows start at odd and even elements; 16-byte, 4-byte pair and 2-byte edge stores).
+NCDHW_ROW_CASES = [
+    mk("ncdhw_rows_odd_wo", 1, 32, 3, 6, 67, 64, pads=VALID,
+       epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_RESIDUAL_BIAS | wl.EPI_SAVE_VALUE, index=42),
+    mk("ncdhw_rows_wo_mod8_3", 1, 48, 2, 5, 77, 96, pads=CR, epi=wl.EPI_BIAS, index=43),
+]
+
+
+@pytest.mark.parametrize("call", NCDHW_ROW_CASES, ids=lambda c: c.name)
+def test_ncdhw_rows(call):
+    gc, _ = run_and_check(call, wl.NDHWC, wl.NCDHW)
+    ref = GpuCall(call, wl.make_inputs("test", call, wl.NDHWC, wl.NDHWC))
+    np.testing.assert_array_equal(oracle.from_layout(gc.y, wl.NCDHW), ref.y)
+
+
 EPI_CASES = [
     mk("epi_bias_res_rbias", 1, 32, 3, 6, 140, 64, pads=P1,
        epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_RESIDUAL_BIAS, index=13),
@@ -169,6 +195,28 @@ def test_norm_channel_major(call, out_layout):
                          ids=lambda c: c.name)
 def test_norm_pixel_major(call):
     run_and_check(call, wl.NDHWC, wl.NDHWC, tuning=vvc.Tuning(kernel=1))
+
+
+# Pixel-major mode of the persistent kernel (Cout <= 128): narrow and 96/128-channel
+# outputs, every epilogue, both layouts, strip / flat / strided tiles, the fused norm.
+PM_CASES = [
+    mk("pm_cout3", 1, 96, 1, 12, 130, 3, kernel=(1, 3, 3), pads=P2D, index=36),
+    mk("pm_cout96_strip_reflect", 1, 64, 3, 9, 70, 96, pads=CR,
+       epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_RESIDUAL_BIAS | wl.EPI_SAVE_VALUE, index=37),
+    mk("pm_cout128_flat", 1, 64, 3, 7, 50, 128, pads=((2, 0, Z), (1, 1, Z), (0, 0, Z)),
+       epi=wl.EPI_BIAS, index=38),
+    mk("pm_cout48_stride2", 1, 32, 3, 13, 29, 48, stride=(1, 2, 2), pads=CR, index=39),
+    mk("pm_cout40_norm", 2, 24, 2, 5, 33, 40, pads=P1,
+       epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_L2NORM_SILU | wl.EPI_SAVE_VALUE, index=40),
+    mk("pm_cout64_pad_br", 1, 64, 4, 9, 140, 64, pads=VALID,
+       epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_RESIDUAL_BIAS | wl.EPI_OUT_PAD_BR, index=41),
+]
+
+
+@pytest.mark.parametrize("call", PM_CASES, ids=lambda c: c.name)
+@pytest.mark.parametrize("out_layout", [wl.NDHWC, wl.NCDHW])
+def test_pixel_major_mode(call, out_layout):
+    run_and_check(call, wl.NDHWC, out_layout, tuning=vvc.Tuning(kernel=3))
 
 
 # Narrow inputs (Cin < 8, Cin * KR * KS <= 64): the spatial taps are gathered by the

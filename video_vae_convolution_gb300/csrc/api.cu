@@ -326,30 +326,49 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
     k.N = static_cast<int>(round_up((long long)tw * rh, 16));
   }
   if (k.N > 256) return CONV3D_ERR_INVALID_ARG;
+  // Pixel-major mode for layers with at most 128 output channels: N = Cout (rounded
+  // to 16) over 128-pixel halves instead of M = 128 channel rows of which only Cout are
+  // real; its epilogue (one pixel per thread) needs no staging.
+  // (Measured slower than channel-major tiles on the 96-channel and narrow layers, so
+  // it runs only on request: conv3d_tuning.kernel = 3.)
+  const bool pm = t.kernel == 3;
+  if (pm && p->Cout > 128) return CONV3D_ERR_UNSUPPORTED;
+  k.pm = pm ? 1 : 0;
+  if (pm) {
+    k.N = static_cast<int>(round_up(k.N, 128));  // whole 128-pixel halves
+    k.pm_halves = k.N / 128;
+    k.pm_n = static_cast<int>(round_up(p->Cout, 16));
+    k.pm_cols = static_cast<int>(round_up(k.pm_n, 32));
+    k.wtap_rows = k.pm_n;
+  } else {
+    k.wtap_rows = 128;
+  }
   k.taps_per_stage = halo ? p->KS : 1;
   k.stages_total = p->KT * p->KR * (halo ? 1 : p->KS) * k.n_chunks;
   const long long act_rows = std::max<long long>((long long)k.rh * k.run_pitch,
                                                  k.N + (halo ? p->KS - 1 : 0));
   k.act_bytes = static_cast<uint32_t>(round_up(round_up(act_rows, 8) * k.row_bytes, 1024));
-  const uint32_t wgt_bytes = static_cast<uint32_t>(k.taps_per_stage * 128 * k.row_bytes);
+  const uint32_t wgt_bytes = static_cast<uint32_t>(k.taps_per_stage * k.wtap_rows * k.row_bytes);
   k.stage_bytes = k.act_bytes + wgt_bytes;
   k.tiles_c = static_cast<int>(cdiv(p->Cout, 128));
-  // fused L2 norm: den[N] in shared memory
-  const bool norm = (p->epi & CONV3D_EPI_L2NORM_SILU) != 0;
+  // fused L2 norm: den[N] in shared memory (channel-major; the pixel-major
+  // epilogue owns whole channel rows)
+  const bool norm = (p->epi & CONV3D_EPI_L2NORM_SILU) != 0 && !pm;
   const size_t norm_bytes = norm ? (size_t)k.N * 4 : 0;
   // Epilogue warpgroups: three hide the latency of the per-element work better
   // (layers with little reduction per output element are bound by it), two leave
   // room for one more pipeline stage.  Three unless that costs a stage on a layer
   // with a long reduction.
   auto stages_for = [&](int groups) {
-    const size_t epi = (size_t)groups * 4 * kEpiWarpBytes;
+    const size_t epi = pm ? 0 : (size_t)groups * 4 * kEpiWarpBytes;
     return static_cast<int>(std::min<size_t>(
         8, (kMaxSmem - 1024 - 256 - epi - norm_bytes) / k.stage_bytes));
   };
   const long long k_total = (long long)p->KT * p->KR * p->KS * p->Cin;
-  const int epi_groups = (stages_for(3) >= stages_for(2) || k_total <= 1152) ? 3 : 2;
+  const int epi_groups =
+      pm ? 2 : ((stages_for(3) >= stages_for(2) || k_total <= 1152) ? 3 : 2);
   k.epi_groups = epi_groups;
-  const size_t kEpiStage = (size_t)epi_groups * 4 * kEpiWarpBytes;
+  const size_t kEpiStage = pm ? 0 : (size_t)epi_groups * 4 * kEpiWarpBytes;
   int stages = stages_for(epi_groups);
   if (t.stages > 0) stages = std::min(stages, t.stages);
   if (stages < 2) return CONV3D_ERR_UNSUPPORTED;
@@ -404,7 +423,7 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.num_tiles = static_cast<int>(tiles * splits);
   k.norm = (norm && splits == 1) ? 1 : 0;
   k.tpu = k.norm ? k.tiles_c : 1;
-  k.acc_cols = static_cast<int>(round_up(k.N, 32));
+  k.acc_cols = pm ? k.pm_halves * k.pm_cols : static_cast<int>(round_up(k.N, 32));
   k.nbuf = (2 * k.acc_cols <= 512) ? 2 : 1;
   int cols = 32;
   while (cols < k.nbuf * k.acc_cols) cols *= 2;
@@ -684,7 +703,7 @@ int make_plan(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
   const Plan before = *pl;
   pl->cm = true;
   rc = plan_cm(p, t, pl, off);
-  if (rc != CONV3D_ERR_UNSUPPORTED || t.kernel == 2) return rc;
+  if (rc != CONV3D_ERR_UNSUPPORTED || t.kernel == 2 || t.kernel == 3) return rc;
   // no channel-major plan for this shape: pixel-major tiles
   *pl = before;
   pl->cm = false;

@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               for (int tl = 0; tl < p.taps_per_stage; ++tl) {
                 const int s = p.halo ? tl : sc.sblk;
                 const int tap = (sc.t * p.KR + sc.r) * p.KS + s;
-                tma_load_2d(wgt + static_cast<uint32_t>(tl * 128 * p.row_bytes), wmap, full,
+                tma_load_2d(wgt + static_cast<uint32_t>(tl * p.wtap_rows * p.row_bytes), wmap, full,
                             tap * p.cp64 + sc.ch * p.kc, c0);
               }
             } else if (p.flat) {
@@ -252,7 +252,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     }
   } else if (warp == kWarpMMA) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(128, p.N);
+      // channel-major: A = weights (M = 128 channels), B = pixels (N = p.N);
+      // pixel-major: A = pixels (M = 128 per half), B = weights (N = p.pm_n)
+      const uint32_t idesc = idesc_bf16_f32(128, p.pm ? p.pm_n : p.N);
       const uint32_t sbo = 8u * static_cast<uint32_t>(p.row_bytes);
       // The high descriptor word (stride, version, swizzle) is fixed; operand
       // views differ only in the start-address field (16-byte units).  The
@@ -260,7 +262,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       // base offset 0.
       const uint32_t desc_hi = static_cast<uint32_t>(sdesc(0u, 16u, sbo, swz, 0u) >> 32);
       const uint32_t desc_lo0 = static_cast<uint32_t>(sdesc(0u, 16u, sbo, swz, 0u));
-      const uint32_t w_tap_step = static_cast<uint32_t>(128 * p.row_bytes) >> 4;
+      const uint32_t w_tap_step = static_cast<uint32_t>(p.wtap_rows * p.row_bytes) >> 4;
+      const uint32_t half_step = static_cast<uint32_t>(128 * p.row_bytes) >> 4;
       const uint32_t a_tap_step = p.halo ? (static_cast<uint32_t>(p.row_bytes) >> 4) : 0u;
       int slot = 0;
       uint32_t phase = 0;
@@ -294,14 +297,32 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           const uint32_t act = sbase + p.stage_bytes * slot;
           const uint32_t b_lo = desc_lo0 + (act >> 4);
           const uint32_t a_lo = desc_lo0 + ((act + p.act_bytes) >> 4);
-          for (int tl = 0; tl < p.taps_per_stage; ++tl) {
-            const uint32_t a_t = a_lo + tl * w_tap_step;
-            const uint32_t b_t = b_lo + tl * a_tap_step;
-            for (int kk = 0; kk < kk_n; ++kk) {
-              const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (a_t + 2u * kk);
-              const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (b_t + 2u * kk);
-              mma_bf16_ss(d, adesc, bdesc, idesc, acc);
-              acc = 1u;
+          if (!p.pm) {
+            for (int tl = 0; tl < p.taps_per_stage; ++tl) {
+              const uint32_t a_t = a_lo + tl * w_tap_step;
+              const uint32_t b_t = b_lo + tl * a_tap_step;
+              for (int kk = 0; kk < kk_n; ++kk) {
+                const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (a_t + 2u * kk);
+                const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (b_t + 2u * kk);
+                mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+                acc = 1u;
+              }
+            }
+          } else {
+            // each 128-pixel half of the tile accumulates into its own columns
+            for (int h = 0; h < p.pm_halves; ++h) {
+              const uint32_t dh = d + static_cast<uint32_t>(h * p.pm_cols);
+              uint32_t acc_h = (it == it_b) ? 0u : 1u;
+              for (int tl = 0; tl < p.taps_per_stage; ++tl) {
+                const uint32_t x_t = b_lo + h * half_step + tl * a_tap_step;  // pixels
+                const uint32_t w_t = a_lo + tl * w_tap_step;                   // weights
+                for (int kk = 0; kk < kk_n; ++kk) {
+                  const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (x_t + 2u * kk);
+                  const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (w_t + 2u * kk);
+                  mma_bf16_ss(dh, adesc, bdesc, idesc, acc_h);
+                  acc_h = 1u;
+                }
+              }
             }
           }
           mma_commit(empty_bar(slot));
@@ -419,7 +440,57 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       t.jlim = p.flat ? p.W : p.tw;
       return t;
     };
-    if (!p.norm) {
+    if (p.pm) {
+      // Pixel-major: thread = one pixel of the 128-pixel half (TMEM lane), columns =
+      // output channels; the per-pixel epilogue reads 16 channels at a time.
+      for (int local = 0;; ++local) {
+        const int tile = cta_tile(p, local);
+        if (tile < 0) break;
+        const TileCoord tc = decode_tile(p, tile);
+        const int buf = (nbuf == 2) ? (local & 1) : 0;
+        const int use = (nbuf == 2) ? (local >> 1) : local;
+        if (!mbar_wait(accf_bar(buf), static_cast<uint32_t>(use & 1), abort_flag, lim)) break;
+        tc_fence_after();
+        const CmTile t = tile_view(tc);
+        for (int h = grp; h < p.pm_halves; h += G) {
+          const int n = h * 128 + q * 32 + lane;
+          Pixel px;
+          px.n = tc.nb;
+          px.d = tc.od;
+          const bool in_tile = cm_pixel(t, n, px.h, px.w);
+          px.valid = in_tile && n < t.npix && px.h < E.Ho && px.w < E.Wo;
+          const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                              static_cast<uint32_t>(buf * acc_cols + h * p.pm_cols);
+          auto load = [&](int c_rel, float(&v)[16]) {
+            uint32_t r[16];
+            tmem_ld16(tb + static_cast<uint32_t>(c_rel), r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]);
+          };
+          if (p.k_splits > 1) {
+            // fp32 partial sums, NDHWC-flat [split][M][Cout]
+            const long long pix =
+                (((long long)px.n * E.Do + px.d) * E.Ho + px.h) * (long long)E.Wo + px.w;
+            for (int c = 0; c < E.Cout; c += 16) {
+              float v[16];
+              load(c, v);
+              if (!px.valid) continue;
+              float* dst = p.partial + ((long long)tc.split * p.M_total + pix) * E.Cout + c;
+              const int cnt = min(16, E.Cout - c);
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
+                if (k < cnt) dst[k] = v[k];
+            }
+          } else {
+            epilogue_pixel(p.epi, px, 0, E.Cout, load);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce_bar(buf));
+      }
+    } else if (!p.norm) {
       for (int local = 0;; ++local) {
         const int tile = cta_tile(p, local);
         if (tile < 0) break;

@@ -108,6 +108,12 @@ struct ConvCMParams {
   // one CTA (tpu consecutive tiles per unit; tpu = 1 otherwise)
   int norm, tpu;
   int epi_groups;          // epilogue warpgroups (2 or 3): block = 128 + 128 * epi_groups
+  // Pixel-major mode (Cout <= 128): the MMA takes the activations as A (M = 128 pixels
+  // per half of the pixel tile) and the weights as B (N = pm_n = Cout rounded up to 16);
+  // the accumulator of half h sits at column h * pm_cols, a thread of the epilogue owns
+  // one pixel and needs no staging.
+  int pm, pm_halves, pm_n, pm_cols;
+  int wtap_rows;           // shared-memory weight rows per tap (128, or pm_n)
   uint32_t norm_off;       // shared den[N] (fp32) of the current pixel tile
   int norm_cs;             // channels per scratch row: Cout rounded up to 8
   uint16_t* vscratch;      // [grid][N][norm_cs] bf16 values, one slice per CTA
