@@ -142,6 +142,21 @@ NCDHW_ROW_CASES = [
 ]
 
 
+# NDHWC blocks on one output row go out through bulk tensor stores (y, value, conv);
+# the rest (row ends, strip halo columns, channel tails) through the per-thread path.
+TMA_STORE_CASES = [
+    mk("bulk_store_bias_value", 1, 64, 3, 6, 150, 96, pads=P1,
+       epi=wl.EPI_BIAS | wl.EPI_SAVE_VALUE, index=44),
+    mk("bulk_store_cout200_strip", 1, 32, 2, 9, 61, 200, pads=CR, epi=wl.EPI_BIAS, index=45),
+    mk("bulk_store_flat_valid", 2, 64, 3, 6, 90, 64, pads=VALID, index=46),
+]
+
+
+@pytest.mark.parametrize("call", TMA_STORE_CASES, ids=lambda c: c.name)
+def test_bulk_store_epilogue(call):
+    run_and_check(call, wl.NDHWC, wl.NDHWC)
+
+
 @pytest.mark.parametrize("call", NCDHW_ROW_CASES, ids=lambda c: c.name)
 def test_ncdhw_rows(call):
     gc, _ = run_and_check(call, wl.NDHWC, wl.NCDHW)

@@ -17,8 +17,9 @@ namespace vvc {
 cudaError_t launch_conv_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const ConvTCParams& p,
                            dim3 grid, size_t smem_bytes, cudaStream_t stream);
 cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
-                           const CUtensorMap& tmWgtLast, const ConvCMParams& p, int grid,
-                           size_t smem_bytes, cudaStream_t stream);
+                           const CUtensorMap& tmWgtLast, const CmOutMaps& om,
+                           const ConvCMParams& p, int grid, size_t smem_bytes,
+                           cudaStream_t stream);
 cudaError_t conv_status_read_clear(int* status, cudaStream_t stream);
 cudaError_t conv_cm_status_read_clear(int* status);
 cudaError_t launch_pack_weight(const void* w, void* out, int Co, int Ci, int taps,
@@ -423,6 +424,13 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.num_tiles = static_cast<int>(tiles * splits);
   k.norm = (norm && splits == 1) ? 1 : 0;
   k.tpu = k.norm ? k.tiles_c : 1;
+  // bulk tensor stores for the output blocks that lie on one output row: NDHWC,
+  // value = B(B(conv) + bias) (no residual, norm or bottom/right pad), 16-byte rows
+  k.tma_store = (p->out_layout == CONV3D_NDHWC && splits == 1 && !pm && p->Cout % 8 == 0 &&
+                 !(p->epi & (CONV3D_EPI_RESIDUAL | CONV3D_EPI_L2NORM_SILU |
+                             CONV3D_EPI_OUT_PAD_BR)))
+                    ? 1
+                    : 0;
   k.acc_cols = pm ? k.pm_halves * k.pm_cols : static_cast<int>(round_up(k.N, 32));
   k.nbuf = (2 * k.acc_cols <= 512) ? 2 : 1;
   int cols = 32;
@@ -844,6 +852,31 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
   return CONV3D_OK;
 }
 
+// Output maps of the bulk-store epilogue (NDHWC bf16, box 32 channels x 32 pixels).
+int encode_out_maps(const conv3d_params* p, const Plan& pl, vvc::CmOutMaps* om) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return CONV3D_ERR_CUDA;
+  const cuuint64_t C = (cuuint64_t)p->Cout;
+  const cuuint64_t gdim[5] = {C, (cuuint64_t)pl.Wo, (cuuint64_t)pl.Ho, (cuuint64_t)pl.Do,
+                              (cuuint64_t)p->N};
+  const cuuint64_t gstr[4] = {C * 2, C * 2 * pl.Wo, C * 2 * pl.Wo * pl.Ho,
+                              C * 2 * pl.Wo * pl.Ho * pl.Do};
+  const cuuint32_t box[5] = {32, 32, 1, 1, 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  auto one = [&](void* base, CUtensorMap* m) {
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, gdim, gstr, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  if (!one(p->y, &om->y)) return CONV3D_ERR_CUDA;
+  om->val = om->y;
+  om->conv = om->y;
+  if ((p->epi & CONV3D_EPI_SAVE_VALUE) && !one(p->value_out, &om->val)) return CONV3D_ERR_CUDA;
+  if ((p->epi & CONV3D_EPI_DEBUG_STORE_CONV) && !one(p->conv_out, &om->conv))
+    return CONV3D_ERR_CUDA;
+  return CONV3D_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -932,7 +965,14 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
     ConvCMParams kp = pl.cp;
     if (kp.k_splits > 1) kp.partial = partial;
     if (kp.norm) kp.vscratch = reinterpret_cast<uint16_t*>(ws + pl.vscratch_off);
-    if (vvc::launch_conv_cm(tmA, tmB, tmBLast, kp, static_cast<int>(pl.grid.x), pl.smem, s) !=
+    vvc::CmOutMaps om;
+    if (kp.tma_store) {
+      rc = encode_out_maps(pm, pl, &om);
+      if (rc) return rc;
+    } else {
+      om.y = om.val = om.conv = tmA;  // not used
+    }
+    if (vvc::launch_conv_cm(tmA, tmB, tmBLast, om, kp, static_cast<int>(pl.grid.x), pl.smem, s) !=
         cudaSuccess)
       return CONV3D_ERR_CUDA;
     if (kp.k_splits > 1 &&

@@ -121,6 +121,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     conv_cm_kernel(const __grid_constant__ CUtensorMap tmAct,
                    const __grid_constant__ CUtensorMap tmWgt,
                    const __grid_constant__ CUtensorMap tmWgtLast,
+                   const __grid_constant__ CmOutMaps om,
                    const __grid_constant__ ConvCMParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -509,12 +510,51 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           uint32_t r[32];
           tmem_ld32(tb + static_cast<uint32_t>(j0), r);
           tmem_ld_wait();
-          if (warp_live) cm_block(E, t, st, lane, cw, j0, r, ch);
+          if (!warp_live) continue;
+          if (p.tma_store) {
+            // the warp's previous bulk store has read the staging block
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            const int qq = t.q0 + j0;
+            const int ib = qq / t.pitch;
+            const int jb = qq - ib * t.pitch;
+            const int hr = t.hoff + ib, wr = t.woff + jb;
+            if (jb + 31 < t.jlim && jb + 31 < t.pitch && j0 + 31 < t.npix && hr < E.Ho &&
+                wr + 31 < E.Wo) {
+              // The 32 pixels are one piece of an output row: the block goes out as
+              // [32 pixels][32 channels] bf16 through bulk tensor stores.
+              uint16_t* yt = reinterpret_cast<uint16_t*>(st);
+              uint16_t* ct = yt + 32 * 32;
+              const bool dbg = (E.flags & EPI_DEBUG_STORE_CONV) != 0;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const uint16_t cb = bf16_bits(__uint_as_float(r[j]));
+                uint16_t vb = cb;
+                if (E.flags & EPI_BIAS) vb = bf16_bits(__fadd_rn(bf16_val(cb), ch.bc));
+                yt[j * 32 + lane] = vb;
+                if (dbg) ct[j * 32 + lane] = cb;
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_5d(&om.y, smem_u32(yt), cw, wr, hr, tc.od, tc.nb);
+                if (E.flags & EPI_SAVE_VALUE)
+                  tma_store_5d(&om.val, smem_u32(yt), cw, wr, hr, tc.od, tc.nb);
+                if (dbg) tma_store_5d(&om.conv, smem_u32(ct), cw, wr, hr, tc.od, tc.nb);
+                bulk_commit_group();
+              }
+              continue;
+            }
+          }
+          cm_block(E, t, st, lane, cw, j0, r, ch);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acce_bar(buf));
       }
+      // every bulk store of this warp completes before the CTA can exit
+      if (p.tma_store && lane == 0) bulk_wait_all();
+      __syncwarp();
     } else {
       // Fused L2 norm: pass 1 per channel tile, pass 2 once per pixel tile.  Every
       // epilogue warp runs the same sequence of named barriers: after a failed wait
@@ -591,7 +631,8 @@ cudaError_t conv_cm_status_read_clear(int* status) {
 }
 
 cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
-                           const CUtensorMap& tmWgtLast, const ConvCMParams& p, int grid,
+                           const CUtensorMap& tmWgtLast, const CmOutMaps& om,
+                           const ConvCMParams& p, int grid,
                            size_t smem_bytes, cudaStream_t stream) {
   static size_t configured = 0;
   if (smem_bytes > configured) {
@@ -602,7 +643,7 @@ cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
     configured = smem_bytes;
   }
   conv_cm_kernel<<<grid, 128 + 128 * p.epi_groups, smem_bytes, stream>>>(tmAct, tmWgt,
-                                                                        tmWgtLast, p);
+                                                                        tmWgtLast, om, p);
   return cudaGetLastError();
 }
 

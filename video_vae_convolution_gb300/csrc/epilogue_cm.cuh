@@ -63,6 +63,7 @@ constexpr int kStageFloats = 32 * kStageVec;  // per warp
 struct CmChan {
   int c0, cnt;
   float b[8], rb[8];
+  float bc;  // bias of the thread's own TMEM channel (bulk-store blocks)
 };
 
 __device__ __forceinline__ CmChan cm_chan(const CmEpi& E, int cw, int lane) {
@@ -75,6 +76,7 @@ __device__ __forceinline__ CmChan cm_chan(const CmEpi& E, int cw, int lane) {
     c.b[e] = ((E.flags & EPI_BIAS) && in) ? __ldg(E.bias + c.c0 + e) : 0.0f;
     c.rb[e] = ((E.flags & EPI_RESIDUAL_BIAS) && in) ? __ldg(E.rbias + c.c0 + e) : 0.0f;
   }
+  c.bc = ((E.flags & EPI_BIAS) && cw + lane < E.Cout) ? __ldg(E.bias + cw + lane) : 0.0f;
   return c;
 }
 

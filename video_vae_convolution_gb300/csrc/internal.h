@@ -1,6 +1,7 @@
 // Host/device parameter blocks shared by the launcher (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cstdint>
 
 namespace vvc {
@@ -114,9 +115,18 @@ struct ConvCMParams {
   // one pixel and needs no staging.
   int pm, pm_halves, pm_n, pm_cols;
   int wtap_rows;           // shared-memory weight rows per tap (128, or pm_n)
+  int tma_store;           // NDHWC output blocks on one output row are written by bulk
+                           // tensor stores (y, value, conv maps) from the staging block
   uint32_t norm_off;       // shared den[N] (fp32) of the current pixel tile
   int norm_cs;             // channels per scratch row: Cout rounded up to 8
   uint16_t* vscratch;      // [grid][N][norm_cs] bf16 values, one slice per CTA
+};
+
+// Output tensor maps of the channel-major kernel's bulk-store epilogue (NDHWC,
+// bf16, box = 32 channels x 32 pixels along W): y, value_out and conv_out (the
+// last two repeat y when not requested).
+struct CmOutMaps {
+  CUtensorMap y, val, conv;
 };
 
 }  // namespace vvc
