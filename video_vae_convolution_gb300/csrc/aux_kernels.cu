@@ -142,6 +142,56 @@ __global__ void __launch_bounds__(256) im2col_hw_kernel(const Im2colArgs a) {
   }
 }
 
+// The same gather for 3 x 3 spatial taps and a fixed channel count: every tap's
+// loads are issued before the values are packed (the loop above waits for each
+// load in turn).
+template <int C>
+__global__ void __launch_bounds__(256) im2col_3x3_kernel(const Im2colArgs a) {
+  const int xblocks = (a.Wo + 255) / 256;
+  if (static_cast<int>(blockIdx.x) >= xblocks) return;  // weights: the generic kernel's blocks
+  const int wo = blockIdx.x * 256 + threadIdx.x;
+  if (wo >= a.Wo) return;
+  const int ho = blockIdx.y;
+  const int nd = blockIdx.z;
+  const int n = nd / a.D, d = nd - n * a.D;
+  const long long plane = (long long)a.H * a.W;
+  const long long cstride = (a.layout == LAYOUT_NDHWC) ? 1 : (long long)a.D * plane;
+  const long long base = (a.layout == LAYOUT_NDHWC)
+                             ? ((long long)n * a.D + d) * plane * C
+                             : ((long long)n * C * a.D + d) * plane;
+  const int pix_stride = (a.layout == LAYOUT_NDHWC) ? C : 1;
+  constexpr int kVals = 9 * C;
+  constexpr int kGroups = (kVals + 7) / 8;
+  uint16_t v[kGroups * 8];
+#pragma unroll
+  for (int r = 0; r < 3; ++r) {
+    const int h = pad_index(ho * a.sh + r - a.ph, a.H, a.reflect_h);
+#pragma unroll
+    for (int s = 0; s < 3; ++s) {
+      const int w = pad_index(wo * a.sw + s - a.pw, a.W, a.reflect_w);
+      const bool in = h >= 0 && h < a.H && w >= 0 && w < a.W;
+      const long long pos = base + ((long long)(in ? h : 0) * a.W + (in ? w : 0)) * pix_stride;
+#pragma unroll
+      for (int c = 0; c < C; ++c)
+        v[(r * 3 + s) * C + c] = in ? __ldg(a.x + pos + c * cstride) : uint16_t(0);
+    }
+  }
+#pragma unroll
+  for (int e = kVals; e < kGroups * 8; ++e) v[e] = 0;
+  uint4* dst = reinterpret_cast<uint4*>(a.out) +
+               ((((long long)nd * a.Ho + ho) * a.Wo + wo) * (a.Ck / 8));
+#pragma unroll
+  for (int g = 0; g < kGroups; ++g) {
+    uint4 q;
+    q.x = v[8 * g] | (uint32_t(v[8 * g + 1]) << 16);
+    q.y = v[8 * g + 2] | (uint32_t(v[8 * g + 3]) << 16);
+    q.z = v[8 * g + 4] | (uint32_t(v[8 * g + 5]) << 16);
+    q.w = v[8 * g + 6] | (uint32_t(v[8 * g + 7]) << 16);
+    dst[g] = q;
+  }
+  for (int g = kGroups; g < a.Ck / 8; ++g) dst[g] = make_uint4(0, 0, 0, 0);
+}
+
 cudaError_t launch_im2col_hw(const void* x, int layout, int N, int C, int D, int H, int W, int Ho,
                              int Wo, int KT, int KR, int KS, int sh, int sw, int ph, int pw,
                              int reflect_h, int reflect_w, int Ck, void* out, const void* wp,
@@ -163,6 +213,25 @@ cudaError_t launch_im2col_hw(const void* x, int layout, int N, int C, int D, int
   const int xblocks = (Wo + 255) / 256;
   a.iblocks = xblocks;
   const int wblocks = 8;
+  if (KR == 3 && KS == 3 && C >= 1 && C <= 7) {
+    // gather through the unrolled kernel; the generic one only repacks the weights
+    const dim3 g(xblocks, Ho, N * D);
+    switch (C) {
+      case 1: im2col_3x3_kernel<1><<<g, 256, 0, s>>>(a); break;
+      case 2: im2col_3x3_kernel<2><<<g, 256, 0, s>>>(a); break;
+      case 3: im2col_3x3_kernel<3><<<g, 256, 0, s>>>(a); break;
+      case 4: im2col_3x3_kernel<4><<<g, 256, 0, s>>>(a); break;
+      case 5: im2col_3x3_kernel<5><<<g, 256, 0, s>>>(a); break;
+      case 6: im2col_3x3_kernel<6><<<g, 256, 0, s>>>(a); break;
+      default: im2col_3x3_kernel<7><<<g, 256, 0, s>>>(a); break;
+    }
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    Im2colArgs aw = a;
+    aw.Wo = 0;  // no row pieces: every block of this launch repacks weights
+    im2col_hw_kernel<<<dim3(wblocks, 1, 1), 256, 0, s>>>(aw);
+    return cudaGetLastError();
+  }
   im2col_hw_kernel<<<dim3(xblocks + wblocks, Ho, N * D), 256, 0, s>>>(a);
   return cudaGetLastError();
 }
