@@ -287,6 +287,21 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
       }
     }
     if (best < 0) return CONV3D_ERR_UNSUPPORTED;
+    // A layer that runs as one wave of work items (and too many items for a split of
+    // its reduction) finishes with its slowest item: fewer rows per tile (a smaller N)
+    // are faster as long as the items still fit in one wave.
+    {
+      const long long per_tile = (long long)Do * p->N * cdiv(p->Cout, 128);
+      const int nt = static_cast<int>(cdiv(Wo, tw));
+      const int pitch = static_cast<int>(round_up(tw + p->KS - 1, 8));
+      auto items = [&](int r) { return nt * cdiv(Ho, r) * per_tile; };
+      const int sms1 = num_sms();
+      if (tw + p->KS - 1 <= 256 && items(rh) <= sms1 && 2 * items(rh) >= sms1) {
+        while (rh > 1 && items(rh - 1) <= sms1 &&
+               round_up((long long)(rh - 2) * pitch + tw, 16) <= 256)
+          --rh;
+      }
+    }
     halo = true;
   } else {
     const int maxw = std::min(256, 256 / sw);
