@@ -350,22 +350,49 @@ def run_gpu(args, rank, world):
                 "peak_source": pk["source"] + " burst bf16",
                 "algorithmic_bytes": dom_call.bytes()}
 
-    # e2e: pinned host inputs -> device, chain, outputs -> pinned host
+    # e2e: pinned host inputs -> device, the chain through the C ABI, outputs -> pinned
+    # host, every step.  The calls are independent, so the copies run on their own
+    # streams: call i's input copy overlaps call i-1's convolution and call i-2's
+    # output copy (events order each call's copy-in, convolution and copy-out, and a
+    # buffer is rewritten only after the previous step is done with it).
     outs_host = [torch.empty(c.y.shape, dtype=torch.bfloat16).pin_memory() for _, _, c in calls]
     h2d = sum(h.numel() * 2 for h in host)
     d2h = sum(o.numel() * 2 for o in outs_host)
     e2e_steps = max(1, min(args.steps, 5))
+    # one copy stream per direction (splitting a copy over several streams measured
+    # slower: concurrent copies in one direction contend)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n = len(calls)
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_conv = [torch.cuda.Event() for _ in range(n)]
+    ev_out = [torch.cuda.Event() for _ in range(n)]
     barrier(world)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(e2e_steps):
-        for (call, lay, c), h in zip(calls, host):
-            c.x.copy_(h, non_blocking=True)
-        chain()
-        for (call, lay, c), o in zip(calls, outs_host):
-            o.copy_(c.y, non_blocking=True)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for step in range(e2e_steps):
+        for i, ((call, lay, c), h, o) in enumerate(zip(calls, host, outs_host)):
+            if step:
+                s_in.wait_event(ev_conv[i])    # the previous step has read c.x
+            with torch.cuda.stream(s_in):
+                c.x.copy_(h, non_blocking=True)
+            ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            if step:
+                stream.wait_event(ev_out[i])   # the previous step's c.y has been copied out
+            rc = c.run(stream)
+            if rc != 0:
+                raise RuntimeError(f"conv3d_fwd failed: {rc}")
+            ev_conv[i].record(stream)
+            s_out.wait_event(ev_conv[i])
+            with torch.cuda.stream(s_out):
+                o.copy_(c.y, non_blocking=True)
+            ev_out[i].record(s_out)
+    for i in range(n):
+        stream.wait_event(ev_out[i])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
