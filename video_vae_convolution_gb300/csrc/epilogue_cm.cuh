@@ -412,6 +412,24 @@ __device__ __forceinline__ void cm_block(const CmEpi& E, const CmTile& t, float*
       const long long yo0 = ((long long)t.nb * E.Cout + cw) * E.Do * plane_y +
                             (long long)t.od * plane_y + (long long)h * E.Wy + w;
       const long long cstep_o = (long long)E.Do * plane_o, cstep_y = (long long)E.Do * plane_y;
+      if (!(E.flags & (EPI_RESIDUAL | EPI_SAVE_VALUE | EPI_DEBUG_STORE_CONV)) && !E.pad) {
+        // y = B(B(conv) + bias): one pointer stepping through the channel planes; the
+        // bias of channel cw + cc comes from lane cc, which holds it for its own channel
+        const bool bias = (E.flags & EPI_BIAS) != 0;
+        uint16_t* yp = E.y + yo0;
+#pragma unroll 8
+        for (int cc = 0; cc < 32; ++cc) {
+          const float bc = __shfl_sync(0xffffffffu, ch.bc, cc);
+          if (cc < cend && pv) {
+            float v = round_bf16(stage[lane][cc]);
+            if (bias) v = __fadd_rn(v, bc);
+            *yp = bf16_bits(v);
+          }
+          yp += cstep_y;
+        }
+        __syncwarp();  // the staging block is rewritten by the next block
+        return;
+      }
       for (int cc0 = 0; cc0 < cend; cc0 += 8) {
         float v[8];
         uint16_t cb[8];
