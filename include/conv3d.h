@@ -154,6 +154,11 @@ typedef struct {
   int32_t im2col;      /* 0 auto, 1 on, 2 off: for Cin * KR * KS <= 64 (Cin < 8) gather
                           the spatial taps into a staged tensor first and run a
                           (KT, 1, 1) convolution over it */
+  int32_t pair;        /* 0 auto (from 4 tap pairs up), 1 on (from 2), 2 off: when the
+                          last 64-channel chunk of the input holds at most 32 channels
+                          (Cin = 96, 160, ...), run the last chunks of two consecutive
+                          (kt, kr) tap pairs as one pipeline stage of 64-byte rows
+                          instead of one half-empty stage each */
 } conv3d_tuning;
 
 /* ---- weight packing ([cuDNN page] "Weight Packing") ------------------------------ */
@@ -207,6 +212,25 @@ int conv3d_fwd_static_scratch(const conv3d_params* p, conv3d_stream_t stream);
 /* Number of kernel launches conv3d_fwd(_ex) enqueues for *p (for accounting). */
 int conv3d_launch_count(const conv3d_params* p, const conv3d_tuning* tuning);
 
+/* The plan conv3d_fwd_ex would run for *p (tests and tuning).  Host only: no
+ * device work; the SM count comes from the current device (152 when there is
+ * none).  Returns CONV3D_OK and fills *info, or the error the call would return
+ * for an unsupported or invalid *p. */
+typedef struct {
+  int32_t kernel;           /* 1 pixel-major kernel (M = pixels), 2 channel-major
+                               persistent kernel (M = output channels) */
+  int32_t mma_n;            /* MMA N: pixels per tile (channel-major) or output
+                               channels per tile (pixel-major) */
+  int32_t stages_per_tile;  /* pipeline stages of one tile's whole reduction */
+  int32_t k_splits;         /* split of the reduction across CTAs */
+  int32_t paired;           /* 1: the last chunks of two tap pairs share a stage */
+  int32_t im2col;           /* 1: the spatial taps are gathered before the conv */
+  int32_t launches;         /* kernel launches of the call */
+  int32_t grid;             /* CTAs of the convolution kernel */
+} conv3d_plan_info;
+
+int conv3d_plan(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_plan_info* info);
+
 /* ---- standalone post-operations ([cuDNN page] "Standalone Normalization and
  *      Padding Variant", contiguous output) ---------------------------------------
  * x: bf16 [rows][C] (rows = N*T*H*W, channels last).  main = B(x + input_bias) when
@@ -231,7 +255,8 @@ const char* conv3d_status_string(int status);
 int conv3d_version(void);
 
 /* sizeof() of the ABI structs, for bindings to check their mirrors:
- * which = 0 conv3d_params, 1 conv3d_tuning, 2 conv3d_pad; 0 otherwise. */
+ * which = 0 conv3d_params, 1 conv3d_tuning, 2 conv3d_pad, 3 conv3d_plan_info;
+ * 0 otherwise. */
 size_t conv3d_struct_size(int which);
 
 #ifdef __cplusplus

@@ -253,6 +253,39 @@ def test_im2col_narrow_input(call, layout):
     assert gc.c.launches >= 2  # the gather runs before the convolution
 
 
+# Paired last chunks: Cin % 64 in 1..32, so the last 32-channel chunks of two tap
+# pairs share a pipeline stage (odd and even pair counts, flat and strip tiles,
+# reflect H, two channel tiles, three chunks, a single chunk, the fused norm).
+RH = ((2, 0, Z), (1, 1, R), (0, 0, Z))    # causal T + reflect H, no W pad
+ONE = vvc.Tuning(k_splits=1, pair=1)        # small cases would otherwise split the reduction
+PAIR_CASES = [
+    (mk("pair_96_flat_valid", 1, 96, 4, 9, 70, 96, pads=VALID, index=41), ONE),
+    (mk("pair_96_strip_zero", 1, 96, 3, 11, 40, 64, index=42), ONE),
+    (mk("pair_160_k2_two_ctiles", 1, 160, 3, 7, 37, 200, kernel=(2, 3, 3),
+        pads=((1, 0, Z), (1, 1, Z), (1, 1, Z)), epi=wl.EPI_BIAS, index=43), ONE),
+    (mk("pair_96_t1_residual", 2, 96, 1, 13, 50, 96, kernel=(1, 3, 3), pads=P2D,
+        epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_RESIDUAL_BIAS, index=44), ONE),
+    (mk("pair_96_reflect_h", 1, 96, 4, 10, 33, 96, pads=RH, index=45), ONE),
+    (mk("pair_24_one_chunk", 1, 24, 3, 8, 45, 48, pads=VALID, index=46), vvc.Tuning(kc=64, k_splits=1, pair=1)),
+    (mk("pair_96_norm", 1, 96, 3, 8, 40, 160, pads=VALID,
+        epi=wl.EPI_BIAS | wl.EPI_L2NORM_SILU, index=47), ONE),
+]
+
+
+@pytest.mark.parametrize("case", PAIR_CASES, ids=lambda c: c[0].name)
+@pytest.mark.parametrize("layout", [wl.NDHWC, wl.NCDHW])
+def test_paired_last_chunks(case, layout):
+    call, tuning = case
+    gc, _ = run_and_check(call, layout, layout, tuning=tuning)
+    assert gc.c.plan.kernel == 2 and gc.c.plan.paired == 1
+
+
+def test_paired_off_matches_oracle():
+    call = PAIR_CASES[0][0]
+    gc, _ = run_and_check(call, tuning=vvc.Tuning(pair=2, k_splits=1))
+    assert gc.c.plan.paired == 0
+
+
 def test_epilogue_split_k_matches():
     call = mk("epi_split", 1, 64, 3, 5, 70, 160, pads=P1,
               epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_L2NORM_SILU, index=17)

@@ -118,6 +118,48 @@ def test_workspace_and_launch_plan():
                                    ctypes.byref(vvc.Tuning(k_splits=1))) == 1
 
 
+def _plan(p, t=None):
+    info = vvc.PlanInfo()
+    rc = vvc._lib().conv3d_plan(ctypes.byref(p), None if t is None else ctypes.byref(t),
+                                ctypes.byref(info))
+    assert rc == vvc.OK
+    return info
+
+
+def _valid(**kw):
+    p = _params(**kw)
+    for i in range(3):
+        p.pad[i].before = p.pad[i].after = 0
+    return p
+
+
+def test_plan_paired_last_chunks():
+    # 96 input channels = one 64-channel chunk + 32: with paired last chunks a 3x3x3
+    # tile runs 9 full stages + ceil(9 / 2) shared ones instead of 9 + 9
+    p = _valid(Cin=96, Cout=96, D=6, H=354, W=642)
+    on = _plan(p)
+    off = _plan(p, vvc.Tuning(pair=2))
+    assert (on.kernel, on.paired, on.stages_per_tile, on.k_splits) == (2, 1, 14, 1)
+    assert (off.paired, off.stages_per_tile) == (0, 18)
+    assert on.mma_n == off.mma_n == 256
+    # 1x3x3 (T = 1): 3 tap pairs stay unpaired unless asked (-> 3 + 2 stages)
+    t1 = _valid(N=4, Cin=96, Cout=96, D=1, H=353, W=641, KT=1)
+    assert (_plan(t1).paired, _plan(t1).stages_per_tile) == (0, 6)
+    forced = _plan(t1, vvc.Tuning(pair=1))
+    assert (forced.paired, forced.stages_per_tile) == (1, 5)
+    # 160 channels: two full chunks per pair + shared last chunks (9 * 2 + 5)
+    assert _plan(_valid(Cin=160, Cout=160, D=8, H=106, W=182)).stages_per_tile == 23
+    # not paired: whole chunks (128), last chunk over 32 channels (112), a split
+    # reduction, reflect padding along W, a single tap pair (1x1x1)
+    assert _plan(_valid(Cin=128, Cout=128, D=6, H=354, W=642)).paired == 0
+    assert _plan(_valid(Cin=112, Cout=96, D=6, H=354, W=642)).paired == 0
+    assert _plan(p, vvc.Tuning(k_splits=2)).paired == 0
+    rw = _params(Cin=96, Cout=96, D=6, H=66, W=130)
+    rw.pad[2].mode = vvc.PAD_REFLECT
+    assert _plan(rw).paired == 0
+    assert _plan(_valid(Cin=96, Cout=96, KT=1, KR=1, KS=1)).paired == 0
+
+
 def test_l2norm_validation():
     lib = vvc._lib()
     assert lib.l2norm_silu(None, 10, 16, None, None, None, 0x1000, 0x2000, None, None) == \

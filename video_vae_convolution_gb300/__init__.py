@@ -45,7 +45,7 @@ EXPORTS = (
     "conv3d_packed_weight_bytes", "conv3d_pack_weight", "conv3d_workspace_bytes",
     "conv3d_workspace_bytes_ex", "conv3d_fwd", "conv3d_fwd_ex", "conv3d_launch_count",
     "l2norm_silu", "conv3d_get_device_status", "conv3d_status_string", "conv3d_version",
-    "conv3d_struct_size", "conv3d_fwd_static_scratch",
+    "conv3d_struct_size", "conv3d_fwd_static_scratch", "conv3d_plan",
 )
 
 
@@ -81,12 +81,18 @@ class Params(ctypes.Structure):
 class Tuning(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "tile_w", "tile_h", "R", "kc", "BN", "halo", "stages", "k_splits", "kernel",
-        "inject", "timeout_ms", "im2col")]
+        "inject", "timeout_ms", "im2col", "pair")]
 
     def __init__(self, **kw):
         super().__init__()
         for k, v in kw.items():
             setattr(self, k, int(v))
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "kernel", "mma_n", "stages_per_tile", "k_splits", "paired", "im2col", "launches",
+        "grid")]
 
 
 _LIB = None
@@ -121,6 +127,8 @@ def _lib():
                 lib.conv3d_fwd_static_scratch.restype = ctypes.c_int
                 lib.conv3d_launch_count.argtypes = [P, T]
                 lib.conv3d_launch_count.restype = ctypes.c_int
+                lib.conv3d_plan.argtypes = [P, T, ctypes.POINTER(PlanInfo)]
+                lib.conv3d_plan.restype = ctypes.c_int
                 lib.l2norm_silu.argtypes = [vp, i64, i32, vp, vp, vp, vp, vp, vp, vp]
                 lib.l2norm_silu.restype = ctypes.c_int
                 lib.conv3d_get_device_status.argtypes = [ctypes.POINTER(i32), vp]
@@ -131,7 +139,7 @@ def _lib():
                 lib.conv3d_version.restype = ctypes.c_int
                 lib.conv3d_struct_size.argtypes = [ctypes.c_int]
                 lib.conv3d_struct_size.restype = sz
-                for which, st in ((0, Params), (1, Tuning), (2, Pad)):
+                for which, st in ((0, Params), (1, Tuning), (2, Pad), (3, PlanInfo)):
                     if lib.conv3d_struct_size(which) != ctypes.sizeof(st):
                         raise RuntimeError(f"ABI struct mismatch for {st.__name__}")
                 _LIB = lib
@@ -266,6 +274,8 @@ class Conv3d:
         self.value_out, self.conv_out, self.workspace = value_out, conv_out, workspace
         self.bias, self.residual, self.residual_bias, self.gamma = bias, residual, residual_bias, gamma
         self.launches = _lib().conv3d_launch_count(ctypes.byref(p), tp)
+        self.plan = PlanInfo()
+        _check(_lib().conv3d_plan(ctypes.byref(p), tp, ctypes.byref(self.plan)), "conv3d_plan")
 
     def run(self, stream=None) -> int:
         tp = ctypes.byref(self.tuning) if self.tuning is not None else None

@@ -18,8 +18,8 @@ cudaError_t launch_conv_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const
                            dim3 grid, size_t smem_bytes, cudaStream_t stream);
 cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
                            const CUtensorMap& tmWgtLast, const CmOutMaps& om,
-                           const ConvCMParams& p, int grid, size_t smem_bytes,
-                           cudaStream_t stream);
+                           const CmHalfMaps& half, const ConvCMParams& p, int grid,
+                           size_t smem_bytes, cudaStream_t stream);
 cudaError_t conv_status_read_clear(int* status, cudaStream_t stream);
 cudaError_t conv_cm_status_read_clear(int* status);
 cudaError_t launch_pack_weight(const void* w, void* out, int Co, int Ci, int taps,
@@ -43,7 +43,7 @@ using vvc::ConvTCParams;
 using vvc::EpiParams;
 
 constexpr size_t kMaxSmem = 232448;  // sm_100 / sm_103 opt-in dynamic shared memory per block
-constexpr int kDefaultSMs = 148;
+constexpr int kDefaultSMs = 152;  // GB300
 // Per-warp epilogue staging block of the channel-major kernel (kStageFloats fp32).
 constexpr size_t kEpiWarpBytes = 32 * 36 * 4;
 
@@ -432,7 +432,29 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   // with the fused norm the channel tiles of a pixel tile share a CTA, so the
   // parallelism that decides the split is the number of pixel tiles
   const long long par = norm ? tiles / k.tiles_c : tiles;
-  const int splits = choose_splits(t, par, k.stages_total, sms, &per);
+  // Paired last chunks: the last 64-channel chunk of a tap pair holds at most 32 real
+  // channels, so two tap pairs share one stage of 32-channel rows (every stage then
+  // carries a full 64-channel MMA group).  One split only; not with the reflect-W
+  // patch (it rewrites 128-byte rows) or the pixel-major mode.  Automatic from four
+  // tap pairs up (3x3x3: 18 -> 14 stages for 96 channels, -5 % time measured); with
+  // three (1x3x3) the saved stage did not pay.
+  const int n_pairs = p->KT * p->KR;
+  const int last_ch = pl->Cst - (k.n_chunks - 1) * kc;
+  const bool reflect_w_pad =
+      p->pad[2].mode == CONV3D_PAD_REFLECT && (p->pad[2].before || p->pad[2].after);
+  const bool pair_ok = t.pair != 2 && !pm && halo && kc == 64 && last_ch >= 1 && last_ch <= 32 &&
+                       n_pairs >= (t.pair == 1 ? 2 : 4) && !reflect_w_pad;
+  int splits = 0;
+  if (pair_ok) {
+    const int total = n_pairs * (k.n_chunks - 1) + (n_pairs + 1) / 2;
+    splits = choose_splits(t, par, total, sms, &per);
+    if (splits == 1) {
+      k.pair = 1;
+      k.stages_total = total;
+    }
+  }
+  if (!k.pair) splits = choose_splits(t, par, k.stages_total, sms, &per);
+  k.n_pairs = n_pairs;
   k.k_splits = splits;
   k.stages_per_split = per;
   if (tiles * splits > 0x7fffffffLL) return CONV3D_ERR_UNSUPPORTED;
@@ -799,7 +821,7 @@ CUtensorMapSwizzle swizzle_of(int kc) {
 }
 
 int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtensorMap* tmA,
-                CUtensorMap* tmB, CUtensorMap* tmBLast) {
+                CUtensorMap* tmB, CUtensorMap* tmBLast, vvc::CmHalfMaps* half) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return CONV3D_ERR_CUDA;
   int kc, act_box, es_w, wgt_rows, wgt_rows_last, cp64;
@@ -854,6 +876,27 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
           boxB, esB, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kc),
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
+  if (half) {
+    // paired last chunks: the same tensors in 32-channel boxes with 64-byte rows
+    if (pl.cm && pl.cp.pair) {
+      cuuint32_t boxAh[5] = {32, boxA[1], boxA[2], boxA[3], boxA[4]};
+      r = enc(&half->act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rankA, const_cast<void*>(xin), gdimA,
+              gstrA, boxAh, esA, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
+      const cuuint32_t rows[2] = {(cuuint32_t)wgt_rows, (cuuint32_t)wgt_rows_last};
+      CUtensorMap* dst[2] = {&half->wgt, &half->wgt_last};
+      for (int i = 0; i < 2; ++i) {
+        cuuint32_t boxBh[2] = {32, rows[i]};
+        r = enc(dst[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p->w_packed), gdimB,
+                gstrB, boxBh, esB, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
+      }
+    } else {
+      half->act = half->wgt = half->wgt_last = *tmB;  // not used
+    }
+  }
   // the last 128-channel tile: a box of its real rows only
   if (wgt_rows_last == wgt_rows) {
     *tmBLast = *tmB;
@@ -939,6 +982,33 @@ int conv3d_launch_count(const conv3d_params* p, const conv3d_tuning* tuning) {
   return pl.launches;
 }
 
+int conv3d_plan(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_plan_info* info) {
+  if (!info) return CONV3D_ERR_INVALID_ARG;
+  Plan pl;
+  const int rc = make_plan(p, tuning, &pl);
+  if (rc) return rc;
+  conv3d_plan_info r{};
+  if (pl.cm) {
+    const ConvCMParams& k = pl.cp;
+    r.kernel = 2;
+    r.mma_n = k.N;
+    r.stages_per_tile = k.stages_total;
+    r.k_splits = k.k_splits;
+    r.paired = k.pair;
+  } else {
+    const ConvTCParams& k = pl.kp;
+    r.kernel = 1;
+    r.mma_n = k.BN;
+    r.stages_per_tile = k.stages_total;
+    r.k_splits = k.k_splits;
+  }
+  r.im2col = pl.im2col ? 1 : 0;
+  r.launches = pl.launches;
+  r.grid = static_cast<int32_t>(pl.grid.x);
+  *info = r;
+  return CONV3D_OK;
+}
+
 int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_stream_t stream) {
   Plan pl;
   int rc = make_plan(p, tuning, &pl);
@@ -973,7 +1043,8 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
     xin = dst;
   }
   CUtensorMap tmA, tmB, tmBLast;
-  rc = encode_maps(pm, pl, xin, &tmA, &tmB, &tmBLast);
+  vvc::CmHalfMaps half;
+  rc = encode_maps(pm, pl, xin, &tmA, &tmB, &tmBLast, &half);
   if (rc) return rc;
   float* partial = reinterpret_cast<float*>(ws + pl.partial_off);
   if (pl.cm) {
@@ -987,7 +1058,8 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
     } else {
       om.y = om.val = om.conv = tmA;  // not used
     }
-    if (vvc::launch_conv_cm(tmA, tmB, tmBLast, om, kp, static_cast<int>(pl.grid.x), pl.smem, s) !=
+    if (vvc::launch_conv_cm(tmA, tmB, tmBLast, om, half, kp, static_cast<int>(pl.grid.x), pl.smem,
+                            s) !=
         cudaSuccess)
       return CONV3D_ERR_CUDA;
     if (kp.k_splits > 1 &&
@@ -1089,6 +1161,7 @@ extern "C" size_t conv3d_struct_size(int which) {
     case 0: return sizeof(conv3d_params);
     case 1: return sizeof(conv3d_tuning);
     case 2: return sizeof(conv3d_pad);
+    case 3: return sizeof(conv3d_plan_info);
     default: return 0;
   }
 }

@@ -71,6 +71,7 @@ __device__ __forceinline__ TileCoord decode_tile(const ConvCMParams& p, int tile
 
 struct StageCoord {
   int t, r, sblk, ch;
+  int pi, np;  // paired schedule: tap pair index; 0 = full chunk, else pairs in the stage
 };
 
 __device__ __forceinline__ StageCoord decode_stage(const ConvCMParams& p, int it) {
@@ -102,6 +103,51 @@ __device__ __forceinline__ void next_stage(const ConvCMParams& p, StageCoord& c)
   ++c.t;
 }
 
+// Paired schedule (ConvCMParams::pair): per group of two tap pairs, the full
+// chunks of the first pair, those of the second, then the last chunks of both in
+// one stage.  (t, r) are the coordinates of tap pair pi (pi = t * KR + r).
+__device__ __forceinline__ void pair_step(const ConvCMParams& p, int& t, int& r) {
+  if (++r == p.KR) {
+    r = 0;
+    ++t;
+  }
+}
+
+__device__ __forceinline__ StageCoord pair_begin(const ConvCMParams& p) {
+  StageCoord c;
+  c.t = c.r = c.sblk = c.pi = 0;
+  c.ch = p.n_chunks > 1 ? 0 : p.n_chunks - 1;
+  c.np = p.n_chunks > 1 ? 0 : min(2, p.n_pairs);
+  return c;
+}
+
+__device__ __forceinline__ void pair_next(const ConvCMParams& p, StageCoord& c) {
+  if (c.np == 0) {
+    if (++c.ch < p.n_chunks - 1) return;
+    c.ch = 0;
+    if ((c.pi & 1) == 0 && c.pi + 1 < p.n_pairs) {  // the group's second pair
+      ++c.pi;
+      pair_step(p, c.t, c.r);
+      return;
+    }
+    if (c.pi & 1) {  // back to the group's first pair for its last-chunk stage
+      --c.pi;
+      if (--c.r < 0) {
+        c.r = p.KR - 1;
+        --c.t;
+      }
+    }
+    c.np = min(2, p.n_pairs - c.pi);
+    c.ch = p.n_chunks - 1;
+    return;
+  }
+  c.pi += 2;  // next group
+  pair_step(p, c.t, c.r);
+  pair_step(p, c.t, c.r);
+  c.np = p.n_chunks > 1 ? 0 : min(2, p.n_pairs - c.pi);
+  c.ch = p.n_chunks > 1 ? 0 : p.n_chunks - 1;
+}
+
 __device__ __forceinline__ void stage_range(const ConvCMParams& p, int split, int& b, int& e) {
   b = split * p.stages_per_split;
   e = min(p.stages_total, b + p.stages_per_split);
@@ -122,6 +168,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                    const __grid_constant__ CUtensorMap tmWgt,
                    const __grid_constant__ CUtensorMap tmWgtLast,
                    const __grid_constant__ CmOutMaps om,
+                   const __grid_constant__ CmHalfMaps hm,
                    const __grid_constant__ ConvCMParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -158,6 +205,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     tma_prefetch_desc(&tmAct);
     tma_prefetch_desc(&tmWgt);
     tma_prefetch_desc(&tmWgtLast);
+    if (p.pair) {
+      tma_prefetch_desc(&hm.act);
+      tma_prefetch_desc(&hm.wgt);
+      tma_prefetch_desc(&hm.wgt_last);
+    }
   }
   if (warp == kWarpMMA) {
     tmem_alloc(smem_u32(tmem_slot), static_cast<uint32_t>(p.tmem_cols));
@@ -191,8 +243,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                                      : (last_ct ? p.tx_bytes_last : p.tx_bytes) - p.act_tx;
         int it_b, it_e;
         stage_range(p, tc.split, it_b, it_e);
-        StageCoord sc = decode_stage(p, it_b);
-        for (int it = it_b; it < it_e; ++it, next_stage(p, sc)) {
+        StageCoord sc = p.pair ? pair_begin(p) : decode_stage(p, it_b);
+        for (int it = it_b; it < it_e; ++it, p.pair ? pair_next(p, sc) : next_stage(p, sc)) {
           if (!mbar_wait(empty_bar(slot), phase ^ 1u, abort_flag, lim)) {
             ok = false;
             break;
@@ -200,11 +252,46 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           const bool skip = (p.inject > 0 && k_global == p.inject - 1);
           if (!skip) {
             const uint32_t full = full_bar(slot);
-            mbar_arrive_expect_tx(full, tx);
+            const int np = p.pair ? sc.np : 0;
+            mbar_arrive_expect_tx(full, np == 0 ? tx : (tx >> 1) * static_cast<uint32_t>(np));
             const uint32_t act = sbase + p.stage_bytes * slot;
             const uint32_t wgt = act + p.act_bytes;
             const int d_in = tc.od * p.st + sc.t - p.pt;
-            if (!act_role) {
+            if (np > 0) {
+              // last chunks of np tap pairs as 32-channel rows of 64 bytes: pair j's
+              // run at act + j * act_bytes / 2, its taps' weights after pair j - 1's
+              int tj = sc.t, rj = sc.r;
+              for (int j = 0; j < np; ++j) {
+                if (j) pair_step(p, tj, rj);
+                if (!act_role) {
+                  const CUtensorMap* hw = last_ct ? &hm.wgt_last : &hm.wgt;
+                  for (int tl = 0; tl < p.KS; ++tl) {
+                    const int tap = (tj * p.KR + rj) * p.KS + tl;
+                    tma_load_2d(wgt + static_cast<uint32_t>((j * p.KS + tl) * p.wtap_rows * 64), hw,
+                                full, tap * p.cp64 + sc.ch * p.kc, c0);
+                  }
+                  continue;
+                }
+                const int dj = tc.od * p.st + tj - p.pt;
+                const uint32_t aj = act + static_cast<uint32_t>(j) * (p.act_bytes >> 1);
+                if (p.flat) {
+                  const int q_start = w0 + (rj - p.ph) * p.W;
+                  for (int b = 0; b < p.nbox; ++b)
+                    tma_load_4d(aj + static_cast<uint32_t>(b * p.box_w * 64), &hm.act, full,
+                                sc.ch * p.kc, q_start + b * p.box_w, dj, tc.nb);
+                } else {
+                  for (int i = 0; i < p.rh; ++i) {
+                    const int ho = h0 + i;
+                    int h_in = ho * p.sh + rj - p.ph;
+                    if (p.reflect_h && ho < p.epi.Ho) h_in = reflect_coord(h_in, p.H);
+                    for (int b = 0; b < p.nbox; ++b)
+                      tma_load_5d(aj + static_cast<uint32_t>((i * p.run_pitch + b * p.box_w) * 64),
+                                  &hm.act, full, sc.ch * p.kc, w0 - p.pw + b * p.box_w, h_in, dj,
+                                  tc.nb);
+                  }
+                }
+              }
+            } else if (!act_role) {
               for (int tl = 0; tl < p.taps_per_stage; ++tl) {
                 const int s = p.halo ? tl : sc.sblk;
                 const int tap = (sc.t * p.KR + sc.r) * p.KS + s;
@@ -266,6 +353,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       const uint32_t w_tap_step = static_cast<uint32_t>(p.wtap_rows * p.row_bytes) >> 4;
       const uint32_t half_step = static_cast<uint32_t>(128 * p.row_bytes) >> 4;
       const uint32_t a_tap_step = p.halo ? (static_cast<uint32_t>(p.row_bytes) >> 4) : 0u;
+      // paired last-chunk stages: 64-byte rows (64-byte swizzle, 512-byte row groups)
+      const uint32_t desc_hi_h = static_cast<uint32_t>(sdesc(0u, 16u, 512u, 4u, 0u) >> 32);
+      const uint32_t w_tap_step_h = static_cast<uint32_t>(p.wtap_rows * 64) >> 4;
+      const uint32_t act_half_step = (p.act_bytes >> 1) >> 4;
       int slot = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -285,7 +376,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         stage_range(p, tc.split, it_b, it_e);
         uint32_t acc = 0u;
         int ch = it_b % p.n_chunks;
-        for (int it = it_b; it < it_e; ++it, ch = (ch + 1 == p.n_chunks) ? 0 : ch + 1) {
+        StageCoord psc = pair_begin(p);  // paired schedule only
+        for (int it = it_b; it < it_e;
+             ++it, ch = (ch + 1 == p.n_chunks) ? 0 : ch + 1, p.pair ? pair_next(p, psc) : void()) {
           const uint32_t bar = p.reflect_w ? ready_bar(slot) : full_bar(slot);
           if (!mbar_wait(bar, phase, abort_flag, lim)) {
             ok = false;
@@ -294,11 +387,26 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           tc_fence_after();
           // K steps of 16 channels that hold real channels: the rest of a
           // chunk beyond C is zero-filled by TMA and contributes nothing.
-          const int kk_n = (min(p.kc, p.C - ch * p.kc) + 15) / 16;
+          const int chs = p.pair ? psc.ch : ch;
+          const int kk_n = (min(p.kc, p.C - chs * p.kc) + 15) / 16;
           const uint32_t act = sbase + p.stage_bytes * slot;
           const uint32_t b_lo = desc_lo0 + (act >> 4);
           const uint32_t a_lo = desc_lo0 + ((act + p.act_bytes) >> 4);
-          if (!p.pm) {
+          if (p.pair && psc.np > 0) {
+            // the last chunks (<= 32 channels) of psc.np tap pairs
+            for (int j = 0; j < psc.np; ++j) {
+              for (int tl = 0; tl < p.KS; ++tl) {
+                const uint32_t a_t = a_lo + static_cast<uint32_t>(j * p.KS + tl) * w_tap_step_h;
+                const uint32_t b_t = b_lo + static_cast<uint32_t>(j) * act_half_step + tl * 4u;
+                for (int kk = 0; kk < kk_n; ++kk) {
+                  const uint64_t adesc = (static_cast<uint64_t>(desc_hi_h) << 32) | (a_t + 2u * kk);
+                  const uint64_t bdesc = (static_cast<uint64_t>(desc_hi_h) << 32) | (b_t + 2u * kk);
+                  mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+                  acc = 1u;
+                }
+              }
+            }
+          } else if (!p.pm) {
             for (int tl = 0; tl < p.taps_per_stage; ++tl) {
               const uint32_t a_t = a_lo + tl * w_tap_step;
               const uint32_t b_t = b_lo + tl * a_tap_step;
@@ -358,8 +466,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const int w0 = tc.twi * p.tw;
         int it_b, it_e;
         stage_range(p, tc.split, it_b, it_e);
-        StageCoord sc = decode_stage(p, it_b);
-        for (int it = it_b; it < it_e; ++it, next_stage(p, sc)) {
+        StageCoord sc = p.pair ? pair_begin(p) : decode_stage(p, it_b);
+        for (int it = it_b; it < it_e; ++it, p.pair ? pair_next(p, sc) : next_stage(p, sc)) {
           if (!mbar_wait(full_bar(slot), phase, abort_flag, lim)) {
             ok = false;
             break;
@@ -632,7 +740,7 @@ cudaError_t conv_cm_status_read_clear(int* status) {
 
 cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
                            const CUtensorMap& tmWgtLast, const CmOutMaps& om,
-                           const ConvCMParams& p, int grid,
+                           const CmHalfMaps& half, const ConvCMParams& p, int grid,
                            size_t smem_bytes, cudaStream_t stream) {
   static size_t configured = 0;
   if (smem_bytes > configured) {
@@ -643,7 +751,7 @@ cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
     configured = smem_bytes;
   }
   conv_cm_kernel<<<grid, 128 + 128 * p.epi_groups, smem_bytes, stream>>>(tmAct, tmWgt,
-                                                                        tmWgtLast, om, p);
+                                                                        tmWgtLast, om, half, p);
   return cudaGetLastError();
 }
 

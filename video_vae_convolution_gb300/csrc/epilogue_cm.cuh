@@ -387,7 +387,13 @@ __device__ __forceinline__ void cm_block(const CmEpi& E, const CmTile& t, float*
     __syncwarp();
     int h0, w0;
     cm_pixel(t, j0, h0, w0);
-    const bool row_aligned = cm_same_row(t, j0, 32) && (w0 & 7) == 0 && (E.Wo & 7) == 0;
+    // a plain y = B(B(conv) + bias) block goes to the per-pixel loop below even when
+    // its row is aligned: one warp-wide 64-byte store per channel plane beats eight
+    // 16-byte stores into 32 different planes
+    const bool plain = !(E.flags & (EPI_RESIDUAL | EPI_SAVE_VALUE | EPI_DEBUG_STORE_CONV)) &&
+                       !E.pad;
+    const bool row_aligned =
+        !plain && cm_same_row(t, j0, 32) && (w0 & 7) == 0 && (E.Wo & 7) == 0;
     if (row_aligned) {
       // unit = (channel = lane, 8 consecutive pixels): 16-byte stores
       for (int k = 0; k < 4; ++k) {
@@ -412,7 +418,7 @@ __device__ __forceinline__ void cm_block(const CmEpi& E, const CmTile& t, float*
       const long long yo0 = ((long long)t.nb * E.Cout + cw) * E.Do * plane_y +
                             (long long)t.od * plane_y + (long long)h * E.Wy + w;
       const long long cstep_o = (long long)E.Do * plane_o, cstep_y = (long long)E.Do * plane_y;
-      if (!(E.flags & (EPI_RESIDUAL | EPI_SAVE_VALUE | EPI_DEBUG_STORE_CONV)) && !E.pad) {
+      if (plain) {
         // y = B(B(conv) + bias): one pointer stepping through the channel planes; the
         // bias of channel cw + cc comes from lane cc, which holds it for its own channel
         const bool bias = (E.flags & EPI_BIAS) != 0;

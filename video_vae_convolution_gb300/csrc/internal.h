@@ -120,6 +120,17 @@ struct ConvCMParams {
   uint32_t norm_off;       // shared den[N] (fp32) of the current pixel tile
   int norm_cs;             // channels per scratch row: Cout rounded up to 8
   uint16_t* vscratch;      // [grid][N][norm_cs] bf16 values, one slice per CTA
+  // Paired last chunks (halo tiles, one split, Cin % 64 in 1..32): tap pairs
+  // P = kt * KR + kr run in groups of two; a group is the full 64-channel chunks of
+  // its first pair, then of its second, then one stage holding the last chunk of
+  // both pairs as 32-channel, 64-byte rows (act: pair j at j * act_bytes / 2;
+  // weights: pair j, tap s at (j * KS + s) * wtap_rows * 64).
+  int pair, n_pairs;
+};
+
+// Tensor maps of the paired last-chunk stages: 32-channel boxes, 64-byte swizzle.
+struct CmHalfMaps {
+  CUtensorMap act, wgt, wgt_last;
 };
 
 // Output tensor maps of the channel-major kernel's bulk-store epilogue (NDHWC,
