@@ -357,6 +357,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       const uint32_t desc_hi_h = static_cast<uint32_t>(sdesc(0u, 16u, 512u, 4u, 0u) >> 32);
       const uint32_t w_tap_step_h = static_cast<uint32_t>(p.wtap_rows * 64) >> 4;
       const uint32_t act_half_step = (p.act_bytes >> 1) >> 4;
+      // Reflect padding along W (at most 1 on each side): for a stored output pixel
+      // only tap 0 can read the reflected pixel left of the row and only tap KS - 1
+      // the one right of it (the other taps stay inside the row; what they read from
+      // the edge rows lands in halo columns that are never stored).  With halo
+      // stages the inner taps go first, so the patch overlaps their MMAs.
+      const bool inner_first = p.reflect_w && p.halo && !p.pm && p.KS >= 3;
       int slot = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -379,7 +385,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         StageCoord psc = pair_begin(p);  // paired schedule only
         for (int it = it_b; it < it_e;
              ++it, ch = (ch + 1 == p.n_chunks) ? 0 : ch + 1, p.pair ? pair_next(p, psc) : void()) {
-          const uint32_t bar = p.reflect_w ? ready_bar(slot) : full_bar(slot);
+          const uint32_t bar = (p.reflect_w && !inner_first) ? ready_bar(slot) : full_bar(slot);
           if (!mbar_wait(bar, phase, abort_flag, lim)) {
             ok = false;
             break;
@@ -407,7 +413,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               }
             }
           } else if (!p.pm) {
-            for (int tl = 0; tl < p.taps_per_stage; ++tl) {
+            auto issue_tap = [&](int tl) {
               const uint32_t a_t = a_lo + tl * w_tap_step;
               const uint32_t b_t = b_lo + tl * a_tap_step;
               for (int kk = 0; kk < kk_n; ++kk) {
@@ -416,6 +422,20 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 mma_bf16_ss(d, adesc, bdesc, idesc, acc);
                 acc = 1u;
               }
+            };
+            if (inner_first) {
+              // taps 1 .. KS - 2 read no patched row for a stored output: they run on
+              // the landed copies while the patcher fills the reflected edge rows
+              for (int tl = 1; tl < p.KS - 1; ++tl) issue_tap(tl);
+              if (!mbar_wait(ready_bar(slot), phase, abort_flag, lim)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_tap(0);
+              issue_tap(p.KS - 1);
+            } else {
+              for (int tl = 0; tl < p.taps_per_stage; ++tl) issue_tap(tl);
             }
           } else {
             // each 128-pixel half of the tile accumulates into its own columns
