@@ -227,6 +227,8 @@ typedef struct {
   int32_t im2col;           /* 1: the spatial taps are gathered before the conv */
   int32_t launches;         /* kernel launches of the call */
   int32_t grid;             /* CTAs of the convolution kernel */
+  int32_t bulk_store;       /* 1: output blocks on one output row go out through bulk
+                               tensor stores (channel-major kernel) */
 } conv3d_plan_info;
 
 int conv3d_plan(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_plan_info* info);

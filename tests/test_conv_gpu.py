@@ -154,7 +154,9 @@ TMA_STORE_CASES = [
 
 @pytest.mark.parametrize("call", TMA_STORE_CASES, ids=lambda c: c.name)
 def test_bulk_store_epilogue(call):
-    run_and_check(call, wl.NDHWC, wl.NDHWC)
+    # one split: a split reduction writes through the separate reduction kernel
+    gc, _ = run_and_check(call, wl.NDHWC, wl.NDHWC, tuning=vvc.Tuning(k_splits=1))
+    assert gc.c.plan.bulk_store == 1
 
 
 @pytest.mark.parametrize("call", NCDHW_ROW_CASES, ids=lambda c: c.name)

@@ -160,6 +160,22 @@ def test_plan_paired_last_chunks():
     assert _plan(_valid(Cin=96, Cout=96, KT=1, KR=1, KS=1)).paired == 0
 
 
+def test_plan_bulk_store():
+    # NCDHW output takes bulk stores when its rows are 16-byte multiples (Wo % 8 == 0)
+    # and no NDHWC debug store runs beside them; NDHWC when Cout % 8 == 0
+    nc = _valid(Cin=96, Cout=96, D=6, H=354, W=642)
+    nc.out_layout = vvc.NCDHW
+    assert _plan(nc).bulk_store == 1
+    assert _plan(_valid(Cin=96, Cout=96, D=6, H=354, W=642)).bulk_store == 1
+    odd = _valid(Cin=96, Cout=96, N=4, D=1, H=353, W=641, KT=1)   # Wo = 639
+    odd.out_layout = vvc.NCDHW
+    assert _plan(odd).bulk_store == 0
+    nc.epi, nc.conv_out = vvc.EPI_DEBUG_STORE_CONV, 0x40000000
+    assert _plan(nc).bulk_store == 0
+    nc.epi, nc.residual = vvc.EPI_RESIDUAL, 0x50000000
+    assert _plan(nc).bulk_store == 0
+
+
 def test_l2norm_validation():
     lib = vvc._lib()
     assert lib.l2norm_silu(None, 10, 16, None, None, None, 0x1000, 0x2000, None, None) == \

@@ -463,7 +463,11 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.tpu = k.norm ? k.tiles_c : 1;
   // bulk tensor stores for the output blocks that lie on one output row: NDHWC,
   // value = B(B(conv) + bias) (no residual, norm or bottom/right pad), 16-byte rows
-  k.tma_store = (p->out_layout == CONV3D_NDHWC && splits == 1 && !pm && p->Cout % 8 == 0 &&
+  // (NCDHW: 16-byte output rows, and no NDHWC debug conv store beside them)
+  const bool store_rows = p->out_layout == CONV3D_NDHWC
+                              ? p->Cout % 8 == 0
+                              : (Wo % 8 == 0 && !(p->epi & CONV3D_EPI_DEBUG_STORE_CONV));
+  k.tma_store = (store_rows && splits == 1 && !pm &&
                  !(p->epi & (CONV3D_EPI_RESIDUAL | CONV3D_EPI_L2NORM_SILU |
                              CONV3D_EPI_OUT_PAD_BR)))
                     ? 1
@@ -910,16 +914,19 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
   return CONV3D_OK;
 }
 
-// Output maps of the bulk-store epilogue (NDHWC bf16, box 32 channels x 32 pixels).
+// Output maps of the bulk-store epilogue, bf16, box 32 channels x 32 pixels along
+// W: NDHWC dims (C, W, H, D, N), or NCDHW dims (W, H, D, C, N).
 int encode_out_maps(const conv3d_params* p, const Plan& pl, vvc::CmOutMaps* om) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return CONV3D_ERR_CUDA;
   const cuuint64_t C = (cuuint64_t)p->Cout;
-  const cuuint64_t gdim[5] = {C, (cuuint64_t)pl.Wo, (cuuint64_t)pl.Ho, (cuuint64_t)pl.Do,
+  const cuuint64_t Wo = (cuuint64_t)pl.Wo, Ho = (cuuint64_t)pl.Ho, Do = (cuuint64_t)pl.Do;
+  const bool cl = p->out_layout == CONV3D_NDHWC;
+  const cuuint64_t gdim[5] = {cl ? C : Wo, cl ? Wo : Ho, cl ? Ho : Do, cl ? Do : C,
                               (cuuint64_t)p->N};
-  const cuuint64_t gstr[4] = {C * 2, C * 2 * pl.Wo, C * 2 * pl.Wo * pl.Ho,
-                              C * 2 * pl.Wo * pl.Ho * pl.Do};
-  const cuuint32_t box[5] = {32, 32, 1, 1, 1};
+  const cuuint64_t gstr[4] = {cl ? C * 2 : Wo * 2, cl ? C * 2 * Wo : Wo * Ho * 2,
+                              cl ? C * 2 * Wo * Ho : Wo * Ho * Do * 2, C * 2 * Wo * Ho * Do};
+  const cuuint32_t box[5] = {32, cl ? 32u : 1u, 1, cl ? 1u : 32u, 1};
   const cuuint32_t es[5] = {1, 1, 1, 1, 1};
   auto one = [&](void* base, CUtensorMap* m) {
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, gdim, gstr, box, es,
@@ -995,6 +1002,7 @@ int conv3d_plan(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_plan
     r.stages_per_tile = k.stages_total;
     r.k_splits = k.k_splits;
     r.paired = k.pair;
+    r.bulk_store = k.tma_store;
   } else {
     const ConvTCParams& k = pl.kp;
     r.kernel = 1;

@@ -647,8 +647,40 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             const int ib = qq / t.pitch;
             const int jb = qq - ib * t.pitch;
             const int hr = t.hoff + ib, wr = t.woff + jb;
-            if (jb + 31 < t.jlim && jb + 31 < t.pitch && j0 + 31 < t.npix && hr < E.Ho &&
-                wr + 31 < E.Wo) {
+            if (!E.ndhwc && jb + 31 < t.jlim && jb + 31 < t.pitch && j0 + 31 < t.npix &&
+                hr < E.Ho && wr + 31 < E.Wo && (wr & 7) == 0) {
+              // NCDHW: the block goes out as [32 channels][32 pixels] bf16, one 64-byte
+              // row per thread (its channel), through bulk tensor stores.  The store's
+              // innermost coordinate is the output column, so it must be a multiple of 8.
+              uint16_t* yt = reinterpret_cast<uint16_t*>(st);
+              const bool bias = (E.flags & EPI_BIAS) != 0;
+              uint32_t wv[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                float a = round_bf16(__uint_as_float(r[2 * j]));
+                float b = round_bf16(__uint_as_float(r[2 * j + 1]));
+                if (bias) {
+                  a = __fadd_rn(a, ch.bc);
+                  b = __fadd_rn(b, ch.bc);
+                }
+                wv[j] = pack_bf16x2(a, b);
+              }
+              uint4* row = reinterpret_cast<uint4*>(yt + lane * 32);
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                row[k] = make_uint4(wv[4 * k], wv[4 * k + 1], wv[4 * k + 2], wv[4 * k + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_5d(&om.y, smem_u32(yt), wr, hr, tc.od, cw, tc.nb);
+                if (E.flags & EPI_SAVE_VALUE)
+                  tma_store_5d(&om.val, smem_u32(yt), wr, hr, tc.od, cw, tc.nb);
+                bulk_commit_group();
+              }
+              continue;
+            }
+            if (E.ndhwc && jb + 31 < t.jlim && jb + 31 < t.pitch && j0 + 31 < t.npix &&
+                hr < E.Ho && wr + 31 < E.Wo) {
               // The 32 pixels are one piece of an output row: the block goes out as
               // [32 pixels][32 channels] bf16 through bulk tensor stores.
               uint16_t* yt = reinterpret_cast<uint16_t*>(st);

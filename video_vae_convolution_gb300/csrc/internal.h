@@ -115,7 +115,8 @@ struct ConvCMParams {
   // one pixel and needs no staging.
   int pm, pm_halves, pm_n, pm_cols;
   int wtap_rows;           // shared-memory weight rows per tap (128, or pm_n)
-  int tma_store;           // NDHWC output blocks on one output row are written by bulk
+  int tma_store;           // output blocks on one output row (NCDHW: starting at a column
+                           // that is a multiple of 8) are written by bulk
                            // tensor stores (y, value, conv maps) from the staging block
   uint32_t norm_off;       // shared den[N] (fp32) of the current pixel tile
   int norm_cs;             // channels per scratch row: Cout rounded up to 8
