@@ -238,12 +238,67 @@ cudaError_t launch_im2col_hw(const void* x, int layout, int N, int C, int D, int
 
 // ---- input staging --------------------------------------------------------------------
 // NCDHW [N][C][S] (S = D*H*W) -> NDHWC [N][S][Cp], channels Cin..Cp-1 zero.
-// A block moves 32 channels x 256 positions through shared memory: each channel
-// row is read as 512 contiguous bytes, and each position's 32 channels are
-// written as four 16-byte stores by four neighbouring lanes.
+// S % 8 == 0 (every channel row starts on a 16-byte boundary): a block moves up to
+// 128 channels x 128 positions through shared memory.  Each channel row is read as
+// 256 contiguous bytes in 16-byte loads, and the positions' channel rows are
+// written as consecutive 16-byte stores, so with Cp <= 128 a block writes one
+// contiguous range of the output.
 __global__ void __launch_bounds__(256) ncdhw_to_ndhwc_kernel(const uint16_t* __restrict__ x,
                                                              uint16_t* __restrict__ out, int C,
                                                              int Cp, long long S) {
+  constexpr int P = 128;
+  __shared__ uint16_t tile[128][P + 2];  // odd word pitch: column reads spread over banks
+  const int n = blockIdx.z;
+  const int c0 = blockIdx.y * 128;
+  const long long s0 = (long long)blockIdx.x * P;
+  const int nc = min(128, Cp - c0);  // output channels of this block (Cp % 8 == 0)
+  const uint16_t* xn = x + (long long)n * C * S;
+  uint16_t* on = out + (long long)n * Cp * S;
+  const int tid = threadIdx.x;
+  if (s0 + P <= S) {
+    // 16 threads per channel row, 8 positions each
+    const int q = (tid & 15) * 8;
+    for (int r = tid >> 4; r < nc; r += 16) {
+      const int c = c0 + r;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (c < C) v = *reinterpret_cast<const uint4*>(xn + (long long)c * S + s0 + q);
+      uint32_t* t = reinterpret_cast<uint32_t*>(&tile[r][q]);
+      t[0] = v.x;
+      t[1] = v.y;
+      t[2] = v.z;
+      t[3] = v.w;
+    }
+  } else {
+    const int pl = tid & (P - 1);
+    const long long sp = s0 + pl;
+    for (int r = tid >> 7; r < nc; r += 2) {
+      const int c = c0 + r;
+      tile[r][pl] = (c < C && sp < S) ? xn[(long long)c * S + sp] : uint16_t(0);
+    }
+  }
+  __syncthreads();
+  const int groups = nc >> 3;  // 16-byte groups per position
+  const int npos = static_cast<int>(S - s0 < P ? S - s0 : P);
+  for (int u = tid; u < npos * groups; u += 256) {
+    const int pl = u / groups, g = u - pl * groups;
+    uint16_t v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = tile[8 * g + e][pl];
+    uint4 w;
+    w.x = v[0] | (uint32_t(v[1]) << 16);
+    w.y = v[2] | (uint32_t(v[3]) << 16);
+    w.z = v[4] | (uint32_t(v[5]) << 16);
+    w.w = v[6] | (uint32_t(v[7]) << 16);
+    *reinterpret_cast<uint4*>(on + (s0 + pl) * Cp + c0 + 8 * g) = w;
+  }
+}
+
+// Any S: a block moves 32 channels x 256 positions through shared memory; each
+// channel row is read as 512 contiguous bytes (2-byte loads), and each position's
+// 32 channels are written as four 16-byte stores by four neighbouring lanes.
+__global__ void __launch_bounds__(256)
+    ncdhw_to_ndhwc_scalar_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ out, int C,
+                                 int Cp, long long S) {
   __shared__ uint16_t tile[32][256 + 2];  // odd word pitch: conflict-free column reads
   const int n = blockIdx.z;
   const long long s0 = (long long)blockIdx.x * 256;
@@ -275,6 +330,7 @@ __global__ void __launch_bounds__(256) ncdhw_to_ndhwc_kernel(const uint16_t* __r
   }
 }
 
+
 // NDHWC [P][C] -> [P][Cp] with zero channels Cin..Cp-1.
 __global__ void pad_channels_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ out,
                                     int C, int Cp, long long P) {
@@ -290,10 +346,18 @@ __global__ void pad_channels_kernel(const uint16_t* __restrict__ x, uint16_t* __
 cudaError_t launch_stage_input(const void* x, int layout, int N, int C, int Cp, long long S,
                                void* out, cudaStream_t s) {
   if (layout == LAYOUT_NCDHW) {
-    dim3 grid(static_cast<unsigned>((S + 255) / 256), static_cast<unsigned>((Cp + 31) / 32),
-              static_cast<unsigned>(N));
-    ncdhw_to_ndhwc_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x),
-                                               static_cast<uint16_t*>(out), C, Cp, S);
+    const bool vec = (S % 8) == 0 && (reinterpret_cast<uintptr_t>(x) % 16) == 0;
+    if (vec) {
+      dim3 grid(static_cast<unsigned>((S + 127) / 128), static_cast<unsigned>((Cp + 127) / 128),
+                static_cast<unsigned>(N));
+      ncdhw_to_ndhwc_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x),
+                                                 static_cast<uint16_t*>(out), C, Cp, S);
+    } else {
+      dim3 grid(static_cast<unsigned>((S + 255) / 256), static_cast<unsigned>((Cp + 31) / 32),
+                static_cast<unsigned>(N));
+      ncdhw_to_ndhwc_scalar_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x),
+                                                        static_cast<uint16_t*>(out), C, Cp, S);
+    }
   } else {
     const long long total = (long long)N * S * Cp;
     long long blocks = (total + 255) / 256;
