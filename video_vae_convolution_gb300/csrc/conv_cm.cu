@@ -163,6 +163,11 @@ __device__ __forceinline__ int cta_tile(const ConvCMParams& p, int l) {
 
 }  // namespace
 
+// kPair: the paired last-chunk schedule (ConvCMParams::pair).  kInner: reflect-W
+// halo stages whose inner W taps run before the edge patch.  Both are template
+// parameters so that the plain instance keeps the shortest producer and MMA-issue
+// loops (the per-stage checks of either mode cost 4-5 % on layers that use neither).
+template <bool kPair, bool kInner>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     conv_cm_kernel(const __grid_constant__ CUtensorMap tmAct,
                    const __grid_constant__ CUtensorMap tmWgt,
@@ -205,7 +210,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     tma_prefetch_desc(&tmAct);
     tma_prefetch_desc(&tmWgt);
     tma_prefetch_desc(&tmWgtLast);
-    if (p.pair) {
+    if (kPair) {
       tma_prefetch_desc(&hm.act);
       tma_prefetch_desc(&hm.wgt);
       tma_prefetch_desc(&hm.wgt_last);
@@ -243,8 +248,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                                      : (last_ct ? p.tx_bytes_last : p.tx_bytes) - p.act_tx;
         int it_b, it_e;
         stage_range(p, tc.split, it_b, it_e);
-        StageCoord sc = p.pair ? pair_begin(p) : decode_stage(p, it_b);
-        for (int it = it_b; it < it_e; ++it, p.pair ? pair_next(p, sc) : next_stage(p, sc)) {
+        StageCoord sc = kPair ? pair_begin(p) : decode_stage(p, it_b);
+        for (int it = it_b; it < it_e; ++it, kPair ? pair_next(p, sc) : next_stage(p, sc)) {
           if (!mbar_wait(empty_bar(slot), phase ^ 1u, abort_flag, lim)) {
             ok = false;
             break;
@@ -252,7 +257,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           const bool skip = (p.inject > 0 && k_global == p.inject - 1);
           if (!skip) {
             const uint32_t full = full_bar(slot);
-            const int np = p.pair ? sc.np : 0;
+            const int np = kPair ? sc.np : 0;
             mbar_arrive_expect_tx(full, np == 0 ? tx : (tx >> 1) * static_cast<uint32_t>(np));
             const uint32_t act = sbase + p.stage_bytes * slot;
             const uint32_t wgt = act + p.act_bytes;
@@ -362,7 +367,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       // the one right of it (the other taps stay inside the row; what they read from
       // the edge rows lands in halo columns that are never stored).  With halo
       // stages the inner taps go first, so the patch overlaps their MMAs.
-      const bool inner_first = p.reflect_w && p.halo && !p.pm && p.KS >= 3;
+      constexpr bool inner_first = kInner;
       int slot = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -384,7 +389,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         int ch = it_b % p.n_chunks;
         StageCoord psc = pair_begin(p);  // paired schedule only
         for (int it = it_b; it < it_e;
-             ++it, ch = (ch + 1 == p.n_chunks) ? 0 : ch + 1, p.pair ? pair_next(p, psc) : void()) {
+             ++it, ch = (ch + 1 == p.n_chunks) ? 0 : ch + 1, kPair ? pair_next(p, psc) : void()) {
           const uint32_t bar = (p.reflect_w && !inner_first) ? ready_bar(slot) : full_bar(slot);
           if (!mbar_wait(bar, phase, abort_flag, lim)) {
             ok = false;
@@ -393,12 +398,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           tc_fence_after();
           // K steps of 16 channels that hold real channels: the rest of a
           // chunk beyond C is zero-filled by TMA and contributes nothing.
-          const int chs = p.pair ? psc.ch : ch;
+          const int chs = kPair ? psc.ch : ch;
           const int kk_n = (min(p.kc, p.C - chs * p.kc) + 15) / 16;
           const uint32_t act = sbase + p.stage_bytes * slot;
           const uint32_t b_lo = desc_lo0 + (act >> 4);
           const uint32_t a_lo = desc_lo0 + ((act + p.act_bytes) >> 4);
-          if (p.pair && psc.np > 0) {
+          if (kPair && psc.np > 0) {
             // the last chunks (<= 32 channels) of psc.np tap pairs
             for (int j = 0; j < psc.np; ++j) {
               for (int tl = 0; tl < p.KS; ++tl) {
@@ -486,8 +491,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const int w0 = tc.twi * p.tw;
         int it_b, it_e;
         stage_range(p, tc.split, it_b, it_e);
-        StageCoord sc = p.pair ? pair_begin(p) : decode_stage(p, it_b);
-        for (int it = it_b; it < it_e; ++it, p.pair ? pair_next(p, sc) : next_stage(p, sc)) {
+        StageCoord sc = kPair ? pair_begin(p) : decode_stage(p, it_b);
+        for (int it = it_b; it < it_e; ++it, kPair ? pair_next(p, sc) : next_stage(p, sc)) {
           if (!mbar_wait(full_bar(slot), phase, abort_flag, lim)) {
             ok = false;
             break;
@@ -794,16 +799,24 @@ cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
                            const CUtensorMap& tmWgtLast, const CmOutMaps& om,
                            const CmHalfMaps& half, const ConvCMParams& p, int grid,
                            size_t smem_bytes, cudaStream_t stream) {
-  static size_t configured = 0;
-  if (smem_bytes > configured) {
-    cudaError_t err = cudaFuncSetAttribute(conv_cm_kernel,
+  // the same condition as the MMA warp's reflect-W handling in the plain instance
+  const bool inner = p.reflect_w && p.halo && !p.pm && p.KS >= 3;
+  if (p.pair && inner) return cudaErrorInvalidValue;  // the plan never pairs reflect-W layers
+  using Kernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CmOutMaps, CmHalfMaps,
+                          ConvCMParams);
+  const int which = p.pair ? 1 : (inner ? 2 : 0);
+  const Kernel kernels[3] = {conv_cm_kernel<false, false>, conv_cm_kernel<true, false>,
+                             conv_cm_kernel<false, true>};
+  static size_t configured[3] = {0, 0, 0};
+  if (smem_bytes > configured[which]) {
+    cudaError_t err = cudaFuncSetAttribute(kernels[which],
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem_bytes));
     if (err != cudaSuccess) return err;
-    configured = smem_bytes;
+    configured[which] = smem_bytes;
   }
-  conv_cm_kernel<<<grid, 128 + 128 * p.epi_groups, smem_bytes, stream>>>(tmAct, tmWgt,
-                                                                        tmWgtLast, om, half, p);
+  kernels[which]<<<grid, 128 + 128 * p.epi_groups, smem_bytes, stream>>>(tmAct, tmWgt, tmWgtLast,
+                                                                         om, half, p);
   return cudaGetLastError();
 }
 
