@@ -164,10 +164,11 @@ __device__ __forceinline__ int cta_tile(const ConvCMParams& p, int l) {
 }  // namespace
 
 // kPair: the paired last-chunk schedule (ConvCMParams::pair).  kInner: reflect-W
-// halo stages whose inner W taps run before the edge patch.  Both are template
-// parameters so that the plain instance keeps the shortest producer and MMA-issue
-// loops (the per-stage checks of either mode cost 4-5 % on layers that use neither).
-template <bool kPair, bool kInner>
+// halo stages whose inner W taps run before the edge patch.  kPM: pixel-major mode.
+// They are template parameters so that the plain instance keeps the shortest
+// producer and MMA-issue loops (the per-stage checks of the first two modes cost
+// 4-5 % each on layers that use neither).
+template <bool kPair, bool kInner, bool kPM>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     conv_cm_kernel(const __grid_constant__ CUtensorMap tmAct,
                    const __grid_constant__ CUtensorMap tmWgt,
@@ -347,7 +348,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (lane == 0) {
       // channel-major: A = weights (M = 128 channels), B = pixels (N = p.N);
       // pixel-major: A = pixels (M = 128 per half), B = weights (N = p.pm_n)
-      const uint32_t idesc = idesc_bf16_f32(128, p.pm ? p.pm_n : p.N);
+      const uint32_t idesc = idesc_bf16_f32(128, kPM ? p.pm_n : p.N);
       const uint32_t sbo = 8u * static_cast<uint32_t>(p.row_bytes);
       // The high descriptor word (stride, version, swizzle) is fixed; operand
       // views differ only in the start-address field (16-byte units).  The
@@ -417,7 +418,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 }
               }
             }
-          } else if (!p.pm) {
+          } else if (!kPM) {
             auto issue_tap = [&](int tl) {
               const uint32_t a_t = a_lo + tl * w_tap_step;
               const uint32_t b_t = b_lo + tl * a_tap_step;
@@ -574,7 +575,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       t.jlim = p.flat ? p.W : p.tw;
       return t;
     };
-    if (p.pm) {
+    if (kPM) {
       // Pixel-major: thread = one pixel of the 128-pixel half (TMEM lane), columns =
       // output channels; the per-pixel epilogue reads 16 channels at a time.
       for (int local = 0;; ++local) {
@@ -801,13 +802,16 @@ cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
                            size_t smem_bytes, cudaStream_t stream) {
   // the same condition as the MMA warp's reflect-W handling in the plain instance
   const bool inner = p.reflect_w && p.halo && !p.pm && p.KS >= 3;
-  if (p.pair && inner) return cudaErrorInvalidValue;  // the plan never pairs reflect-W layers
+  // the plan never pairs reflect-W or pixel-major layers
+  if (p.pair && (inner || p.pm)) return cudaErrorInvalidValue;
   using Kernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CmOutMaps, CmHalfMaps,
                           ConvCMParams);
-  const int which = p.pair ? 1 : (inner ? 2 : 0);
-  const Kernel kernels[3] = {conv_cm_kernel<false, false>, conv_cm_kernel<true, false>,
-                             conv_cm_kernel<false, true>};
-  static size_t configured[3] = {0, 0, 0};
+  const int which = p.pm ? 3 : (p.pair ? 1 : (inner ? 2 : 0));
+  const Kernel kernels[4] = {conv_cm_kernel<false, false, false>,
+                             conv_cm_kernel<true, false, false>,
+                             conv_cm_kernel<false, true, false>,
+                             conv_cm_kernel<false, false, true>};
+  static size_t configured[4] = {0, 0, 0, 0};
   if (smem_bytes > configured[which]) {
     cudaError_t err = cudaFuncSetAttribute(kernels[which],
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
