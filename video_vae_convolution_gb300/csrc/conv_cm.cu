@@ -404,7 +404,24 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           const uint32_t act = sbase + p.stage_bytes * slot;
           const uint32_t b_lo = desc_lo0 + (act >> 4);
           const uint32_t a_lo = desc_lo0 + ((act + p.act_bytes) >> 4);
-          if (kPair && psc.np > 0) {
+          if (kPair && psc.np == 2 && p.KS == 3 && kk_n == 2) {
+            // the last 32-channel chunks of two tap pairs, 3 W taps: straight-line issue
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+#pragma unroll
+              for (int tl = 0; tl < 3; ++tl) {
+                const uint32_t a_t = a_lo + static_cast<uint32_t>(j * 3 + tl) * w_tap_step_h;
+                const uint32_t b_t = b_lo + static_cast<uint32_t>(j) * act_half_step + tl * 4u;
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                  const uint64_t adesc = (static_cast<uint64_t>(desc_hi_h) << 32) | (a_t + 2u * kk);
+                  const uint64_t bdesc = (static_cast<uint64_t>(desc_hi_h) << 32) | (b_t + 2u * kk);
+                  mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+                  acc = 1u;
+                }
+              }
+            }
+          } else if (kPair && psc.np > 0) {
             // the last chunks (<= 32 channels) of psc.np tap pairs
             for (int j = 0; j < psc.np; ++j) {
               for (int tl = 0; tl < p.KS; ++tl) {
@@ -419,9 +436,21 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               }
             }
           } else if (!kPM) {
+            // a full 64-channel chunk (4 K steps) issues from straight-line code
+            const bool full4 = kk_n == 4;
             auto issue_tap = [&](int tl) {
               const uint32_t a_t = a_lo + tl * w_tap_step;
               const uint32_t b_t = b_lo + tl * a_tap_step;
+              if (full4) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (a_t + 2u * kk);
+                  const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (b_t + 2u * kk);
+                  mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+                  acc = 1u;
+                }
+                return;
+              }
               for (int kk = 0; kk < kk_n; ++kk) {
                 const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (a_t + 2u * kk);
                 const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (b_t + 2u * kk);
@@ -440,6 +469,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               tc_fence_after();
               issue_tap(0);
               issue_tap(p.KS - 1);
+            } else if (p.taps_per_stage == 3) {
+              issue_tap(0);
+              issue_tap(1);
+              issue_tap(2);
             } else {
               for (int tl = 0; tl < p.taps_per_stage; ++tl) issue_tap(tl);
             }
