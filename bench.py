@@ -41,7 +41,7 @@ L2_FLUSH_BYTES = 256 << 20
 # sources: a changed kernel reports null until it is captured again.
 KERNEL_SOURCES = ["conv_cm.cu", "epilogue_cm.cuh", "epilogue.cuh", "kernel_common.cuh",
                   "ptx.cuh", "internal.h"]
-NCU_TRAFFIC = {"fa21ee721957a9fc": 262686208 + 140327680}
+NCU_TRAFFIC = {"c12cc6698faa4ec8": 262765824 + 140476928}
 
 
 def kernel_source_hash():
@@ -358,7 +358,7 @@ def run_gpu(args, rank, world):
     outs_host = [torch.empty(c.y.shape, dtype=torch.bfloat16).pin_memory() for _, _, c in calls]
     h2d = sum(h.numel() * 2 for h in host)
     d2h = sum(o.numel() * 2 for o in outs_host)
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = max(1, min(args.steps, 10))
     # one copy stream per direction (splitting a copy over several streams measured
     # slower: concurrent copies in one direction contend)
     s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -366,6 +366,31 @@ def run_gpu(args, rank, world):
     ev_in = [torch.cuda.Event() for _ in range(n)]
     ev_conv = [torch.cuda.Event() for _ in range(n)]
     ev_out = [torch.cuda.Event() for _ in range(n)]
+    def e2e_steps_run(count):
+        for step in range(count):
+            for i, ((call, lay, c), h, o) in enumerate(zip(calls, host, outs_host)):
+                if step:
+                    s_in.wait_event(ev_conv[i])    # the previous step has read c.x
+                with torch.cuda.stream(s_in):
+                    c.x.copy_(h, non_blocking=True)
+                ev_in[i].record(s_in)
+                stream.wait_event(ev_in[i])
+                if step:
+                    stream.wait_event(ev_out[i])   # the previous step's c.y has been copied out
+                rc = c.run(stream)
+                if rc != 0:
+                    raise RuntimeError(f"conv3d_fwd failed: {rc}")
+                ev_conv[i].record(stream)
+                s_out.wait_event(ev_conv[i])
+                with torch.cuda.stream(s_out):
+                    o.copy_(c.y, non_blocking=True)
+                ev_out[i].record(s_out)
+        for i in range(n):
+            stream.wait_event(ev_out[i])
+
+    # untimed warm-up passes (first use of the copy streams and pinned buffers)
+    e2e_steps_run(max(1, min(args.warmup, 3)))
+    torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -373,26 +398,7 @@ def run_gpu(args, rank, world):
     e0.record(stream)
     s_in.wait_event(e0)
     s_out.wait_event(e0)
-    for step in range(e2e_steps):
-        for i, ((call, lay, c), h, o) in enumerate(zip(calls, host, outs_host)):
-            if step:
-                s_in.wait_event(ev_conv[i])    # the previous step has read c.x
-            with torch.cuda.stream(s_in):
-                c.x.copy_(h, non_blocking=True)
-            ev_in[i].record(s_in)
-            stream.wait_event(ev_in[i])
-            if step:
-                stream.wait_event(ev_out[i])   # the previous step's c.y has been copied out
-            rc = c.run(stream)
-            if rc != 0:
-                raise RuntimeError(f"conv3d_fwd failed: {rc}")
-            ev_conv[i].record(stream)
-            s_out.wait_event(ev_conv[i])
-            with torch.cuda.stream(s_out):
-                o.copy_(c.y, non_blocking=True)
-            ev_out[i].record(s_out)
-    for i in range(n):
-        stream.wait_event(ev_out[i])
+    e2e_steps_run(e2e_steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
