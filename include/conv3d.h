@@ -154,10 +154,10 @@ typedef struct {
   int32_t im2col;      /* 0 auto, 1 on, 2 off: for Cin * KR * KS <= 64 (Cin < 8) gather
                           the spatial taps into a staged tensor first and run a
                           (KT, 1, 1) convolution over it */
-  int32_t pair;        /* 0 auto (from 4 tap pairs up), 1 on (from 2), 2 off: when the
-                          last 64-channel chunk of the input holds at most 32 channels
-                          (Cin = 96, 160, ...), run the last chunks of two consecutive
-                          (kt, kr) tap pairs as one pipeline stage of 64-byte rows
+  int32_t pair;        /* 0 auto (= on), 1 on, 2 off: when the last 64-channel chunk of
+                          the input holds at most 32 channels (Cin = 96, 160, ...) and
+                          there are at least 2 (kt, kr) tap pairs, run the last chunks of
+                          two consecutive tap pairs as one pipeline stage of 64-byte rows
                           instead of one half-empty stage each */
 } conv3d_tuning;
 

@@ -142,11 +142,10 @@ def test_plan_paired_last_chunks():
     assert (on.kernel, on.paired, on.stages_per_tile, on.k_splits) == (2, 1, 14, 1)
     assert (off.paired, off.stages_per_tile) == (0, 18)
     assert on.mma_n == off.mma_n == 256
-    # 1x3x3 (T = 1): 3 tap pairs stay unpaired unless asked (-> 3 + 2 stages)
+    # 1x3x3 (T = 1): 3 tap pairs -> 2 full stages + ceil(3 / 2) shared ones
     t1 = _valid(N=4, Cin=96, Cout=96, D=1, H=353, W=641, KT=1)
-    assert (_plan(t1).paired, _plan(t1).stages_per_tile) == (0, 6)
-    forced = _plan(t1, vvc.Tuning(pair=1))
-    assert (forced.paired, forced.stages_per_tile) == (1, 5)
+    assert (_plan(t1).paired, _plan(t1).stages_per_tile) == (1, 5)
+    assert (_plan(t1, vvc.Tuning(pair=2)).paired, _plan(t1, vvc.Tuning(pair=2)).stages_per_tile) == (0, 6)
     # 160 channels: two full chunks per pair + shared last chunks (9 * 2 + 5)
     assert _plan(_valid(Cin=160, Cout=160, D=8, H=106, W=182)).stages_per_tile == 23
     # not paired: whole chunks (128), last chunk over 32 channels (112), a split

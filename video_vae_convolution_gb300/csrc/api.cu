@@ -435,15 +435,15 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   // Paired last chunks: the last 64-channel chunk of a tap pair holds at most 32 real
   // channels, so two tap pairs share one stage of 32-channel rows (every stage then
   // carries a full 64-channel MMA group).  One split only; not with the reflect-W
-  // patch (it rewrites 128-byte rows) or the pixel-major mode.  Automatic from four
-  // tap pairs up (3x3x3: 18 -> 14 stages for 96 channels, -5 % time measured); with
-  // three (1x3x3) the saved stage did not pay.
+  // patch (it rewrites 128-byte rows) or the pixel-major mode.  From two tap pairs up
+  // (3x3x3: 18 -> 14 stages for 96 channels; 1x3x3: 6 -> 5; both about -5 % time
+  // measured once every stage issues its MMAs from straight-line code).
   const int n_pairs = p->KT * p->KR;
   const int last_ch = pl->Cst - (k.n_chunks - 1) * kc;
   const bool reflect_w_pad =
       p->pad[2].mode == CONV3D_PAD_REFLECT && (p->pad[2].before || p->pad[2].after);
   const bool pair_ok = t.pair != 2 && !pm && halo && kc == 64 && last_ch >= 1 && last_ch <= 32 &&
-                       n_pairs >= (t.pair == 1 ? 2 : 4) && !reflect_w_pad;
+                       n_pairs >= 2 && !reflect_w_pad;
   int splits = 0;
   if (pair_ok) {
     const int total = n_pairs * (k.n_chunks - 1) + (n_pairs + 1) / 2;

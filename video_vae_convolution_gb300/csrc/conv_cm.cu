@@ -298,11 +298,19 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 }
               }
             } else if (!act_role) {
-              for (int tl = 0; tl < p.taps_per_stage; ++tl) {
-                const int s = p.halo ? tl : sc.sblk;
-                const int tap = (sc.t * p.KR + sc.r) * p.KS + s;
-                tma_load_2d(wgt + static_cast<uint32_t>(tl * p.wtap_rows * p.row_bytes), wmap, full,
-                            tap * p.cp64 + sc.ch * p.kc, c0);
+              const int x0 = (sc.t * p.KR + sc.r) * p.KS * p.cp64 + sc.ch * p.kc;
+              const uint32_t wstep = static_cast<uint32_t>(p.wtap_rows * p.row_bytes);
+              if (p.halo && p.taps_per_stage == 3) {
+                // the three W taps of a halo stage: consecutive weight boxes
+                tma_load_2d(wgt, wmap, full, x0, c0);
+                tma_load_2d(wgt + wstep, wmap, full, x0 + p.cp64, c0);
+                tma_load_2d(wgt + 2u * wstep, wmap, full, x0 + 2 * p.cp64, c0);
+              } else {
+                for (int tl = 0; tl < p.taps_per_stage; ++tl) {
+                  const int s = p.halo ? tl : sc.sblk;
+                  tma_load_2d(wgt + static_cast<uint32_t>(tl) * wstep, wmap, full,
+                              x0 + s * p.cp64, c0);
+                }
               }
             } else if (p.flat) {
               // flattened (H*W) positions: output q reads input q + (r - ph) * W + s
@@ -444,6 +452,16 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               if (full4) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
+                  const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (a_t + 2u * kk);
+                  const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (b_t + 2u * kk);
+                  mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+                  acc = 1u;
+                }
+                return;
+              }
+              if (kk_n == 2) {  // a 32-channel last chunk
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
                   const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (a_t + 2u * kk);
                   const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (b_t + 2u * kk);
                   mma_bf16_ss(d, adesc, bdesc, idesc, acc);
