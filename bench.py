@@ -38,19 +38,32 @@ L2_FLUSH_BYTES = 256 << 20
 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from one ncu
 # capture (profiles/conv_cm_wan96_ndhwc.md), keyed by a hash of the kernel's
-# sources: a changed kernel reports null until it is captured again.
+# sources (comments and whitespace left out): a changed kernel reports null until
+# it is captured again.
 KERNEL_SOURCES = ["conv_cm.cu", "epilogue_cm.cuh", "epilogue.cuh", "kernel_common.cuh",
                   "ptx.cuh", "internal.h"]
-NCU_TRAFFIC = {"dbc819beb98ba877": 262620928 + 140352512}
+NCU_TRAFFIC = {"f2e0061935f07fe9": 262620928 + 140352512}
 
 
-def kernel_source_hash():
+def source_code_only(text):
+    """C++ source text without comments and whitespace (what the compiler sees)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return "".join(text.split())
+
+
+def kernel_source_hash(read=None):
     import hashlib
     h = hashlib.sha1()
     d = os.path.join(ROOT, "video_vae_convolution_gb300", "csrc")
     for f in KERNEL_SOURCES:
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(fh.read())
+        if read is None:
+            with open(os.path.join(d, f), encoding="utf-8") as fh:
+                text = fh.read()
+        else:
+            text = read(f)
+        h.update(source_code_only(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -6,23 +6,29 @@
 // as the hardware allows: the accumulator is D[channel][pixel] in TMEM, each
 // tcgen05.mma is M = 128 output channels (packed weights, cuDNN frontend doc
 // "Fused Conv3D + Bias + Residual + RMSNorm + SiLU", "Weight Packing") by
-// N = up to 256 output pixels (activations) by K = 16.  On sm_103a an MMA costs
-// about the same issue time for any N up to ~192, so a 256-pixel N keeps the
-// tensor pipe busy even when the layer has only 96 or 128 output channels.
+// N = up to 256 output pixels (activations) by K = 16.  On sm_103a an MMA's
+// cost grows with N (M = 128: about 64 cycles at N = 128, 128 at N = 256 when the
+// issuing thread keeps up), so the tensor pipe stays busy with N = 256 even when
+// the layer has only 96 or 128 output channels; what it cannot hide is the
+// issuing thread's own work between MMAs, so the common stage shapes issue from
+// straight-line code.
 //
 // Persistent CTAs walk a static list of tiles (128 channels x one pixel tile,
 // times a slice of the reduction when it is split).  A pixel tile is either one
 // run of up to 256 output pixels of one output row (halo mode, stride 1 along W:
-// one TMA run of tw + KS - 1 input pixels serves all KS taps as shifted views)
-// or rh rows of tw pixels (direct mode: one TMA box per row and tap, element
-// stride = conv stride).  Channel chunks are 64 wide (128-byte swizzled rows).
-// The accumulator is double buffered in TMEM so the epilogue of one tile runs
-// under the MMAs of the next.
+// one TMA run of tw + KS - 1 input pixels serves all KS taps as shifted views),
+// 256 consecutive positions of the flattened H*W plane (flat mode), or rh rows
+// of tw pixels (direct mode: one TMA box per row and tap, element stride = conv
+// stride).  Channel chunks are 64 wide (128-byte swizzled rows); with the paired
+// schedule the last 32-channel chunks of two tap pairs share a stage as 64-byte
+// rows.  The accumulator is double buffered in TMEM so the epilogue of one tile
+// runs under the MMAs of the next.
 //
 // Warp roles (128 + 128 G threads): 0 activation producer, 1 MMA issuer + TMEM
 // owner, 2 reflect-W patcher, 3 weight producer, 4.. epilogue in G warpgroups
-// (G = 2 or 3) that take every G-th 32-pixel column block (a warp reads the TMEM lane quarter warp % 4: thread =
-// output channel; stores are coalesced across channels for NDHWC output).
+// (G = 2 or 3) that take every G-th 32-pixel column block (a warp reads the TMEM
+// lane quarter warp % 4: thread = output channel).  Output blocks on one output
+// row go out through bulk tensor stores, the others through per-thread stores.
 // Waits are bounded; a time-out records CONV3D_ERR_DEVICE_TIMEOUT.
 #include <cuda.h>
 #include <cuda_runtime.h>
