@@ -15,9 +15,10 @@ Sources (web pages, cited by title and section):
 * ROCm/FlyDSL PR "[Flydsl] Add Qwen-Image VAE classic conv shapes to conv3d
   tests" — the T=1 causal identity ("T=1 degeneration") and the downsample
   ZeroPad2d((0,1,0,1)) + stride-2 conv ("Downsample Conv2d").
-* cuDNN frontend doc "Fused Conv3D + Bias + Residual + RMSNorm + SiLU" — the
-  Operation Contract (rounding points), "Weight Packing", "Standalone
-  Normalization and Padding Variant", "Spatial Padding Variant".
+* [cuDNN-PO] cuDNN frontend doc "Fused Conv3D + Bias + Residual + RMSNorm +
+  SiLU" — the Operation Contract (rounding points), "Weight Packing",
+  "Normalization and Padding Variant", "Standalone Normalization and Padding
+  Variant", "Spatial Padding Variant".
 
 bf16 values are carried as ``numpy.uint16`` bit patterns throughout.
 
@@ -277,6 +278,67 @@ def pad_bottom_right(t_ndhwc: np.ndarray) -> np.ndarray:
     out = np.zeros((N, D, H + 1, W + 1, C), dtype=t_ndhwc.dtype)
     out[:, :, :H, :W, :] = t_ndhwc
     return out
+
+
+def pad_cache_fused(act, history_frames, padded_init, cache_init):
+    """What the fused normalization-and-padding convolution writes ([cuDNN-PO],
+    "Normalization and Padding Variant"), applied to caller-supplied initial
+    buffers so that the regions the kernel leaves alone keep their contents.
+
+    act: the activated current frames [N, Tc, Hc, Wc, C] (bf16 bits), Tc = T - 2.
+    padded_init: [N, Tc + 2, Hc + 2, Wc + 2, C]; cache_init: [N, K, Hc, Wc, C] with
+    K = min(2, Tc + P), P = history_frames in 0..2.  Returns (padded, cache):
+    * every plane's one-pixel spatial border is zero;
+    * the planes before the P history planes (t < 2 - P) are zero;
+    * the history planes' interiors (2 - P <= t < 2) are untouched;
+    * the current frames fill the interiors of planes 2 .. Tc + 1;
+    * the last min(2, Tc) current frames fill the tail of the cache; its head
+      (older frames) is untouched.
+    """
+    act = _u16(act)
+    N, Tc, Hc, Wc, C = act.shape
+    P = int(history_frames)
+    assert 0 <= P <= 2
+    K = min(2, Tc + P)
+    padded = _u16(padded_init).copy()
+    cache = _u16(cache_init).copy()
+    assert padded.shape == (N, Tc + 2, Hc + 2, Wc + 2, C)
+    assert cache.shape == (N, K, Hc, Wc, C)
+    padded[:, :, 0, :, :] = 0
+    padded[:, :, -1, :, :] = 0
+    padded[:, :, :, 0, :] = 0
+    padded[:, :, :, -1, :] = 0
+    padded[:, :2 - P] = 0
+    padded[:, 2:, 1:-1, 1:-1, :] = act
+    kc = min(2, Tc)
+    cache[:, K - kc:] = act[:, Tc - kc:]
+    return padded, cache
+
+
+def pad_cache_standalone(act, previous=None):
+    """Padded output and cache of the standalone post-operations ([cuDNN-PO],
+    "Standalone Normalization and Padding Variant"), which also copy the history.
+
+    act: activated frames [N, T, H, W, C] (bf16 bits); previous: None or the
+    P = 1 or 2 prior activated frames [N, P, H, W, C].  Returns (padded
+    [N, T + 2, H + 2, W + 2, C], cache [N, min(2, T + P), H, W, C]): the frames
+    [previous..., act...] end at plane T + 1 of the padded tensor (history in
+    planes 2 - P .. 1, zeros before it and on every spatial border), and the
+    cache holds the last min(2, T + P) of them.
+    """
+    act = _u16(act)
+    N, T, H, W, C = act.shape
+    padded = np.zeros((N, T + 2, H + 2, W + 2, C), dtype=np.uint16)
+    padded[:, 2:, 1:-1, 1:-1, :] = act
+    seq = act
+    if previous is not None:
+        prev = _u16(previous)
+        P = prev.shape[1]
+        assert prev.shape == (N, P, H, W, C) and 1 <= P <= 2
+        padded[:, 2 - P:2, 1:-1, 1:-1, :] = prev
+        seq = np.concatenate([prev, act], axis=1)
+    K = min(2, seq.shape[1])
+    return padded, np.ascontiguousarray(seq[:, seq.shape[1] - K:])
 
 
 def forward(x, layout, w, stride=(1, 1, 1), pads=((0, 0, 0),) * 3, out_layout=NDHWC,

@@ -417,3 +417,76 @@ def test_forward_small_workload_against_torch(orc):
     x64 = inp["x"].double().permute(0, 4, 1, 2, 3).numpy()
     ref = torch_conv(x64, inp["w"].double().numpy(), call.stride, call.pads)
     np.testing.assert_array_equal(out["conv"], bf16_bits_from_f32(ref.astype(np.float32)))
+
+
+# ---- padded output + two-frame cache ([cuDNN-PO] "Normalization and Padding Variant",
+#      "Standalone Normalization and Padding Variant") ------------------------------------
+
+def _frames(N, T, H, W, C, seed):
+    rng = np.random.default_rng(seed)
+    # nonzero bf16 bit patterns (sign 0, exponent 1..254), so a stray zero shows
+    return rng.integers(0x0080, 0x7F00, size=(N, T, H, W, C)).astype(np.uint16)
+
+
+def test_pad_cache_worked_examples(orc):
+    # one current frame, no history: planes 0 and 1 all zero, plane 2 = the frame
+    # inside a zero border; the cache holds that single frame
+    act = np.arange(1, 1 + 2 * 3 * 2, dtype=np.uint16).reshape(1, 1, 2, 3, 2)
+    padded, cache = orc.pad_cache_fused(act, 0, np.full((1, 3, 4, 5, 2), 9, np.uint16),
+                                        np.full((1, 1, 2, 3, 2), 9, np.uint16))
+    assert not padded[:, :2].any()
+    assert padded[0, 2, 1, 1].tolist() == [1, 2] and padded[0, 2, 2, 3].tolist() == [11, 12]
+    assert not padded[0, 2, 0].any() and not padded[0, 2, 3].any()
+    assert not padded[0, 2, :, 0].any() and not padded[0, 2, :, 4].any()
+    assert np.array_equal(cache, act)
+    # standalone, two history frames and one new one: the cache is the newest
+    # history frame followed by the new frame
+    prev = _frames(1, 2, 2, 3, 2, 1)
+    padded, cache = orc.pad_cache_standalone(act, prev)
+    assert padded.shape == (1, 3, 4, 5, 2) and cache.shape == (1, 2, 2, 3, 2)
+    assert np.array_equal(padded[:, 0, 1:-1, 1:-1], prev[:, 0])
+    assert np.array_equal(padded[:, 1, 1:-1, 1:-1], prev[:, 1])
+    assert np.array_equal(cache[:, 0], prev[:, 1]) and np.array_equal(cache[:, 1], act[:, 0])
+
+
+@pytest.mark.parametrize("P", [0, 1, 2])
+@pytest.mark.parametrize("Tc", [1, 2, 3, 5])
+def test_pad_cache_fused_leaves_history_and_borders(orc, P, Tc):
+    N, H, W, C = 2, 3, 4, 8
+    act = _frames(N, Tc, H, W, C, 10 + Tc)
+    K = min(2, Tc + P)
+    sentinel = 0x3F80  # bf16 1.0: not written by the kernel wherever it survives
+    padded, cache = orc.pad_cache_fused(
+        act, P, np.full((N, Tc + 2, H + 2, W + 2, C), sentinel, np.uint16),
+        np.full((N, K, H, W, C), sentinel, np.uint16))
+    border = np.ones((H + 2, W + 2), bool)
+    border[1:-1, 1:-1] = False
+    assert not padded[:, :, border].any()                  # every plane's border is zero
+    assert not padded[:, :2 - P].any()                     # missing history planes are zero
+    assert (padded[:, 2 - P:2, 1:-1, 1:-1] == sentinel).all()  # history interiors untouched
+    assert np.array_equal(padded[:, 2:, 1:-1, 1:-1], act)  # current frames, in order
+    kc = min(2, Tc)
+    assert np.array_equal(cache[:, K - kc:], act[:, Tc - kc:])  # newest frames at the tail
+    assert (cache[:, :K - kc] == sentinel).all()           # older frames are the caller's
+
+
+@pytest.mark.parametrize("P", [0, 1, 2])
+@pytest.mark.parametrize("Tc", [1, 2, 3])
+def test_pad_cache_fused_plus_history_step_is_standalone(orc, P, Tc):
+    # The page gives the fused variant plus a caller-side step (history frames into
+    # the history planes' interiors, older cache frames from the previous cache) and
+    # the standalone variant that does both itself: the two must produce the same.
+    N, H, W, C = 1, 2, 3, 8
+    act = _frames(N, Tc, H, W, C, 20 + P)
+    prev = _frames(N, P, H, W, C, 30 + Tc) if P else None
+    K = min(2, Tc + P)
+    padded, cache = orc.pad_cache_fused(act, P, np.full((N, Tc + 2, H + 2, W + 2, C), 7, np.uint16),
+                                        np.full((N, K, H, W, C), 7, np.uint16))
+    for j in range(P):                         # history frame j of P -> plane 2 - P + j
+        padded[:, 2 - P + j, 1:-1, 1:-1] = prev[:, j]
+    older = max(K - Tc, 0)                     # cache slots the current frames do not fill
+    for j in range(older):                     # the newest `older` history frames, in order
+        cache[:, j] = prev[:, P - older + j]
+    ref_padded, ref_cache = orc.pad_cache_standalone(act, prev)
+    assert np.array_equal(padded, ref_padded)
+    assert np.array_equal(cache, ref_cache)
