@@ -452,9 +452,14 @@ def run_case(args):
     if args.tune:
         tun = vvc.Tuning(**{k: int(v) for k, v in (kv.split("=") for kv in args.tune.split(","))})
     wp = vvc.pack_weight(inp["w"].to(dev))
+    epi, extra = call.epi, {}
+    if args.pad_cache >= 0:
+        # padded output + two-frame cache after the fused norm, P history frames
+        epi |= vvc.EPI_PAD_CACHE
+        extra = {"history_frames": args.pad_cache}
     c = vvc.Conv3d(inp["x"].to(dev), wp, call.Cout, call.kernel, call.stride, call.pads, lay, lay,
-                   call.epi, bias=g("bias"), residual=g("residual"),
-                   residual_bias=g("residual_bias"), gamma=g("gamma"), tuning=tun)
+                   epi, bias=g("bias"), residual=g("residual"),
+                   residual_bias=g("residual_bias"), gamma=g("gamma"), tuning=tun, **extra)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
@@ -473,10 +478,63 @@ def run_case(args):
         ts.append(a.elapsed_time(b))
     assert vvc.device_status() == 0
     ms = statistics.median(ts)
-    print(json.dumps({"case": call.name, "layout": args.layout, "ms": round(ms, 4),
-                      "tflops": round(call.flops / (ms * 1e-3) / 1e12, 1),
-                      "gbs": round(call.bytes() / (ms * 1e-3) / 1e9, 1),
-                      "launches": c.launches, "tune": args.tune}), flush=True)
+    line = {"case": call.name, "layout": args.layout, "ms": round(ms, 4),
+            "tflops": round(call.flops / (ms * 1e-3) / 1e12, 1),
+            "gbs": round(call.bytes() / (ms * 1e-3) / 1e9, 1),
+            "launches": c.launches, "tune": args.tune}
+    if args.pad_cache >= 0:
+        line["pad_cache"] = args.pad_cache
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_norm_pad(args):
+    """The standalone post-operations with padded output and cache, timed alone,
+    beside the contiguous standalone call on the same input."""
+    import video_vae_convolution_gb300 as vvc
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    C, T, H, W, P = (int(v) for v in args.norm_pad.split(","))
+    gen = torch.Generator().manual_seed(4000 + C)
+    x = torch.randn((1, T, H, W, C), generator=gen).to(torch.bfloat16).to(dev)
+    gamma = (1 + 0.1 * torch.randn(C, generator=gen)).to(torch.bfloat16).float().to(dev)
+    bias = (0.1 * torch.randn(C, generator=gen)).to(dev)
+    prev = torch.randn((1, P, H, W, C), generator=gen).to(torch.bfloat16).to(dev) if P else None
+    padded = torch.empty((1, T + 2, H + 2, W + 2, C), dtype=torch.bfloat16, device=dev)
+    cache = torch.empty((1, min(2, T + P), H, W, C), dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    ms_pad = timed(lambda: vvc.l2norm_silu_pad(x, gamma, bias, previous=prev, padded=padded,
+                                               cache=cache, stream=stream))
+    ms_flat = timed(lambda: vvc.l2norm_silu(x, gamma, bias, y=y, stream=stream))
+    assert vvc.device_status() == 0
+    # algorithmic bytes: read x (+ history), write the padded tensor and the cache
+    nbytes = 2 * (x.numel() + padded.numel() + cache.numel() + (prev.numel() if P else 0))
+    print(json.dumps({"case": f"l2norm_silu_pad C{C} [1,{T},{H},{W}] P{P}",
+                      "ms": round(ms_pad, 4), "gbs": round(nbytes / (ms_pad * 1e-3) / 1e9, 1),
+                      "ms_contiguous": round(ms_flat, 4),
+                      "gbs_contiguous": round(4 * x.numel() / (ms_flat * 1e-3) / 1e9, 1),
+                      "launches": 2}), flush=True)
     return 0
 
 
@@ -491,8 +549,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pad-cache", type=int, default=-1,
+                    help="with --case: padded output + cache, this many history frames")
+    ap.add_argument("--norm-pad", default="",
+                    help="time the standalone padded post-operations: C,T,H,W,P")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl != "reference" else args.warmup
+    if args.norm_pad:
+        return run_norm_pad(args)
     if args.case:
         return run_case(args)
     rank, world = dist_init(args)

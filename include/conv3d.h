@@ -96,6 +96,17 @@ enum {
   CONV3D_EPI_SAVE_VALUE = 16,     /* also write value (pre-normalisation) to value_out */
   CONV3D_EPI_OUT_PAD_BR = 32,     /* y gets a zero bottom row and right column:
                                      y spatial extent (Ho + 1, Wo + 1); not with L2NORM */
+  CONV3D_EPI_PAD_CACHE = 64,      /* [cuDNN page] "Normalization and Padding Variant":
+                                     requires L2NORM_SILU, NDHWC output, Cout % 8 == 0.
+                                     y is the padded output [N, Do + 2, Ho + 2, Wo + 2,
+                                     Cout]: the activations fill the interiors of planes
+                                     2 .. Do + 1; every plane's one-pixel spatial border
+                                     and the planes before the history_frames history
+                                     planes are zeroed; the history planes' interiors
+                                     are not written (the caller fills them).  cache_out
+                                     [N, K, Ho, Wo, Cout], K = min(2, Do + history_frames):
+                                     the last min(2, Do) activated frames go to its tail;
+                                     its first K - min(2, Do) frames are not written. */
   CONV3D_EPI_DEBUG_STORE_CONV = 1 << 30 /* test aid: also write B(acc) to conv_out, NDHWC */
 };
 
@@ -106,12 +117,17 @@ enum {
  *  pad        (T, H, W) paddings.  Output extent per dimension:
  *             (L + before + after - K) / stride + 1.
  *  y          output, bf16, `out_layout`, [N, Cout, Do, Ho, Wo] or [N, Do, Ho, Wo, Cout]
- *             (Ho + 1, Wo + 1 with CONV3D_EPI_OUT_PAD_BR).
+ *             (Ho + 1, Wo + 1 with CONV3D_EPI_OUT_PAD_BR; [N, Do + 2, Ho + 2, Wo + 2, Cout]
+ *             with CONV3D_EPI_PAD_CACHE).
  *  bias, residual_bias, gamma   fp32 [Cout], as the flags require (else NULL).
  *  residual   bf16, `out_layout`, unpadded output shape (with CONV3D_EPI_RESIDUAL).
  *  value_out  bf16, `out_layout`, unpadded output shape (with CONV3D_EPI_SAVE_VALUE).
  *  conv_out   bf16 NDHWC unpadded output shape (with CONV3D_EPI_DEBUG_STORE_CONV).
- *  workspace  device scratch of at least conv3d_workspace_bytes() (may be NULL if 0). */
+ *  workspace  device scratch of at least conv3d_workspace_bytes() (may be NULL if 0).
+ *  cache_out  bf16 NDHWC [N, min(2, Do + history_frames), Ho, Wo, Cout] (with
+ *             CONV3D_EPI_PAD_CACHE, else ignored).
+ *  history_frames   0, 1 or 2 activated frames the caller keeps in planes
+ *             2 - history_frames .. 1 of y (with CONV3D_EPI_PAD_CACHE, else ignored). */
 typedef struct {
   const void* x;
   int32_t layout;
@@ -131,6 +147,8 @@ typedef struct {
   void* conv_out;
   void* workspace;
   size_t workspace_bytes;
+  void* cache_out;
+  int32_t history_frames;
 } conv3d_params;
 
 /* Optional plan overrides (tests and tuning).  0 (or -1 where noted) = automatic. */
@@ -243,6 +261,23 @@ int conv3d_plan(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_plan
 int l2norm_silu(const void* x, int64_t rows, int32_t C, const float* input_bias,
                 const void* residual, const float* residual_bias, const float* gamma,
                 void* y, void* value_out, conv3d_stream_t stream);
+
+/* The same post-operations with padded output and cache ([cuDNN page] "Standalone
+ * Normalization and Padding Variant").  x: bf16 NDHWC [N, T, H, W, C], C % 8 == 0.
+ * previous: NULL, or the history_frames (1 or 2) prior activated frames, bf16
+ * [N, history_frames, H, W, C].  padded_out: bf16 [N, T + 2, H + 2, W + 2, C]: the
+ * frames [previous..., activated x...] end at plane T + 1 (history in planes
+ * 2 - history_frames .. 1), zeros before them and on every plane's one-pixel
+ * spatial border.  cache_out: bf16 [N, min(2, T + history_frames), H, W, C], the
+ * last frames of that sequence.  value_out (optional): the pre-normalisation value,
+ * [N, T, H, W, C].  input_bias, residual, residual_bias as in l2norm_silu.  All
+ * pointers 16-byte aligned; outputs must not overlap each other or any input.
+ * Two launches on `stream`; nothing is allocated. */
+int l2norm_silu_pad(const void* x, int32_t N, int32_t T, int32_t H, int32_t W, int32_t C,
+                    const float* input_bias, const void* residual, const float* residual_bias,
+                    const float* gamma, const void* previous, int32_t history_frames,
+                    void* padded_out, void* cache_out, void* value_out,
+                    conv3d_stream_t stream);
 
 /* ---- status ---------------------------------------------------------------------- */
 

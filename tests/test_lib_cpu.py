@@ -185,3 +185,50 @@ def test_l2norm_validation():
         vvc.ERR_OVERLAP
     assert lib.l2norm_silu(0x1002, 10, 16, None, None, None, 0x4000, 0x8000, None, None) == \
         vvc.ERR_MISALIGNED
+
+
+def test_pad_cache_validation_and_plan():
+    lib = vvc._lib()
+    base = dict(Cin=32, Cout=40, D=5, H=7, W=9)
+    p = _valid(**base)
+    p.epi = vvc.EPI_L2NORM_SILU | vvc.EPI_PAD_CACHE
+    p.gamma, p.cache_out, p.history_frames = 0x300000, 0x40000000, 1
+    n_pc, n = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.conv3d_workspace_bytes_ex(ctypes.byref(p), None, ctypes.byref(n_pc)) == vvc.OK
+    q = _valid(**base)
+    q.epi, q.gamma = vvc.EPI_L2NORM_SILU, 0x300000
+    assert lib.conv3d_workspace_bytes_ex(ctypes.byref(q), None, ctypes.byref(n)) == vvc.OK
+    # the contiguous activations [N, Do, Ho, Wo, Cout] sit after the call's own scratch
+    assert n_pc.value >= n.value + 3 * 5 * 7 * 40 * 2
+    assert _plan(p).launches == _plan(q).launches + 1
+    for bad in (dict(epi=vvc.EPI_PAD_CACHE),                                 # no norm
+                dict(history_frames=3), dict(history_frames=-1),
+                dict(cache_out=None), dict(out_layout=vvc.NCDHW)):
+        r = _valid(**base)
+        r.epi = vvc.EPI_L2NORM_SILU | vvc.EPI_PAD_CACHE
+        r.gamma, r.cache_out, r.history_frames = 0x300000, 0x40000000, 1
+        for k, v in bad.items():
+            setattr(r, k, v)
+        assert lib.conv3d_launch_count(ctypes.byref(r), None) == vvc.ERR_INVALID_ARG, bad
+    r = _valid(Cin=32, Cout=36, D=5, H=7, W=9)                              # Cout % 8 != 0
+    r.epi = vvc.EPI_L2NORM_SILU | vvc.EPI_PAD_CACHE
+    r.gamma, r.cache_out = 0x300000, 0x40000000
+    assert lib.conv3d_launch_count(ctypes.byref(r), None) == vvc.ERR_INVALID_ARG
+
+
+def test_l2norm_silu_pad_validation():
+    lib = vvc._lib()
+    a = dict(x=0x100000, g=0x200000, padded=0x10000000, cache=0x20000000)
+
+    def call(N=1, T=2, H=3, W=4, C=16, prev=None, P=0, **kw):
+        d = dict(a, **kw)
+        return lib.l2norm_silu_pad(d["x"], N, T, H, W, C, None, None, None, d["g"], prev, P,
+                                   d["padded"], d["cache"], None, None)
+    assert call(C=12) == vvc.ERR_INVALID_ARG                 # C % 8 != 0
+    assert call(P=1) == vvc.ERR_INVALID_ARG                  # history without frames
+    assert call(prev=0x30000000, P=0) == vvc.ERR_INVALID_ARG  # frames without a count
+    assert call(prev=0x30000000, P=3) == vvc.ERR_INVALID_ARG
+    assert call(g=0) == vvc.ERR_INVALID_ARG
+    assert call(x=0x100008) == vvc.ERR_MISALIGNED
+    assert call(padded=0x100000 + 64) == vvc.ERR_OVERLAP    # padded output over the input
+    assert call(cache=0x10000000 + 32) == vvc.ERR_OVERLAP   # cache over the padded output

@@ -28,6 +28,7 @@ EPI_RESIDUAL_BIAS = 4
 EPI_L2NORM_SILU = 8
 EPI_SAVE_VALUE = 16
 EPI_OUT_PAD_BR = 32
+EPI_PAD_CACHE = 64
 EPI_DEBUG_STORE_CONV = 1 << 30
 
 OK = 0
@@ -45,7 +46,7 @@ EXPORTS = (
     "conv3d_packed_weight_bytes", "conv3d_pack_weight", "conv3d_workspace_bytes",
     "conv3d_workspace_bytes_ex", "conv3d_fwd", "conv3d_fwd_ex", "conv3d_launch_count",
     "l2norm_silu", "conv3d_get_device_status", "conv3d_status_string", "conv3d_version",
-    "conv3d_struct_size", "conv3d_fwd_static_scratch", "conv3d_plan",
+    "conv3d_struct_size", "conv3d_fwd_static_scratch", "conv3d_plan", "l2norm_silu_pad",
 )
 
 
@@ -75,6 +76,7 @@ class Params(ctypes.Structure):
         ("residual_bias", ctypes.c_void_p), ("gamma", ctypes.c_void_p),
         ("value_out", ctypes.c_void_p), ("conv_out", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("cache_out", ctypes.c_void_p), ("history_frames", ctypes.c_int32),
     ]
 
 
@@ -131,6 +133,8 @@ def _lib():
                 lib.conv3d_plan.restype = ctypes.c_int
                 lib.l2norm_silu.argtypes = [vp, i64, i32, vp, vp, vp, vp, vp, vp, vp]
                 lib.l2norm_silu.restype = ctypes.c_int
+                lib.l2norm_silu_pad.argtypes = [vp] + [i32] * 5 + [vp] * 5 + [i32] + [vp] * 4
+                lib.l2norm_silu_pad.restype = ctypes.c_int
                 lib.conv3d_get_device_status.argtypes = [ctypes.POINTER(i32), vp]
                 lib.conv3d_get_device_status.restype = ctypes.c_int
                 lib.conv3d_status_string.argtypes = [ctypes.c_int]
@@ -224,7 +228,8 @@ class Conv3d:
     def __init__(self, x, w_packed, Cout, kernel, stride=(1, 1, 1),
                  pads=((0, 0, PAD_ZERO),) * 3, layout=NDHWC, out_layout=NDHWC, epi=0,
                  bias=None, residual=None, residual_bias=None, gamma=None, y=None,
-                 value_out=None, conv_out=None, workspace=None, tuning: Optional[Tuning] = None):
+                 value_out=None, conv_out=None, workspace=None, tuning: Optional[Tuning] = None,
+                 cache_out=None, history_frames=0):
         N, C, D, H, W = _dims(x, layout)
         KT, KR, KS = kernel
         Do, Ho, Wo = out_dims(D, H, W, kernel, stride, pads)
@@ -232,9 +237,15 @@ class Conv3d:
         self.dims = (N, C, D, H, W)
         self.out_dims = (Do, Ho, Wo)
         pad_br = bool(epi & EPI_OUT_PAD_BR)
+        if y is None and epi & EPI_PAD_CACHE:
+            # padded output: two leading planes and a one-pixel spatial border
+            y = torch.empty((N, Do + 2, Ho + 2, Wo + 2, Cout), dtype=torch.bfloat16, device=dev)
         if y is None:
             y = torch.empty(out_shape(N, Cout, Do, Ho, Wo, out_layout, pad_br),
                             dtype=torch.bfloat16, device=dev)
+        if epi & EPI_PAD_CACHE and cache_out is None:
+            cache_out = torch.empty((N, min(2, Do + history_frames), Ho, Wo, Cout),
+                                    dtype=torch.bfloat16, device=dev)
         if epi & EPI_SAVE_VALUE and value_out is None:
             value_out = torch.empty(out_shape(N, Cout, Do, Ho, Wo, out_layout),
                                     dtype=torch.bfloat16, device=dev)
@@ -258,6 +269,9 @@ class Conv3d:
         p.gamma = None if gamma is None else gamma.data_ptr()
         p.value_out = None if value_out is None else value_out.data_ptr()
         p.conv_out = None if conv_out is None else conv_out.data_ptr()
+        p.cache_out = None if cache_out is None else cache_out.data_ptr()
+        p.history_frames = history_frames
+        self.cache_out = cache_out
         self.tuning = tuning
         tp = ctypes.byref(tuning) if tuning is not None else None
         nbytes = ctypes.c_size_t(0)
@@ -308,6 +322,27 @@ def l2norm_silu(x: torch.Tensor, gamma: torch.Tensor, input_bias=None, residual=
                               _ptr(residual_bias), _ptr(gamma), _ptr(y), _ptr(value),
                               _stream(stream)), "l2norm_silu")
     return (y, value) if save_value else y
+
+
+def l2norm_silu_pad(x: torch.Tensor, gamma: torch.Tensor, input_bias=None, residual=None,
+                    residual_bias=None, previous=None, save_value=False, padded=None,
+                    cache=None, stream=None):
+    """Standalone post-operations with padded output and cache on channels-last bf16
+    x [N, T, H, W, C] (C % 8 == 0); previous: None or 1-2 prior activated frames
+    [N, P, H, W, C].  Returns (padded [N, T+2, H+2, W+2, C], cache
+    [N, min(2, T+P), H, W, C], value or None)."""
+    N, T, H, W, C = x.shape
+    P = 0 if previous is None else previous.shape[1]
+    if padded is None:
+        padded = torch.empty((N, T + 2, H + 2, W + 2, C), dtype=x.dtype, device=x.device)
+    if cache is None:
+        cache = torch.empty((N, min(2, T + P), H, W, C), dtype=x.dtype, device=x.device)
+    value = torch.empty_like(x) if save_value else None
+    _check(_lib().l2norm_silu_pad(_ptr(x), N, T, H, W, C, _ptr(input_bias), _ptr(residual),
+                                  _ptr(residual_bias), _ptr(gamma), _ptr(previous), P,
+                                  _ptr(padded), _ptr(cache), _ptr(value), _stream(stream)),
+           "l2norm_silu_pad")
+    return padded, cache, value
 
 
 def device_status(stream=None) -> int:

@@ -12,6 +12,7 @@
 
 #include "conv3d.h"
 #include "internal.h"
+#include "pad_cache.h"
 
 namespace vvc {
 cudaError_t launch_conv_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const ConvTCParams& p,
@@ -96,6 +97,10 @@ struct Plan {
   dim3 grid;
   size_t smem = 0;
   int launches = 0;
+  // padded output + cache: the kernels write the activations to a contiguous
+  // [N, Do, Ho, Wo, Cout] scratch buffer at pc_off, and one more launch places them
+  bool pad_cache = false;
+  size_t pc_off = 0, pc_bytes = 0;
 };
 
 struct Span {
@@ -140,8 +145,16 @@ int validate_shape(const conv3d_params* p, int* Do, int* Ho, int* Wo) {
   const unsigned e = p->epi;
   const unsigned known = CONV3D_EPI_BIAS | CONV3D_EPI_RESIDUAL | CONV3D_EPI_RESIDUAL_BIAS |
                          CONV3D_EPI_L2NORM_SILU | CONV3D_EPI_SAVE_VALUE |
-                         CONV3D_EPI_OUT_PAD_BR | CONV3D_EPI_DEBUG_STORE_CONV;
+                         CONV3D_EPI_OUT_PAD_BR | CONV3D_EPI_PAD_CACHE |
+                         CONV3D_EPI_DEBUG_STORE_CONV;
   if (e & ~known) return CONV3D_ERR_INVALID_ARG;
+  if (e & CONV3D_EPI_PAD_CACHE) {
+    // padded output + cache: the activations of the fused norm, channels last
+    if (!(e & CONV3D_EPI_L2NORM_SILU) || (e & CONV3D_EPI_OUT_PAD_BR) ||
+        p->out_layout != CONV3D_NDHWC || p->Cout % 8 != 0 || p->history_frames < 0 ||
+        p->history_frames > 2 || !p->cache_out)
+      return CONV3D_ERR_INVALID_ARG;
+  }
   if ((e & CONV3D_EPI_RESIDUAL_BIAS) && !(e & CONV3D_EPI_RESIDUAL)) return CONV3D_ERR_INVALID_ARG;
   if ((e & CONV3D_EPI_OUT_PAD_BR) && (e & CONV3D_EPI_L2NORM_SILU)) return CONV3D_ERR_INVALID_ARG;
   if (!p->x || !p->w_packed || !p->y) return CONV3D_ERR_INVALID_ARG;
@@ -184,7 +197,7 @@ void fill_epi(const conv3d_params* p, const Plan& pl, EpiParams* e) {
   e->Do = pl.Do;
   e->Ho = pl.Ho;
   e->Wo = pl.Wo;
-  e->flags = p->epi;
+  e->flags = p->epi & ~static_cast<unsigned>(CONV3D_EPI_PAD_CACHE);
   e->bias = p->bias;
   e->residual = static_cast<const uint16_t*>(p->residual);
   e->rbias = p->residual_bias;
@@ -696,7 +709,7 @@ int plan_pm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   return CONV3D_OK;
 }
 
-int make_plan(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
+int make_plan_conv(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
   int rc = validate_shape(p, &pl->Do, &pl->Ho, &pl->Wo);
   if (rc) return rc;
   rc = check_supported(p);
@@ -763,14 +776,19 @@ int check_pointers(const conv3d_params* p, const Plan& pl) {
   auto mis = [](const void* q) { return q && (reinterpret_cast<uintptr_t>(q) & 15u); };
   if (mis(p->x) || mis(p->w_packed) || mis(p->y) || mis(p->residual) || mis(p->value_out) ||
       mis(p->conv_out) || mis(p->bias) || mis(p->residual_bias) || mis(p->gamma) ||
-      (pl.ws_bytes && mis(p->workspace)))
+      (pl.ws_bytes && mis(p->workspace)) || (pl.pad_cache && mis(p->cache_out)))
     return CONV3D_ERR_MISALIGNED;
   if (pl.ws_bytes && (!p->workspace || p->workspace_bytes < pl.ws_bytes))
     return CONV3D_ERR_WORKSPACE;
   const bool padbr = (p->epi & CONV3D_EPI_OUT_PAD_BR) != 0;
   const size_t out_elems = (size_t)p->N * p->Cout * pl.Do * pl.Ho * pl.Wo;
   const size_t y_elems =
-      (size_t)p->N * p->Cout * pl.Do * (pl.Ho + (padbr ? 1 : 0)) * (pl.Wo + (padbr ? 1 : 0));
+      pl.pad_cache
+          ? (size_t)p->N * p->Cout * (pl.Do + 2) * (pl.Ho + 2) * (pl.Wo + 2)
+          : (size_t)p->N * p->Cout * pl.Do * (pl.Ho + (padbr ? 1 : 0)) * (pl.Wo + (padbr ? 1 : 0));
+  const size_t cache_elems = pl.pad_cache ? (size_t)p->N * p->Cout * pl.Ho * pl.Wo *
+                                                std::min(2, pl.Do + p->history_frames)
+                                          : 0;
   auto span = [](const void* q, size_t bytes) {
     Span s;
     s.lo = reinterpret_cast<uintptr_t>(q);
@@ -790,6 +808,7 @@ int check_pointers(const conv3d_params* p, const Plan& pl) {
       span((p->epi & CONV3D_EPI_SAVE_VALUE) ? p->value_out : nullptr, out_elems * 2),
       span((p->epi & CONV3D_EPI_DEBUG_STORE_CONV) ? p->conv_out : nullptr, out_elems * 2),
       span(pl.ws_bytes ? p->workspace : nullptr, pl.ws_bytes),
+      span(pl.pad_cache ? p->cache_out : nullptr, cache_elems * 2),
   };
   for (size_t i = 0; i < sizeof(out) / sizeof(out[0]); ++i) {
     for (size_t j = 0; j < sizeof(in) / sizeof(in[0]); ++j)
@@ -797,6 +816,19 @@ int check_pointers(const conv3d_params* p, const Plan& pl) {
     for (size_t j = i + 1; j < sizeof(out) / sizeof(out[0]); ++j)
       if (overlaps(out[i], out[j])) return CONV3D_ERR_OVERLAP;
   }
+  return CONV3D_OK;
+}
+
+// The plan of a call: the convolution's own plan, plus (padded output + cache) the
+// scratch activation buffer after its workspace and the launch that places them.
+int make_plan(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
+  const int rc = make_plan_conv(p, tu, pl);
+  if (rc || !(p->epi & CONV3D_EPI_PAD_CACHE)) return rc;
+  pl->pad_cache = true;
+  pl->pc_off = static_cast<size_t>(round_up(pl->ws_bytes, 256));
+  pl->pc_bytes = (size_t)p->N * pl->Do * pl->Ho * pl->Wo * p->Cout * 2;
+  pl->ws_bytes = pl->pc_off + pl->pc_bytes;
+  pl->launches += 1;
   return CONV3D_OK;
 }
 
@@ -1017,6 +1049,30 @@ int conv3d_plan(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_plan
   return CONV3D_OK;
 }
 
+// Padded output + cache: the activations at `act` (contiguous [N, Do, Ho, Wo, Cout])
+// go to the interiors of planes 2.. of y, the newest frames to the cache tail, and
+// the borders and missing history planes are zeroed; nothing else is written.
+int place_pad_cache(const conv3d_params* p, const Plan& pl, const void* act, cudaStream_t s) {
+  if (!pl.pad_cache) return CONV3D_OK;
+  vvc::PadCacheArgs a{};
+  a.act = static_cast<const uint16_t*>(act);
+  a.a_sh = (long long)pl.Wo * p->Cout;
+  a.a_st = a.a_sh * pl.Ho;
+  a.a_sn = a.a_st * pl.Do;
+  a.prev = nullptr;
+  a.padded = static_cast<uint16_t*>(p->y);
+  a.cache = static_cast<uint16_t*>(p->cache_out);
+  a.N = p->N;
+  a.Tc = pl.Do;
+  a.Hc = pl.Ho;
+  a.Wc = pl.Wo;
+  a.C = p->Cout;
+  a.P = p->history_frames;
+  a.K = std::min(2, pl.Do + p->history_frames);
+  a.copy_interior = 1;
+  return vvc::launch_pad_cache(a, s) == cudaSuccess ? CONV3D_OK : CONV3D_ERR_CUDA;
+}
+
 int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_stream_t stream) {
   Plan pl;
   int rc = make_plan(p, tuning, &pl);
@@ -1026,7 +1082,12 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const void* xin = p->x;
   uint8_t* ws = static_cast<uint8_t*>(p->workspace);
-  const conv3d_params* pm = p;  // the convolution the tensor maps describe
+  // where the kernels write y: the caller's y, or (padded output + cache) the
+  // contiguous scratch activations that the last launch places
+  void* yk = pl.pad_cache ? static_cast<void*>(ws + pl.pc_off) : p->y;
+  conv3d_params pk = *p;
+  pk.y = yk;
+  const conv3d_params* pm = &pk;  // the convolution the tensor maps describe
   conv3d_params q;
   if (pl.im2col) {
     void* dst = ws + pl.stage_off;
@@ -1041,6 +1102,7 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
     q = pl.q;
     q.x = dst;
     q.w_packed = wr;
+    q.y = yk;
     pm = &q;
     xin = dst;
   } else if (pl.stage) {
@@ -1057,6 +1119,7 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
   float* partial = reinterpret_cast<float*>(ws + pl.partial_off);
   if (pl.cm) {
     ConvCMParams kp = pl.cp;
+    kp.epi.y = yk;
     if (kp.k_splits > 1) kp.partial = partial;
     if (kp.norm) kp.vscratch = reinterpret_cast<uint16_t*>(ws + pl.vscratch_off);
     vvc::CmOutMaps om;
@@ -1073,16 +1136,17 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
     if (kp.k_splits > 1 &&
         vvc::launch_splitk_epilogue(partial, kp.k_splits, kp.M_total, kp.epi, s) != cudaSuccess)
       return CONV3D_ERR_CUDA;
-    return CONV3D_OK;
+    return place_pad_cache(p, pl, yk, s);
   }
   ConvTCParams kp = pl.kp;
+  kp.epi.y = yk;
   if (kp.k_splits > 1) kp.partial = partial;
   if (vvc::launch_conv_tc(tmA, tmB, kp, pl.grid, pl.smem, s) != cudaSuccess)
     return CONV3D_ERR_CUDA;
   if (kp.k_splits > 1 &&
       vvc::launch_splitk_epilogue(partial, kp.k_splits, kp.M_total, kp.epi, s) != cudaSuccess)
     return CONV3D_ERR_CUDA;
-  return CONV3D_OK;
+  return place_pad_cache(p, pl, yk, s);
 }
 
 int conv3d_fwd(const conv3d_params* p, conv3d_stream_t stream) {
@@ -1132,6 +1196,81 @@ int l2norm_silu(const void* x, int64_t rows, int32_t C, const float* input_bias,
   e.sqrt_c = std::sqrt(static_cast<float>(C));
   cudaError_t err = vvc::launch_l2norm_silu(x, rows, e, reinterpret_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? CONV3D_OK : CONV3D_ERR_CUDA;
+}
+
+int l2norm_silu_pad(const void* x, int32_t N, int32_t T, int32_t H, int32_t W, int32_t C,
+                    const float* input_bias, const void* residual, const float* residual_bias,
+                    const float* gamma, const void* previous, int32_t history_frames,
+                    void* padded_out, void* cache_out, void* value_out,
+                    conv3d_stream_t stream) {
+  if (!x || !gamma || !padded_out || !cache_out || N < 1 || T < 1 || H < 1 || W < 1 || C < 8 ||
+      C % 8 != 0 || history_frames < 0 || history_frames > 2 ||
+      (history_frames > 0) != (previous != nullptr) || (residual_bias && !residual))
+    return CONV3D_ERR_INVALID_ARG;
+  const long long rows = (long long)N * T * H * W;
+  const long long padded_rows = (long long)N * (T + 2) * (H + 2) * (W + 2);
+  if (padded_rows > 0x7fffffffLL) return CONV3D_ERR_UNSUPPORTED;
+  auto mis = [](const void* q) { return q && (reinterpret_cast<uintptr_t>(q) & 15u); };
+  if (mis(x) || mis(input_bias) || mis(residual) || mis(residual_bias) || mis(gamma) ||
+      mis(previous) || mis(padded_out) || mis(cache_out) || mis(value_out))
+    return CONV3D_ERR_MISALIGNED;
+  const int K = std::min(2, T + history_frames);
+  const size_t tb = (size_t)rows * C * 2;
+  auto span = [](const void* q, size_t bytes) {
+    Span s;
+    s.lo = reinterpret_cast<uintptr_t>(q);
+    s.hi = q ? s.lo + bytes : s.lo;
+    return s;
+  };
+  const Span in[] = {span(x, tb), span(input_bias, (size_t)C * 4), span(residual, tb),
+                     span(residual_bias, (size_t)C * 4), span(gamma, (size_t)C * 4),
+                     span(previous, (size_t)N * history_frames * H * W * C * 2)};
+  const Span out[] = {span(padded_out, (size_t)padded_rows * C * 2),
+                      span(cache_out, (size_t)N * K * H * W * C * 2), span(value_out, tb)};
+  for (size_t i = 0; i < sizeof(out) / sizeof(out[0]); ++i) {
+    for (const Span& sp : in)
+      if (overlaps(out[i], sp)) return CONV3D_ERR_OVERLAP;
+    for (size_t j = i + 1; j < sizeof(out) / sizeof(out[0]); ++j)
+      if (overlaps(out[i], out[j])) return CONV3D_ERR_OVERLAP;
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // 1: the post-operations, each row written to its padded interior position
+  EpiParams e{};
+  e.y = padded_out;
+  e.out_layout = vvc::LAYOUT_NDHWC;
+  e.N = 1;
+  e.Cout = C;
+  e.Do = e.Ho = e.Wo = 1;
+  e.flags = vvc::EPI_L2NORM_SILU | (input_bias ? vvc::EPI_BIAS : 0u) |
+            (residual ? vvc::EPI_RESIDUAL : 0u) | (residual_bias ? vvc::EPI_RESIDUAL_BIAS : 0u) |
+            (value_out ? vvc::EPI_SAVE_VALUE : 0u);
+  e.bias = input_bias;
+  e.residual = static_cast<const uint16_t*>(residual);
+  e.rbias = residual_bias;
+  e.gamma = gamma;
+  e.value_out = static_cast<uint16_t*>(value_out);
+  e.sqrt_c = std::sqrt(static_cast<float>(C));
+  if (vvc::launch_l2norm_silu_pad(x, N, T, H, W, e, s) != cudaSuccess) return CONV3D_ERR_CUDA;
+  // 2: borders, missing history planes, history copies and the cache, the
+  // activations read back from the padded interiors
+  vvc::PadCacheArgs a{};
+  const long long Wp = W + 2, Hp = H + 2;
+  a.act = static_cast<const uint16_t*>(padded_out) + ((2 * Hp + 1) * Wp + 1) * C;
+  a.a_sh = Wp * C;
+  a.a_st = Hp * Wp * C;
+  a.a_sn = (T + 2LL) * Hp * Wp * C;
+  a.prev = static_cast<const uint16_t*>(previous);
+  a.padded = static_cast<uint16_t*>(padded_out);
+  a.cache = static_cast<uint16_t*>(cache_out);
+  a.N = N;
+  a.Tc = T;
+  a.Hc = H;
+  a.Wc = W;
+  a.C = C;
+  a.P = history_frames;
+  a.K = K;
+  a.copy_interior = 0;
+  return vvc::launch_pad_cache(a, s) == cudaSuccess ? CONV3D_OK : CONV3D_ERR_CUDA;
 }
 
 int conv3d_get_device_status(int32_t* status, conv3d_stream_t stream) {

@@ -12,6 +12,7 @@
 
 #include "epilogue.cuh"
 #include "internal.h"
+#include "pad_cache.h"
 
 namespace vvc {
 
@@ -493,12 +494,239 @@ __global__ void l2norm_silu_kernel(const uint16_t* __restrict__ x, long long row
   epilogue_pixel(e, px, 0, C, load);
 }
 
+cudaError_t launch_norm_rows(const void* x, long long rows, const EpiParams& e, int T, int H,
+                             int W, int padded, cudaStream_t s);
+size_t norm_rows_smem(int C, int R);
+
 cudaError_t launch_l2norm_silu(const void* x, long long rows, const EpiParams& e,
                                cudaStream_t s) {
+  if (e.Cout % 8 == 0 && norm_rows_smem(e.Cout, 1) != 0)  // 16-byte rows: staged kernel
+    return launch_norm_rows(x, rows, e, 1, 1, 1, 0, s);
   const int threads = 128;
   const long long blocks = (rows + threads - 1) / threads;
   l2norm_silu_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
       static_cast<const uint16_t*>(x), rows, e);
+  return cudaGetLastError();
+}
+
+// ---- padded output + two-frame cache (cuDNN frontend doc "Fused Conv3D + Bias +
+//      Residual + RMSNorm + SiLU", "Normalization and Padding Variant" and
+//      "Standalone Normalization and Padding Variant") ---------------------------------
+
+// Standalone post-operations, C % 8 == 0, rows staged through shared memory.  A
+// block takes R consecutive rows (pixels) of x:
+//   1. every element's value = B(B(x + bias) + B(residual + residual_bias)) (steps
+//      as the flags ask) is computed from 16-byte loads, coalesced across the block,
+//      and kept as bf16 in shared memory (value_out written here);
+//   2. one thread per row sums value^2 in channel order: den = max(sqrt(.), 1e-12);
+//   3. every element's activation B(B(B(B(value / den) * sqrt(C)) * gamma) / (1 +
+//      exp(-.))) goes out in 16-byte stores, to row r of y or (padded) to the
+//      interior position (n, t + 2, h + 1, w + 1) of [N, T + 2, H + 2, W + 2, C].
+// The rounding steps and the order of the sum are those of epilogue_pixel.
+constexpr int kNormRows = 32;
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ uint4 f32_to_bf16x8(const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    w[i] = uint32_t(bf16_bits(f[2 * i])) | (uint32_t(bf16_bits(f[2 * i + 1])) << 16);
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__global__ void __launch_bounds__(256) l2norm_silu_rows_kernel(const uint16_t* __restrict__ x,
+                                                               long long rows, EpiParams e,
+                                                               int T, int H, int W, int padded,
+                                                               int R) {
+  extern __shared__ uint4 norm_smem[];
+  const int C = e.Cout;
+  const int G = C >> 3;          // 16-byte groups per row
+  const int pitch = G + 1;       // staged row pitch in 16-byte words
+  uint4* stage = norm_smem;
+  float* den = reinterpret_cast<float*>(norm_smem + (size_t)R * pitch);
+  long long* dst_row = reinterpret_cast<long long*>(den + R + (R & 1));
+  const long long r0 = (long long)blockIdx.x * R;
+  const int nr = static_cast<int>(rows - r0 < R ? rows - r0 : R);
+  const bool bias = (e.flags & EPI_BIAS) != 0, res = (e.flags & EPI_RESIDUAL) != 0;
+  const bool rbias = (e.flags & EPI_RESIDUAL_BIAS) != 0, save = (e.flags & EPI_SAVE_VALUE) != 0;
+  for (int u = threadIdx.x; u < nr * G; u += blockDim.x) {
+    const int r = u / G, g = u - r * G;
+    const long long off = (r0 + r) * C + 8 * g;
+    float v[8];
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(x + off), v);
+    if (bias) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = round_bf16(__fadd_rn(v[i], __ldg(e.bias + 8 * g + i)));
+    }
+    if (res) {
+      float sk[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(e.residual + off), sk);
+      if (rbias) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          sk[i] = round_bf16(__fadd_rn(sk[i], __ldg(e.rbias + 8 * g + i)));
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = round_bf16(__fadd_rn(v[i], sk[i]));
+    }
+    const uint4 vb = f32_to_bf16x8(v);
+    stage[r * pitch + g] = vb;
+    if (save) *reinterpret_cast<uint4*>(e.value_out + off) = vb;
+  }
+  __syncthreads();
+  if (threadIdx.x < nr) {
+    const int r = threadIdx.x;
+    float ss = 0.0f;
+    for (int g = 0; g < G; ++g) {
+      float v[8];
+      bf16x8_to_f32(stage[r * pitch + g], v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = __fadd_rn(ss, __fmul_rn(v[i], v[i]));
+    }
+    den[r] = norm_den(ss);
+    long long q = r0 + r;
+    if (padded) {
+      const int w = static_cast<int>(q % W);
+      q /= W;
+      const int h = static_cast<int>(q % H);
+      q /= H;
+      const int t = static_cast<int>(q % T);
+      const long long n = q / T;
+      q = ((n * (T + 2) + t + 2) * (H + 2) + h + 1) * (W + 2) + w + 1;
+    }
+    dst_row[r] = q;
+  }
+  __syncthreads();
+  uint16_t* y = static_cast<uint16_t*>(e.y);
+  for (int u = threadIdx.x; u < nr * G; u += blockDim.x) {
+    const int r = u / G, g = u - r * G;
+    float v[8];
+    bf16x8_to_f32(stage[r * pitch + g], v);
+    const float d = den[r];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = norm_silu1(v[i], d, e.sqrt_c, __ldg(e.gamma + 8 * g + i));
+    *reinterpret_cast<uint4*>(y + dst_row[r] * C + 8 * g) = f32_to_bf16x8(v);
+  }
+}
+
+// Shared memory of one row-staged block, or 0 when R rows do not fit.
+size_t norm_rows_smem(int C, int R) {
+  const size_t b = (size_t)R * (C / 8 + 1) * 16 + (size_t)(R + (R & 1)) * 4 + (size_t)R * 8;
+  return b <= 200 * 1024 ? b : 0;
+}
+
+cudaError_t launch_norm_rows(const void* x, long long rows, const EpiParams& e, int T, int H,
+                             int W, int padded, cudaStream_t s) {
+  int R = kNormRows;
+  while (R > 1 && norm_rows_smem(e.Cout, R) == 0) R /= 2;
+  const size_t smem = norm_rows_smem(e.Cout, R);
+  if (smem == 0) return cudaErrorInvalidValue;
+  static size_t configured = 48 * 1024;
+  if (smem > configured) {
+    const cudaError_t err = cudaFuncSetAttribute(
+        l2norm_silu_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    configured = smem;
+  }
+  const long long blocks = (rows + R - 1) / R;
+  l2norm_silu_rows_kernel<<<static_cast<unsigned>(blocks), 256, smem, s>>>(
+      static_cast<const uint16_t*>(x), rows, e, T, H, W, padded, R);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_l2norm_silu_pad(const void* x, int N, int T, int H, int W, const EpiParams& e,
+                                   cudaStream_t s) {
+  return launch_norm_rows(x, (long long)N * T * H * W, e, T, H, W, 1, s);
+}
+
+// Everything of the padded output and the cache that is not the activations'
+// own padded interiors, one 16-byte group of 8 channels per work item:
+//   padded [N, Tc + 2, Hc + 2, Wc + 2, C]: zero on every plane's spatial border and
+//     on the planes before the P history planes; history plane 2 - P + j takes
+//     prev[:, j] when prev is given (else its interior is left alone); plane t >= 2
+//     takes activated frame t - 2 when copy_interior (else left alone);
+//   cache [N, K, Hc, Wc, C]: slot k holds frame Tc + P - K + k of the sequence
+//     [prev..., activated...]; slots that fall on prev are left alone without prev.
+// Activated frame (n, t) pixel (h, w) is at act + n a_sn + t a_st + h a_sh + w C.
+// Index type I: 32-bit when every work item index fits (no 64-bit divisions).
+template <class I>
+__global__ void pad_cache_kernel(PadCacheArgs a) {
+  const I G = static_cast<I>(a.C >> 3);
+  const I Tp = a.Tc + 2, Hp = a.Hc + 2, Wp = a.Wc + 2;
+  const I Hc = a.Hc, Wc = a.Wc, K = a.K;
+  const I n_pad = static_cast<I>(a.N) * Tp * Hp * Wp * G;
+  const I n_all = n_pad + static_cast<I>(a.N) * K * Hc * Wc * G;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  auto act_at = [&](long long n, int t, int h, int w, int g) {
+    return *reinterpret_cast<const uint4*>(a.act + n * a.a_sn + t * a.a_st + h * a.a_sh +
+                                           (long long)w * a.C + 8 * g);
+  };
+  auto prev_at = [&](long long n, int t, int h, int w, int g) {
+    return *reinterpret_cast<const uint4*>(
+        a.prev + (((n * a.P + t) * a.Hc + h) * a.Wc + w) * a.C + 8 * g);
+  };
+  const I step = static_cast<I>(gridDim.x) * blockDim.x;
+  for (I i = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_all; i += step) {
+    if (i < n_pad) {
+      I q = i;
+      const int g = static_cast<int>(q % G);
+      q /= G;
+      const int wp = static_cast<int>(q % Wp);
+      q /= Wp;
+      const int hp = static_cast<int>(q % Hp);
+      q /= Hp;
+      const int tp = static_cast<int>(q % Tp);
+      const long long n = static_cast<long long>(q / Tp);
+      uint4* dst = reinterpret_cast<uint4*>(a.padded) + i;
+      if (hp == 0 || hp == Hp - 1 || wp == 0 || wp == Wp - 1 || tp < 2 - a.P) {
+        *dst = zero;
+      } else if (tp >= 2) {
+        if (a.copy_interior) *dst = act_at(n, tp - 2, hp - 1, wp - 1, g);
+      } else if (a.prev) {
+        *dst = prev_at(n, tp - (2 - a.P), hp - 1, wp - 1, g);
+      }
+    } else {
+      const I j = i - n_pad;
+      I q = j;
+      const int g = static_cast<int>(q % G);
+      q /= G;
+      const int w = static_cast<int>(q % Wc);
+      q /= Wc;
+      const int h = static_cast<int>(q % Hc);
+      q /= Hc;
+      const int k = static_cast<int>(q % K);
+      const long long n = static_cast<long long>(q / K);
+      const int sidx = a.Tc + a.P - a.K + k;  // position in [prev..., activated...]
+      uint4* dst = reinterpret_cast<uint4*>(a.cache) + j;
+      if (sidx >= a.P)
+        *dst = act_at(n, sidx - a.P, h, w, g);
+      else if (a.prev)
+        *dst = prev_at(n, sidx, h, w, g);
+    }
+  }
+}
+
+cudaError_t launch_pad_cache(const PadCacheArgs& a, cudaStream_t s) {
+  const long long G = a.C / 8;
+  const long long total = (long long)a.N * (a.Tc + 2) * (a.Hc + 2) * (a.Wc + 2) * G +
+                          (long long)a.N * a.K * a.Hc * a.Wc * G;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  if (blocks < 1) blocks = 1;
+  // 32-bit indices while every item index (and the last grid stride past it) fits
+  if (total + (long long)blocks * threads < 0xFFFFFFFFLL)
+    pad_cache_kernel<uint32_t><<<static_cast<unsigned>(blocks), threads, 0, s>>>(a);
+  else
+    pad_cache_kernel<unsigned long long><<<static_cast<unsigned>(blocks), threads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
