@@ -341,6 +341,36 @@ def pad_cache_standalone(act, previous=None):
     return padded, np.ascontiguousarray(seq[:, seq.shape[1] - K:])
 
 
+def group_norm_silu(x, groups, gamma, beta, eps=1e-6, time_isolated=True, silu=True):
+    """Channels-last GroupNorm followed by SiLU, as the MiniMax-H3 comment on the
+    FlyDSL issue describes the layers between the encoder's convolutions: groups of
+    C / groups contiguous channels, statistics per (n, d, group) over H x W x C/groups
+    when time_isolated (the time-to-batch reshape), else per (n, group) over
+    D x H x W x C/groups.
+
+    x: bf16 bits [N, D, H, W, C]; gamma, beta: fp32 [C].  In fp64: mean and biased
+    variance of each group, g = B((x - mean) / sqrt(var + eps) * gamma + beta), and
+    with silu y = B(g / (1 + exp(-g))); returns y (bf16 bits).
+    """
+    xb = _u16(x)
+    N, D, H, W, C = xb.shape
+    assert C % groups == 0
+    xf = bf16_to_f32(xb).astype(np.float64)
+    cg = C // groups
+    # (n, slice, positions, group, channel in group); one slice per frame when isolated
+    v = xf.reshape(N, D, H * W, groups, cg) if time_isolated else \
+        xf.reshape(N, 1, D * H * W, groups, cg)
+    axes = (2, 4)
+    mean = v.mean(axis=axes, keepdims=True)
+    var = ((v - mean) ** 2).mean(axis=axes, keepdims=True)
+    t = (v - mean) / np.sqrt(var + eps)
+    t = t.reshape(xf.shape) * np.asarray(gamma, np.float64) + np.asarray(beta, np.float64)
+    g = bf16_to_f32(round_bf16(t)).astype(np.float64)  # B() of the fp64 value via fp32
+    if not silu:
+        return round_bf16(g)
+    return round_bf16(g / (1.0 + np.exp(-g)))
+
+
 def forward(x, layout, w, stride=(1, 1, 1), pads=((0, 0, 0),) * 3, out_layout=NDHWC,
             flags=0, bias=None, residual=None, residual_bias=None, gamma=None,
             out_pad_br=False, nthreads=0):

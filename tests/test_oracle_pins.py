@@ -490,3 +490,66 @@ def test_pad_cache_fused_plus_history_step_is_standalone(orc, P, Tc):
     ref_padded, ref_cache = orc.pad_cache_standalone(act, prev)
     assert np.array_equal(padded, ref_padded)
     assert np.array_equal(cache, ref_cache)
+
+
+# ---- channels-last GroupNorm + SiLU (FlyDSL issue, MiniMax-H3 comment: the GroupNorm
+#      between the encoder's convolutions, time-isolated groups) -------------------------
+
+def _gn_inputs(orc, shape, C, seed):
+    rng = np.random.default_rng(seed)
+    x = orc.round_bf16(rng.standard_normal(shape).astype(np.float32) * 2 + 0.5)
+    gamma = (1 + 0.2 * rng.standard_normal(C)).astype(np.float32)
+    beta = (0.2 * rng.standard_normal(C)).astype(np.float32)
+    return x, gamma, beta
+
+
+@pytest.mark.parametrize("isolated", [True, False])
+def test_group_norm_matches_torch(orc, isolated):
+    # without the SiLU, the normalised value is torch's group_norm in fp64 over the
+    # NCDHW view: per frame (frames as batch) when time-isolated, else per clip
+    N, D, H, W, C, G = 2, 3, 4, 5, 24, 6
+    x, gamma, beta = _gn_inputs(orc, (N, D, H, W, C), C, 3)
+    got = orc.bf16_to_f32(orc.group_norm_silu(x, G, gamma, beta, eps=1e-6,
+                                              time_isolated=isolated, silu=False))
+    xt = torch.from_numpy(orc.bf16_to_f32(x).astype(np.float64))
+    if isolated:
+        v = xt.reshape(N * D, H, W, C).permute(0, 3, 1, 2)      # frames as batch, NCHW
+    else:
+        v = xt.permute(0, 4, 1, 2, 3)                          # NCDHW
+    ref = torch.nn.functional.group_norm(v, G, torch.from_numpy(gamma.astype(np.float64)),
+                                         torch.from_numpy(beta.astype(np.float64)), eps=1e-6)
+    ref = (ref.permute(0, 2, 3, 1).reshape(N, D, H, W, C) if isolated
+           else ref.permute(0, 2, 3, 4, 1))
+    ref_b = orc.bf16_to_f32(orc.round_bf16(ref.numpy()))
+    np.testing.assert_array_equal(got, ref_b)
+    # the SiLU step: torch's silu in fp64 on the bf16 normalised values, rounded once
+    with_silu = orc.group_norm_silu(x, G, gamma, beta, eps=1e-6, time_isolated=isolated)
+    silu_ref = F.silu(torch.from_numpy(got.astype(np.float64))).numpy()
+    np.testing.assert_array_equal(with_silu, orc.round_bf16(silu_ref))
+
+
+def test_group_norm_closed_forms(orc):
+    N, D, H, W, C, G = 1, 2, 3, 3, 16, 4
+    _, gamma, beta = _gn_inputs(orc, (N, D, H, W, C), C, 4)
+    # a constant group normalises to zero: the output is B(beta) (SiLU off), and with
+    # the SiLU of beta = 0 it is 0
+    x = np.full((N, D, H, W, C), orc.round_bf16(np.float32(1.75)), np.uint16)
+    y = orc.bf16_to_f32(orc.group_norm_silu(x, G, gamma, beta, silu=False))
+    np.testing.assert_array_equal(y, np.broadcast_to(orc.bf16_to_f32(orc.round_bf16(beta)), y.shape))
+    y0 = orc.group_norm_silu(x, G, gamma, np.zeros(C, np.float32))
+    assert not orc.bf16_to_f32(y0).any()
+    # time isolation: rescaling one frame changes nothing anywhere
+    x, gamma, beta = _gn_inputs(orc, (N, D, H, W, C), C, 5)
+    # (frame 1 scaled by 2: exact in bf16; a group's normalised values do not change)
+    xs = orc.bf16_to_f32(x).copy()
+    xs[:, 1] *= 2.0
+    xs_b = orc.round_bf16(xs)
+    a = orc.group_norm_silu(x, G, gamma, beta, eps=0.0)   # eps = 0: the identity is exact
+    b = orc.group_norm_silu(xs_b, G, gamma, beta, eps=0.0)
+    assert np.array_equal(a[:, 0], b[:, 0])
+    assert np.array_equal(a[:, 1], b[:, 1])
+    # negating x and gamma negates the normalised value exactly
+    n1 = orc.bf16_to_f32(orc.group_norm_silu(x, G, gamma, np.zeros(C, np.float32), silu=False))
+    n2 = orc.bf16_to_f32(orc.group_norm_silu(x ^ np.uint16(0x8000), G, -gamma,
+                                             np.zeros(C, np.float32), silu=False))
+    np.testing.assert_array_equal(n1, n2)
