@@ -538,6 +538,46 @@ def run_norm_pad(args):
     return 0
 
 
+def run_group_norm(args):
+    """Channels-last GroupNorm + SiLU with time-isolated groups, timed alone."""
+    import video_vae_convolution_gb300 as vvc
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    C, D, H, W, G = (int(v) for v in args.group_norm.split(","))
+    gen = torch.Generator().manual_seed(5000 + C)
+    x = torch.randn((1, D, H, W, C), generator=gen).to(torch.bfloat16).to(dev)
+    gamma = (1 + 0.1 * torch.randn(C, generator=gen)).to(dev)
+    beta = (0.1 * torch.randn(C, generator=gen)).to(dev)
+    y = torch.empty_like(x)
+    ws = torch.empty(vvc._lib().group_norm_workspace_bytes(1, D, H, W, C, G, 1),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    run = lambda: vvc.group_norm_silu(x, G, gamma, beta, y=y, workspace=ws, stream=stream)
+    for _ in range(args.warmup):
+        flush.zero_()
+        run()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    assert vvc.device_status() == 0
+    ms = statistics.median(ts)
+    nbytes = 4 * x.numel()  # algorithmic: x read once, y written once
+    print(json.dumps({"case": f"group_norm_silu C{C} [1,{D},{H},{W}] G{G} time-isolated",
+                      "ms": round(ms, 4), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                      "launches": 2}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--workload", default="wan")
@@ -553,8 +593,12 @@ def main():
                     help="with --case: padded output + cache, this many history frames")
     ap.add_argument("--norm-pad", default="",
                     help="time the standalone padded post-operations: C,T,H,W,P")
+    ap.add_argument("--group-norm", default="",
+                    help="time the channels-last GroupNorm + SiLU: C,D,H,W,groups")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl != "reference" else args.warmup
+    if args.group_norm:
+        return run_group_norm(args)
     if args.norm_pad:
         return run_norm_pad(args)
     if args.case:

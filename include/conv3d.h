@@ -279,6 +279,25 @@ int l2norm_silu_pad(const void* x, int32_t N, int32_t T, int32_t H, int32_t W, i
                     void* padded_out, void* cache_out, void* value_out,
                     conv3d_stream_t stream);
 
+/* ---- channels-last GroupNorm (+ SiLU) ([FlyDSL issue] MiniMax-H3 comment, "An extra
+ *      argument for NDHWC": the GroupNorm between the encoder's convolutions, with
+ *      time-isolated groups) ------------------------------------------------------------
+ * x, y: bf16 NDHWC [N, D, H, W, C], C % 8 == 0, 8 <= C <= 2048; groups divides C and a
+ * group is C / groups contiguous channels.  Statistics per (n, d, group) over
+ * H * W * C / groups elements when time_isolated (each frame on its own), else per
+ * (n, group) over D * H * W * C / groups: mean and biased variance, accumulated in fp32
+ * per block and combined in fp64.  y = B((x - mean) / sqrt(var + eps) * gamma[c] +
+ * beta[c]), then with silu y = B(y / (1 + exp(-y))).  gamma, beta: fp32 [C], or NULL for
+ * 1 and 0.  workspace: at least group_norm_workspace_bytes() bytes of device memory.
+ * All pointers 16-byte aligned; y must not overlap x, gamma, beta or the workspace.
+ * Two launches on `stream`; nothing is allocated. */
+size_t group_norm_workspace_bytes(int32_t N, int32_t D, int32_t H, int32_t W, int32_t C,
+                                  int32_t groups, int32_t time_isolated);
+int group_norm_silu(const void* x, int32_t N, int32_t D, int32_t H, int32_t W, int32_t C,
+                    int32_t groups, int32_t time_isolated, float eps, const float* gamma,
+                    const float* beta, int32_t silu, void* y, void* workspace,
+                    size_t workspace_bytes, conv3d_stream_t stream);
+
 /* ---- status ---------------------------------------------------------------------- */
 
 /* Synchronises `stream`, then reads and clears the device status word: *status

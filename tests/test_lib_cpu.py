@@ -232,3 +232,21 @@ def test_l2norm_silu_pad_validation():
     assert call(x=0x100008) == vvc.ERR_MISALIGNED
     assert call(padded=0x100000 + 64) == vvc.ERR_OVERLAP    # padded output over the input
     assert call(cache=0x10000000 + 32) == vvc.ERR_OVERLAP   # cache over the padded output
+
+
+def test_group_norm_validation():
+    lib = vvc._lib()
+    assert lib.group_norm_workspace_bytes(1, 2, 3, 4, 128, 32, 1) > 0
+    assert lib.group_norm_workspace_bytes(1, 2, 3, 4, 120, 32, 1) == 0   # groups must divide C
+    assert lib.group_norm_workspace_bytes(1, 2, 3, 4, 12, 4, 1) == 0     # C % 8 != 0
+    assert lib.group_norm_workspace_bytes(1, 2, 3, 4, 4096, 32, 1) == 0  # C > 2048
+    ws = lib.group_norm_workspace_bytes(1, 2, 3, 4, 128, 32, 1)
+
+    def call(x=0x100000, y=0x200000, w=0x300000, wb=ws, C=128, G=32, eps=1e-6):
+        return lib.group_norm_silu(x, 1, 2, 3, 4, C, G, 1, eps, None, None, 1, y, w, wb, None)
+    assert call(C=96, G=7) == vvc.ERR_INVALID_ARG
+    assert call(eps=-1.0) == vvc.ERR_INVALID_ARG
+    assert call(y=0x200008) == vvc.ERR_MISALIGNED
+    assert call(wb=ws - 16) == vvc.ERR_WORKSPACE
+    assert call(y=0x100000 + 256) == vvc.ERR_OVERLAP   # y over x
+    assert call(w=0x200000 + 64) == vvc.ERR_OVERLAP    # workspace over y

@@ -47,6 +47,7 @@ EXPORTS = (
     "conv3d_workspace_bytes_ex", "conv3d_fwd", "conv3d_fwd_ex", "conv3d_launch_count",
     "l2norm_silu", "conv3d_get_device_status", "conv3d_status_string", "conv3d_version",
     "conv3d_struct_size", "conv3d_fwd_static_scratch", "conv3d_plan", "l2norm_silu_pad",
+    "group_norm_workspace_bytes", "group_norm_silu",
 )
 
 
@@ -135,6 +136,11 @@ def _lib():
                 lib.l2norm_silu.restype = ctypes.c_int
                 lib.l2norm_silu_pad.argtypes = [vp] + [i32] * 5 + [vp] * 5 + [i32] + [vp] * 4
                 lib.l2norm_silu_pad.restype = ctypes.c_int
+                lib.group_norm_workspace_bytes.argtypes = [i32] * 7
+                lib.group_norm_workspace_bytes.restype = sz
+                lib.group_norm_silu.argtypes = ([vp] + [i32] * 7 + [ctypes.c_float, vp, vp, i32, vp,
+                                                vp, sz, vp])
+                lib.group_norm_silu.restype = ctypes.c_int
                 lib.conv3d_get_device_status.argtypes = [ctypes.POINTER(i32), vp]
                 lib.conv3d_get_device_status.restype = ctypes.c_int
                 lib.conv3d_status_string.argtypes = [ctypes.c_int]
@@ -343,6 +349,24 @@ def l2norm_silu_pad(x: torch.Tensor, gamma: torch.Tensor, input_bias=None, resid
                                   _ptr(padded), _ptr(cache), _ptr(value), _stream(stream)),
            "l2norm_silu_pad")
     return padded, cache, value
+
+
+def group_norm_silu(x: torch.Tensor, groups: int, gamma=None, beta=None, eps=1e-6,
+                    time_isolated=True, silu=True, y=None, workspace=None, stream=None):
+    """Channels-last GroupNorm (+ SiLU) of bf16 x [N, D, H, W, C] (C % 8 == 0): per
+    frame when time_isolated, else per clip; returns y (same shape)."""
+    N, D, H, W, C = x.shape
+    if y is None:
+        y = torch.empty_like(x)
+    nbytes = _lib().group_norm_workspace_bytes(N, D, H, W, C, groups, int(time_isolated))
+    if nbytes == 0:
+        raise Conv3dError(ERR_INVALID_ARG, "group_norm_silu")
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    _check(_lib().group_norm_silu(_ptr(x), N, D, H, W, C, groups, int(time_isolated), eps,
+                                  _ptr(gamma), _ptr(beta), int(silu), _ptr(y), _ptr(workspace),
+                                  workspace.numel(), _stream(stream)), "group_norm_silu")
+    return y
 
 
 def device_status(stream=None) -> int:

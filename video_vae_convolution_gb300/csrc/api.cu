@@ -12,6 +12,7 @@
 
 #include "conv3d.h"
 #include "internal.h"
+#include "group_norm.h"
 #include "pad_cache.h"
 
 namespace vvc {
@@ -1271,6 +1272,76 @@ int l2norm_silu_pad(const void* x, int32_t N, int32_t T, int32_t H, int32_t W, i
   a.K = K;
   a.copy_interior = 0;
   return vvc::launch_pad_cache(a, s) == cudaSuccess ? CONV3D_OK : CONV3D_ERR_CUDA;
+}
+
+namespace {
+// Geometry of a GroupNorm call; false when the shape is not supported.
+bool group_norm_shape(int32_t N, int32_t D, int32_t H, int32_t W, int32_t C, int32_t groups,
+                      int32_t time_isolated, vvc::GroupNormArgs* a, int* threads) {
+  if (N < 1 || D < 1 || H < 1 || W < 1 || C < 8 || C > 2048 || C % 8 != 0 || groups < 1 ||
+      C % groups != 0)
+    return false;
+  const long long slices = time_isolated ? (long long)N * D : (long long)N;
+  const long long P = time_isolated ? (long long)H * W : (long long)D * H * W;
+  if (slices > 65535 || P * C > (1LL << 40)) return false;
+  long long chunk = 0;
+  int chunks = 0;
+  vvc::group_norm_geometry(C, P, threads, &chunk, &chunks);
+  a->P = P;
+  a->chunk = chunk;
+  a->chunks = chunks;
+  a->slices = static_cast<int>(slices);
+  a->C = C;
+  a->groups = groups;
+  return true;
+}
+}  // namespace
+
+size_t group_norm_workspace_bytes(int32_t N, int32_t D, int32_t H, int32_t W, int32_t C,
+                                  int32_t groups, int32_t time_isolated) {
+  vvc::GroupNormArgs a{};
+  int threads = 0;
+  if (!group_norm_shape(N, D, H, W, C, groups, time_isolated, &a, &threads)) return 0;
+  return (size_t)a.slices * a.chunks * a.groups * sizeof(double2);
+}
+
+int group_norm_silu(const void* x, int32_t N, int32_t D, int32_t H, int32_t W, int32_t C,
+                    int32_t groups, int32_t time_isolated, float eps, const float* gamma,
+                    const float* beta, int32_t silu, void* y, void* workspace,
+                    size_t workspace_bytes, conv3d_stream_t stream) {
+  vvc::GroupNormArgs a{};
+  int threads = 0;
+  if (!x || !y || !workspace || !(eps >= 0.0f) || eps > 1e30f ||
+      !group_norm_shape(N, D, H, W, C, groups, time_isolated, &a, &threads))
+    return CONV3D_ERR_INVALID_ARG;
+  auto mis = [](const void* q) { return q && (reinterpret_cast<uintptr_t>(q) & 15u); };
+  if (mis(x) || mis(y) || mis(gamma) || mis(beta) || mis(workspace)) return CONV3D_ERR_MISALIGNED;
+  const size_t need = (size_t)a.slices * a.chunks * a.groups * sizeof(double2);
+  if (workspace_bytes < need) return CONV3D_ERR_WORKSPACE;
+  const size_t tb = (size_t)N * D * H * W * C * 2;
+  auto span = [](const void* q, size_t bytes) {
+    Span s;
+    s.lo = reinterpret_cast<uintptr_t>(q);
+    s.hi = q ? s.lo + bytes : s.lo;
+    return s;
+  };
+  const Span in[] = {span(x, tb), span(gamma, (size_t)C * 4), span(beta, (size_t)C * 4)};
+  const Span out[] = {span(y, tb), span(workspace, need)};
+  for (size_t i = 0; i < 2; ++i) {
+    for (const Span& sp : in)
+      if (overlaps(out[i], sp)) return CONV3D_ERR_OVERLAP;
+  }
+  if (overlaps(out[0], out[1])) return CONV3D_ERR_OVERLAP;
+  a.x = static_cast<const uint16_t*>(x);
+  a.y = static_cast<uint16_t*>(y);
+  a.gamma = gamma;
+  a.beta = beta;
+  a.partial = static_cast<double2*>(workspace);
+  a.silu = silu ? 1 : 0;
+  a.eps = eps;
+  return vvc::launch_group_norm(a, threads, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? CONV3D_OK
+             : CONV3D_ERR_CUDA;
 }
 
 int conv3d_get_device_status(int32_t* status, conv3d_stream_t stream) {
