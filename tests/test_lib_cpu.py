@@ -250,3 +250,30 @@ def test_group_norm_validation():
     assert call(wb=ws - 16) == vvc.ERR_WORKSPACE
     assert call(y=0x100000 + 256) == vvc.ERR_OVERLAP   # y over x
     assert call(w=0x200000 + 64) == vvc.ERR_OVERLAP    # workspace over y
+
+
+def test_ndhwc_calls_plan_no_transpose():
+    # every call of the benchmark workloads in NDHWC runs the convolution alone (plus the
+    # split reduction, or the spatial gather of a narrow input): no layout staging launch
+    import workloads as wl
+    lib = vvc._lib()
+    for w in ("wan", "ladder", "fused160", "t1"):
+        for call in wl.all_workloads()[w].calls:
+            p = vvc.Params()
+            p.x, p.w_packed, p.y = 0x100000, 0x200000, 0x10000000
+            p.layout = p.out_layout = vvc.NDHWC
+            p.N, p.Cin, p.D, p.H, p.W = call.N, call.Cin, call.D, call.H, call.W
+            p.Cout = call.Cout
+            p.KT, p.KR, p.KS = call.kernel
+            for i in range(3):
+                p.stride[i] = call.stride[i]
+                b, a, m = call.pads[i]
+                p.pad[i].before, p.pad[i].after = b, a
+                p.pad[i].mode = vvc.PAD_ZERO if m == wl.ZERO else vvc.PAD_REFLECT
+            p.epi = call.epi
+            p.bias = p.residual_bias = p.gamma = 0x300000
+            p.residual = 0x400000
+            info = _plan(p)
+            expected = 1 + (info.k_splits > 1) + info.im2col
+            assert info.launches == expected, (call.name, info.launches, expected)
+            assert info.im2col == (call.Cin < 8), call.name
