@@ -307,7 +307,9 @@ int conv3d_get_device_status(int32_t* status, conv3d_stream_t stream);
 
 const char* conv3d_status_string(int status);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor).  2.00: conv3d_params gained cache_out and
+ * history_frames, conv3d_tuning gained pair; conv3d_plan, l2norm_silu_pad and the GroupNorm
+ * calls were added. */
 int conv3d_version(void);
 
 /* sizeof() of the ABI structs, for bindings to check their mirrors:

@@ -41,6 +41,9 @@ ERR_CUDA = -6
 ERR_DEVICE_TIMEOUT = -7
 ERR_SCRATCH_LIMIT = -8
 
+# ABI version of the C library this binding mirrors (major * 100 + minor).
+ABI_VERSION = 200
+
 # Every function the C header declares (checked by the tests against include/conv3d.h).
 EXPORTS = (
     "conv3d_packed_weight_bytes", "conv3d_pack_weight", "conv3d_workspace_bytes",
@@ -149,6 +152,8 @@ def _lib():
                 lib.conv3d_version.restype = ctypes.c_int
                 lib.conv3d_struct_size.argtypes = [ctypes.c_int]
                 lib.conv3d_struct_size.restype = sz
+                if lib.conv3d_version() // 100 != ABI_VERSION // 100:
+                    raise RuntimeError(f"library ABI {lib.conv3d_version()}, binding {ABI_VERSION}")
                 for which, st in ((0, Params), (1, Tuning), (2, Pad), (3, PlanInfo)):
                     if lib.conv3d_struct_size(which) != ctypes.sizeof(st):
                         raise RuntimeError(f"ABI struct mismatch for {st.__name__}")

@@ -1370,7 +1370,7 @@ const char* conv3d_status_string(int status) {
   }
 }
 
-int conv3d_version(void) { return 100; }
+int conv3d_version(void) { return 200; }
 
 }  // extern "C"
 
