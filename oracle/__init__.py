@@ -371,6 +371,23 @@ def group_norm_silu(x, groups, gamma, beta, eps=1e-6, time_isolated=True, silu=T
     return round_bf16(g / (1.0 + np.exp(-g)))
 
 
+def upsample2x_nearest(x):
+    """Nearest-exact x2 spatial upsampling of NDHWC bf16 bits [N, D, H, W, C] (ROCm/FlyDSL
+    PR "Add Qwen-Image VAE classic conv shapes ...", "Upsample Conv2d": the decoder's
+    convolution runs at the doubled H x W after it).  At scale 2 the source of output
+    (h, w) is (floor((h + 0.5) / 2), floor((w + 0.5) / 2)) = (h // 2, w // 2)."""
+    xb = _u16(x)
+    return np.ascontiguousarray(np.repeat(np.repeat(xb, 2, axis=2), 2, axis=3))
+
+
+def upsample2x_conv_acc(x, w, nthreads=0):
+    """fp32 accumulator of the 3x3 (KT = 1), zero-pad-1, stride-1 convolution of the x2
+    nearest-upsampled NDHWC input: the plain definition, with the upsampled tensor
+    written out."""
+    return conv3d_acc(upsample2x_nearest(x), NDHWC, w, (1, 1, 1),
+                      ((0, 0, PAD_ZERO), (1, 1, PAD_ZERO), (1, 1, PAD_ZERO)), nthreads)
+
+
 def forward(x, layout, w, stride=(1, 1, 1), pads=((0, 0, 0),) * 3, out_layout=NDHWC,
             flags=0, bias=None, residual=None, residual_bias=None, gamma=None,
             out_pad_br=False, nthreads=0):

@@ -553,3 +553,48 @@ def test_group_norm_closed_forms(orc):
     n2 = orc.bf16_to_f32(orc.group_norm_silu(x ^ np.uint16(0x8000), G, -gamma,
                                              np.zeros(C, np.float32), silu=False))
     np.testing.assert_array_equal(n1, n2)
+
+
+# ---- x2 nearest upsampling before a 3x3 convolution (FlyDSL PR, "Upsample Conv2d") ------
+
+def test_upsample2x_nearest_matches_torch(orc):
+    rng = np.random.default_rng(11)
+    x = orc.round_bf16(rng.standard_normal((2, 1, 5, 7, 8)).astype(np.float32))
+    got = orc.upsample2x_nearest(x)
+    xt = torch.from_numpy(orc.bf16_to_f32(x)).permute(0, 4, 1, 2, 3)[:, :, 0]   # NCHW
+    ref = F.interpolate(xt, scale_factor=2, mode="nearest-exact")
+    ref = ref.permute(0, 2, 3, 1).unsqueeze(1).numpy()
+    np.testing.assert_array_equal(orc.bf16_to_f32(got), ref)
+
+
+def test_upsample2x_conv_parity_classes(orc):
+    # Output (2i + ph, 2j + pw) of the zero-pad-1 3x3 convolution of the x2 nearest
+    # upsampled input reads upsampled rows 2i + ph + r - 1 (r = 0..2), i.e. low-res rows
+    # i + (-1, 0, 0)[r] for ph = 0 and i + (0, 0, 1)[r] for ph = 1 (columns alike): each
+    # parity class is a convolution of the low-res input with the same 9 weights and a
+    # tap -> offset table.  The fused kernel computes exactly this.
+    rng = np.random.default_rng(12)
+    N, H, W, Ci, Co = 1, 5, 6, 8, 4
+    x = orc.round_bf16(rng.standard_normal((N, 1, H, W, Ci)).astype(np.float32))
+    w = orc.round_bf16((rng.standard_normal((Co, Ci, 1, 3, 3)) / 8).astype(np.float32))
+    xf = orc.bf16_to_f32(x).astype(np.float64)[:, 0]            # [N, H, W, Ci]
+    wf = orc.bf16_to_f32(w).astype(np.float64)[:, :, 0]         # [Co, Ci, 3, 3]
+    up = np.repeat(np.repeat(xf, 2, axis=1), 2, axis=2)         # [N, 2H, 2W, Ci]
+    upp = np.pad(up, ((0, 0), (1, 1), (1, 1), (0, 0)))
+    direct = np.zeros((N, 2 * H, 2 * W, Co))
+    for r in range(3):
+        for s in range(3):
+            direct += np.einsum("nhwc,oc->nhwo", upp[:, r:r + 2 * H, s:s + 2 * W], wf[:, :, r, s])
+    off = ((-1, 0, 0), (0, 0, 1))
+    xp = np.pad(xf, ((0, 0), (1, 1), (1, 1), (0, 0)))           # low-res, zero border
+    for ph in range(2):
+        for pw in range(2):
+            cls = np.zeros((N, H, W, Co))
+            for r in range(3):
+                for s in range(3):
+                    a, b = 1 + off[ph][r], 1 + off[pw][s]
+                    cls += np.einsum("nhwc,oc->nhwo", xp[:, a:a + H, b:b + W], wf[:, :, r, s])
+            np.testing.assert_allclose(direct[:, ph::2, pw::2], cls, rtol=1e-12, atol=1e-12)
+    # the oracle's fp32 accumulator of the plain definition agrees with fp64
+    acc = orc.upsample2x_conv_acc(x, w)[:, 0]
+    np.testing.assert_allclose(acc, direct, rtol=1e-5, atol=1e-5)
