@@ -1,16 +1,22 @@
 """Benchmark: bf16 implicit-GEMM conv3d on one GB300 (per layer TFLOP/s and chain ms).
 
-Workload (one step = one pass of the whole chain): the Wan-like channel-constant
-chain of valid convolutions (pad applied outside) — x [1,96,6,354,642] with
-w [96,96,3,3,3]; x [1,384,3,46,82] with w [384,384,3,3,3]; rank-4 x [4,96,353,641]
-with w [96,96,3,3] — each run once with NCDHW input/output and once with NDHWC
-throughout.  Inputs are seeded synthetic tensors of those shapes.
+Headline workload (one step = one pass of the whole chain): the 30-call causal
+video-VAE encoder tile of the FlyDSL issue's MiniMax-H3 "Shapes" table, N = 1,
+17 frames, every call a 3x3x3 convolution with causal temporal zero pad 2 and
+reflect spatial pad 1 (conv_in 3->128 at 256^2, 128->128 x4, the strided and
+widening calls down to 1024->1024 at 16^2, conv_out 1024->48), NDHWC throughout,
+each call reading the previous call's output.  Inputs are seeded synthetic
+tensors of those shapes (the real model's activations and weights are not
+needed to time the convolutions).
 
-Prints one JSON line.  `value` is chain TFLOP/s (algorithmic FLOP of the six
-calls / device time of one chain), inputs resident in HBM, L2 flushed between
-steps.  `e2e` is the same metric with pinned host inputs copied in and outputs
-copied out inside the timed region.  `--impl reference` times the CPU oracle
-on a bounded sample of the same workload.
+Prints one JSON line.  `value` is chain TFLOP/s (algorithmic FLOP of the 30 calls
+/ device time of one chain), the chain's input resident in HBM, L2 flushed
+between steps.  `e2e` is the same metric with the chain's input copied in from
+pinned host memory and its output copied out inside the timed region.  `layers`
+holds per-call rows of the ladder (times inside the chain) and of the other
+workloads (the Wan-like chain, the fused 160 blocks, the T=1 image-VAE layers),
+each timed alone after an L2 flush.  `--impl reference` times the CPU oracle on a
+bounded sample of the ladder.
 """
 
 from __future__ import annotations
@@ -32,17 +38,18 @@ import torch  # noqa: E402
 
 import workloads as wl  # noqa: E402
 
-WORKLOAD_NAME = "wan"
+WORKLOAD_NAME = "ladder"
+METRIC = "bf16 conv3d TFLOP/s (chain)"
 L2_FLUSH_BYTES = 256 << 20
 
 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from one ncu
-# capture (profiles/conv_cm_wan96_ndhwc.md), keyed by a hash of the kernel's
-# sources (comments and whitespace left out): a changed kernel reports null until
-# it is captured again.
+# capture (profiles/), keyed by a hash of the kernel's sources (comments and
+# whitespace left out) and the call it was captured on: a changed kernel reports
+# null until it is captured again.
 KERNEL_SOURCES = ["conv_cm.cu", "epilogue_cm.cuh", "epilogue.cuh", "kernel_common.cuh",
                   "ptx.cuh", "internal.h"]
-NCU_TRAFFIC = {"f2e0061935f07fe9": 262620928 + 140352512}
+NCU_TRAFFIC = {}
 
 
 def source_code_only(text):
@@ -67,8 +74,8 @@ def kernel_source_hash(read=None):
     return h.hexdigest()[:16]
 
 
-def measured_traffic():
-    return NCU_TRAFFIC.get(kernel_source_hash())
+def measured_traffic(call_name):
+    return NCU_TRAFFIC.get((kernel_source_hash(), call_name))
 
 
 def peaks():
@@ -82,6 +89,29 @@ def peaks():
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                 "source": "fallback"}
+
+
+def cpu_info(threads=None):
+    """CPU model, logical CPUs (nproc) and the oracle's OpenMP thread count."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return {"cpu_model": model or "unknown", "nproc": os.cpu_count(), "omp_threads": threads}
 
 
 class ClockSampler:
@@ -181,87 +211,100 @@ def max_over_ranks(v, world):
     return float(t.item())
 
 
-def chain_calls():
-    w = wl.wan()
-    out = []
-    for lay in (wl.NCDHW, wl.NDHWC):
-        for call in w.calls:
-            out.append((call, lay))
-    return out
-
-
-def workload_config(args, extra=None):
-    cfg = {"workload": "wan_chain: valid 3x3x3 96->96 [1,96,6,354,642], 384->384 "
-                       "[1,384,3,46,82], 3x3 96->96 [4,96,353,641]; each NCDHW->NCDHW and "
-                       "NDHWC->NDHWC",
-           "calls_per_step": 6, "l2": "flushed between steps (256 MiB write, untimed)",
-           "inputs": "seeded synthetic N(0,1) bf16, weights N(0,1/sqrt(fan_in))"}
+def workload_config(world=1, extra=None):
+    cfg = {"workload": "causal VAE encoder ladder, 30 calls chained: conv_in 3->128 "
+                       "[1,17,256,256]; 128->128 x4, 128->128 s(1,2,2); 128->256, 256->256 x3 "
+                       "@[17,128,128], s(2,2,2); 256->256 x4 @[9,64,64], s(2,2,2); 256->512, "
+                       "512->512 x3 @[5,32,32], s(1,2,2); 512->512 x4, 512->1024, "
+                       "1024->1024 x3 @[5,16,16]; conv_out 1024->48; 3x3x3, causal T pad "
+                       "(2,0) zero + reflect H,W (1,1); NDHWC in and out",
+           "calls_per_step": 30, "layout": "NDHWC",
+           "l2": "flushed between steps (256 MiB write, untimed); inside a step each call "
+                 "reads the previous call's output",
+           "inputs": "seeded synthetic: x N(0,1) bf16, weights N(0,1/sqrt(fan_in)) bf16",
+           "parallelism": f"replicas x{world}"}
     if extra:
         cfg.update(extra)
     return cfg
 
 
+def call_class(name):
+    """Layer class of a ladder call: its name without the repeat index."""
+    base, _, idx = name.rpartition("_")
+    return base if idx.isdigit() and base else name
+
+
 # ---- CPU oracle legs ------------------------------------------------------------------------
 
-def oracle_rate(target_s=12.0, max_points=None):
-    """Times the oracle on sampled output pixels of every chain call; returns
-    (TFLOP/s, cores, sample description)."""
+def oracle_ladder_rate(target_s=12.0):
+    """Times the oracle on sampled output pixels of each layer class of the ladder
+    and extrapolates to the whole chain.  Returns (TFLOP/s, extrapolated chain ms,
+    threads, sample description)."""
     import oracle
     oracle.build()
-    cores = oracle.num_threads(0)
-    flops = 0.0
-    t_total = 0.0
-    samples = []
-    per_call = target_s / 3.0
-    for call in wl.wan().calls:
-        inp = wl.make_inputs("wan", call, wl.NDHWC)
+    threads = oracle.num_threads(0)
+    calls = wl.ladder().calls
+    classes = {}
+    for c in calls:
+        classes.setdefault(call_class(c.name), []).append(c)
+    per_class = max(0.2, target_s / len(classes))
+    chain_s = 0.0
+    pixels = 0
+    spent_total = 0.0
+    for cls, members in classes.items():
+        call = members[0]
+        inp = wl.make_inputs("ladder", call, wl.NDHWC)
         xb, wb = wl.bits(inp["x"]), wl.bits(inp["w"])
         Do, Ho, Wo = call.out_dims()
         fpp = 2.0 * call.Cout * call.K  # FLOP per output pixel
         rng = np.random.default_rng(1)
-        n = 64
-        spent = 0.0
-        while spent < per_call and (max_points is None or n <= max_points):
+        n = 16
+        spent = flops = 0.0
+        while spent < per_class:
             pts = np.stack([rng.integers(0, call.N, n), rng.integers(0, Do, n),
                             rng.integers(0, Ho, n), rng.integers(0, Wo, n)], 1)
             t0 = time.perf_counter()
             oracle.conv3d_acc_points(xb, wl.NDHWC, wb, pts, call.stride, call.pads)
-            dt = time.perf_counter() - t0
-            spent += dt
-            t_total += dt
+            spent += time.perf_counter() - t0
             flops += fpp * n
-            samples.append(n)
+            pixels += n
             n = min(n * 2, 1 << 16)
-    rate = flops / t_total / 1e12
-    desc = (f"oracle direct conv (fp64 accumulate) on {sum(samples)} sampled output pixels "
-            f"across the 3 chain shapes, {t_total:.1f} s")
-    return rate, cores, desc
+        rate = flops / spent  # FLOP/s on this class
+        chain_s += sum(c.flops for c in members) / rate
+        spent_total += spent
+    total = sum(c.flops for c in calls)
+    desc = (f"oracle direct conv (fp64 accumulate) on {pixels} sampled output pixels of the "
+            f"{len(classes)} ladder layer classes ({spent_total:.1f} s), extrapolated to the "
+            f"30-call chain by each class's FLOP")
+    return total / chain_s / 1e12, chain_s * 1e3, threads, desc
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
     # bounded: the whole run stays within about two minutes of CPU time
-    budget = max(1.0, min(8.0, 120.0 / max(1, args.steps + args.warmup)))
-    rates = []
+    budget = max(1.5, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
     for _ in range(args.warmup):
-        oracle_rate(target_s=min(1.0, budget))
+        oracle_ladder_rate(target_s=min(1.5, budget))
     t0 = time.perf_counter()
-    desc = ""
-    cores = 0
+    rates, chain_ms = [], []
+    desc, threads = "", 0
     for _ in range(args.steps):
-        r, cores, desc = oracle_rate(target_s=budget)
+        r, ms, threads, desc = oracle_ladder_rate(target_s=budget)
         rates.append(r)
+        chain_ms.append(ms)
     elapsed = time.perf_counter() - t0
     value = statistics.median(rates)
-    total_flop = sum(c.flops for c, _ in chain_calls())
-    line = {"impl": "reference", "metric": "bf16 conv3d TFLOP/s (chain)", "value": value,
+    info = cpu_info(threads)
+    line = {"impl": "reference", "metric": METRIC, "value": value,
             "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": total_flop / (value * 1e12) * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(args),
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                             "sample": desc},
+            "ms_per_step": statistics.median(chain_ms),
+            "ms_per_step_note": "extrapolated from the oracle's time on sampled output pixels "
+                                "(a full chain would take this long)",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(world),
+            "cpu_baseline": dict({"value": value, "unit": "TFLOP/s", "cores": threads,
+                                  "kind": "oracle", "sample": desc}, **info),
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "wall_s": elapsed}
@@ -271,6 +314,97 @@ def run_reference(args, rank, world):
 
 # ---- GPU arm -------------------------------------------------------------------------------
 
+def device_inputs(call, dev, layout, seed):
+    """Synthetic inputs of one call drawn on the device (same distributions as the
+    workloads module; used for the per-layer rows, where only the timing counts)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    N, C, D, H, W = call.N, call.Cin, call.D, call.H, call.W
+    shape = (N, C, D, H, W) if layout == wl.NCDHW else (N, D, H, W, C)
+    x = torch.randn(shape, generator=g, device=dev).to(torch.bfloat16)
+    kt, kr, ks = call.kernel
+    w = (torch.randn((call.Cout, C, kt, kr, ks), generator=g, device=dev) /
+         float(np.sqrt(C * kt * kr * ks))).to(torch.bfloat16)
+    Do, Ho, Wo = call.out_dims()
+    out = {"x": x, "w": w, "bias": None, "residual": None, "residual_bias": None, "gamma": None}
+    if call.epi & wl.EPI_BIAS:
+        out["bias"] = 0.1 * torch.randn(call.Cout, generator=g, device=dev)
+    if call.epi & wl.EPI_RESIDUAL:
+        rs = (N, call.Cout, Do, Ho, Wo) if layout == wl.NCDHW else (N, Do, Ho, Wo, call.Cout)
+        out["residual"] = torch.randn(rs, generator=g, device=dev).to(torch.bfloat16)
+    if call.epi & wl.EPI_RESIDUAL_BIAS:
+        out["residual_bias"] = 0.1 * torch.randn(call.Cout, generator=g, device=dev)
+    if call.epi & wl.EPI_L2NORM_SILU:
+        out["gamma"] = (1 + 0.1 * torch.randn(call.Cout, generator=g, device=dev)).to(
+            torch.bfloat16).float()
+    return out
+
+
+def layer_row(call, ms, pk, launches, layout, workload, extra=None):
+    tf = call.flops / (ms * 1e-3) / 1e12
+    gbs = call.bytes() / (ms * 1e-3) / 1e9
+    row = {"workload": workload, "name": call.name,
+           "layout": "NCDHW" if layout == wl.NCDHW else "NDHWC",
+           "cin": call.Cin, "cout": call.Cout, "kernel": list(call.kernel),
+           "stride": list(call.stride), "ms": round(ms, 4), "tflops": round(tf, 1),
+           "frac_bf16": round(tf / pk["bf16_tflops"], 3), "gbs": round(gbs, 1),
+           "frac_hbm": round(gbs / pk["hbm_gbs"], 3), "launches": launches}
+    if extra:
+        row.update(extra)
+    return row
+
+
+def time_alone(c, stream, flush, reps, warm=2):
+    """Median device time of one call, L2 flushed before each launch."""
+    for _ in range(warm):
+        flush.zero_()
+        c(stream)
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        rc = c.run(stream)
+        b.record(stream)
+        if rc != 0:
+            raise RuntimeError(f"conv3d_fwd failed: {rc}")
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+
+def other_layers(dev, stream, flush, pk, reps):
+    """Per-call rows of the Wan-like chain (both layouts), the fused 160 blocks and
+    the T=1 image-VAE layers (both layouts), each call timed alone."""
+    import video_vae_convolution_gb300 as vvc
+    rows = []
+    sums = {}
+    for name in ("wan", "fused160", "t1"):
+        w = wl.all_workloads()[name]
+        for call in w.calls:
+            for lay, out_lay in w.layouts:
+                inp = device_inputs(call, dev, lay, wl.seed_of(name, call))
+                wp = vvc.pack_weight(inp["w"])
+                c = vvc.Conv3d(inp["x"], wp, call.Cout, call.kernel, call.stride, call.pads,
+                               lay, out_lay, call.epi, bias=inp["bias"],
+                               residual=inp["residual"], residual_bias=inp["residual_bias"],
+                               gamma=inp["gamma"])
+                ms = time_alone(c, stream, flush, reps)
+                rows.append(layer_row(call, ms, pk, c.launches, lay, name))
+                key = (name, rows[-1]["layout"])
+                sums[key] = sums.get(key, 0.0) + ms
+                del c, wp, inp
+        torch.cuda.empty_cache()
+    wan_flop = sum(c.flops for c in wl.wan().calls)
+    wan = {"calls": "3 shapes, each NCDHW->NCDHW and NDHWC->NDHWC, timed alone",
+           "ms_ndhwc": round(sums[("wan", "NDHWC")], 4),
+           "ms_ncdhw": round(sums[("wan", "NCDHW")], 4),
+           "tflops": round(2 * wan_flop / ((sums[("wan", "NDHWC")] +
+                                            sums[("wan", "NCDHW")]) * 1e-3) / 1e12, 1)}
+    return rows, wan
+
+
 def run_gpu(args, rank, world):
     import video_vae_convolution_gb300 as vvc
 
@@ -278,29 +412,38 @@ def run_gpu(args, rank, world):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     pk = peaks()
+    # the ladder: seeded inputs (CPU recipe), each call reading the previous output
     calls = []
-    host = []
-    for call, lay in chain_calls():
-        inp = wl.make_inputs("wan", call, lay, lay)
-        x = inp["x"].to(dev)
+    x = None
+    host_in = None
+    for call in wl.ladder().calls:
+        if x is None:
+            inp = wl.make_inputs("ladder", call, wl.NDHWC, wl.NDHWC)
+            host_in = inp["x"].pin_memory()
+            x = inp["x"].to(dev)
+        else:
+            inp = {"w": wl.make_inputs("ladder", call, wl.NDHWC, wl.NDHWC, crop=(1, 3, 3))["w"]}
         wp = vvc.pack_weight(inp["w"].to(dev))
-        c = vvc.Conv3d(x, wp, call.Cout, call.kernel, call.stride, call.pads, lay, lay, 0)
-        calls.append((call, lay, c))
-        host.append(inp["x"].pin_memory())
+        c = vvc.Conv3d(x, wp, call.Cout, call.kernel, call.stride, call.pads, wl.NDHWC,
+                       wl.NDHWC, call.epi)
+        calls.append((call, c))
+        x = c.y
     torch.cuda.synchronize()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    total_flop = sum(call.flops for call, _, _ in calls)
-    launches_per_step = sum(c.launches for _, _, c in calls)
+    total_flop = sum(call.flops for call, _ in calls)
+    launches_per_step = sum(c.launches for _, c in calls)
+    # launches besides the convolution and its split reduction (input staging)
+    staging_launches = sum(c.launches - 1 - (1 if c.plan.k_splits > 1 else 0) for _, c in calls)
 
     def chain(evs=None):
-        for i, (_, _, c) in enumerate(calls):
+        for i, (_, c) in enumerate(calls):
             if evs is not None:
-                evs[i][0].record(stream)
+                evs[i].record(stream)
             rc = c.run(stream)
             if rc != 0:
                 raise RuntimeError(f"conv3d_fwd failed: {rc}")
-            if evs is not None:
-                evs[i][1].record(stream)
+        if evs is not None:
+            evs[-1].record(stream)
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -310,7 +453,6 @@ def run_gpu(args, rank, world):
 
     sampler = ClockSampler(dev.index)
     sampler.start()
-    per_call = [[] for _ in calls]
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
@@ -318,8 +460,7 @@ def run_gpu(args, rank, world):
     step_ev = []
     for _ in range(args.steps):
         flush.zero_()
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in calls]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
         chain(evs)
         step_ev.append(evs)
     torch.cuda.synchronize()
@@ -330,108 +471,102 @@ def run_gpu(args, rank, world):
     status = vvc.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status}")
+    per_call = [[] for _ in calls]
     step_ms = []
     for evs in step_ev:
-        tot = 0.0
-        for i, (a, b) in enumerate(evs):
-            ms = a.elapsed_time(b)
-            per_call[i].append(ms)
-            tot += ms
-        step_ms.append(tot)
+        step_ms.append(evs[0].elapsed_time(evs[-1]))
+        for i in range(len(calls)):
+            per_call[i].append(evs[i].elapsed_time(evs[i + 1]))
     ms_step = statistics.mean(step_ms)
     ms_step = max_over_ranks(ms_step, world)
     value = world * total_flop / (ms_step * 1e-3) / 1e12
 
     layers = []
-    for (call, lay, c), ts in zip(calls, per_call):
+    class_ms = {}
+    for (call, c), ts in zip(calls, per_call):
         ms = statistics.median(ts)
-        tf = call.flops / (ms * 1e-3) / 1e12
-        layers.append({"name": call.name, "layout": "NCDHW" if lay == wl.NCDHW else "NDHWC",
-                       "ms": round(ms, 4), "tflops": round(tf, 1),
-                       "frac_bf16": round(tf / pk["bf16_tflops"], 3),
-                       "gbs": round(call.bytes() / (ms * 1e-3) / 1e9, 1),
-                       "launches": c.launches})
-    # dominant kernel: the 96->96 3-D call in NDHWC (one conv launch)
-    dom_i = next(i for i, (call, lay, c) in enumerate(calls)
-                 if call.name == "wan_96_3d" and lay == wl.NDHWC)
-    dom_call, _, dom_c = calls[dom_i]
-    dom_ms = statistics.mean(per_call[dom_i])
+        layers.append(layer_row(call, ms, pk, c.launches, wl.NDHWC, "ladder",
+                                {"timed": "inside the chain"}))
+        class_ms.setdefault(call_class(call.name), []).append((call, c, ms))
+    # dominant kernel: the layer class with the largest share of the chain's time
+    dom_cls, members = max(class_ms.items(), key=lambda kv: sum(m[2] for m in kv[1]))
+    dom_call, dom_c, _ = members[0]
+    dom_ms = statistics.mean(m[2] for m in members)
     achieved = dom_call.flops / (dom_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(achieved / pk["bf16_tflops"], 4),
-                "traffic": measured_traffic(), "kernel": "vvc::conv_cm_kernel (wan_96_3d, NDHWC)",
+                "traffic": measured_traffic(dom_call.name),
+                "kernel": f"vvc::conv_cm_kernel ({dom_cls}: {dom_call.Cin}->{dom_call.Cout} "
+                          f"[{dom_call.D},{dom_call.H},{dom_call.W}], {len(members)} calls, "
+                          f"{dom_c.launches} launch(es) each)",
+                "share_of_chain": round(sum(m[2] for m in members) / ms_step, 3),
                 "peak_source": pk["source"] + " burst bf16",
-                "algorithmic_bytes": dom_call.bytes()}
+                "algorithmic_flop": dom_call.flops, "algorithmic_bytes": dom_call.bytes()}
 
-    # e2e: pinned host inputs -> device, the chain through the C ABI, outputs -> pinned
-    # host, every step.  The calls are independent, so the copies run on their own
-    # streams: call i's input copy overlaps call i-1's convolution and call i-2's
-    # output copy (events order each call's copy-in, convolution and copy-out, and a
-    # buffer is rewritten only after the previous step is done with it).
-    outs_host = [torch.empty(c.y.shape, dtype=torch.bfloat16).pin_memory() for _, _, c in calls]
-    h2d = sum(h.numel() * 2 for h in host)
-    d2h = sum(o.numel() * 2 for o in outs_host)
-    e2e_steps = max(1, min(args.steps, 10))
-    # one copy stream per direction (splitting a copy over several streams measured
-    # slower: concurrent copies in one direction contend)
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    n = len(calls)
-    ev_in = [torch.cuda.Event() for _ in range(n)]
-    ev_conv = [torch.cuda.Event() for _ in range(n)]
-    ev_out = [torch.cuda.Event() for _ in range(n)]
-    def e2e_steps_run(count):
-        for step in range(count):
-            for i, ((call, lay, c), h, o) in enumerate(zip(calls, host, outs_host)):
-                if step:
-                    s_in.wait_event(ev_conv[i])    # the previous step has read c.x
-                with torch.cuda.stream(s_in):
-                    c.x.copy_(h, non_blocking=True)
-                ev_in[i].record(s_in)
-                stream.wait_event(ev_in[i])
-                if step:
-                    stream.wait_event(ev_out[i])   # the previous step's c.y has been copied out
-                rc = c.run(stream)
-                if rc != 0:
-                    raise RuntimeError(f"conv3d_fwd failed: {rc}")
-                ev_conv[i].record(stream)
-                s_out.wait_event(ev_conv[i])
-                with torch.cuda.stream(s_out):
-                    o.copy_(c.y, non_blocking=True)
-                ev_out[i].record(s_out)
-        for i in range(n):
-            stream.wait_event(ev_out[i])
+    # e2e: the chain's input from pinned host memory and its output back, every step
+    out_host = torch.empty(calls[-1][1].y.shape, dtype=torch.bfloat16).pin_memory()
+    x0 = calls[0][1].x
+    y_last = calls[-1][1].y
+    h2d = host_in.numel() * 2
+    d2h = out_host.numel() * 2
 
-    # untimed warm-up passes (first use of the copy streams and pinned buffers)
-    e2e_steps_run(max(1, min(args.warmup, 3)))
+    def e2e_step():
+        x0.copy_(host_in, non_blocking=True)
+        chain()
+        out_host.copy_(y_last, non_blocking=True)
+
+    for _ in range(max(2, min(args.warmup, 3))):
+        e2e_step()
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, args.steps)
     e0.record(stream)
-    s_in.wait_event(e0)
-    s_out.wait_event(e0)
-    e2e_steps_run(e2e_steps)
+    for _ in range(e2e_steps):
+        e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, world)
     e2e_val = world * total_flop / (e2e_ms * 1e-3) / 1e12
 
-    line = {"metric": "bf16 conv3d TFLOP/s (chain)", "value": round(value, 2),
+    # per-layer rows of the other workloads (each call alone, L2 flushed)
+    other, wan = ([], None)
+    if not args.ladder_only:
+        other, wan = other_layers(dev, stream, flush, pk, reps=max(3, min(args.steps, 10)))
+    layers += other
+    wide = [r for r in layers if r["cin"] >= 128 and r["cout"] >= 128 and
+            r["kernel"] == [3, 3, 3] and r["layout"] == "NDHWC"]
+    narrow = [r for r in layers if (min(r["cin"], r["cout"]) <= 16) and r["layout"] == "NDHWC"]
+    targets = {
+        "wide_3x3x3_ge128_ndhwc": {"calls": len(wide),
+                                   "at_or_above_0.60": sum(r["frac_bf16"] >= 0.6 for r in wide),
+                                   "min_frac_bf16": min((r["frac_bf16"] for r in wide),
+                                                        default=None)},
+        "narrow_ndhwc": {"calls": len(narrow),
+                         "at_or_above_0.70_hbm": sum(r["frac_hbm"] >= 0.7 for r in narrow),
+                         "min_frac_hbm": min((r["frac_hbm"] for r in narrow), default=None)},
+        "ladder_staging_launches": staging_launches,
+    }
+
+    line = {"metric": METRIC, "value": round(value, 2),
             "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(args, {"parallelism": f"replicas x{world}"}),
+            "config": workload_config(world),
             "roofline": roofline, "clocks": clocks,
             "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": launches_per_step * args.steps,
+            "targets": targets, "wan_chain": wan,
             "layers": layers, "wall_s": round(wall, 3)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        r, cores, desc = oracle_rate(target_s=12.0)
-        line["cpu_baseline"] = {"value": r, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                                "sample": desc}
+        r, ms, threads, desc = oracle_ladder_rate(target_s=12.0)
+        line["cpu_baseline"] = dict({"value": r, "unit": "TFLOP/s", "cores": threads,
+                                     "kind": "oracle", "sample": desc,
+                                     "ms_per_step_extrapolated": ms}, **cpu_info(threads))
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -580,7 +715,7 @@ def run_group_norm(args):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--workload", default="wan")
+    ap.add_argument("--workload", default="ladder")
     ap.add_argument("--case", default=None, help="time one call of --workload alone")
     ap.add_argument("--layout", default="ndhwc", choices=["ndhwc", "ncdhw"])
     ap.add_argument("--tune", default="", help="plan overrides, e.g. R=2,kc=32")
@@ -589,6 +724,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ladder-only", action="store_true",
+                    help="time the ladder chain only (no per-layer rows of the other workloads)")
     ap.add_argument("--pad-cache", type=int, default=-1,
                     help="with --case: padded output + cache, this many history frames")
     ap.add_argument("--norm-pad", default="",

@@ -210,15 +210,21 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning,
  * For callers that cannot allocate device memory when they run a convolution
  * (they only hold buffers handed to them, or allocation is forbidden in their
  * latency-critical or timed region): the scratch conv3d_fwd would take from
- * p->workspace (input staging copy, split-reduction partial sums) comes from a
- * static device array of 16 MiB that the library module holds on every GPU it
- * is loaded on, until the process exits.  p->workspace is ignored; inputs and
- * outputs are the caller's as for conv3d_fwd.
- *  - Calls whose conv3d_workspace_bytes() exceeds 16 MiB return
- *    CONV3D_ERR_SCRATCH_LIMIT and launch nothing.
+ * p->workspace (the channels-last staging copy of the input, the gathered taps
+ * and repacked weights of a narrow input, split-reduction partial sums, the
+ * fused norm's bf16 value rows, and the contiguous activations that the padded
+ * output + cache places) comes from a static device array of 16 MiB that the
+ * library module holds on every GPU it is loaded on, until the process exits.
+ * p->workspace is ignored; inputs and outputs are the caller's as for conv3d_fwd.
+ *  - A fused-norm call whose channel-major value rows do not fit runs on the
+ *    pixel-major kernel, which needs none of them.  Other calls whose
+ *    conv3d_workspace_bytes() exceeds 16 MiB return CONV3D_ERR_SCRATCH_LIMIT and
+ *    launch nothing.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture on the device.
+ *    before any stream capture on the device.  The address is kept per device
+ *    together with the CUDA context it was found in, and looked up again (also a
+ *    first call, in this sense) when a device reset has replaced the context.
  *  - All calls share the one array per device and it keeps the last call's
  *    contents; every byte a call reads is written earlier in the same call, so
  *    nothing needs clearing.  Calls that can run at the same time on the GPU

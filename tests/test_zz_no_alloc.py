@@ -37,7 +37,7 @@ def _within_tolerance(a_bits, b_bits):
     return bool(np.all(np.abs(a - b) <= 2.0 ** -7 * np.abs(b) + 1e-3))
 
 
-def _prepare(call, layout, seed_shift):
+def _prepare(call, layout, seed_shift, extra_epi=0, tuning=None, **kw):
     c = call
     inp = wl.make_inputs("test", wl.ConvCall(c.name, c.N, c.Cin, c.D, c.H, c.W, c.Cout,
                                              kernel=c.kernel, stride=c.stride, pads=c.pads,
@@ -46,9 +46,12 @@ def _prepare(call, layout, seed_shift):
     dev = torch.device("cuda")
     g = lambda k: None if inp[k] is None else inp[k].to(dev)
     wp = vvc.pack_weight(inp["w"].to(dev))
-    return vvc.Conv3d(inp["x"].to(dev), wp, call.Cout, call.kernel, call.stride, call.pads,
-                      layout, layout, call.epi, bias=g("bias"), residual=g("residual"),
-                      residual_bias=g("residual_bias"), gamma=g("gamma"))
+    conv = vvc.Conv3d(inp["x"].to(dev), wp, call.Cout, call.kernel, call.stride, call.pads,
+                      layout, layout, call.epi | extra_epi, bias=g("bias"),
+                      residual=g("residual"), residual_bias=g("residual_bias"),
+                      gamma=g("gamma"), tuning=tuning, **kw)
+    conv.inputs = inp
+    return conv
 
 
 def _static_call(conv: vvc.Conv3d) -> int:
@@ -101,3 +104,60 @@ def test_static_scratch_rejects_oversize():
     assert b"16 MiB" in vvc._lib().conv3d_status_string(rc)
     torch.cuda.synchronize()
     assert bool(torch.all(c.y == 1.0))
+
+
+def test_static_scratch_norm_falls_back_to_pixel_major():
+    """A fused-norm call whose channel-major value rows (152 CTAs x 256 pixels x 256
+    channels of bf16 = 19.9 MB) do not fit the 16 MiB array runs on the pixel-major
+    kernel, which needs no scratch: same output as conv3d_fwd_ex with kernel = 1,
+    bit for bit, and the oracle epilogue on its own B(conv) within 3 bf16 ulp."""
+    call = wl.ConvCall("noalloc_norm_fallback", 1, 32, 4, 40, 256, 256, pads=((1, 1, Z),) * 3,
+                       epi=wl.EPI_BIAS | wl.EPI_L2NORM_SILU, index=43)
+    c0 = _prepare(call, wl.NDHWC, 0)
+    assert c0.plan.kernel == 2 and c0.workspace_bytes > (16 << 20)
+    pm = _prepare(call, wl.NDHWC, 0, extra_epi=vvc.EPI_DEBUG_STORE_CONV,
+                  tuning=vvc.Tuning(kernel=1))
+    assert pm.workspace_bytes == 0
+    for _ in range(2):  # two calls in a row
+        pm()
+        torch.cuda.synchronize()
+        ref = _bits(pm.y)
+        conv_ref = _bits(pm.conv_out)
+        pm.y.fill_(float("nan"))
+        pm.conv_out.fill_(float("nan"))
+        rc = _static_call(pm)
+        assert rc == vvc.OK, vvc._lib().conv3d_status_string(rc)
+        torch.cuda.synchronize()
+        assert vvc.device_status() == 0
+        got = _bits(pm.y)
+        assert np.array_equal(got, ref)
+        assert np.array_equal(_bits(pm.conv_out), conv_ref)
+    inp = pm.inputs
+    e = oracle.epilogue(_bits(pm.conv_out), oracle.BIAS | oracle.L2NORM_SILU,
+                        inp["bias"].numpy(), None, None, inp["gamma"].numpy())
+    ordinal = lambda u: np.where(u & 0x8000, -(u.astype(np.int32) & 0x7FFF),
+                                 u.astype(np.int32) & 0x7FFF)
+    assert np.abs(ordinal(got) - ordinal(e["act"])).max() <= 3
+
+
+def test_static_scratch_pad_cache():
+    """Padded output + cache: the contiguous activations that the last launch places
+    live in the static array.  Same padded output and cache as conv3d_fwd."""
+    call = wl.ConvCall("noalloc_pad_cache", 1, 16, 4, 8, 16, 32, pads=((1, 1, Z),) * 3,
+                       epi=wl.EPI_BIAS | wl.EPI_L2NORM_SILU, index=44)
+    for shift in (0, 100):
+        c = _prepare(call, wl.NDHWC, shift, extra_epi=vvc.EPI_PAD_CACHE, history_frames=1)
+        assert 0 < c.workspace_bytes <= (16 << 20)
+        c.y.fill_(3.0)
+        c.cache_out.fill_(3.0)
+        c()
+        torch.cuda.synchronize()
+        ref_y, ref_c = _bits(c.y), _bits(c.cache_out)
+        c.y.fill_(3.0)
+        c.cache_out.fill_(3.0)
+        rc = _static_call(c)
+        assert rc == vvc.OK, vvc._lib().conv3d_status_string(rc)
+        torch.cuda.synchronize()
+        assert vvc.device_status() == 0
+        assert np.array_equal(_bits(c.y), ref_y)
+        assert np.array_equal(_bits(c.cache_out), ref_c)

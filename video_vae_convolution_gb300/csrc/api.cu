@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "conv3d.h"
 #include "internal.h"
@@ -49,18 +50,22 @@ constexpr int kDefaultSMs = 152;  // GB300
 // Per-warp epilogue staging block of the channel-major kernel (kStageFloats fp32).
 constexpr size_t kEpiWarpBytes = 32 * 36 * 4;
 
+// SM count of the current device (cached per device; 152 when there is none).
 int num_sms() {
-  static int cached = 0;
-  if (cached) return cached;
+  static int cached[vvc::kMaxDevices] = {};
   int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) == cudaSuccess &&
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) {
-    cached = n;
-  } else {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= vvc::kMaxDevices) {
     (void)cudaGetLastError();
-    cached = kDefaultSMs;
+    return kDefaultSMs;
   }
-  return cached;
+  const int c = __atomic_load_n(&cached[dev], __ATOMIC_RELAXED);
+  if (c) return c;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    n = kDefaultSMs;
+  }
+  __atomic_store_n(&cached[dev], n, __ATOMIC_RELAXED);
+  return n;
 }
 
 inline long long round_up(long long a, long long b) { return (a + b - 1) / b * b; }
@@ -1391,31 +1396,68 @@ extern "C" size_t conv3d_struct_size(int which) {
 // framework, allocators that forbid allocation inside a timed or latency-critical
 // region, or embedders whose memory is fully reserved up front.  For them the
 // scratch that conv3d_fwd takes from the caller's workspace (the channels-last
-// staging copy of the input and the split-reduction partial sums) lives instead
-// in one file-scope device array that the CUDA module holds from load until exit.
+// staging copy of the input, the gathered taps and repacked weights of a narrow
+// input, the split-reduction partial sums, the fused norm's value rows and the
+// contiguous activations of the padded output + cache) lives instead in one
+// file-scope device array that the CUDA module holds from load until exit.
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB per device
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-// Device address of g_static_scratch, resolved once per device.  In host code the
-// array's name is only a host-side stand-in, so the address must come from
-// cudaGetSymbolAddress with that device current.
-constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+// Device address of g_static_scratch, resolved once per device and context.  In
+// host code the array's name is only a host-side stand-in, so the address must
+// come from cudaGetSymbolAddress with that device current.  A device reset
+// destroys the context and may reload the module elsewhere, so each cached
+// address is kept with the context it was resolved in and looked up again when
+// the current context differs.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(ptr);
+  }
+  return fn;
+}
+
+struct ScratchSlot {
+  CUcontext ctx;
+  void* ptr;
+};
+ScratchSlot g_scratch_slot[vvc::kMaxDevices] = {};
+std::mutex g_scratch_mu;
 
 int static_scratch_for_current_device(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= vvc::kMaxDevices)
     return CONV3D_ERR_CUDA;
-  void* ptr = __atomic_load_n(&g_scratch_addr[dev], __ATOMIC_ACQUIRE);
-  if (!ptr) {
+  CtxGetCurrentFn get = ctx_get_current_fn();
+  CUcontext ctx = nullptr;
+  if (!get || get(&ctx) != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
+  if (!ctx) {
+    // the runtime has not made this thread's context current yet; the symbol
+    // lookup does (it initialises the device's primary context)
+    void* tmp = nullptr;
+    if (cudaGetSymbolAddress(&tmp, g_static_scratch) != cudaSuccess) return CONV3D_ERR_CUDA;
+    if (get(&ctx) != CUDA_SUCCESS || !ctx) return CONV3D_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  ScratchSlot& slot = g_scratch_slot[dev];
+  if (slot.ptr == nullptr || slot.ctx != ctx) {
+    void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr)
       return CONV3D_ERR_CUDA;
-    __atomic_store_n(&g_scratch_addr[dev], ptr, __ATOMIC_RELEASE);
+    slot.ctx = ctx;
+    slot.ptr = ptr;
   }
-  *out = ptr;
+  *out = slot.ptr;
   return CONV3D_OK;
 }
 
@@ -1444,8 +1486,9 @@ extern "C" int conv3d_fwd_static_scratch(const conv3d_params* p, conv3d_stream_t
     q.workspace = scratch;
     q.workspace_bytes = kStaticScratchBytes;
   }
-  // Nothing in the scratch needs to start at zero: the staging copy, every
-  // partial sum and the fused-norm value rows are written before they are read
-  // within the same call.
+  // Nothing in the scratch needs to start at zero: the staging copy, the gathered
+  // taps and repacked weights, every partial sum, the fused-norm value rows and
+  // the padded-output activations are written before they are read within the
+  // same call.
   return conv3d_fwd_ex(&q, tp, stream);
 }

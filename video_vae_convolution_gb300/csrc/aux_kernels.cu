@@ -629,12 +629,10 @@ cudaError_t launch_norm_rows(const void* x, long long rows, const EpiParams& e, 
   while (R > 1 && norm_rows_smem(e.Cout, R) == 0) R /= 2;
   const size_t smem = norm_rows_smem(e.Cout, R);
   if (smem == 0) return cudaErrorInvalidValue;
-  static size_t configured = 48 * 1024;
-  if (smem > configured) {
-    const cudaError_t err = cudaFuncSetAttribute(
-        l2norm_silu_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static int opted_in[kMaxDevices] = {};
+  if (smem > 48 * 1024) {
+    const cudaError_t err = opt_in_smem(l2norm_silu_rows_kernel, opted_in);
     if (err != cudaSuccess) return err;
-    configured = smem;
   }
   const long long blocks = (rows + R - 1) / R;
   l2norm_silu_rows_kernel<<<static_cast<unsigned>(blocks), 256, smem, s>>>(

@@ -868,14 +868,9 @@ cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
                              conv_cm_kernel<true, false, false>,
                              conv_cm_kernel<false, true, false>,
                              conv_cm_kernel<false, false, true>};
-  static size_t configured[4] = {0, 0, 0, 0};
-  if (smem_bytes > configured[which]) {
-    cudaError_t err = cudaFuncSetAttribute(kernels[which],
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem_bytes));
-    if (err != cudaSuccess) return err;
-    configured[which] = smem_bytes;
-  }
+  static int opted_in[4][kMaxDevices] = {};
+  cudaError_t err = opt_in_smem(kernels[which], opted_in[which]);
+  if (err != cudaSuccess) return err;
   kernels[which]<<<grid, 128 + 128 * p.epi_groups, smem_bytes, stream>>>(tmAct, tmWgt, tmWgtLast,
                                                                          om, half, p);
   return cudaGetLastError();

@@ -350,14 +350,9 @@ __global__ void __launch_bounds__(256, 1)
 
 cudaError_t launch_conv_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const ConvTCParams& p,
                            dim3 grid, size_t smem_bytes, cudaStream_t stream) {
-  static size_t configured = 0;
-  if (smem_bytes > configured) {
-    cudaError_t err = cudaFuncSetAttribute(conv_tc_kernel,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem_bytes));
-    if (err != cudaSuccess) return err;
-    configured = smem_bytes;
-  }
+  static int opted_in[kMaxDevices] = {};
+  cudaError_t err = opt_in_smem(conv_tc_kernel, opted_in);
+  if (err != cudaSuccess) return err;
   conv_tc_kernel<<<grid, 256, smem_bytes, stream>>>(tmA, tmB, p);
   return cudaGetLastError();
 }

@@ -2,9 +2,33 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <cstdint>
 
 namespace vvc {
+
+// Largest device ordinal the per-device host caches hold.
+constexpr int kMaxDevices = 64;
+
+// Opts a kernel in to the device's full dynamic shared memory, once per device
+// (the attribute belongs to the function on the current device).  `done` is the
+// kernel's own per-device flag table; concurrent first calls both set the same
+// value, which is harmless.
+template <class Kernel>
+inline cudaError_t opt_in_smem(Kernel kernel, int (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (__atomic_load_n(&done[dev], __ATOMIC_ACQUIRE)) return cudaSuccess;
+  int max_optin = 0;
+  err = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
+  if (err != cudaSuccess) return err;
+  __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
+  return cudaSuccess;
+}
 
 enum : unsigned {
   EPI_BIAS = 1u,
