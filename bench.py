@@ -219,6 +219,10 @@ def workload_config(world=1, extra=None):
                        "1024->1024 x3 @[5,16,16]; conv_out 1024->48; 3x3x3, causal T pad "
                        "(2,0) zero + reflect H,W (1,1); NDHWC in and out",
            "calls_per_step": 30, "layout": "NDHWC",
+           "intermediates": "each call but the last writes its output inside a haloed tensor "
+                            "(2 zero frames before it, a 1-pixel reflect border around it: the "
+                            "next call's padding) and the next call reads it as a valid "
+                            "convolution; conv_in pads the model input itself",
            "l2": "flushed between steps (256 MiB write, untimed); inside a step each call "
                  "reads the previous call's output",
            "inputs": "seeded synthetic: x N(0,1) bf16, weights N(0,1/sqrt(fan_in)) bf16",
@@ -405,18 +409,23 @@ def other_layers(dev, stream, flush, pk, reps):
     return rows, wan
 
 
-def run_gpu(args, rank, world):
-    import video_vae_convolution_gb300 as vvc
+LADDER_HALO = ((2, 0, wl.ZERO), (1, 1, wl.REFLECT), (1, 1, wl.REFLECT))
+VALID = ((0, 0, wl.ZERO),) * 3
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
-    torch.cuda.set_device(dev)
-    stream = torch.cuda.current_stream()
-    pk = peaks()
-    # the ladder: seeded inputs (CPU recipe), each call reading the previous output
+
+def build_ladder(dev, halo):
+    """The 30 ladder calls on the device, each reading the previous call's output.
+    halo: every call but the last writes its output inside a haloed tensor (two
+    zero frames before it, the reflect border around it) and every call but the
+    first reads the previous haloed tensor as a valid convolution; otherwise each
+    call applies its own causal + reflect padding.  Returns (calls, pinned host
+    copy of the chain's input)."""
+    import video_vae_convolution_gb300 as vvc
     calls = []
     x = None
     host_in = None
-    for call in wl.ladder().calls:
+    ladder = wl.ladder().calls
+    for i, call in enumerate(ladder):
         if x is None:
             inp = wl.make_inputs("ladder", call, wl.NDHWC, wl.NDHWC)
             host_in = inp["x"].pin_memory()
@@ -424,16 +433,20 @@ def run_gpu(args, rank, world):
         else:
             inp = {"w": wl.make_inputs("ladder", call, wl.NDHWC, wl.NDHWC, crop=(1, 3, 3))["w"]}
         wp = vvc.pack_weight(inp["w"].to(dev))
-        c = vvc.Conv3d(x, wp, call.Cout, call.kernel, call.stride, call.pads, wl.NDHWC,
-                       wl.NDHWC, call.epi)
+        last = i == len(ladder) - 1
+        pads = call.pads if (i == 0 or not halo) else VALID
+        kw = {"out_halo": LADDER_HALO} if (halo and not last) else {}
+        c = vvc.Conv3d(x, wp, call.Cout, call.kernel, call.stride, pads, wl.NDHWC, wl.NDHWC,
+                       call.epi, **kw)
         calls.append((call, c))
         x = c.y
-    torch.cuda.synchronize()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    total_flop = sum(call.flops for call, _ in calls)
-    launches_per_step = sum(c.launches for _, c in calls)
-    # launches besides the convolution and its split reduction (input staging)
-    staging_launches = sum(c.launches - 1 - (1 if c.plan.k_splits > 1 else 0) for _, c in calls)
+    return calls, host_in
+
+
+def time_chain(calls, stream, flush, steps, warmup, world, sampler=None):
+    """Times `steps` passes of the chain (L2 flushed before each); returns (mean step
+    ms over the steps, per-call median ms, wall seconds)."""
+    import video_vae_convolution_gb300 as vvc
 
     def chain(evs=None):
         for i, (_, c) in enumerate(calls):
@@ -445,20 +458,18 @@ def run_gpu(args, rank, world):
         if evs is not None:
             evs[-1].record(stream)
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, warmup)):
         flush.zero_()
         chain()
     torch.cuda.synchronize()
     assert vvc.device_status() == 0
-
-    sampler = ClockSampler(dev.index)
-    sampler.start()
     barrier(world)
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
-    sampler.begin()
+    if sampler is not None:
+        sampler.begin()
     step_ev = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         flush.zero_()
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
         chain(evs)
@@ -466,8 +477,8 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - t_wall
-    sampler.end()
-    clocks = sampler.stop()
+    if sampler is not None:
+        sampler.end()
     status = vvc.device_status()
     if status != 0:
         raise RuntimeError(f"device status {status}")
@@ -477,16 +488,35 @@ def run_gpu(args, rank, world):
         step_ms.append(evs[0].elapsed_time(evs[-1]))
         for i in range(len(calls)):
             per_call[i].append(evs[i].elapsed_time(evs[i + 1]))
-    ms_step = statistics.mean(step_ms)
+    return statistics.mean(step_ms), [statistics.median(t) for t in per_call], wall, chain
+
+
+def run_gpu(args, rank, world):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    pk = peaks()
+    calls, host_in = build_ladder(dev, halo=True)
+    torch.cuda.synchronize()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    total_flop = sum(call.flops for call, _ in calls)
+    launches_per_step = sum(c.launches for _, c in calls)
+    # launches besides the convolution and its split reduction (input staging)
+    staging_launches = sum(c.launches - 1 - (1 if c.plan.k_splits > 1 else 0) for _, c in calls)
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    ms_step, call_ms, wall, chain = time_chain(calls, stream, flush, args.steps, args.warmup,
+                                               world, sampler)
+    clocks = sampler.stop()
     ms_step = max_over_ranks(ms_step, world)
     value = world * total_flop / (ms_step * 1e-3) / 1e12
 
     layers = []
     class_ms = {}
-    for (call, c), ts in zip(calls, per_call):
-        ms = statistics.median(ts)
+    for (call, c), ms in zip(calls, call_ms):
         layers.append(layer_row(call, ms, pk, c.launches, wl.NDHWC, "ladder",
-                                {"timed": "inside the chain"}))
+                                {"timed": "inside the chain, haloed intermediates"}))
         class_ms.setdefault(call_class(call.name), []).append((call, c, ms))
     # dominant kernel: the layer class with the largest share of the chain's time
     dom_cls, members = max(class_ms.items(), key=lambda kv: sum(m[2] for m in kv[1]))
@@ -532,19 +562,37 @@ def run_gpu(args, rank, world):
     e2e_ms = max_over_ranks(e2e_ms, world)
     e2e_val = world * total_flop / (e2e_ms * 1e-3) / 1e12
 
+    # the same ladder with every call applying its own padding (no haloed tensors)
+    plain_calls, _ = build_ladder(dev, halo=False)
+    plain_ms, plain_call_ms, _, _ = time_chain(plain_calls, stream, flush, args.steps,
+                                               args.warmup, world)
+    for (call, c), ms in zip(plain_calls, plain_call_ms):
+        layers.append(layer_row(call, ms, pk, c.launches, wl.NDHWC, "ladder_per_call_padding",
+                                {"timed": "inside the chain, each call pads its own input"}))
+    ladder_plain = {"ms_per_step": round(plain_ms, 4),
+                    "tflops": round(total_flop / (plain_ms * 1e-3) / 1e12, 2),
+                    "launches_per_step": sum(c.launches for _, c in plain_calls)}
+    del plain_calls
+    torch.cuda.empty_cache()
+
     # per-layer rows of the other workloads (each call alone, L2 flushed)
     other, wan = ([], None)
     if not args.ladder_only:
         other, wan = other_layers(dev, stream, flush, pk, reps=max(3, min(args.steps, 10)))
     layers += other
+    def wide_stats(rows):
+        return {"calls": len(rows), "at_or_above_0.60": sum(r["frac_bf16"] >= 0.6 for r in rows),
+                "min_frac_bf16": min((r["frac_bf16"] for r in rows), default=None)}
+
     wide = [r for r in layers if r["cin"] >= 128 and r["cout"] >= 128 and
             r["kernel"] == [3, 3, 3] and r["layout"] == "NDHWC"]
-    narrow = [r for r in layers if (min(r["cin"], r["cout"]) <= 16) and r["layout"] == "NDHWC"]
+    narrow = [r for r in layers if (min(r["cin"], r["cout"]) <= 16) and r["layout"] == "NDHWC" and
+              r["workload"] != "ladder_per_call_padding"]
     targets = {
-        "wide_3x3x3_ge128_ndhwc": {"calls": len(wide),
-                                   "at_or_above_0.60": sum(r["frac_bf16"] >= 0.6 for r in wide),
-                                   "min_frac_bf16": min((r["frac_bf16"] for r in wide),
-                                                        default=None)},
+        "wide_3x3x3_ge128_ndhwc": wide_stats(
+            [r for r in wide if r["workload"] != "ladder_per_call_padding"]),
+        "wide_3x3x3_ge128_ndhwc_ladder_per_call_padding": wide_stats(
+            [r for r in wide if r["workload"] == "ladder_per_call_padding"]),
         "narrow_ndhwc": {"calls": len(narrow),
                          "at_or_above_0.70_hbm": sum(r["frac_hbm"] >= 0.7 for r in narrow),
                          "min_frac_hbm": min((r["frac_hbm"] for r in narrow), default=None)},
@@ -560,7 +608,7 @@ def run_gpu(args, rank, world):
             "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": launches_per_step * args.steps,
-            "targets": targets, "wan_chain": wan,
+            "targets": targets, "wan_chain": wan, "ladder_per_call_padding": ladder_plain,
             "layers": layers, "wall_s": round(wall, 3)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r, ms, threads, desc = oracle_ladder_rate(target_s=12.0)

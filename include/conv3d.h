@@ -127,7 +127,22 @@ enum {
  *  cache_out  bf16 NDHWC [N, min(2, Do + history_frames), Ho, Wo, Cout] (with
  *             CONV3D_EPI_PAD_CACHE, else ignored).
  *  history_frames   0, 1 or 2 activated frames the caller keeps in planes
- *             2 - history_frames .. 1 of y (with CONV3D_EPI_PAD_CACHE, else ignored). */
+ *             2 - history_frames .. 1 of y (with CONV3D_EPI_PAD_CACHE, else ignored).
+ *  out_halo   (T, H, W) halo around the output inside y, so that the next call of a
+ *             chain can read y as an already padded input and run a valid
+ *             convolution (ROCm/FlyDSL issue "[Feature]: conv3d_implicit — ...",
+ *             MiniMax-H3 comment: the causal temporal zero pad and the reflect
+ *             spatial pad of every encoder convolution).  All zero: no halo, y is
+ *             the plain output.  Otherwise y is NDHWC [N, Do + tb + ta, Ho + hb + ha,
+ *             Wo + wb + wa, Cout] (tb = out_halo[0].before, ...), the output at
+ *             offset (tb, hb, wb).  The T halo frames are never written (the caller
+ *             keeps them, e.g. zeroed once for a causal chain); out_halo[0].mode must
+ *             be CONV3D_PAD_ZERO.  H and W halos are at most 1 on a side and are
+ *             written by every call: CONV3D_PAD_REFLECT fills them as PyTorch
+ *             'reflect' padding of the output would (needs Ho, Wo >= 2),
+ *             CONV3D_PAD_ZERO with zeros.  Requires NDHWC output, Cout % 8 == 0,
+ *             and none of L2NORM_SILU, OUT_PAD_BR, PAD_CACHE.  residual, value_out
+ *             and conv_out keep the unpadded output shape. */
 typedef struct {
   const void* x;
   int32_t layout;
@@ -149,6 +164,7 @@ typedef struct {
   size_t workspace_bytes;
   void* cache_out;
   int32_t history_frames;
+  conv3d_pad out_halo[3];
 } conv3d_params;
 
 /* Optional plan overrides (tests and tuning).  0 (or -1 where noted) = automatic. */
@@ -315,7 +331,7 @@ const char* conv3d_status_string(int status);
 
 /* Library ABI version (major * 100 + minor).  2.00: conv3d_params gained cache_out and
  * history_frames, conv3d_tuning gained pair; conv3d_plan, l2norm_silu_pad and the GroupNorm
- * calls were added. */
+ * calls were added.  3.00: conv3d_params gained out_halo. */
 int conv3d_version(void);
 
 /* sizeof() of the ABI structs, for bindings to check their mirrors:

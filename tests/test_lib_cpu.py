@@ -277,3 +277,47 @@ def test_ndhwc_calls_plan_no_transpose():
             expected = 1 + (info.k_splits > 1) + info.im2col
             assert info.launches == expected, (call.name, info.launches, expected)
             assert info.im2col == (call.Cin < 8), call.name
+
+
+def _halo(p, halo):
+    for i, (b, a, m) in enumerate(halo):
+        p.out_halo[i].before, p.out_halo[i].after, p.out_halo[i].mode = b, a, m
+    return p
+
+
+def test_output_halo_validation():
+    R, Z = vvc.PAD_REFLECT, vvc.PAD_ZERO
+    ok = ((2, 0, Z), (1, 1, R), (1, 1, R))
+    info = vvc.PlanInfo()
+    assert vvc._lib().conv3d_plan(ctypes.byref(_halo(_params(), ok)), None,
+                                  ctypes.byref(info)) == vvc.OK
+    bad = [
+        dict(halo=((1, 0, R), (1, 1, R), (1, 1, R))),      # the T halo is never written
+        dict(halo=((0, 0, Z), (2, 1, R), (1, 1, R))),      # at most one pixel a side
+        dict(halo=((0, 0, Z), (1, 1, 5), (1, 1, R))),      # unknown mode
+        dict(halo=ok, out_layout=vvc.NCDHW),               # NDHWC only
+        dict(halo=ok, Cout=36),                            # 16-byte channel rows
+        dict(halo=ok, epi=vvc.EPI_L2NORM_SILU, gamma=0x300000),
+        dict(halo=ok, epi=vvc.EPI_OUT_PAD_BR | vvc.EPI_RESIDUAL, residual=0x300000),
+        dict(halo=ok, H=2, KR=3, pad_h=0),                 # reflection needs Ho >= 2
+    ]
+    for case in bad:
+        halo = case.pop("halo")
+        pad_h = case.pop("pad_h", None)
+        p = _params(**case)
+        if pad_h is not None:
+            p.pad[1].before = p.pad[1].after = pad_h
+        assert fwd(_halo(p, halo)) == vvc.ERR_INVALID_ARG, case
+
+
+def test_output_halo_overlap_counts_the_whole_tensor():
+    # y [1, 6, 14, 14, 32] with the halo: a workspace or value_out that starts inside
+    # it must be rejected, although it would lie past an unpadded output
+    R, Z = vvc.PAD_REFLECT, vvc.PAD_ZERO
+    p = _halo(_params(epi=vvc.EPI_SAVE_VALUE), ((2, 0, Z), (1, 1, R), (1, 1, R)))
+    plain_bytes = 1 * 4 * 12 * 12 * 32 * 2
+    p.value_out = p.y + plain_bytes + 1024  # past the plain output, inside the haloed y
+    ws = ctypes.c_size_t(0)
+    assert vvc._lib().conv3d_workspace_bytes(ctypes.byref(p), ctypes.byref(ws)) == vvc.OK
+    p.workspace, p.workspace_bytes = 0x40000000, ws.value
+    assert fwd(p) == vvc.ERR_OVERLAP

@@ -42,7 +42,7 @@ ERR_DEVICE_TIMEOUT = -7
 ERR_SCRATCH_LIMIT = -8
 
 # ABI version of the C library this binding mirrors (major * 100 + minor).
-ABI_VERSION = 200
+ABI_VERSION = 300
 
 # Every function the C header declares (checked by the tests against include/conv3d.h).
 EXPORTS = (
@@ -81,6 +81,7 @@ class Params(ctypes.Structure):
         ("value_out", ctypes.c_void_p), ("conv_out", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("cache_out", ctypes.c_void_p), ("history_frames", ctypes.c_int32),
+        ("out_halo", Pad * 3),
     ]
 
 
@@ -240,7 +241,7 @@ class Conv3d:
                  pads=((0, 0, PAD_ZERO),) * 3, layout=NDHWC, out_layout=NDHWC, epi=0,
                  bias=None, residual=None, residual_bias=None, gamma=None, y=None,
                  value_out=None, conv_out=None, workspace=None, tuning: Optional[Tuning] = None,
-                 cache_out=None, history_frames=0):
+                 cache_out=None, history_frames=0, out_halo=None):
         N, C, D, H, W = _dims(x, layout)
         KT, KR, KS = kernel
         Do, Ho, Wo = out_dims(D, H, W, kernel, stride, pads)
@@ -251,6 +252,11 @@ class Conv3d:
         if y is None and epi & EPI_PAD_CACHE:
             # padded output: two leading planes and a one-pixel spatial border
             y = torch.empty((N, Do + 2, Ho + 2, Wo + 2, Cout), dtype=torch.bfloat16, device=dev)
+        if out_halo is not None and y is None:
+            # haloed NDHWC output; zeros, so that the unwritten T halo frames read 0
+            (tb, ta, _), (hb, ha, _), (wb, wa, _) = out_halo
+            y = torch.zeros((N, Do + tb + ta, Ho + hb + ha, Wo + wb + wa, Cout),
+                            dtype=torch.bfloat16, device=dev)
         if y is None:
             y = torch.empty(out_shape(N, Cout, Do, Ho, Wo, out_layout, pad_br),
                             dtype=torch.bfloat16, device=dev)
@@ -282,6 +288,10 @@ class Conv3d:
         p.conv_out = None if conv_out is None else conv_out.data_ptr()
         p.cache_out = None if cache_out is None else cache_out.data_ptr()
         p.history_frames = history_frames
+        if out_halo is not None:
+            for i in range(3):
+                p.out_halo[i].before, p.out_halo[i].after, p.out_halo[i].mode = out_halo[i]
+        self.out_halo = out_halo
         self.cache_out = cache_out
         self.tuning = tuning
         tp = ctypes.byref(tuning) if tuning is not None else None

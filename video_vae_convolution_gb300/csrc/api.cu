@@ -123,6 +123,20 @@ int out_extent(int L, int b, int a, int K, int s) {
   return static_cast<int>(num / s + 1);
 }
 
+bool has_halo(const conv3d_params* p) {
+  for (int i = 0; i < 3; ++i)
+    if (p->out_halo[i].before || p->out_halo[i].after) return true;
+  return false;
+}
+
+// Extents of y: [N, Do + tb + ta, Ho + hb + ha, Wo + wb + wa] with an output halo.
+void y_extent(const conv3d_params* p, int Do, int Ho, int Wo, long long* Dy, long long* Hy,
+              long long* Wy) {
+  *Dy = (long long)Do + p->out_halo[0].before + p->out_halo[0].after;
+  *Hy = (long long)Ho + p->out_halo[1].before + p->out_halo[1].after;
+  *Wy = (long long)Wo + p->out_halo[2].before + p->out_halo[2].after;
+}
+
 // Geometry and flag validation; no CUDA calls.
 int validate_shape(const conv3d_params* p, int* Do, int* Ho, int* Wo) {
   if (!p) return CONV3D_ERR_INVALID_ARG;
@@ -160,6 +174,21 @@ int validate_shape(const conv3d_params* p, int* Do, int* Ho, int* Wo) {
         p->out_layout != CONV3D_NDHWC || p->Cout % 8 != 0 || p->history_frames < 0 ||
         p->history_frames > 2 || !p->cache_out)
       return CONV3D_ERR_INVALID_ARG;
+  }
+  if (has_halo(p)) {
+    // output halo: NDHWC, 16-byte channel rows, unwritten zero-mode T halo, H / W
+    // halos of at most one pixel per side (reflection needs two output pixels)
+    const conv3d_pad* hl = p->out_halo;
+    if (p->out_layout != CONV3D_NDHWC || p->Cout % 8 != 0 ||
+        (e & (CONV3D_EPI_L2NORM_SILU | CONV3D_EPI_OUT_PAD_BR | CONV3D_EPI_PAD_CACHE)) ||
+        hl[0].mode != CONV3D_PAD_ZERO || hl[0].before < 0 || hl[0].after < 0)
+      return CONV3D_ERR_INVALID_ARG;
+    for (int i = 1; i < 3; ++i) {
+      if (hl[i].before < 0 || hl[i].before > 1 || hl[i].after < 0 || hl[i].after > 1 ||
+          (hl[i].mode != CONV3D_PAD_ZERO && hl[i].mode != CONV3D_PAD_REFLECT))
+        return CONV3D_ERR_INVALID_ARG;
+      if (hl[i].mode == CONV3D_PAD_REFLECT && o[i] < 2) return CONV3D_ERR_INVALID_ARG;
+    }
   }
   if ((e & CONV3D_EPI_RESIDUAL_BIAS) && !(e & CONV3D_EPI_RESIDUAL)) return CONV3D_ERR_INVALID_ARG;
   if ((e & CONV3D_EPI_OUT_PAD_BR) && (e & CONV3D_EPI_L2NORM_SILU)) return CONV3D_ERR_INVALID_ARG;
@@ -211,6 +240,17 @@ void fill_epi(const conv3d_params* p, const Plan& pl, EpiParams* e) {
   e->value_out = static_cast<uint16_t*>(p->value_out);
   e->conv_out = static_cast<uint16_t*>(p->conv_out);
   e->sqrt_c = std::sqrt(static_cast<float>(p->Cout));
+  e->halo = has_halo(p) ? 1 : 0;
+  long long Dy, Hy, Wy;
+  y_extent(p, pl.Do, pl.Ho, pl.Wo, &Dy, &Hy, &Wy);
+  e->Dy = static_cast<int>(Dy);
+  e->Hy = static_cast<int>(Hy);
+  e->Wy = static_cast<int>(Wy);
+  e->d0 = p->out_halo[0].before;
+  e->h0 = p->out_halo[1].before;
+  e->w0 = p->out_halo[2].before;
+  e->h_mode = p->out_halo[1].mode == CONV3D_PAD_REFLECT ? 2 : 1;
+  e->w_mode = p->out_halo[2].mode == CONV3D_PAD_REFLECT ? 2 : 1;
 }
 
 // Split of the reduction so that small layers still fill the GPU.  Each split
@@ -788,10 +828,12 @@ int check_pointers(const conv3d_params* p, const Plan& pl) {
     return CONV3D_ERR_WORKSPACE;
   const bool padbr = (p->epi & CONV3D_EPI_OUT_PAD_BR) != 0;
   const size_t out_elems = (size_t)p->N * p->Cout * pl.Do * pl.Ho * pl.Wo;
+  long long Dy, Hy, Wy;
+  y_extent(p, pl.Do, pl.Ho, pl.Wo, &Dy, &Hy, &Wy);
   const size_t y_elems =
       pl.pad_cache
           ? (size_t)p->N * p->Cout * (pl.Do + 2) * (pl.Ho + 2) * (pl.Wo + 2)
-          : (size_t)p->N * p->Cout * pl.Do * (pl.Ho + (padbr ? 1 : 0)) * (pl.Wo + (padbr ? 1 : 0));
+          : (size_t)p->N * p->Cout * Dy * (Hy + (padbr ? 1 : 0)) * (Wy + (padbr ? 1 : 0));
   const size_t cache_elems = pl.pad_cache ? (size_t)p->N * p->Cout * pl.Ho * pl.Wo *
                                                 std::min(2, pl.Do + p->history_frames)
                                           : 0;
@@ -966,12 +1008,29 @@ int encode_out_maps(const conv3d_params* p, const Plan& pl, vvc::CmOutMaps* om) 
                               cl ? C * 2 * Wo * Ho : Wo * Ho * Do * 2, C * 2 * Wo * Ho * Do};
   const cuuint32_t box[5] = {32, cl ? 32u : 1u, 1, cl ? 1u : 32u, 1};
   const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  auto one = [&](void* base, CUtensorMap* m) {
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, gdim, gstr, box, es,
+  auto one_g = [&](void* base, const cuuint64_t* dim, const cuuint64_t* str, CUtensorMap* m) {
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dim, str, box, es,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
-  if (!one(p->y, &om->y)) return CONV3D_ERR_CUDA;
+  auto one = [&](void* base, CUtensorMap* m) { return one_g(base, gdim, gstr, m); };
+  if (has_halo(p)) {
+    // y holds the output at an offset: om.y views the output inside it (same
+    // extents, y's strides), om.yfull the whole haloed tensor
+    long long Dy, Hy, Wy;
+    y_extent(p, pl.Do, pl.Ho, pl.Wo, &Dy, &Hy, &Wy);
+    const cuuint64_t fdim[5] = {C, (cuuint64_t)Wy, (cuuint64_t)Hy, (cuuint64_t)Dy,
+                                (cuuint64_t)p->N};
+    const cuuint64_t fstr[4] = {C * 2, C * 2 * Wy, C * 2 * Wy * Hy, C * 2 * Wy * Hy * Dy};
+    const size_t origin = (((size_t)p->out_halo[0].before * Hy + p->out_halo[1].before) * Wy +
+                           p->out_halo[2].before) * C * 2;
+    void* inner = static_cast<uint8_t*>(p->y) + origin;
+    if (!one_g(inner, gdim, fstr, &om->y) || !one_g(p->y, fdim, fstr, &om->yfull))
+      return CONV3D_ERR_CUDA;
+  } else {
+    if (!one(p->y, &om->y)) return CONV3D_ERR_CUDA;
+    om->yfull = om->y;
+  }
   om->val = om->y;
   om->conv = om->y;
   if ((p->epi & CONV3D_EPI_SAVE_VALUE) && !one(p->value_out, &om->val)) return CONV3D_ERR_CUDA;
@@ -1133,7 +1192,7 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
       rc = encode_out_maps(pm, pl, &om);
       if (rc) return rc;
     } else {
-      om.y = om.val = om.conv = tmA;  // not used
+      om.y = om.val = om.conv = om.yfull = tmA;  // not used
     }
     if (vvc::launch_conv_cm(tmA, tmB, tmBLast, om, half, kp, static_cast<int>(pl.grid.x), pl.smem,
                             s) !=
@@ -1375,7 +1434,7 @@ const char* conv3d_status_string(int status) {
   }
 }
 
-int conv3d_version(void) { return 200; }
+int conv3d_version(void) { return 300; }
 
 }  // extern "C"
 

@@ -613,6 +613,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     E.gamma = p.epi.gamma;
     E.sqrt_c = p.epi.sqrt_c;
     E.M_total = p.M_total;
+    E.halo = p.epi.halo != 0;
+    E.ep = &p.epi;
     float* st = reinterpret_cast<float*>(smem + p.epi_off) + (warp - kWarpEpi0) * kStageFloats;
     const int nbuf = p.nbuf, acc_cols = p.acc_cols, Ncols = p.N;
     auto tile_view = [&](const TileCoord& tc) {
@@ -759,12 +761,51 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               }
               fence_proxy_async_smem();
               __syncwarp();
+              // haloed y: om.y views the output inside y; the halo rows that copy
+              // this block go out through om.yfull (the whole haloed y, so every
+              // coordinate is >= 0), zero halo rows and the halo columns beside or
+              // reflecting the block's pixels through plain stores
+              int hpos[3], wpos[3];
+              bool hzero[3], wzero[3];
+              const int nh = E.halo ? halo_axis(hr, E.Ho, p.epi.h0, p.epi.Hy - E.Ho - p.epi.h0,
+                                                p.epi.h_mode, hpos, hzero)
+                                    : 1;
               if (lane == 0) {
                 tma_store_5d(&om.y, smem_u32(yt), cw, wr, hr, tc.od, tc.nb);
+                for (int a = 1; a < nh; ++a)
+                  if (!hzero[a])
+                    tma_store_5d(&om.yfull, smem_u32(yt), cw, wr + p.epi.w0, hpos[a] + p.epi.h0,
+                                 tc.od + p.epi.d0, tc.nb);
                 if (E.flags & EPI_SAVE_VALUE)
                   tma_store_5d(&om.val, smem_u32(yt), cw, wr, hr, tc.od, tc.nb);
                 if (dbg) tma_store_5d(&om.conv, smem_u32(ct), cw, wr, hr, tc.od, tc.nb);
                 bulk_commit_group();
+              }
+              if (E.halo) {
+                const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+                // zero halo rows beside this row: 32 pixels x 64 bytes, 16 bytes a lane
+                for (int a = 1; a < nh; ++a) {
+                  if (!hzero[a]) continue;
+                  for (int u = lane; u < 128; u += 32) {
+                    const int j = u >> 2, part = u & 3;
+                    *reinterpret_cast<uint4*>(
+                        E.y + halo_offset(p.epi, tc.nb, tc.od, hpos[a], wr + j, cw + 8 * part)) =
+                        zero4;
+                  }
+                }
+                // halo columns: only the pixels next to the row ends have any
+                const int part = lane & 3;
+                for (int j = lane >> 2; j < 32; j += 8) {
+                  const int nw = halo_axis(wr + j, E.Wo, p.epi.w0, p.epi.Wy - E.Wo - p.epi.w0,
+                                           p.epi.w_mode, wpos, wzero);
+                  if (nw == 1) continue;
+                  const uint4 val = *reinterpret_cast<const uint4*>(yt + j * 32 + 8 * part);
+                  for (int b = 1; b < nw; ++b)
+                    for (int a = 0; a < nh; ++a)
+                      *reinterpret_cast<uint4*>(E.y + halo_offset(p.epi, tc.nb, tc.od, hpos[a],
+                                                                   wpos[b], cw + 8 * part)) =
+                          (wzero[b] || hzero[a]) ? zero4 : val;
+                }
               }
               continue;
             }

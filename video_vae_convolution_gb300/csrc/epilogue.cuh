@@ -159,8 +159,64 @@ __device__ __forceinline__ void epi_norm_silu16(const EpiParams& e, int c, int c
   }
 }
 
+// Positions along one axis of a haloed y that take output coordinate i (extent L;
+// at most one halo pixel before and after): i itself, plus the halo pixel that
+// reflects it (mode 2: -1 holds 1, L holds L - 2) or the zero halo pixel beside it
+// (mode 1: -1 beside 0, L beside L - 1).  zero[k] marks a zero fill.  Returns the
+// count (up to 3 when L == 3 under reflection).
+__device__ __forceinline__ int halo_axis(int i, int L, int before, int after, int mode,
+                                         int (&pos)[3], bool (&zero)[3]) {
+  int n = 0;
+  pos[n] = i;
+  zero[n++] = false;
+  if (mode == 2) {
+    if (before && i == 1) {
+      pos[n] = -1;
+      zero[n++] = false;
+    }
+    if (after && i == L - 2) {
+      pos[n] = L;
+      zero[n++] = false;
+    }
+  } else if (mode == 1) {
+    if (before && i == 0) {
+      pos[n] = -1;
+      zero[n++] = true;
+    }
+    if (after && i == L - 1) {
+      pos[n] = L;
+      zero[n++] = true;
+    }
+  }
+  return n;
+}
+
+// Element offset in a haloed NDHWC y of channel c of output pixel (n, d, h, w),
+// h and w in output coordinates (-1 .. L for the halo).
+__device__ __forceinline__ long long halo_offset(const EpiParams& e, int n, int d, int h, int w,
+                                                 int c) {
+  return ((((long long)n * e.Dy + d + e.d0) * e.Hy + h + e.h0) * (long long)e.Wy + w + e.w0) *
+             e.Cout + c;
+}
+
+// Calls put(offset, zero) for every halo position of a haloed y that output pixel
+// (n, d, h, w) fills besides its own (reflected copies and zero neighbours), with
+// offset the element offset of channel c there.
+template <class Put>
+__device__ __forceinline__ void halo_extras(const EpiParams& e, int n, int d, int h, int w, int c,
+                                            Put&& put) {
+  int ph[3], pw[3];
+  bool zh[3], zw[3];
+  const int nh = halo_axis(h, e.Ho, e.h0, e.Hy - e.Ho - e.h0, e.h_mode, ph, zh);
+  const int nw = halo_axis(w, e.Wo, e.w0, e.Wy - e.Wo - e.w0, e.w_mode, pw, zw);
+  for (int a = 0; a < nh; ++a)
+    for (int b = 0; b < nw; ++b)
+      if (a || b) put(halo_offset(e, n, d, ph[a], pw[b], c), zh[a] || zw[b]);
+}
+
 // Writes y (and value_out / conv_out) for one chunk of one pixel; adds the
-// zero bottom row / right column of OUT_PAD_BR next to border pixels.
+// zero bottom row / right column of OUT_PAD_BR next to border pixels, and the
+// halo copies of a haloed y.
 __device__ __forceinline__ void epi_store16(const EpiParams& e, const Pixel& px, int c, int cnt,
                                             const float (&y)[16], const uint16_t (&yb_in)[16],
                                             bool use_bits) {
@@ -170,6 +226,17 @@ __device__ __forceinline__ void epi_store16(const EpiParams& e, const Pixel& px,
   const bool pad = (e.flags & EPI_OUT_PAD_BR) != 0;
   const int Hy = e.Ho + (pad ? 1 : 0), Wy = e.Wo + (pad ? 1 : 0);
   uint16_t* yp = static_cast<uint16_t*>(e.y);
+  if (e.halo) {
+    // NDHWC: the pixel's own position, then its reflected copies / zero neighbours
+    auto put = [&](long long off, bool zero) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (i < cnt) yp[off + i] = zero ? uint16_t(0) : yb[i];
+    };
+    put(halo_offset(e, px.n, px.d, px.h, px.w, c), false);
+    halo_extras(e, px.n, px.d, px.h, px.w, c, put);
+    return;
+  }
   store_chunk(yp, e.out_layout, e.Cout, e.Do, Hy, Wy, px.n, px.d, px.h, px.w, c, cnt, yb);
   if (pad) {
     uint16_t z[16];

@@ -37,6 +37,8 @@ struct CmEpi {
   const float* gamma;
   float sqrt_c;
   long long M_total;
+  bool halo;              // y is haloed (NDHWC): addresses and extras from *ep
+  const EpiParams* ep;    // the launch's epilogue parameters (kernel parameter space)
 };
 
 struct CmTile {
@@ -183,8 +185,10 @@ __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, 
   // base address per block; values converted two at a time.
   if (vec && !E.split && !E.pad && jb + 31 < t.jlim && jb + 31 < t.pitch && j0 + 31 < t.npix &&
       t.hoff + ib < E.Ho && t.woff + jb + 31 < E.Wo) {
-    const long long o0 =
-        ((nd * E.Ho + t.hoff + ib) * E.Wo + t.woff + jb + (lane >> 2)) * E.Cout + ch.c0;
+    const int hrow = t.hoff + ib, wcol = t.woff + jb + (lane >> 2);
+    const long long o0 = ((nd * E.Ho + hrow) * E.Wo + wcol) * E.Cout + ch.c0;
+    // y offset of the thread's first pixel (a haloed y has its own geometry)
+    const long long oy0 = E.halo ? halo_offset(*E.ep, t.nb, t.od, hrow, wcol, ch.c0) : o0;
     const long long step = 8LL * E.Cout;  // the thread's next pixel is 8 pixels on
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -225,9 +229,14 @@ __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, 
         v.w = pack_bf16x2(__fadd_rn(bf16x2_lo(v.w), bf16x2_lo(sk.w)),
                           __fadd_rn(bf16x2_hi(v.w), bf16x2_hi(sk.w)));
       }
-      *reinterpret_cast<uint4*>(E.y + o) = v;
+      *reinterpret_cast<uint4*>(E.y + oy0 + k * step) = v;
       if (E.flags & EPI_SAVE_VALUE) *reinterpret_cast<uint4*>(E.val + o) = v;
       if (E.flags & EPI_DEBUG_STORE_CONV) *reinterpret_cast<uint4*>(E.conv + o) = cb;
+      if (E.halo) {
+        halo_extras(*E.ep, t.nb, t.od, hrow, wcol + 8 * k, ch.c0, [&](long long off, bool zero) {
+          *reinterpret_cast<uint4*>(E.y + off) = zero ? make_uint4(0u, 0u, 0u, 0u) : v;
+        });
+      }
     }
     return;
   }
@@ -269,7 +278,19 @@ __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, 
     uint16_t vb[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) vb[e] = bf16_bits(v[e]);
-    const long long yo = ((nd * E.Hy + h) * E.Wy + w) * E.Cout + ch.c0;
+    const long long yo = E.halo ? halo_offset(*E.ep, t.nb, t.od, h, w, ch.c0)
+                                : ((nd * E.Hy + h) * E.Wy + w) * E.Cout + ch.c0;
+    if (E.halo) {
+      // (a haloed y has Cout % 8 == 0, so the thread's 8 channels are one 16-byte group)
+      const uint4 pv = pack8(vb);
+      reinterpret_cast<uint4*>(E.y + yo)[0] = pv;
+      if (E.flags & EPI_SAVE_VALUE) reinterpret_cast<uint4*>(E.val + ou)[0] = pv;
+      if (E.flags & EPI_DEBUG_STORE_CONV) reinterpret_cast<uint4*>(E.conv + ou)[0] = pack8(cb);
+      halo_extras(*E.ep, t.nb, t.od, h, w, ch.c0, [&](long long off, bool zero) {
+        *reinterpret_cast<uint4*>(E.y + off) = zero ? make_uint4(0u, 0u, 0u, 0u) : pv;
+      });
+      continue;
+    }
     if (vec) {
       const uint4 pv = pack8(vb);
       reinterpret_cast<uint4*>(E.y + yo)[0] = pv;

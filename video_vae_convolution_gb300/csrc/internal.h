@@ -55,6 +55,13 @@ struct EpiParams {
   uint16_t* value_out;     // bf16, out_layout, unpadded (SAVE_VALUE)
   uint16_t* conv_out;      // bf16 NDHWC unpadded (DEBUG_STORE_CONV)
   float sqrt_c;            // sqrtf((float)Cout)
+  // Output halo (NDHWC y only; halo = 1): y is [N, Dy, Hy, Wy, Cout] with the output
+  // at offset (d0, h0, w0).  Along H and W the halo is at most one pixel on a side
+  // (before = h0 / w0, after = Hy - Ho - h0 / Wy - Wo - w0), filled by reflection
+  // (mode 2: halo -1 takes row 1, halo Ho takes row Ho - 2) or with zeros (mode 1);
+  // the d0 leading and trailing frames are not written.
+  int halo;
+  int Dy, Hy, Wy, d0, h0, w0, h_mode, w_mode;
 };
 
 // Implicit-GEMM convolution on tcgen05 (one CTA = R M-tiles x BN output channels).
@@ -159,10 +166,12 @@ struct CmHalfMaps {
 };
 
 // Output tensor maps of the channel-major kernel's bulk-store epilogue (NDHWC,
-// bf16, box = 32 channels x 32 pixels along W): y, value_out and conv_out (the
-// last two repeat y when not requested).
+// bf16, box = 32 channels x 32 pixels along W): y (for a haloed y, the view of the
+// output inside it), value_out and conv_out (the last two repeat y when not
+// requested), and the whole haloed y.
 struct CmOutMaps {
   CUtensorMap y, val, conv;
+  CUtensorMap yfull;  // haloed y: the whole tensor (halo rows that copy a block)
 };
 
 }  // namespace vvc
