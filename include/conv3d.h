@@ -269,6 +269,9 @@ typedef struct {
   int32_t grid;             /* CTAs of the convolution kernel */
   int32_t bulk_store;       /* 1: output blocks on one output row go out through bulk
                                tensor stores (channel-major kernel) */
+  int32_t flat;             /* channel-major tiles: 0 rows of pixels, 1 runs of the
+                               flattened H*W plane, 2 runs of the flattened D*H*W volume
+                               (tiles span frames) */
 } conv3d_plan_info;
 
 int conv3d_plan(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_plan_info* info);

@@ -59,15 +59,24 @@ CASES = [
     # (call, tuning, halo)
     (wl.ConvCall("halo_strip_reflect", 1, 32, 4, 10, 40, 64, pads=CR, epi=wl.EPI_BIAS, index=70),
      None, LADDER_HALO),
+    (wl.ConvCall("halo_strip_bulk", 1, 32, 4, 10, 40, 64, pads=CR, index=88),
+     dict(k_splits=1), LADDER_HALO),
     (wl.ConvCall("halo_flat_valid", 1, 64, 5, 12, 34, 96, pads=VALID, index=71), None,
      LADDER_HALO),
+    (wl.ConvCall("halo_flat_bulk", 1, 64, 5, 12, 34, 96, pads=VALID, index=89),
+     dict(k_splits=1), LADDER_HALO),
+    (wl.ConvCall("halo_zero_bulk", 1, 32, 3, 9, 20, 32, pads=((1, 1, Z),) * 3, index=90),
+     dict(k_splits=1), ((1, 1, Z), (1, 1, Z), (1, 1, Z))),
     (wl.ConvCall("halo_zero_mode", 1, 32, 3, 9, 20, 32, pads=((1, 1, Z),) * 3, index=72), None,
      ((1, 1, Z), (1, 1, Z), (1, 1, Z))),
     (wl.ConvCall("halo_asym", 1, 16, 3, 7, 19, 48, pads=CR, epi=wl.EPI_BIAS, index=73), None,
      ((0, 2, Z), (1, 0, R), (0, 1, R))),
     (wl.ConvCall("halo_h3", 1, 32, 3, 3, 70, 32, pads=CR, index=74), None, LADDER_HALO),
     (wl.ConvCall("halo_residual", 1, 64, 3, 8, 36, 64, pads=CR,
-                 epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_RESIDUAL_BIAS, index=75), None,
+                 epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_RESIDUAL_BIAS, index=75),
+     dict(k_splits=1), LADDER_HALO),
+    (wl.ConvCall("halo_residual_split", 1, 64, 3, 8, 36, 64, pads=CR,
+                 epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_RESIDUAL_BIAS, index=91), None,
      LADDER_HALO),
     (wl.ConvCall("halo_split", 1, 128, 3, 6, 6, 128, pads=CR, epi=wl.EPI_BIAS, index=76),
      dict(k_splits=3), LADDER_HALO),
@@ -79,6 +88,48 @@ CASES = [
      None, LADDER_HALO),
     (wl.ConvCall("halo_narrow_in", 1, 3, 4, 16, 64, 32, pads=CR, index=80), None, LADDER_HALO),
 ]
+
+
+FLAT3_CASES = [
+    # valid convolutions over small planes: the tiles run across frames
+    (wl.ConvCall("flat3_valid", 1, 64, 6, 10, 10, 64, pads=VALID, epi=wl.EPI_BIAS, index=82),
+     dict(k_splits=1)),
+    (wl.ConvCall("flat3_valid_split", 1, 64, 6, 10, 10, 64, pads=VALID, epi=wl.EPI_BIAS,
+                 index=87), None),
+    (wl.ConvCall("flat3_causal_t", 1, 128, 5, 9, 11, 96, pads=((2, 0, Z), (0, 0, Z), (0, 0, Z)),
+                 index=83), None),
+    (wl.ConvCall("flat3_split", 1, 256, 7, 18, 18, 256, pads=VALID, epi=wl.EPI_BIAS, index=84),
+     None),
+    (wl.ConvCall("flat3_paired", 1, 96, 6, 12, 12, 64, pads=VALID, index=85), dict(k_splits=1)),
+    (wl.ConvCall("flat3_residual", 1, 64, 4, 8, 8, 32, pads=VALID,
+                 epi=wl.EPI_BIAS | wl.EPI_RESIDUAL, index=86), None),
+]
+
+
+@pytest.mark.parametrize("case", FLAT3_CASES, ids=lambda c: c[0].name)
+def test_flat_volume_tiles(case):
+    call, tune = case
+    inp = wl.make_inputs("test", call, wl.NDHWC, wl.NDHWC)
+    tuning = vvc.Tuning(**tune) if tune else None
+    gc = GpuCall(call, inp, wl.NDHWC, wl.NDHWC, tuning=tuning)
+    assert gc.c.plan.flat == 2, call.name
+    if call.name == "flat3_paired":
+        assert gc.c.plan.paired == 1
+    check_conv(gc.conv, full_reference(gc), call.name)
+    check_epilogue(gc)
+    # and into a haloed tensor: the same output inside it
+    dev = torch.device("cuda")
+    Do, Ho, Wo = gc.c.out_dims
+    y = torch.full((1, Do + 2, Ho + 2, Wo + 2, call.Cout), 7.0, dtype=torch.bfloat16, device=dev)
+    g = lambda k: None if inp[k] is None else inp[k].to(dev)
+    c = vvc.Conv3d(inp["x"].to(dev), gc.w_packed, call.Cout, call.kernel, call.stride,
+                   call.pads, wl.NDHWC, wl.NDHWC, call.epi, bias=g("bias"),
+                   residual=g("residual"), y=y, out_halo=LADDER_HALO, tuning=tuning)
+    assert c.plan.flat == 2
+    c()
+    torch.cuda.synchronize()
+    assert vvc.device_status() == 0
+    np.testing.assert_array_equal(_bits(y), _expected_halo(gc.y, LADDER_HALO))
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c[0].name)

@@ -99,7 +99,7 @@ class Tuning(ctypes.Structure):
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "kernel", "mma_n", "stages_per_tile", "k_splits", "paired", "im2col", "launches",
-        "grid", "bulk_store")]
+        "grid", "bulk_store", "flat")]
 
 
 _LIB = None

@@ -301,12 +301,28 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
                        p->pad[2].after == 0 &&
                        (p->pad[1].mode == CONV3D_PAD_ZERO ||
                         (p->pad[1].before == 0 && p->pad[1].after == 0));
-  const long long q_total = (long long)(Ho - 1) * p->W + Wo;  // flattened output range
+  long long q_total = (long long)(Ho - 1) * p->W + Wo;  // flattened output range
+  // flattened D*H*W: tiles run across frames, so small planes fill whole 256-pixel
+  // tiles (no H / W padding: a row above the plane would be the previous frame's
+  // last row; T zero padding reads positions outside the volume)
+  const long long q3 = ((long long)(Do - 1) * p->H + (Ho - 1)) * p->W + Wo;
+  const bool flat3_ok = flat_ok && p->stride[0] == 1 && p->pad[1].before == 0 &&
+                        p->pad[1].after == 0 && p->pad[0].mode == CONV3D_PAD_ZERO &&
+                        p->out_layout == CONV3D_NDHWC &&
+                        !(p->epi & CONV3D_EPI_L2NORM_SILU) && t.kernel != 3 &&
+                        q3 < 0x7fffff00LL;
+  bool flat3 = false;
   if (t.tile_w <= 0 && t.halo != 2 && flat_ok && q_total < 0x7fffff00LL) {
     // flattened H*W: a tile is 256 consecutive positions with row pitch W
     flat = true;
     halo = true;
     rh = 1;
+    const long long tiles2 = (long long)Do * cdiv(q_total, std::min<long long>(256, round_up(q_total, 16)));
+    const long long tiles3 = cdiv(q3, std::min<long long>(256, round_up(q3, 16)));
+    if (flat3_ok && Do > 1 && tiles3 < tiles2) {
+      flat3 = true;
+      q_total = q3;
+    }
     tw = static_cast<int>(std::min<long long>(256, round_up(q_total, 16)));
   } else if (t.tile_w > 0) {
     tw = t.tile_w;
@@ -374,6 +390,8 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.rh = rh;
   k.halo = halo ? 1 : 0;
   k.flat = flat ? 1 : 0;
+  k.flat3 = flat3 ? 1 : 0;
+  k.tiles_d = flat3 ? 1 : Do;
   if (flat) {
     k.nbox = static_cast<int>(cdiv(tw + p->KS - 1, 256));
     k.box_w = k.nbox == 1 ? tw + p->KS - 1
@@ -485,7 +503,7 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   }
   k.tiles_w = static_cast<int>(flat ? cdiv(q_total, tw) : cdiv(Wo, tw));
   k.tiles_h = static_cast<int>(flat ? 1 : cdiv(Ho, rh));
-  const long long tiles = (long long)k.tiles_w * k.tiles_h * Do * p->N * k.tiles_c;
+  const long long tiles = (long long)k.tiles_w * k.tiles_h * k.tiles_d * p->N * k.tiles_c;
   const int sms = num_sms();
   int per = 0;
   // with the fused norm the channel tiles of a pixel tile share a CTA, so the
@@ -937,7 +955,15 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
   cuuint32_t boxA[5] = {(cuuint32_t)kc, (cuuint32_t)act_box, 1, 1, 1};
   cuuint32_t esA[5] = {1, (cuuint32_t)es_w, 1, 1, 1};
   cuuint32_t rankA = 5;
-  if (flat) {
+  if (flat && pl.cm && pl.cp.flat3) {
+    // D, H and W merged into one dimension of D*H*W positions (dims C, D*H*W, 1, N)
+    gdimA[1] = (cuuint64_t)p->D * p->H * p->W;
+    gdimA[2] = 1;
+    gdimA[3] = (cuuint64_t)p->N;
+    gstrA[1] = gstrA[3];
+    gstrA[2] = gstrA[3];
+    rankA = 4;
+  } else if (flat) {
     // H and W merged into one dimension of H*W positions (dims C, H*W, D, N)
     gdimA[1] = (cuuint64_t)p->H * p->W;
     gdimA[2] = (cuuint64_t)p->D;
@@ -1100,6 +1126,7 @@ int conv3d_plan(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_plan
     r.k_splits = k.k_splits;
     r.paired = k.pair;
     r.bulk_store = k.tma_store;
+    r.flat = k.flat ? (k.flat3 ? 2 : 1) : 0;
   } else {
     const ConvTCParams& k = pl.kp;
     r.kernel = 1;

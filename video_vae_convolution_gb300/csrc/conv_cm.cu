@@ -66,8 +66,8 @@ __device__ __forceinline__ TileCoord decode_tile(const ConvCMParams& p, int tile
   tile /= p.tiles_c;
   c.split = tile % p.k_splits;
   tile /= p.k_splits;
-  c.od = tile % p.epi.Do;
-  tile /= p.epi.Do;
+  c.od = tile % p.tiles_d;
+  tile /= p.tiles_d;
   c.twi = tile % p.tiles_w;
   tile /= p.tiles_w;
   c.thi = tile % p.tiles_h;
@@ -287,10 +287,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 const int dj = tc.od * p.st + tj - p.pt;
                 const uint32_t aj = act + static_cast<uint32_t>(j) * (p.act_bytes >> 1);
                 if (p.flat) {
-                  const int q_start = w0 + (rj - p.ph) * p.W;
+                  const int q_start = p.flat3 ? w0 + ((tj - p.pt) * p.H + rj - p.ph) * p.W
+                                              : w0 + (rj - p.ph) * p.W;
                   for (int b = 0; b < p.nbox; ++b)
                     tma_load_4d(aj + static_cast<uint32_t>(b * p.box_w * 64), &hm.act, full,
-                                sc.ch * p.kc, q_start + b * p.box_w, dj, tc.nb);
+                                sc.ch * p.kc, q_start + b * p.box_w, p.flat3 ? 0 : dj, tc.nb);
                 } else {
                   for (int i = 0; i < p.rh; ++i) {
                     const int ho = h0 + i;
@@ -319,11 +320,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 }
               }
             } else if (p.flat) {
-              // flattened (H*W) positions: output q reads input q + (r - ph) * W + s
-              const int q_start = w0 + (sc.r - p.ph) * p.W;
+              // flattened (H*W) positions: output q reads input q + (r - ph) * W + s;
+              // flattened (D*H*W) positions: q + ((t - pt) * H + r - ph) * W + s
+              const int q_start = p.flat3 ? w0 + ((sc.t - p.pt) * p.H + sc.r - p.ph) * p.W
+                                          : w0 + (sc.r - p.ph) * p.W;
               for (int b = 0; b < p.nbox; ++b)
                 tma_load_4d(act + static_cast<uint32_t>(b * p.box_w * p.row_bytes), &tmAct,
-                            full, sc.ch * p.kc, q_start + b * p.box_w, d_in, tc.nb);
+                            full, sc.ch * p.kc, q_start + b * p.box_w, p.flat3 ? 0 : d_in,
+                            tc.nb);
             } else {
               // one run per output row of the tile, run_pitch rows apart: halo runs
               // of tw + KS - 1 pixels (all KS taps), or tw pixels at one tap
@@ -632,6 +636,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       t.hoff = p.flat ? 0 : t.h0;
       t.woff = p.flat ? 0 : t.w0;
       t.jlim = p.flat ? p.W : p.tw;
+      t.vrows = p.flat3 ? p.H : 0;
       return t;
     };
     if (kPM) {
@@ -711,9 +716,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             const int qq = t.q0 + j0;
             const int ib = qq / t.pitch;
             const int jb = qq - ib * t.pitch;
-            const int hr = t.hoff + ib, wr = t.woff + jb;
+            const int wr = t.woff + jb;
+            int od, hr;  // output frame and row (a tile of the flattened volume spans frames)
+            cm_frame_row(t, t.hoff + ib, od, hr);
             if (!E.ndhwc && jb + 31 < t.jlim && jb + 31 < t.pitch && j0 + 31 < t.npix &&
-                hr < E.Ho && wr + 31 < E.Wo && (wr & 7) == 0) {
+                hr < E.Ho && od < E.Do && wr + 31 < E.Wo && (wr & 7) == 0) {
               // NCDHW: the block goes out as [32 channels][32 pixels] bf16, one 64-byte
               // row per thread (its channel), through bulk tensor stores.  The store's
               // innermost coordinate is the output column, so it must be a multiple of 8.
@@ -737,15 +744,15 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                tma_store_5d(&om.y, smem_u32(yt), wr, hr, tc.od, cw, tc.nb);
+                tma_store_5d(&om.y, smem_u32(yt), wr, hr, od, cw, tc.nb);
                 if (E.flags & EPI_SAVE_VALUE)
-                  tma_store_5d(&om.val, smem_u32(yt), wr, hr, tc.od, cw, tc.nb);
+                  tma_store_5d(&om.val, smem_u32(yt), wr, hr, od, cw, tc.nb);
                 bulk_commit_group();
               }
               continue;
             }
             if (E.ndhwc && jb + 31 < t.jlim && jb + 31 < t.pitch && j0 + 31 < t.npix &&
-                hr < E.Ho && wr + 31 < E.Wo) {
+                hr < E.Ho && od < E.Do && wr + 31 < E.Wo) {
               // The 32 pixels are one piece of an output row: the block goes out as
               // [32 pixels][32 channels] bf16 through bulk tensor stores.
               uint16_t* yt = reinterpret_cast<uint16_t*>(st);
@@ -771,14 +778,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                                                 p.epi.h_mode, hpos, hzero)
                                     : 1;
               if (lane == 0) {
-                tma_store_5d(&om.y, smem_u32(yt), cw, wr, hr, tc.od, tc.nb);
+                tma_store_5d(&om.y, smem_u32(yt), cw, wr, hr, od, tc.nb);
                 for (int a = 1; a < nh; ++a)
                   if (!hzero[a])
                     tma_store_5d(&om.yfull, smem_u32(yt), cw, wr + p.epi.w0, hpos[a] + p.epi.h0,
-                                 tc.od + p.epi.d0, tc.nb);
+                                 od + p.epi.d0, tc.nb);
                 if (E.flags & EPI_SAVE_VALUE)
-                  tma_store_5d(&om.val, smem_u32(yt), cw, wr, hr, tc.od, tc.nb);
-                if (dbg) tma_store_5d(&om.conv, smem_u32(ct), cw, wr, hr, tc.od, tc.nb);
+                  tma_store_5d(&om.val, smem_u32(yt), cw, wr, hr, od, tc.nb);
+                if (dbg) tma_store_5d(&om.conv, smem_u32(ct), cw, wr, hr, od, tc.nb);
                 bulk_commit_group();
               }
               if (E.halo) {
@@ -789,7 +796,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                   for (int u = lane; u < 128; u += 32) {
                     const int j = u >> 2, part = u & 3;
                     *reinterpret_cast<uint4*>(
-                        E.y + halo_offset(p.epi, tc.nb, tc.od, hpos[a], wr + j, cw + 8 * part)) =
+                        E.y + halo_offset(p.epi, tc.nb, od, hpos[a], wr + j, cw + 8 * part)) =
                         zero4;
                   }
                 }
@@ -802,7 +809,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                   const uint4 val = *reinterpret_cast<const uint4*>(yt + j * 32 + 8 * part);
                   for (int b = 1; b < nw; ++b)
                     for (int a = 0; a < nh; ++a)
-                      *reinterpret_cast<uint4*>(E.y + halo_offset(p.epi, tc.nb, tc.od, hpos[a],
+                      *reinterpret_cast<uint4*>(E.y + halo_offset(p.epi, tc.nb, od, hpos[a],
                                                                    wpos[b], cw + 8 * part)) =
                           (wzero[b] || hzero[a]) ? zero4 : val;
                 }

@@ -51,7 +51,21 @@ struct CmTile {
   // the same as a row/column split of q = q0 + n by pitch: output row hoff + q / pitch,
   // column woff + q % pitch, in the tile while the column index is below jlim
   int q0, hoff, woff, jlim;
+  // vrows > 0: the tile runs over the flattened volume; its row index counts rows of
+  // the input volume, frame = row / vrows (the input height), row in frame = the rest
+  int vrows;
 };
+
+// Output frame and row of tile row index hv (see CmTile::vrows).
+__device__ __forceinline__ void cm_frame_row(const CmTile& t, int hv, int& d, int& h) {
+  if (t.vrows) {
+    d = hv / t.vrows;
+    h = hv - d * t.vrows;
+  } else {
+    d = t.od;
+    h = hv;
+  }
+}
 
 // Per-warp staging block: 32 rows (pixels) of 32 channels, fp32.  Rows are
 // kStageVec floats apart where a thread reads 8 channels of a pixel as two
@@ -80,6 +94,20 @@ __device__ __forceinline__ CmChan cm_chan(const CmEpi& E, int cw, int lane) {
   }
   c.bc = ((E.flags & EPI_BIAS) && cw + lane < E.Cout) ? __ldg(E.bias + cw + lane) : 0.0f;
   return c;
+}
+
+// Row index (see CmTile::vrows) and column of tile pixel j0 + pl from the block
+// origin (ib, jb) of pixel j0; true when the pixel belongs to the tile.
+__device__ __forceinline__ bool cm_unit_pos_v(const CmTile& t, int ib, int jb, int j0, int pl,
+                                              int& hv, int& w) {
+  int i = ib, j = jb + pl;
+  while (j >= t.pitch) {
+    j -= t.pitch;
+    ++i;
+  }
+  hv = t.hoff + i;
+  w = t.woff + j;
+  return j < t.jlim && j0 + pl < t.npix;
 }
 
 // Row / column of tile pixel j0 + pl from the block origin (ib, jb) of pixel j0;
@@ -177,18 +205,20 @@ __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, 
   const int q = t.q0 + j0;
   const int ib = q / t.pitch;
   const int jb = q - ib * t.pitch;
-  const long long nd = (long long)t.nb * E.Do + t.od;
   const bool vec = (ch.cnt == 8) && ((E.Cout & 7) == 0);
   const int g = lane & 3;
+  int fd, hrow;  // frame and row of the block's first pixel
+  cm_frame_row(t, t.hoff + ib, fd, hrow);
   // Fast path: the block's 32 pixels are consecutive pixels of one output row, all
   // inside the output, and the thread's 8 channels are a full 16-byte group.  One
   // base address per block; values converted two at a time.
   if (vec && !E.split && !E.pad && jb + 31 < t.jlim && jb + 31 < t.pitch && j0 + 31 < t.npix &&
-      t.hoff + ib < E.Ho && t.woff + jb + 31 < E.Wo) {
-    const int hrow = t.hoff + ib, wcol = t.woff + jb + (lane >> 2);
+      hrow < E.Ho && fd < E.Do && t.woff + jb + 31 < E.Wo) {
+    const long long nd = (long long)t.nb * E.Do + fd;
+    const int wcol = t.woff + jb + (lane >> 2);
     const long long o0 = ((nd * E.Ho + hrow) * E.Wo + wcol) * E.Cout + ch.c0;
     // y offset of the thread's first pixel (a haloed y has its own geometry)
-    const long long oy0 = E.halo ? halo_offset(*E.ep, t.nb, t.od, hrow, wcol, ch.c0) : o0;
+    const long long oy0 = E.halo ? halo_offset(*E.ep, t.nb, fd, hrow, wcol, ch.c0) : o0;
     const long long step = 8LL * E.Cout;  // the thread's next pixel is 8 pixels on
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -233,7 +263,7 @@ __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, 
       if (E.flags & EPI_SAVE_VALUE) *reinterpret_cast<uint4*>(E.val + o) = v;
       if (E.flags & EPI_DEBUG_STORE_CONV) *reinterpret_cast<uint4*>(E.conv + o) = cb;
       if (E.halo) {
-        halo_extras(*E.ep, t.nb, t.od, hrow, wcol + 8 * k, ch.c0, [&](long long off, bool zero) {
+        halo_extras(*E.ep, t.nb, fd, hrow, wcol + 8 * k, ch.c0, [&](long long off, bool zero) {
           *reinterpret_cast<uint4*>(E.y + off) = zero ? make_uint4(0u, 0u, 0u, 0u) : v;
         });
       }
@@ -242,8 +272,11 @@ __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, 
   }
   for (int k = 0; k < 4; ++k) {
     const int pl = 8 * k + (lane >> 2);
-    int h, w;
-    if (ch.cnt <= 0 || !cm_unit_pos(E, t, ib, jb, j0, pl, h, w)) continue;
+    int hv, h, w, d;
+    if (ch.cnt <= 0 || !cm_unit_pos_v(t, ib, jb, j0, pl, hv, w)) continue;
+    cm_frame_row(t, hv, d, h);
+    if (h >= E.Ho || w >= E.Wo || d >= E.Do) continue;
+    const long long nd = (long long)t.nb * E.Do + d;
     float a[8];
     {
       const float4 lo = *reinterpret_cast<const float4*>(st + pl * kStageVec + 8 * g);
@@ -278,7 +311,7 @@ __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, 
     uint16_t vb[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) vb[e] = bf16_bits(v[e]);
-    const long long yo = E.halo ? halo_offset(*E.ep, t.nb, t.od, h, w, ch.c0)
+    const long long yo = E.halo ? halo_offset(*E.ep, t.nb, d, h, w, ch.c0)
                                 : ((nd * E.Hy + h) * E.Wy + w) * E.Cout + ch.c0;
     if (E.halo) {
       // (a haloed y has Cout % 8 == 0, so the thread's 8 channels are one 16-byte group)
@@ -286,7 +319,7 @@ __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, 
       reinterpret_cast<uint4*>(E.y + yo)[0] = pv;
       if (E.flags & EPI_SAVE_VALUE) reinterpret_cast<uint4*>(E.val + ou)[0] = pv;
       if (E.flags & EPI_DEBUG_STORE_CONV) reinterpret_cast<uint4*>(E.conv + ou)[0] = pack8(cb);
-      halo_extras(*E.ep, t.nb, t.od, h, w, ch.c0, [&](long long off, bool zero) {
+      halo_extras(*E.ep, t.nb, d, h, w, ch.c0, [&](long long off, bool zero) {
         *reinterpret_cast<uint4*>(E.y + off) = zero ? make_uint4(0u, 0u, 0u, 0u) : pv;
       });
       continue;

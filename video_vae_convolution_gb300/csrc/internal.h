@@ -113,6 +113,11 @@ struct ConvCMParams {
   int flat;                // 1 (with halo): H and W merged; a tile is tw consecutive
                            // positions of the flattened plane, row pitch W (needs
                            // stride 1, no W padding, zero H padding)
+  int flat3;               // 1 (with flat): D, H and W merged; a tile is tw consecutive
+                           // positions of the flattened volume and may span frames
+                           // (needs stride 1 and no H / W padding; T zero padding reads
+                           // positions outside the volume)
+  int tiles_d;             // output frames in the tile index (1 with flat3)
   int nbox;                // activation boxes per stage (halo: 1..2, direct: rh)
   int box_w;               // loaded elements per activation box
   int run_pitch;           // shared-memory rows between the runs of consecutive output
