@@ -193,6 +193,9 @@ typedef struct {
                           there are at least 2 (kt, kr) tap pairs, run the last chunks of
                           two consecutive tap pairs as one pipeline stage of 64-byte rows
                           instead of one half-empty stage each */
+  int32_t prefetch;    /* weight L2 prefetch distance in pipeline stages: 0 auto (on for
+                          layers whose CTAs run few tiles, so that every weight slice is a
+                          first read from HBM), -1 off, > 0 that many stages ahead */
 } conv3d_tuning;
 
 /* ---- weight packing ([cuDNN page] "Weight Packing") ------------------------------ */

@@ -88,7 +88,7 @@ class Params(ctypes.Structure):
 class Tuning(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "tile_w", "tile_h", "R", "kc", "BN", "halo", "stages", "k_splits", "kernel",
-        "inject", "timeout_ms", "im2col", "pair")]
+        "inject", "timeout_ms", "im2col", "pair", "prefetch")]
 
     def __init__(self, **kw):
         super().__init__()

@@ -256,7 +256,25 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         int it_b, it_e;
         stage_range(p, tc.split, it_b, it_e);
         StageCoord sc = kPair ? pair_begin(p) : decode_stage(p, it_b);
+        // weight L2 prefetch (plain schedule): pf runs wpref stages ahead of sc
+        const bool pref = !kPair && !act_role && p.wpref > 0;
+        StageCoord pf = sc;
+        int it_pf = it_b;
+        auto prefetch_stage = [&](const StageCoord& c) {
+          const int x0 = (c.t * p.KR + c.r) * p.KS * p.cp64 + c.ch * p.kc;
+          for (int tl = 0; tl < p.taps_per_stage; ++tl)
+            tma_prefetch_l2_2d(wmap, x0 + (p.halo ? tl : c.sblk) * p.cp64, c0);
+        };
+        if (pref) {
+          for (; it_pf < it_e && it_pf < it_b + p.wpref; ++it_pf, next_stage(p, pf))
+            prefetch_stage(pf);
+        }
         for (int it = it_b; it < it_e; ++it, kPair ? pair_next(p, sc) : next_stage(p, sc)) {
+          if (pref && it_pf < it_e) {
+            prefetch_stage(pf);
+            ++it_pf;
+            next_stage(p, pf);
+          }
           if (!mbar_wait(empty_bar(slot), phase ^ 1u, abort_flag, lim)) {
             ok = false;
             break;

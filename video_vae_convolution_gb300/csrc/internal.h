@@ -163,6 +163,10 @@ struct ConvCMParams {
   // both pairs as 32-channel, 64-byte rows (act: pair j at j * act_bytes / 2;
   // weights: pair j, tap s at (j * KS + s) * wtap_rows * 64).
   int pair, n_pairs;
+  // Weight L2 prefetch: the weight producer asks L2 for the weight boxes of the stage
+  // wpref stages ahead of the one it loads (0 = off).  Small layers read every weight
+  // slice from HBM once, and two pipeline stages cannot hide that latency.
+  int wpref;
 };
 
 // Tensor maps of the paired last-chunk stages: 32-channel boxes, 64-byte swizzle.
