@@ -47,7 +47,8 @@ L2_FLUSH_BYTES = 256 << 20
 # capture (profiles/), keyed by a hash of the kernel's sources (comments and
 # whitespace left out) and the call it was captured on: a changed kernel reports
 # null until it is captured again.
-KERNEL_SOURCES = ["conv_cm.cu", "epilogue_cm.cuh", "epilogue.cuh", "kernel_common.cuh",
+KERNEL_SOURCES = ["conv_cm.cu", "conv_cm_kernel.cuh", "conv_cm_halo.cu", "epilogue_cm.cuh",
+                  "epilogue.cuh", "kernel_common.cuh",
                   "ptx.cuh", "internal.h"]
 NCU_TRAFFIC = {}
 

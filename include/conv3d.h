@@ -185,9 +185,13 @@ typedef struct {
                           bounded wait runs out; the call then reports a timeout */
   int32_t timeout_ms;  /* device wait limit (0 = default: 4000 ms, or the environment
                           variable CONV3D_TIMEOUT_MS when set) */
-  int32_t im2col;      /* 0 auto, 1 on, 2 off: for Cin * KR * KS <= 64 (Cin < 8) gather
-                          the spatial taps into a staged tensor first and run a
-                          (KT, 1, 1) convolution over it */
+  int32_t im2col;      /* narrow inputs (Cin < 8): 0 auto, 1 gather the spatial taps into
+                          a staged tensor first and run a (KT, 1, 1) convolution over it
+                          (Cin * KR * KS <= 64), 2 neither, 3 gather the taps inside the
+                          convolution kernel from TMA copies of the raw input rows
+                          (Cin * KR * KS <= 32, W stride 1, W padding <= 1; not with
+                          L2NORM_SILU).  Auto: 3 where it applies, else 1 where that
+                          applies */
   int32_t pair;        /* 0 auto (= on), 1 on, 2 off: when the last 64-channel chunk of
                           the input holds at most 32 channels (Cin = 96, 160, ...) and
                           there are at least 2 (kt, kr) tap pairs, run the last chunks of
@@ -267,7 +271,8 @@ typedef struct {
   int32_t stages_per_tile;  /* pipeline stages of one tile's whole reduction */
   int32_t k_splits;         /* split of the reduction across CTAs */
   int32_t paired;           /* 1: the last chunks of two tap pairs share a stage */
-  int32_t im2col;           /* 1: the spatial taps are gathered before the conv */
+  int32_t im2col;           /* 1: the spatial taps are gathered into a staged tensor
+                               before the conv, 2: inside the conv kernel */
   int32_t launches;         /* kernel launches of the call */
   int32_t grid;             /* CTAs of the convolution kernel */
   int32_t bulk_store;       /* 1: output blocks on one output row go out through bulk

@@ -251,8 +251,34 @@ IM2COL_CASES = [
 @pytest.mark.parametrize("call", IM2COL_CASES, ids=lambda c: c.name)
 @pytest.mark.parametrize("layout", [wl.NDHWC, wl.NCDHW])
 def test_im2col_narrow_input(call, layout):
-    gc, _ = run_and_check(call, layout, wl.NDHWC)
-    assert gc.c.launches >= 2  # the gather runs before the convolution
+    gc, _ = run_and_check(call, layout, wl.NDHWC, tuning=vvc.Tuning(im2col=1))
+    assert gc.c.launches >= 2  # the staged gather runs before the convolution
+    assert gc.c.plan.im2col == 1
+
+
+# In-kernel gather of narrow inputs (Cin * KR * KS <= 32, W stride 1): raw input rows
+# copied by TMA, expanded in shared memory, resident weights; one launch.
+GATHER_CASES = [
+    mk("gather_cin3_causal_reflect", 1, 3, 4, 9, 64, 96, pads=CR, index=36),
+    mk("gather_cin3_t1_zero", 1, 3, 1, 17, 40, 96, kernel=(1, 3, 3), pads=P2D, index=37),
+    mk("gather_cin1_zero_bias", 2, 1, 3, 7, 32, 32, pads=P1, epi=wl.EPI_BIAS, index=38),
+    mk("gather_cin3_wide_row", 1, 3, 3, 5, 600, 64, pads=CR, index=39),
+    mk("gather_cin2_two_ctiles", 1, 2, 3, 6, 40, 200, pads=CR, epi=wl.EPI_BIAS, index=48),
+    mk("gather_cin3_residual", 1, 3, 3, 8, 64, 128, pads=CR,
+       epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_RESIDUAL_BIAS, index=49),
+    mk("gather_cin3_stride_th", 1, 3, 7, 12, 48, 64, stride=(2, 2, 1), pads=CR, index=50),
+    mk("gather_cin3_valid", 1, 3, 4, 8, 24, 48, pads=VALID, index=51),
+    mk("gather_cin4_k322", 1, 4, 5, 9, 32, 64, kernel=(3, 2, 2),
+       pads=((2, 0, Z), (1, 0, Z), (0, 1, Z)), index=52),
+]
+
+
+@pytest.mark.parametrize("call", GATHER_CASES, ids=lambda c: c.name)
+@pytest.mark.parametrize("layout", [wl.NDHWC, wl.NCDHW])
+@pytest.mark.parametrize("out_layout", [wl.NDHWC, wl.NCDHW])
+def test_gather_narrow_input(call, layout, out_layout):
+    gc, _ = run_and_check(call, layout, out_layout)
+    assert gc.c.launches == 1 and gc.c.plan.im2col == 2, (gc.c.launches, gc.c.plan.im2col)
 
 
 # Paired last chunks: Cin % 64 in 1..32, so the last 32-channel chunks of two tap

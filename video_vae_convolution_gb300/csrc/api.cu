@@ -421,10 +421,13 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   if (k.N > 256) return CONV3D_ERR_INVALID_ARG;
   // Pixel-major mode for layers with at most 128 output channels: N = Cout (rounded
   // to 16) over 128-pixel halves instead of M = 128 channel rows of which only Cout are
-  // real; its epilogue (one pixel per thread) needs no staging.
-  // (Measured slower than channel-major tiles on the 96-channel and narrow layers, so
-  // it runs only on request: conv3d_tuning.kernel = 3.)
-  const bool pm = t.kernel == 3;
+  // real; its epilogue (one pixel per thread) needs no staging.  Automatic for
+  // Cout <= 16 (the RGB output convolution: 3 of 128 channel rows would be real);
+  // measured slower than channel-major tiles on the 32- to 96-channel layers, where
+  // it runs only on request (conv3d_tuning.kernel = 3).
+  const bool pm = t.kernel == 3 ||
+                  (t.kernel == 0 && p->Cout <= 16 && !(p->epi & CONV3D_EPI_L2NORM_SILU) &&
+                   !has_halo(p));
   if (pm && p->Cout > 128) return CONV3D_ERR_UNSUPPORTED;
   k.pm = pm ? 1 : 0;
   if (pm) {
@@ -597,6 +600,127 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.st = p->stride[0];
   k.sh = p->stride[1];
   k.sw = sw;
+  k.pt = p->pad[0].before;
+  k.ph = p->pad[1].before;
+  k.pw = p->pad[2].before;
+  k.reflect_h = (p->pad[1].mode == CONV3D_PAD_REFLECT && (p->pad[1].before || p->pad[1].after));
+  k.reflect_w = (p->pad[2].mode == CONV3D_PAD_REFLECT && (p->pad[2].before || p->pad[2].after));
+  k.cp64 = static_cast<int>(round_up(p->Cin, 64));
+  k.inject = t.inject;
+  k.timeout_ns = (unsigned long long)(t.timeout_ms > 0 ? t.timeout_ms : default_timeout_ms()) *
+                 1000000ULL;
+  fill_epi(p, *pl, &k.epi);
+  return CONV3D_OK;
+}
+
+// Narrow-input gather plan (Cin < 8, KR * KS * Cin <= 32, stride 1 along W, W
+// padding <= 1): channel-major tiles of one output row (N = up to 256 pixels), one
+// stage per temporal tap whose K = KR * KS * Cin values are gathered in shared
+// memory from TMA copies of the raw input rows (ConvCMParams::gather); no staged
+// copy of the input and no separate launch.  Returns CONV3D_ERR_UNSUPPORTED when
+// the shape does not fit it.
+int plan_gather(const conv3d_params* p, const conv3d_tuning& t, Plan* pl) {
+  ConvCMParams& k = pl->cp;
+  std::memset(&k, 0, sizeof(k));
+  const int Do = pl->Do, Ho = pl->Ho, Wo = pl->Wo;
+  const int C = p->Cin;
+  const bool cl = p->layout == CONV3D_NDHWC;
+  const int krs = p->KR * p->KS;
+  const bool pads_ok = p->pad[2].before <= 1 && p->pad[2].after <= 1 &&
+                       (p->pad[1].mode == CONV3D_PAD_ZERO ||
+                        (p->pad[1].before <= 1 && p->pad[1].after <= 1));
+  if (C >= 8 || krs < 2 || krs * C > 32 || p->stride[2] != 1 || !pads_ok ||
+      (p->epi & CONV3D_EPI_L2NORM_SILU) || (cl ? ((long long)p->W * C) % 8 : p->W % 8) != 0)
+    return CONV3D_ERR_UNSUPPORTED;
+  const int tiles_c = static_cast<int>(cdiv(p->Cout, 128));
+  const size_t wres_bytes = (size_t)tiles_c * p->KT * 128 * 64;
+  if (wres_bytes > (64u << 10)) return CONV3D_ERR_UNSUPPORTED;
+  k.gather = 1;
+  k.kc = 32;
+  k.row_bytes = 64;
+  k.n_chunks = 1;
+  k.tw = std::min(Wo, 256);
+  k.rh = 1;
+  k.halo = 0;
+  k.nbox = 1;
+  k.box_w = k.tw;
+  k.run_pitch = k.tw;
+  k.N = static_cast<int>(round_up(k.tw, 16));
+  k.wtap_rows = 128;
+  k.taps_per_stage = 1;
+  k.stages_total = p->KT;
+  k.g_K = krs * C;
+  k.g_cpp = cl ? C : 1;
+  k.g_planes = cl ? 1 : C;
+  // groups of 8 values per raw row: the row's first group is rounded down, so one
+  // more group than the values cover; rows are whole 128-byte lines
+  const long long vals = (long long)(k.tw + p->KS - 1) * k.g_cpp;
+  const int nG = static_cast<int>(round_up(cdiv(vals + 7, 8), 8));
+  if (nG > 256) return CONV3D_ERR_UNSUPPORTED;
+  k.g_row_bytes = nG * 16;
+  const int raw_rows = k.g_planes * p->KR;
+  k.g_raw_off = static_cast<uint32_t>(round_up((long long)k.N * 64, 1024));
+  k.act_bytes = k.g_raw_off;
+  k.stage_bytes = static_cast<uint32_t>(
+      round_up(k.g_raw_off + (long long)raw_rows * k.g_row_bytes, 1024));
+  k.tx_bytes = k.tx_bytes_last = k.act_tx = static_cast<uint32_t>(raw_rows * k.g_row_bytes);
+  k.wgt_rows = static_cast<int>(std::min<long long>(128, round_up(p->Cout, 8)));
+  k.wgt_rows_last = static_cast<int>(round_up(p->Cout - 128LL * (tiles_c - 1), 8));
+  k.tiles_c = tiles_c;
+  auto stages_for = [&](int groups) {
+    const size_t epi = (size_t)groups * 4 * kEpiWarpBytes;
+    const long long avail = (long long)kMaxSmem - 1024 - 256 - (long long)epi -
+                            (long long)wres_bytes - 1024;
+    return static_cast<int>(std::min<long long>(8, std::max<long long>(0, avail / k.stage_bytes)));
+  };
+  const int epi_groups = 3;
+  k.epi_groups = epi_groups;
+  int stages = stages_for(epi_groups);
+  if (t.stages > 0) stages = std::min(stages, t.stages);
+  if (stages < 2) return CONV3D_ERR_UNSUPPORTED;
+  k.stages = stages;
+  k.bar_off = k.stage_bytes * stages;
+  k.tiles_w = static_cast<int>(cdiv(Wo, k.tw));
+  k.tiles_h = Ho;
+  k.tiles_d = Do;
+  const long long tiles = (long long)k.tiles_w * Ho * Do * p->N * tiles_c;
+  if (tiles > 0x7fffffffLL) return CONV3D_ERR_UNSUPPORTED;
+  k.k_splits = 1;
+  k.stages_per_split = p->KT;
+  k.num_tiles = static_cast<int>(tiles);
+  k.tpu = 1;
+  const bool store_rows = p->out_layout == CONV3D_NDHWC
+                              ? p->Cout % 8 == 0
+                              : (Wo % 8 == 0 && !(p->epi & CONV3D_EPI_DEBUG_STORE_CONV));
+  k.tma_store = (store_rows && !(p->epi & (CONV3D_EPI_RESIDUAL | CONV3D_EPI_OUT_PAD_BR))) ? 1 : 0;
+  k.acc_cols = static_cast<int>(round_up(k.N, 32));
+  k.nbuf = (2 * k.acc_cols <= 512) ? 2 : 1;
+  int cols = 32;
+  while (cols < k.nbuf * k.acc_cols) cols *= 2;
+  k.tmem_cols = cols;
+  k.M_total = (long long)p->N * Do * Ho * Wo;
+  const int sms = num_sms();
+  const int grid = static_cast<int>(std::min<long long>(k.num_tiles, sms));
+  pl->ws_bytes = 0;
+  pl->grid = dim3(static_cast<unsigned>(grid), 1, 1);
+  k.epi_off = k.bar_off + 256;
+  k.norm_off = static_cast<uint32_t>(k.epi_off + (size_t)epi_groups * 4 * kEpiWarpBytes);
+  k.g_wres_off = static_cast<uint32_t>(round_up(k.norm_off, 1024));
+  pl->smem = 1024 + k.g_wres_off + wres_bytes;
+  if (pl->smem > kMaxSmem) return CONV3D_ERR_UNSUPPORTED;
+  pl->launches = 1;
+  pl->stage = false;
+  pl->Cst = C;
+  k.C = C;
+  k.D = p->D;
+  k.H = p->H;
+  k.W = p->W;
+  k.KT = p->KT;
+  k.KR = p->KR;
+  k.KS = p->KS;
+  k.st = p->stride[0];
+  k.sh = p->stride[1];
+  k.sw = 1;
   k.pt = p->pad[0].before;
   k.ph = p->pad[1].before;
   k.pw = p->pad[2].before;
@@ -796,6 +920,18 @@ int make_plan_conv(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
   if (tu) t = *tu;
   size_t off = 0;
   const int krs = p->KR * p->KS;
+  // Narrow input: gather the taps in the convolution kernel itself.  Automatic for
+  // one temporal tap (the T = 1 image layers: 3->96 at 1024^2 0.128 -> 0.105 ms);
+  // with KT > 1 every input row is expanded once per temporal tap, and the staged
+  // gather below, which expands each row once, measured faster (conv_in 3->128 on
+  // [17, 256, 256]: 0.151 ms staged, 0.189 ms in the kernel).
+  if ((t.im2col == 3 || (t.im2col == 0 && p->KT == 1)) && t.kernel != 1) {
+    const Plan before = *pl;
+    pl->cm = true;
+    rc = plan_gather(p, t, pl);
+    if (rc == CONV3D_OK || t.im2col == 3) return rc;
+    *pl = before;
+  }
   if (t.im2col != 2 && krs > 1 && p->Cin < 8 && (long long)krs * p->Cin <= 64 &&
       pl->Ho <= 65535 && (long long)p->N * p->D <= 65535) {
     // narrow input: gather the KR x KS spatial taps of every output pixel
@@ -959,6 +1095,36 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
     wgt_rows = k.sub_n;
     wgt_rows_last = k.sub_n;
     cp64 = k.cp64;
+  }
+  if (pl.cm && pl.cp.gather) {
+    // gather mode: the raw input as runs of 16-byte groups of 8 values, dims
+    // (8, W * C / 8, H, D, N) for NDHWC or (8, W / 8, H, D, N * C) for NCDHW; one box =
+    // g_row_bytes / 16 groups of one row
+    const ConvCMParams& k = pl.cp;
+    const bool cl = p->layout == CONV3D_NDHWC;
+    const cuuint64_t row = cl ? (cuuint64_t)p->W * p->Cin : (cuuint64_t)p->W;
+    const cuuint64_t gdim[5] = {8, row / 8, (cuuint64_t)p->H, (cuuint64_t)p->D,
+                                (cuuint64_t)p->N * (cl ? 1 : p->Cin)};
+    const cuuint64_t gstr[4] = {16, row * 2, row * 2 * p->H, row * 2 * p->H * p->D};
+    const cuuint32_t box[5] = {8, (cuuint32_t)(k.g_row_bytes / 16), 1, 1, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult rg = enc(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(xin), gdim,
+                      gstr, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rg != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
+    // the weights are read directly; valid maps of them fill the unused slots
+    const cuuint64_t Kt = (cuuint64_t)p->KT * p->KR * p->KS * k.cp64;
+    const cuuint64_t gdB[2] = {Kt, (cuuint64_t)p->Cout};
+    const cuuint64_t gsB[1] = {Kt * 2};
+    const cuuint32_t bxB[2] = {32, (cuuint32_t)k.wgt_rows};
+    const cuuint32_t esB[2] = {1, 1};
+    rg = enc(tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(p->w_packed), gdB, gsB,
+             bxB, esB, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rg != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
+    *tmBLast = *tmB;
+    if (half) half->act = half->wgt = half->wgt_last = *tmB;
+    return CONV3D_OK;
   }
   // activations: NDHWC bf16, dims (C, W, H, D, N); one box = kc channels x a run of
   // input pixels along W (element stride = the W stride of the convolution)
@@ -1148,7 +1314,7 @@ int conv3d_plan(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_plan
     r.stages_per_tile = k.stages_total;
     r.k_splits = k.k_splits;
   }
-  r.im2col = pl.im2col ? 1 : 0;
+  r.im2col = pl.im2col ? 1 : ((pl.cm && pl.cp.gather) ? 2 : 0);
   r.launches = pl.launches;
   r.grid = static_cast<int32_t>(pl.grid.x);
   *info = r;
@@ -1226,6 +1392,7 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
   if (pl.cm) {
     ConvCMParams kp = pl.cp;
     kp.epi.y = yk;
+    kp.g_wp = static_cast<const uint16_t*>(p->w_packed);
     if (kp.k_splits > 1) kp.partial = partial;
     if (kp.norm) kp.vscratch = reinterpret_cast<uint16_t*>(ws + pl.vscratch_off);
     vvc::CmOutMaps om;

@@ -159,36 +159,21 @@ __device__ __forceinline__ void epi_norm_silu16(const EpiParams& e, int c, int c
   }
 }
 
-// Positions along one axis of a haloed y that take output coordinate i (extent L;
-// at most one halo pixel before and after): i itself, plus the halo pixel that
-// reflects it (mode 2: -1 holds 1, L holds L - 2) or the zero halo pixel beside it
-// (mode 1: -1 beside 0, L beside L - 1).  zero[k] marks a zero fill.  Returns the
-// count (up to 3 when L == 3 under reflection).
-__device__ __forceinline__ int halo_axis(int i, int L, int before, int after, int mode,
-                                         int (&pos)[3], bool (&zero)[3]) {
-  int n = 0;
-  pos[n] = i;
-  zero[n++] = false;
+// Halo positions along one axis of a haloed y that take output coordinate i
+// besides i itself (extent L; at most one halo pixel before and after), as bits:
+// 1 = position -1, 4 = position L, with 2 / 8 marking a zero fill of that position.
+// Reflection (mode 2): -1 holds 1, L holds L - 2; zeros (mode 1): -1 beside 0, L
+// beside L - 1.
+__device__ __forceinline__ int halo_bits(int i, int L, int before, int after, int mode) {
+  int b = 0;
   if (mode == 2) {
-    if (before && i == 1) {
-      pos[n] = -1;
-      zero[n++] = false;
-    }
-    if (after && i == L - 2) {
-      pos[n] = L;
-      zero[n++] = false;
-    }
+    if (before && i == 1) b |= 1;
+    if (after && i == L - 2) b |= 4;
   } else if (mode == 1) {
-    if (before && i == 0) {
-      pos[n] = -1;
-      zero[n++] = true;
-    }
-    if (after && i == L - 1) {
-      pos[n] = L;
-      zero[n++] = true;
-    }
+    if (before && i == 0) b |= 3;
+    if (after && i == L - 1) b |= 12;
   }
-  return n;
+  return b;
 }
 
 // Element offset in a haloed NDHWC y of channel c of output pixel (n, d, h, w),
@@ -205,13 +190,23 @@ __device__ __forceinline__ long long halo_offset(const EpiParams& e, int n, int 
 template <class Put>
 __device__ __forceinline__ void halo_extras(const EpiParams& e, int n, int d, int h, int w, int c,
                                             Put&& put) {
-  int ph[3], pw[3];
-  bool zh[3], zw[3];
-  const int nh = halo_axis(h, e.Ho, e.h0, e.Hy - e.Ho - e.h0, e.h_mode, ph, zh);
-  const int nw = halo_axis(w, e.Wo, e.w0, e.Wy - e.Wo - e.w0, e.w_mode, pw, zw);
-  for (int a = 0; a < nh; ++a)
-    for (int b = 0; b < nw; ++b)
-      if (a || b) put(halo_offset(e, n, d, ph[a], pw[b], c), zh[a] || zw[b]);
+  const int bh = halo_bits(h, e.Ho, e.h0, e.Hy - e.Ho - e.h0, e.h_mode);
+  const int bw = halo_bits(w, e.Wo, e.w0, e.Wy - e.Wo - e.w0, e.w_mode);
+  if ((bh | bw) == 0) return;
+  // the halo columns of one row (hh), zero when the row or the column is a zero fill
+  auto cols = [&](int hh, bool zr) {
+    if (bw & 1) put(halo_offset(e, n, d, hh, -1, c), zr || (bw & 2));
+    if (bw & 4) put(halo_offset(e, n, d, hh, e.Wo, c), zr || (bw & 8));
+  };
+  cols(h, false);
+  if (bh & 1) {
+    put(halo_offset(e, n, d, -1, w, c), (bh & 2) != 0);
+    cols(-1, (bh & 2) != 0);
+  }
+  if (bh & 4) {
+    put(halo_offset(e, n, d, e.Ho, w, c), (bh & 8) != 0);
+    cols(e.Ho, (bh & 8) != 0);
+  }
 }
 
 // Writes y (and value_out / conv_out) for one chunk of one pixel; adds the

@@ -535,6 +535,46 @@ __device__ __forceinline__ void cm_block(const CmEpi& E, const CmTile& t, float*
   __syncwarp();
 }
 
+// Halo writes of a bulk-stored NDHWC block (32 pixels of output row hr from column wr,
+// channels cw..cw + 31, staged as bf16 [pixel][32] at yt) besides the bulk stores of
+// the block and of its reflected rows: zero halo rows beside the row, and the halo
+// columns of the block's pixels next to the row ends (in the row and its halo rows).
+// bh: halo_bits of the row.  16 bytes a lane.
+static __device__ __noinline__ void cm_halo_block(const EpiParams& e, const uint16_t* yt, int lane,
+                                           int nb, int od, int hr, int wr, int cw, int bh) {
+  const uint4 zero4 = make_uint4(0u, 0u, 0u, 0u);
+  const int part = lane & 3;
+  for (int side = 0; side < 2; ++side) {
+    const int hb = side ? (bh >> 2) : bh;  // bits of halo row -1 / Ho
+    if ((hb & 3) != 3) continue;           // only zero halo rows are written here
+    const int hh = side ? e.Ho : -1;
+    for (int u = lane; u < 128; u += 32)
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(e.y) +
+                                halo_offset(e, nb, od, hh, wr + (u >> 2), cw + 8 * (u & 3))) =
+          zero4;
+  }
+  for (int j = lane >> 2; j < 32; j += 8) {
+    const int bw = halo_bits(wr + j, e.Wo, e.w0, e.Wy - e.Wo - e.w0, e.w_mode);
+    if (!bw) continue;
+    const uint4 val = *reinterpret_cast<const uint4*>(yt + j * 32 + 8 * part);
+    uint16_t* y = static_cast<uint16_t*>(e.y);
+    for (int cs = 0; cs < 2; ++cs) {
+      const int b = cs ? (bw >> 2) : bw;
+      if (!(b & 1)) continue;
+      const int ww = cs ? e.Wo : -1;
+      const bool zc = (b & 2) != 0;
+      *reinterpret_cast<uint4*>(y + halo_offset(e, nb, od, hr, ww, cw + 8 * part)) =
+          zc ? zero4 : val;
+      if (bh & 1)
+        *reinterpret_cast<uint4*>(y + halo_offset(e, nb, od, -1, ww, cw + 8 * part)) =
+            (zc || (bh & 2)) ? zero4 : val;
+      if (bh & 4)
+        *reinterpret_cast<uint4*>(y + halo_offset(e, nb, od, e.Ho, ww, cw + 8 * part)) =
+            (zc || (bh & 8)) ? zero4 : val;
+    }
+  }
+}
+
 // ---- fused L2 norm over the channel row ---------------------------------------------
 //
 // The norm needs every output channel of a pixel, while a tile holds 128 of them.

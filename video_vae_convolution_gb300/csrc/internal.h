@@ -167,6 +167,16 @@ struct ConvCMParams {
   // wpref stages ahead of the one it loads (0 = off).  Small layers read every weight
   // slice from HBM once, and two pipeline stages cannot hide that latency.
   int wpref;
+  // Narrow-input gather mode (gather = 1; C = the real input channels, KR * KS * C <=
+  // 32): one stage per temporal tap kt over tiles of one output row (rh = 1, direct
+  // pixel order).  The activation map views the input as runs of 16-byte groups
+  // (dims 8, W * C / 8 or W / 8, H, D, N or N * C); a stage's raw region (g_raw_off
+  // past the operand rows) receives g_planes * KR rows of g_row_bytes; the expansion
+  // turns them into 64-byte operand rows of K = g_K values.  The weights of every
+  // (channel tile, kt) stay resident at g_wres_off, read once from g_wp.
+  int gather, g_K, g_cpp, g_planes, g_row_bytes;
+  uint32_t g_raw_off, g_wres_off;
+  const uint16_t* g_wp;     // packed weights [Cout][KT][KR][KS][cp64]
 };
 
 // Tensor maps of the paired last-chunk stages: 32-channel boxes, 64-byte swizzle.
