@@ -380,12 +380,13 @@ def time_alone(c, stream, flush, reps, warm=2):
 
 
 def other_layers(dev, stream, flush, pk, reps):
-    """Per-call rows of the Wan-like chain (both layouts), the fused 160 blocks and
-    the T=1 image-VAE layers (both layouts), each call timed alone."""
+    """Per-call rows of the Wan-like chain (both layouts), the fused 160 blocks, the
+    T=1 image-VAE layers (both layouts) and the decoder's upsample convolutions (x2
+    nearest upsample fused into the convolution), each call timed alone."""
     import video_vae_convolution_gb300 as vvc
     rows = []
     sums = {}
-    for name in ("wan", "fused160", "t1"):
+    for name in ("wan", "fused160", "t1", "up2"):
         w = wl.all_workloads()[name]
         for call in w.calls:
             for lay, out_lay in w.layouts:
@@ -394,7 +395,7 @@ def other_layers(dev, stream, flush, pk, reps):
                 c = vvc.Conv3d(inp["x"], wp, call.Cout, call.kernel, call.stride, call.pads,
                                lay, out_lay, call.epi, bias=inp["bias"],
                                residual=inp["residual"], residual_bias=inp["residual_bias"],
-                               gamma=inp["gamma"])
+                               gamma=inp["gamma"], input_upsample=call.upsample)
                 ms = time_alone(c, stream, flush, reps)
                 rows.append(layer_row(call, ms, pk, c.launches, lay, name))
                 key = (name, rows[-1]["layout"])
@@ -641,9 +642,11 @@ def run_case(args):
         # padded output + two-frame cache after the fused norm, P history frames
         epi |= vvc.EPI_PAD_CACHE
         extra = {"history_frames": args.pad_cache}
-    c = vvc.Conv3d(inp["x"].to(dev), wp, call.Cout, call.kernel, call.stride, call.pads, lay, lay,
-                   epi, bias=g("bias"), residual=g("residual"),
-                   residual_bias=g("residual_bias"), gamma=g("gamma"), tuning=tun, **extra)
+    out_lay = wl.NDHWC if call.upsample else lay
+    c = vvc.Conv3d(inp["x"].to(dev), wp, call.Cout, call.kernel, call.stride, call.pads, lay,
+                   out_lay, epi, bias=g("bias"), residual=g("residual"),
+                   residual_bias=g("residual_bias"), gamma=g("gamma"), tuning=tun,
+                   input_upsample=call.upsample, **extra)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):

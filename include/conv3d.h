@@ -142,7 +142,16 @@ enum {
  *             'reflect' padding of the output would (needs Ho, Wo >= 2),
  *             CONV3D_PAD_ZERO with zeros.  Requires NDHWC output, Cout % 8 == 0,
  *             and none of L2NORM_SILU, OUT_PAD_BR, PAD_CACHE.  residual, value_out
- *             and conv_out keep the unpadded output shape. */
+ *             and conv_out keep the unpadded output shape.
+ *  input_upsample   0, or 2: the convolution reads the nearest-exact x2 upsampling of x
+ *             along H and W (ROCm/FlyDSL PR "[Flydsl] Add Qwen-Image VAE classic conv
+ *             shapes to conv3d tests", "Upsample Conv2d": the decoder's 3x3 convolution
+ *             after nearest-exact x2), without writing the upsampled tensor: x is the
+ *             low-resolution [N, D, H, W, Cin] (or NCDHW) tensor, and the convolution
+ *             geometry (output extent, padding) applies to the [2H, 2W] upsampled grid.
+ *             Requires KR = KS = 3, H and W stride 1 and zero padding (1, 1) along H and
+ *             W (output [.., 2H, 2W]), NDHWC output, Cout % 8 == 0, and no RESIDUAL,
+ *             L2NORM_SILU, SAVE_VALUE, OUT_PAD_BR, PAD_CACHE or out_halo. */
 typedef struct {
   const void* x;
   int32_t layout;
@@ -165,6 +174,7 @@ typedef struct {
   void* cache_out;
   int32_t history_frames;
   conv3d_pad out_halo[3];
+  int32_t input_upsample;
 } conv3d_params;
 
 /* Optional plan overrides (tests and tuning).  0 (or -1 where noted) = automatic. */

@@ -54,7 +54,7 @@ class GpuCall:
     """Runs one workload call on the GPU; keeps CPU copies of inputs and outputs."""
 
     def __init__(self, call: wl.ConvCall, inp: dict, layout=wl.NDHWC, out_layout=wl.NDHWC,
-                 tuning=None, debug_conv=True, extra_epi=0):
+                 tuning=None, debug_conv=True, extra_epi=0, extra_kw=None):
         self.call, self.inp, self.layout, self.out_layout = call, inp, layout, out_layout
         dev = torch.device("cuda")
         x = inp["x"].to(dev)
@@ -64,7 +64,8 @@ class GpuCall:
         g = lambda k: None if inp[k] is None else inp[k].to(dev).contiguous()
         self.c = vvc.Conv3d(x, self.w_packed, call.Cout, call.kernel, call.stride, call.pads,
                             layout, out_layout, epi, bias=g("bias"), residual=g("residual"),
-                            residual_bias=g("residual_bias"), gamma=g("gamma"), tuning=tuning)
+                            residual_bias=g("residual_bias"), gamma=g("gamma"), tuning=tuning,
+                            **(extra_kw or {}))
         rc = self.c.run()
         assert rc == vvc.OK, vvc._lib().conv3d_status_string(rc)
         torch.cuda.synchronize()

@@ -81,7 +81,7 @@ class Params(ctypes.Structure):
         ("value_out", ctypes.c_void_p), ("conv_out", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("cache_out", ctypes.c_void_p), ("history_frames", ctypes.c_int32),
-        ("out_halo", Pad * 3),
+        ("out_halo", Pad * 3), ("input_upsample", ctypes.c_int32),
     ]
 
 
@@ -241,10 +241,11 @@ class Conv3d:
                  pads=((0, 0, PAD_ZERO),) * 3, layout=NDHWC, out_layout=NDHWC, epi=0,
                  bias=None, residual=None, residual_bias=None, gamma=None, y=None,
                  value_out=None, conv_out=None, workspace=None, tuning: Optional[Tuning] = None,
-                 cache_out=None, history_frames=0, out_halo=None):
+                 cache_out=None, history_frames=0, out_halo=None, input_upsample=0):
         N, C, D, H, W = _dims(x, layout)
         KT, KR, KS = kernel
-        Do, Ho, Wo = out_dims(D, H, W, kernel, stride, pads)
+        up = 2 if input_upsample == 2 else 1  # the convolution reads the x2 upsampled grid
+        Do, Ho, Wo = out_dims(D, H * up, W * up, kernel, stride, pads)
         dev = x.device
         self.dims = (N, C, D, H, W)
         self.out_dims = (Do, Ho, Wo)
@@ -291,6 +292,7 @@ class Conv3d:
         if out_halo is not None:
             for i in range(3):
                 p.out_halo[i].before, p.out_halo[i].after, p.out_halo[i].mode = out_halo[i]
+        p.input_upsample = input_upsample
         self.out_halo = out_halo
         self.cache_out = cache_out
         self.tuning = tuning

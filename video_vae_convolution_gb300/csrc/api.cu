@@ -152,7 +152,11 @@ int validate_shape(const conv3d_params* p, int* Do, int* Ho, int* Wo) {
     if (p->pad[i].mode != CONV3D_PAD_ZERO && p->pad[i].mode != CONV3D_PAD_REFLECT)
       return CONV3D_ERR_INVALID_ARG;
   }
-  const int L[3] = {p->D, p->H, p->W};
+  if (p->input_upsample != 0 && p->input_upsample != 2) return CONV3D_ERR_INVALID_ARG;
+  const int up = p->input_upsample == 2 ? 2 : 1;  // the convolution reads the x2 grid
+  if ((long long)p->H * up > 0x3fffffffLL || (long long)p->W * up > 0x3fffffffLL)
+    return CONV3D_ERR_INVALID_ARG;
+  const int L[3] = {p->D, p->H * up, p->W * up};
   const int K[3] = {p->KT, p->KR, p->KS};
   int o[3];
   for (int i = 0; i < 3; ++i) {
@@ -189,6 +193,16 @@ int validate_shape(const conv3d_params* p, int* Do, int* Ho, int* Wo) {
         return CONV3D_ERR_INVALID_ARG;
       if (hl[i].mode == CONV3D_PAD_REFLECT && o[i] < 2) return CONV3D_ERR_INVALID_ARG;
     }
+  }
+  if (p->input_upsample == 2) {
+    // x2 nearest upsampled input before a 3x3, pad-1, stride-1 (along H and W) conv
+    if (p->KR != 3 || p->KS != 3 || p->stride[1] != 1 || p->stride[2] != 1 ||
+        p->pad[1].before != 1 || p->pad[1].after != 1 || p->pad[1].mode != CONV3D_PAD_ZERO ||
+        p->pad[2].before != 1 || p->pad[2].after != 1 || p->pad[2].mode != CONV3D_PAD_ZERO ||
+        p->out_layout != CONV3D_NDHWC || p->Cout % 8 != 0 || has_halo(p) ||
+        (e & (CONV3D_EPI_RESIDUAL | CONV3D_EPI_L2NORM_SILU | CONV3D_EPI_SAVE_VALUE |
+              CONV3D_EPI_OUT_PAD_BR | CONV3D_EPI_PAD_CACHE)))
+      return CONV3D_ERR_INVALID_ARG;
   }
   if ((e & CONV3D_EPI_RESIDUAL_BIAS) && !(e & CONV3D_EPI_RESIDUAL)) return CONV3D_ERR_INVALID_ARG;
   if ((e & CONV3D_EPI_OUT_PAD_BR) && (e & CONV3D_EPI_L2NORM_SILU)) return CONV3D_ERR_INVALID_ARG;
@@ -251,6 +265,7 @@ void fill_epi(const conv3d_params* p, const Plan& pl, EpiParams* e) {
   e->w0 = p->out_halo[2].before;
   e->h_mode = p->out_halo[1].mode == CONV3D_PAD_REFLECT ? 2 : 1;
   e->w_mode = p->out_halo[2].mode == CONV3D_PAD_REFLECT ? 2 : 1;
+  e->up2 = p->input_upsample == 2 ? 1 : 0;
 }
 
 // Split of the reduction so that small layers still fill the GPU.  Each split
@@ -366,7 +381,8 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
     // its reduction) finishes with its slowest item: fewer rows per tile (a smaller N)
     // are faster as long as the items still fit in one wave.
     {
-      const long long per_tile = (long long)Do * p->N * cdiv(p->Cout, 128);
+      const long long per_tile =
+          (long long)Do * p->N * cdiv(p->Cout, 128) * (p->input_upsample == 2 ? 4 : 1);
       const int nt = static_cast<int>(cdiv(Wo, tw));
       const int pitch = static_cast<int>(round_up(tw + p->KS - 1, 8));
       auto items = [&](int r) { return nt * cdiv(Ho, r) * per_tile; };
@@ -425,9 +441,11 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   // Cout <= 16 (the RGB output convolution: 3 of 128 channel rows would be real);
   // measured slower than channel-major tiles on the 32- to 96-channel layers, where
   // it runs only on request (conv3d_tuning.kernel = 3).
-  const bool pm = t.kernel == 3 ||
-                  (t.kernel == 0 && p->Cout <= 16 && !(p->epi & CONV3D_EPI_L2NORM_SILU) &&
-                   !has_halo(p));
+  const bool up2 = p->input_upsample == 2;
+  if (up2 && (!halo || flat || t.kernel == 3)) return CONV3D_ERR_UNSUPPORTED;
+  const bool pm = !up2 && (t.kernel == 3 ||
+                           (t.kernel == 0 && p->Cout <= 16 &&
+                            !(p->epi & CONV3D_EPI_L2NORM_SILU) && !has_halo(p)));
   if (pm && p->Cout > 128) return CONV3D_ERR_UNSUPPORTED;
   k.pm = pm ? 1 : 0;
   if (pm) {
@@ -506,7 +524,10 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   }
   k.tiles_w = static_cast<int>(flat ? cdiv(q_total, tw) : cdiv(Wo, tw));
   k.tiles_h = static_cast<int>(flat ? 1 : cdiv(Ho, rh));
-  const long long tiles = (long long)k.tiles_w * k.tiles_h * k.tiles_d * p->N * k.tiles_c;
+  k.up2 = up2 ? 1 : 0;
+  k.ncls = up2 ? 4 : 1;
+  const long long tiles =
+      (long long)k.tiles_w * k.tiles_h * k.tiles_d * p->N * k.tiles_c * k.ncls;
   const int sms = num_sms();
   int per = 0;
   // with the fused norm the channel tiles of a pixel tile share a CTA, so the
@@ -522,8 +543,8 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   const int last_ch = pl->Cst - (k.n_chunks - 1) * kc;
   const bool reflect_w_pad =
       p->pad[2].mode == CONV3D_PAD_REFLECT && (p->pad[2].before || p->pad[2].after);
-  const bool pair_ok = t.pair != 2 && !pm && halo && kc == 64 && last_ch >= 1 && last_ch <= 32 &&
-                       n_pairs >= 2 && !reflect_w_pad;
+  const bool pair_ok = t.pair != 2 && !pm && !up2 && halo && kc == 64 && last_ch >= 1 &&
+                       last_ch <= 32 && n_pairs >= 2 && !reflect_w_pad;
   int splits = 0;
   if (pair_ok) {
     const int total = n_pairs * (k.n_chunks - 1) + (n_pairs + 1) / 2;
@@ -533,7 +554,11 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
       k.stages_total = total;
     }
   }
-  if (!k.pair) splits = choose_splits(t, par, k.stages_total, sms, &per);
+  if (!k.pair) {
+    conv3d_tuning t1 = t;
+    if (up2) t1.k_splits = 1;  // the split reduction writes plain output pixels
+    splits = choose_splits(t1, par, k.stages_total, sms, &per);
+  }
   k.n_pairs = n_pairs;
   k.k_splits = splits;
   k.stages_per_split = per;
@@ -549,7 +574,8 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
                               : (Wo % 8 == 0 && !(p->epi & CONV3D_EPI_DEBUG_STORE_CONV));
   k.tma_store = (store_rows && splits == 1 && !pm &&
                  !(p->epi & (CONV3D_EPI_RESIDUAL | CONV3D_EPI_L2NORM_SILU |
-                             CONV3D_EPI_OUT_PAD_BR)))
+                             CONV3D_EPI_OUT_PAD_BR)) &&
+                 !(up2 && (p->epi & CONV3D_EPI_DEBUG_STORE_CONV)))
                     ? 1
                     : 0;
   k.acc_cols = pm ? k.pm_halves * k.pm_cols : static_cast<int>(round_up(k.N, 32));
@@ -918,6 +944,28 @@ int make_plan_conv(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
   if (rc) return rc;
   conv3d_tuning t{};
   if (tu) t = *tu;
+  if (p->input_upsample == 2) {
+    // x2 upsampled input: the channel-major kernel tiles the low-resolution grid (a
+    // 3x3, pad-1 convolution of it, once per parity class); the output is twice as
+    // large along H and W
+    if (t.kernel == 1 || t.kernel == 3) return CONV3D_ERR_UNSUPPORTED;
+    pl->stage = (p->layout == CONV3D_NCDHW) || (p->Cin % 8 != 0);
+    pl->Cst = static_cast<int>(round_up(p->Cin, 8));
+    size_t off0 = 0;
+    if (pl->stage) {
+      pl->stage_off = 0;
+      pl->stage_bytes = (size_t)p->N * p->D * p->H * p->W * pl->Cst * 2;
+      off0 = static_cast<size_t>(round_up(pl->stage_bytes, 256));
+    }
+    const int Ho = pl->Ho, Wo = pl->Wo;
+    pl->Ho = p->H;
+    pl->Wo = p->W;
+    pl->cm = true;
+    rc = plan_cm(p, t, pl, off0);
+    pl->Ho = Ho;
+    pl->Wo = Wo;
+    return rc;
+  }
   size_t off = 0;
   const int krs = p->KR * p->KS;
   // Narrow input: gather the taps in the convolution kernel itself.  Automatic for
@@ -1239,6 +1287,18 @@ int encode_out_maps(const conv3d_params* p, const Plan& pl, vvc::CmOutMaps* om) 
   }
   om->val = om->y;
   om->conv = om->y;
+  for (int k = 0; k < 4; ++k) om->ycls[k] = om->y;
+  if (p->input_upsample == 2) {
+    // the outputs of parity class k = 2 ph + pw: [N, Do, Ho / 2, Wo / 2, C] at rows
+    // 2 h + ph, columns 2 w + pw of y
+    const cuuint64_t Hl = Ho / 2, Wl = Wo / 2;
+    const cuuint64_t cdim[5] = {C, Wl, Hl, Do, (cuuint64_t)p->N};
+    const cuuint64_t cstr[4] = {C * 4, C * 4 * Wo, C * 2 * Wo * Ho, C * 2 * Wo * Ho * Do};
+    for (int k = 0; k < 4; ++k) {
+      void* base = static_cast<uint8_t*>(p->y) + ((size_t)(k >> 1) * Wo + (k & 1)) * C * 2;
+      if (!one_g(base, cdim, cstr, &om->ycls[k])) return CONV3D_ERR_CUDA;
+    }
+  }
   if ((p->epi & CONV3D_EPI_SAVE_VALUE) && !one(p->value_out, &om->val)) return CONV3D_ERR_CUDA;
   if ((p->epi & CONV3D_EPI_DEBUG_STORE_CONV) && !one(p->conv_out, &om->conv))
     return CONV3D_ERR_CUDA;

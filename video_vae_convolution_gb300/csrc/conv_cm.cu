@@ -35,18 +35,21 @@ cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
   // the plan never pairs reflect-W or pixel-major layers
   if (p.pair && (inner || p.pm)) return cudaErrorInvalidValue;
   if (p.gather && (p.pair || p.pm)) return cudaErrorInvalidValue;
-  const int which = p.gather ? 4 : (p.pm ? 3 : (p.pair ? 1 : (inner ? 2 : 0)));
+  if (p.up2 && (p.pair || p.pm || p.gather || inner || p.epi.halo || !p.halo))
+    return cudaErrorInvalidValue;
+  const int which = p.up2 ? 5 : (p.gather ? 4 : (p.pm ? 3 : (p.pair ? 1 : (inner ? 2 : 0))));
   if (p.epi.halo)
     return launch_conv_cm_halo(tmAct, tmWgt, tmWgtLast, om, half, p, which, grid, smem_bytes,
                                stream);
   using Kernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CmOutMaps, CmHalfMaps,
                           ConvCMParams);
-  const Kernel kernels[5] = {conv_cm_kernel<false, false, false, false, false>,
-                             conv_cm_kernel<true, false, false, false, false>,
-                             conv_cm_kernel<false, true, false, false, false>,
-                             conv_cm_kernel<false, false, true, false, false>,
-                             conv_cm_kernel<false, false, false, true, false>};
-  static int opted_in[5][kMaxDevices] = {};
+  const Kernel kernels[6] = {conv_cm_kernel<false, false, false, false, false, false>,
+                             conv_cm_kernel<true, false, false, false, false, false>,
+                             conv_cm_kernel<false, true, false, false, false, false>,
+                             conv_cm_kernel<false, false, true, false, false, false>,
+                             conv_cm_kernel<false, false, false, true, false, false>,
+                             conv_cm_kernel<false, false, false, false, false, true>};
+  static int opted_in[6][kMaxDevices] = {};
   cudaError_t err = opt_in_smem(kernels[which], opted_in[which]);
   if (err != cudaSuccess) return err;
   kernels[which]<<<grid, 128 + 128 * p.epi_groups, smem_bytes, stream>>>(tmAct, tmWgt, tmWgtLast,

@@ -23,11 +23,11 @@ cudaError_t launch_conv_cm_halo(const CUtensorMap& tmAct, const CUtensorMap& tmW
   using Kernel = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CmOutMaps, CmHalfMaps,
                           ConvCMParams);
   if (which < 0 || which > 4) return cudaErrorInvalidValue;
-  const Kernel kernels[5] = {conv_cm_kernel<false, false, false, false, true>,
-                             conv_cm_kernel<true, false, false, false, true>,
-                             conv_cm_kernel<false, true, false, false, true>,
-                             conv_cm_kernel<false, false, true, false, true>,
-                             conv_cm_kernel<false, false, false, true, true>};
+  const Kernel kernels[5] = {conv_cm_kernel<false, false, false, false, true, false>,
+                             conv_cm_kernel<true, false, false, false, true, false>,
+                             conv_cm_kernel<false, true, false, false, true, false>,
+                             conv_cm_kernel<false, false, true, false, true, false>,
+                             conv_cm_kernel<false, false, false, true, true, false>};
   static int opted_in[5][kMaxDevices] = {};
   cudaError_t err = opt_in_smem(kernels[which], opted_in[which]);
   if (err != cudaSuccess) return err;

@@ -62,7 +62,7 @@ struct IntC {
 };
 
 struct TileCoord {
-  int ct, split, twi, thi, od, nb;
+  int ct, cls, split, twi, thi, od, nb;
 };
 
 // Tile index, fastest first: channel tile, split, output depth, W tile, H tile,
@@ -73,6 +73,11 @@ __device__ __forceinline__ TileCoord decode_tile(const ConvCMParams& p, int tile
   TileCoord c;
   c.ct = tile % p.tiles_c;
   tile /= p.tiles_c;
+  c.cls = 0;
+  if (p.ncls > 1) {  // parity class of an x2 upsampled input
+    c.cls = tile % p.ncls;
+    tile /= p.ncls;
+  }
   c.split = tile % p.k_splits;
   tile /= p.k_splits;
   c.od = tile % p.tiles_d;
@@ -181,11 +186,12 @@ __device__ __forceinline__ int cta_tile(const ConvCMParams& p, int l) {
 // kPair: the paired last-chunk schedule (ConvCMParams::pair).  kInner: reflect-W
 // halo stages whose inner W taps run before the edge patch.  kPM: pixel-major mode.
 // kGather: narrow-input gather mode (ConvCMParams::gather).  kHalo: the output goes
-// into a haloed tensor (EpiParams::halo).
+// into a haloed tensor (EpiParams::halo).  kUp2: the input is read x2 upsampled
+// (ConvCMParams::up2).
 // They are template parameters so that the plain instance keeps the shortest
 // producer and MMA-issue loops (the per-stage checks of the first two modes cost
 // 4-5 % each on layers that use neither).
-template <bool kPair, bool kInner, bool kPM, bool kGather, bool kHalo>
+template <bool kPair, bool kInner, bool kPM, bool kGather, bool kHalo, bool kUp2>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     conv_cm_kernel(const __grid_constant__ CUtensorMap tmAct,
                    const __grid_constant__ CUtensorMap tmWgt,
@@ -543,6 +549,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               for (int i = 0; i < p.rh; ++i) {
                 const int ho = h0 + i;
                 int h_in = ho * p.sh + sc.r - p.ph;
+                // x2 upsampled input: class row offsets (-1, 0, 0) or (0, 0, 1)
+                if (kUp2) h_in = ho + ((tc.cls >> 1) ? (sc.r == 2 ? 1 : 0) : (sc.r == 0 ? -1 : 0));
                 if (p.reflect_h && ho < p.epi.Ho) h_in = reflect_coord(h_in, p.H);
                 for (int b = 0; b < p.nbox; ++b)
                   tma_load_5d(act + static_cast<uint32_t>((i * p.run_pitch + b * p.box_w) *
@@ -680,7 +688,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             const bool full4 = kk_n == 4;
             auto issue_tap = [&](int tl) {
               const uint32_t a_t = a_lo + tl * w_tap_step;
-              const uint32_t b_t = b_lo + tl * a_tap_step;
+              // x2 upsampled input: W taps read the run shifted by (0, 1, 1) or (1, 1, 2)
+              const int tsh = kUp2 ? (tl == 1 ? 1 : (tl == 0 ? (tc.cls & 1) : 1 + (tc.cls & 1))) : tl;
+              const uint32_t b_t = b_lo + tsh * a_tap_step;
               if (full4) {
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
@@ -866,6 +876,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     E.sqrt_c = p.epi.sqrt_c;
     E.M_total = p.M_total;
     E.halo = kHalo;  // compile-time: calls without a halo carry none of its code
+    E.up2 = kUp2;
     E.ep = &p.epi;
     float* st = reinterpret_cast<float*>(smem + p.epi_off) + (warp - kWarpEpi0) * kStageFloats;
     const int nbuf = p.nbuf, acc_cols = p.acc_cols, Ncols = p.N;
@@ -885,6 +896,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       t.woff = p.flat ? 0 : t.w0;
       t.jlim = p.flat ? p.W : p.tw;
       t.vrows = p.flat3 ? p.H : 0;
+      t.cls = tc.cls;
       return t;
     };
     if (kPM) {
@@ -1024,7 +1036,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                                                 p.epi.h_mode)
                                     : 0;
               if (lane == 0) {
-                tma_store_5d(&om.y, smem_u32(yt), cw, wr, hr, od, tc.nb);
+                tma_store_5d(kUp2 ? &om.ycls[tc.cls] : &om.y, smem_u32(yt), cw, wr, hr, od, tc.nb);
                 if ((bh & 3) == 1)
                   tma_store_5d(&om.yfull, smem_u32(yt), cw, wr + p.epi.w0, p.epi.h0 - 1,
                                od + p.epi.d0, tc.nb);

@@ -39,6 +39,7 @@ struct CmEpi {
   long long M_total;
   bool halo;              // y is haloed (NDHWC): addresses and extras from *ep
   const EpiParams* ep;    // the launch's epilogue parameters (kernel parameter space)
+  bool up2;               // x2 upsampled input: y is [N, Do, 2 Ho, 2 Wo, Cout]
 };
 
 struct CmTile {
@@ -54,7 +55,17 @@ struct CmTile {
   // vrows > 0: the tile runs over the flattened volume; its row index counts rows of
   // the input volume, frame = row / vrows (the input height), row in frame = the rest
   int vrows;
+  int cls;  // parity class of an x2 upsampled input (output row 2 h + cls / 2, column
+            // 2 w + cls % 2)
 };
+
+// Element offset of channel c of tile output (nd = n * Do + d, h, w) in y and conv_out
+// when the input is x2 upsampled: the class's pixel of the [2 Ho, 2 Wo] output.
+__device__ __forceinline__ long long cm_up2_offset(const CmEpi& E, const CmTile& t, long long nd,
+                                                   int h, int w, int c) {
+  return ((nd * (2LL * E.Ho) + 2 * h + (t.cls >> 1)) * (2LL * E.Wo) + 2 * w + (t.cls & 1)) *
+             E.Cout + c;
+}
 
 // Output frame and row of tile row index hv (see CmTile::vrows).
 __device__ __forceinline__ void cm_frame_row(const CmTile& t, int hv, int& d, int& h) {
@@ -218,8 +229,11 @@ __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, 
     const int wcol = t.woff + jb + (lane >> 2);
     const long long o0 = ((nd * E.Ho + hrow) * E.Wo + wcol) * E.Cout + ch.c0;
     // y offset of the thread's first pixel (a haloed y has its own geometry)
-    const long long oy0 = E.halo ? halo_offset(*E.ep, t.nb, fd, hrow, wcol, ch.c0) : o0;
+    const long long oy0 = E.halo  ? halo_offset(*E.ep, t.nb, fd, hrow, wcol, ch.c0)
+                          : E.up2 ? cm_up2_offset(E, t, nd, hrow, wcol, ch.c0)
+                                  : o0;
     const long long step = 8LL * E.Cout;  // the thread's next pixel is 8 pixels on
+    const long long ystep = E.up2 ? 2 * step : step;  // (every other output pixel)
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int pl = 8 * k + (lane >> 2);
@@ -259,9 +273,10 @@ __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, 
         v.w = pack_bf16x2(__fadd_rn(bf16x2_lo(v.w), bf16x2_lo(sk.w)),
                           __fadd_rn(bf16x2_hi(v.w), bf16x2_hi(sk.w)));
       }
-      *reinterpret_cast<uint4*>(E.y + oy0 + k * step) = v;
+      *reinterpret_cast<uint4*>(E.y + oy0 + k * ystep) = v;
       if (E.flags & EPI_SAVE_VALUE) *reinterpret_cast<uint4*>(E.val + o) = v;
-      if (E.flags & EPI_DEBUG_STORE_CONV) *reinterpret_cast<uint4*>(E.conv + o) = cb;
+      if (E.flags & EPI_DEBUG_STORE_CONV)
+        *reinterpret_cast<uint4*>(E.conv + (E.up2 ? oy0 + k * ystep : o)) = cb;
       if (E.halo) {
         halo_extras(*E.ep, t.nb, fd, hrow, wcol + 8 * k, ch.c0, [&](long long off, bool zero) {
           *reinterpret_cast<uint4*>(E.y + off) = zero ? make_uint4(0u, 0u, 0u, 0u) : v;
@@ -311,8 +326,16 @@ __device__ __forceinline__ void cm_block_ndhwc(const CmEpi& E, const CmTile& t, 
     uint16_t vb[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) vb[e] = bf16_bits(v[e]);
-    const long long yo = E.halo ? halo_offset(*E.ep, t.nb, d, h, w, ch.c0)
-                                : ((nd * E.Hy + h) * E.Wy + w) * E.Cout + ch.c0;
+    const long long yo = E.halo  ? halo_offset(*E.ep, t.nb, d, h, w, ch.c0)
+                         : E.up2 ? cm_up2_offset(E, t, nd, h, w, ch.c0)
+                                 : ((nd * E.Hy + h) * E.Wy + w) * E.Cout + ch.c0;
+    if (E.up2) {
+      // x2 upsampled input (Cout % 8 == 0; no residual or saved value): y and the
+      // debug conv store take the class's output pixel
+      reinterpret_cast<uint4*>(E.y + yo)[0] = pack8(vb);
+      if (E.flags & EPI_DEBUG_STORE_CONV) reinterpret_cast<uint4*>(E.conv + yo)[0] = pack8(cb);
+      continue;
+    }
     if (E.halo) {
       // (a haloed y has Cout % 8 == 0, so the thread's 8 channels are one 16-byte group)
       const uint4 pv = pack8(vb);

@@ -62,6 +62,10 @@ struct EpiParams {
   // the d0 leading and trailing frames are not written.
   int halo;
   int Dy, Hy, Wy, d0, h0, w0, h_mode, w_mode;
+  // x2 upsampled input (up2 = 1): Ho and Wo are the extents of the low-resolution
+  // grid the tiles cover; y (and conv_out) is [N, Do, 2 Ho, 2 Wo, Cout] and the tile of
+  // parity class cls writes output (2 h + cls / 2, 2 w + cls % 2)
+  int up2;
 };
 
 // Implicit-GEMM convolution on tcgen05 (one CTA = R M-tiles x BN output channels).
@@ -174,6 +178,11 @@ struct ConvCMParams {
   // past the operand rows) receives g_planes * KR rows of g_row_bytes; the expansion
   // turns them into 64-byte operand rows of K = g_K values.  The weights of every
   // (channel tile, kt) stay resident at g_wres_off, read once from g_wp.
+  // x2 upsampled input (up2): the tiles run over the low-resolution grid once per
+  // parity class (ncls = 4, class index next to the channel tile in the tile order);
+  // class cls reads low-res row h + (-1, 0, 0)[r] (cls / 2 == 0) or h + (0, 0, 1)[r],
+  // and its W taps are the run views shifted by (0, 1, 1) or (1, 1, 2) (cls % 2)
+  int up2, ncls;
   int gather, g_K, g_cpp, g_planes, g_row_bytes;
   uint32_t g_raw_off, g_wres_off;
   const uint16_t* g_wp;     // packed weights [Cout][KT][KR][KS][cp64]
@@ -191,6 +200,7 @@ struct CmHalfMaps {
 struct CmOutMaps {
   CUtensorMap y, val, conv;
   CUtensorMap yfull;  // haloed y: the whole tensor (halo rows that copy a block)
+  CUtensorMap ycls[4];  // x2 upsampled input: y seen as the outputs of one parity class
 };
 
 }  // namespace vvc

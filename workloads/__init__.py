@@ -15,6 +15,8 @@ Workloads are shaped like the VAE convolution layers the source pages list:
   "Fused Conv3D + Bias + Residual + RMSNorm + SiLU", "Requirements" table).
 * "t1": the T=1 image-VAE convolutions (ROCm/FlyDSL PR "[Flydsl] Add
   Qwen-Image VAE classic conv shapes to conv3d tests", "Test shapes").
+* "up2": the decoder's 3x3 convolutions after a nearest-exact x2 upsample (same
+  PR, "Upsample Conv2d"), with the upsample fused into the convolution's input.
 * "tiny": a small correctness case.
 
 Seeds: seed = 1000 * workload_id + call_index, plus 0 for x, 1 for W, 2 for
@@ -46,7 +48,7 @@ EPI_L2NORM_SILU = 8
 EPI_SAVE_VALUE = 16
 EPI_OUT_PAD_BR = 32
 
-WORKLOAD_IDS = {"tiny": 1, "wan": 2, "ladder": 3, "fused160": 4, "t1": 5, "test": 9}
+WORKLOAD_IDS = {"tiny": 1, "wan": 2, "ladder": 3, "fused160": 4, "t1": 5, "up2": 6, "test": 9}
 
 
 @dataclass
@@ -67,6 +69,7 @@ class ConvCall:
     zero_pad_br_input: bool = False  # input made by ZeroPad2d((0,1,0,1))
     rank4: bool = False              # originally a 2-D (NCHW) convolution
     index: int = 0
+    upsample: int = 0                # 2: the convolution reads the x2 nearest upsample of x
 
     @property
     def K(self) -> int:
@@ -75,7 +78,8 @@ class ConvCall:
 
     def out_dims(self):
         kt, kr, ks = self.kernel
-        L = (self.D, self.H, self.W)
+        up = 2 if self.upsample == 2 else 1
+        L = (self.D, self.H * up, self.W * up)
         K = (kt, kr, ks)
         return tuple((L[i] + self.pads[i][0] + self.pads[i][1] - K[i]) // self.stride[i] + 1
                      for i in range(3))
@@ -91,7 +95,8 @@ class ConvCall:
         return 2 * self.M * self.Cout * self.K
 
     def bytes(self) -> int:
-        """Algorithmic bytes: input + output (+ residual, + value) + weights, once."""
+        """Algorithmic bytes: input + output (+ residual, + value) + weights, once (the
+        input of an upsampling call is the low-resolution tensor)."""
         Do, Ho, Wo = self.out_dims()
         out_elems = self.N * Do * Ho * Wo * self.Cout
         if self.epi & EPI_OUT_PAD_BR:
@@ -206,9 +211,19 @@ def t1() -> Workload:
     return Workload("t1", calls, layouts=[(NDHWC, NDHWC), (NCDHW, NCDHW)])
 
 
+def up2() -> Workload:
+    p = _same2d()
+    spec = [("dec_d0_384_256", 384, 128, 192), ("dec_d1_384_512", 384, 256, 192),
+            ("dec_d2_192_1024", 192, 512, 96)]
+    calls = [ConvCall(name, 1, cin, 1, hw, hw, cout, kernel=(1, 3, 3), pads=p, epi=EPI_BIAS,
+                      rank4=True, upsample=2, index=i)
+             for i, (name, cin, hw, cout) in enumerate(spec)]
+    return Workload("up2", calls, layouts=[(NDHWC, NDHWC), (NCDHW, NDHWC)])
+
+
 def all_workloads():
     return {"tiny": tiny(), "wan": wan(), "ladder": ladder(), "fused160": fused160(),
-            "t1": t1()}
+            "t1": t1(), "up2": up2()}
 
 
 # ---- generation -------------------------------------------------------------------
