@@ -50,7 +50,10 @@ L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["conv_cm.cu", "conv_cm_kernel.cuh", "conv_cm_halo.cu", "epilogue_cm.cuh",
                   "epilogue.cuh", "kernel_common.cuh",
                   "ptx.cuh", "internal.h"]
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/conv_cm_ladder_L0_halo.md: L0_0 as in the haloed ladder chain
+    ("6f5e5913bff893d0", "L0_0"): 325141760 + 253436160,
+}
 
 
 def source_code_only(text):
@@ -503,8 +506,9 @@ def run_gpu(args, rank, world):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     total_flop = sum(call.flops for call, _ in calls)
     launches_per_step = sum(c.launches for _, c in calls)
-    # launches besides the convolution and its split reduction (input staging)
-    staging_launches = sum(c.launches - 1 - (1 if c.plan.k_splits > 1 else 0) for _, c in calls)
+    # input staging launches (the staged tap gather of a narrow input; NDHWC needs no
+    # layout staging)
+    staging_launches = sum(1 for _, c in calls if c.plan.im2col == 1)
 
     sampler = ClockSampler(dev.index)
     sampler.start()
@@ -643,7 +647,20 @@ def run_case(args):
         epi |= vvc.EPI_PAD_CACHE
         extra = {"history_frames": args.pad_cache}
     out_lay = wl.NDHWC if call.upsample else lay
-    c = vvc.Conv3d(inp["x"].to(dev), wp, call.Cout, call.kernel, call.stride, call.pads, lay,
+    x = inp["x"].to(dev)
+    pads = call.pads
+    if args.chain_halo and args.workload == "ladder":
+        # as in the ladder chain: the input arrives haloed (2 zero frames, a 1-pixel
+        # border) and is read as a valid convolution; the output goes into a haloed
+        # tensor unless this is the chain's last call
+        if call.name != "conv_in":
+            xp = torch.zeros((call.N, call.D + 2, call.H + 2, call.W + 2, call.Cin),
+                             dtype=torch.bfloat16, device=dev)
+            xp[:, 2:, 1:-1, 1:-1] = x
+            x, pads = xp, VALID
+        if call.name != "conv_out":
+            extra = dict(extra, out_halo=LADDER_HALO)
+    c = vvc.Conv3d(x, wp, call.Cout, call.kernel, call.stride, pads, lay,
                    out_lay, epi, bias=g("bias"), residual=g("residual"),
                    residual_bias=g("residual_bias"), gamma=g("gamma"), tuning=tun,
                    input_upsample=call.upsample, **extra)
@@ -671,6 +688,8 @@ def run_case(args):
             "launches": c.launches, "tune": args.tune}
     if args.pad_cache >= 0:
         line["pad_cache"] = args.pad_cache
+    if args.chain_halo:
+        line["chain_halo"] = True
     print(json.dumps(line), flush=True)
     return 0
 
@@ -776,6 +795,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--chain-halo", action="store_true",
+                    help="with --workload ladder --case: run the call as in the chained ladder "
+                         "(haloed input read as a valid convolution, haloed output)")
     ap.add_argument("--ladder-only", action="store_true",
                     help="time the ladder chain only (no per-layer rows of the other workloads)")
     ap.add_argument("--pad-cache", type=int, default=-1,

@@ -10,6 +10,8 @@
 //    Padding Variant", contiguous output).
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "epilogue.cuh"
 #include "internal.h"
 #include "pad_cache.h"
@@ -213,7 +215,14 @@ cudaError_t launch_im2col_hw(const void* x, int layout, int N, int C, int D, int
   a.units = (long long)N * D * Ho * Wo * (Ck / 8);
   const int xblocks = (Wo + 255) / 256;
   a.iblocks = xblocks;
+  // blocks that repack the weights beside the generic gather (the extra blocks of its
+  // grid), and in a launch of their own after the 3 x 3 gather: enough there to finish
+  // in about a microsecond (8 blocks took 13 us for the 128 x 3 x 64 repacked weights
+  // of the RGB input convolution)
   const int wblocks = 8;
+  const long long wtotal = (long long)Cout * KT * a.cp2;
+  const int wblocks_own =
+      static_cast<int>(std::min<long long>(152, std::max<long long>(1, (wtotal + 2047) / 2048)));
   if (KR == 3 && KS == 3 && C >= 1 && C <= 7) {
     // gather through the unrolled kernel; the generic one only repacks the weights
     const dim3 g(xblocks, Ho, N * D);
@@ -230,7 +239,7 @@ cudaError_t launch_im2col_hw(const void* x, int layout, int N, int C, int D, int
     if (err != cudaSuccess) return err;
     Im2colArgs aw = a;
     aw.Wo = 0;  // no row pieces: every block of this launch repacks weights
-    im2col_hw_kernel<<<dim3(wblocks, 1, 1), 256, 0, s>>>(aw);
+    im2col_hw_kernel<<<dim3(wblocks_own, 1, 1), 256, 0, s>>>(aw);
     return cudaGetLastError();
   }
   im2col_hw_kernel<<<dim3(xblocks + wblocks, Ho, N * D), 256, 0, s>>>(a);

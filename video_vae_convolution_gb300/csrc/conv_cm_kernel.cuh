@@ -1048,7 +1048,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 if (dbg) tma_store_5d(&om.conv, smem_u32(ct), cw, wr, hr, od, tc.nb);
                 bulk_commit_group();
               }
-              if (E.halo) cm_halo_block(p.epi, yt, lane, tc.nb, od, hr, wr, cw, bh);
+              // (only blocks next to a border have halo rows or columns to fill)
+              if (E.halo && ((bh & 10) || wr <= 1 || wr + 32 >= E.Wo - 1))
+                cm_halo_block(p.epi, yt, lane, tc.nb, od, hr, wr, cw, bh);
               continue;
             }
           }
