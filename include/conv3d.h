@@ -66,6 +66,7 @@ enum {
 /* ---- layouts and padding ------------------------------------------------------ */
 enum { CONV3D_NCDHW = 0, CONV3D_NDHWC = 1 };
 enum { CONV3D_PAD_ZERO = 0, CONV3D_PAD_REFLECT = 1 };
+enum { CONV3D_DTYPE_BF16 = 0, CONV3D_DTYPE_E4M3 = 1 };
 
 /* Padding of one spatial dimension.  Zero: coordinates outside [0, L) read 0
  * (a causal temporal pad is before = 2, after = 0).  Reflect: PyTorch 'reflect'
@@ -111,8 +112,10 @@ enum {
 };
 
 /* One convolution call.
- *  x          input, bf16, `layout`: NCDHW [N, Cin, D, H, W] or NDHWC [N, D, H, W, Cin].
- *  w_packed   weights packed by conv3d_pack_weight: [Cout][KT][KR][KS][Cin_pad64] bf16.
+ *  x          input, bf16 (or e4m3, see dtype), `layout`: NCDHW [N, Cin, D, H, W] or
+ *             NDHWC [N, D, H, W, Cin].
+ *  w_packed   weights packed by conv3d_pack_weight: [Cout][KT][KR][KS][Cin_pad64] bf16
+ *             (e4m3: conv3d_pack_weight_e4m3).
  *  stride     (T, H, W) strides >= 1.
  *  pad        (T, H, W) paddings.  Output extent per dimension:
  *             (L + before + after - K) / stride + 1.
@@ -151,7 +154,22 @@ enum {
  *             geometry (output extent, padding) applies to the [2H, 2W] upsampled grid.
  *             Requires KR = KS = 3, H and W stride 1 and zero padding (1, 1) along H and
  *             W (output [.., 2H, 2W]), NDHWC output, Cout % 8 == 0, and no RESIDUAL,
- *             L2NORM_SILU, SAVE_VALUE, OUT_PAD_BR, PAD_CACHE or out_halo. */
+ *             L2NORM_SILU, SAVE_VALUE, OUT_PAD_BR, PAD_CACHE or out_halo.
+ *  dtype      element type of x and w_packed: CONV3D_DTYPE_BF16 (0), or
+ *             CONV3D_DTYPE_E4M3 (1): FP8 e4m3fn activations and weights with bf16
+ *             output (ROCm/FlyDSL PR "[Flydsl] Add Qwen-Image VAE classic conv shapes
+ *             to conv3d tests", "Summary" and "Test shapes": the FP8 suite feeds e4m3fn
+ *             activations and weights, fp32 bias, and takes a bf16 output).  e4m3 x is
+ *             NDHWC [N, D, H, W, Cin] bytes with Cin % 16 == 0; w_packed comes from
+ *             conv3d_pack_weight_e4m3.  Products accumulate in fp32 as for bf16.  Not
+ *             with input_upsample, the pixel-major kernel (conv3d_tuning.kernel = 1
+ *             or 3, or Cout <= 16), or a narrow-input gather.
+ *  fp8_scale  with CONV3D_DTYPE_E4M3: the accumulator is multiplied by fp8_scale
+ *             (fp32, round to nearest) before the epilogue, conv = B(fp8_scale * acc),
+ *             so per-tensor dequantisation scales of x and w enter as their product;
+ *             must be finite and nonzero (1 for unscaled e4m3 values).  Ignored for
+ *             bf16.  The pages give no scale convention; one per-tensor factor is the
+ *             plainest that covers both unscaled and scaled e4m3 tensors. */
 typedef struct {
   const void* x;
   int32_t layout;
@@ -175,6 +193,8 @@ typedef struct {
   int32_t history_frames;
   conv3d_pad out_halo[3];
   int32_t input_upsample;
+  int32_t dtype;
+  float fp8_scale;
 } conv3d_params;
 
 /* Optional plan overrides (tests and tuning).  0 (or -1 where noted) = automatic. */
@@ -223,6 +243,18 @@ size_t conv3d_packed_weight_bytes(int32_t Cout, int32_t Cin, int32_t KT, int32_t
  * Pack once; repack after the source weights change. */
 int conv3d_pack_weight(const void* w_oitrs, int32_t Cout, int32_t Cin, int32_t KT,
                        int32_t KR, int32_t KS, void* w_packed, conv3d_stream_t stream);
+
+/* FP8 e4m3fn weights (dtype CONV3D_DTYPE_E4M3): bytes of the packed weight,
+ * Cout * KT * KR * KS * round_up(Cin, 128). */
+size_t conv3d_packed_weight_bytes_e4m3(int32_t Cout, int32_t Cin, int32_t KT, int32_t KR,
+                                       int32_t KS);
+
+/* Packs e4m3fn OITRS [Cout][Cin][KT][KR][KS] bytes (device) into OTRSI
+ * [Cout][KT][KR][KS][Cin_pad128] bytes (device), zero-filling channels
+ * Cin..Cin_pad128-1 (the byte 0 is +0 in e4m3).  Same ownership and errors as
+ * conv3d_pack_weight; both pointers 16-byte aligned and not overlapping. */
+int conv3d_pack_weight_e4m3(const void* w_oitrs, int32_t Cout, int32_t Cin, int32_t KT,
+                            int32_t KR, int32_t KS, void* w_packed, conv3d_stream_t stream);
 
 /* ---- convolution ---------------------------------------------------------------- */
 
@@ -352,7 +384,9 @@ const char* conv3d_status_string(int status);
 
 /* Library ABI version (major * 100 + minor).  2.00: conv3d_params gained cache_out and
  * history_frames, conv3d_tuning gained pair; conv3d_plan, l2norm_silu_pad and the GroupNorm
- * calls were added.  3.00: conv3d_params gained out_halo. */
+ * calls were added.  3.00: conv3d_params gained out_halo and input_upsample.  3.10:
+ * conv3d_params gained dtype and fp8_scale; conv3d_pack_weight_e4m3 and
+ * conv3d_packed_weight_bytes_e4m3 were added. */
 int conv3d_version(void);
 
 /* sizeof() of the ABI structs, for bindings to check their mirrors:

@@ -371,6 +371,57 @@ def group_norm_silu(x, groups, gamma, beta, eps=1e-6, time_isolated=True, silu=T
     return round_bf16(g / (1.0 + np.exp(-g)))
 
 
+# ---- FP8 e4m3 operands ----------------------------------------------------------------
+# ROCm/FlyDSL PR "[Flydsl] Add Qwen-Image VAE classic conv shapes to conv3d tests",
+# "Summary" / "Test shapes": the FP8 suite feeds e4m3fn activations and weights and
+# takes a bf16 output.  e4m3fn (the "fn" variant: finite, no infinities) packs a sign
+# bit, a 4-bit exponent with bias 7 and a 3-bit mantissa; exponent 0 holds the
+# subnormals m/8 * 2^-6, and only S.1111.111 is NaN (so the largest finite value is
+# 1.75 * 2^8 = 448).  The pages give no scale convention; the library takes one
+# per-tensor factor that multiplies the fp32 accumulator (conv = B(scale * acc)).
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Values of e4m3fn codes (uint8), from the format's definition."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where((c & 0x80) != 0, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_to_bf16(codes) -> np.ndarray:
+    """bf16 bits of e4m3fn values.  Exact: 3 mantissa bits and exponents 2^-9 .. 2^8
+    fit bf16's 7 mantissa bits and 8-bit exponent, so the fp32 bit pattern of the value
+    has 16 trailing zero bits.  (Looked up per code in the 256 decoded values.)"""
+    f = e4m3_to_f64(np.arange(256, dtype=np.uint8)).astype(np.float32)
+    u = f.view(np.uint32)
+    finite = np.isfinite(f)
+    assert np.all((u[finite] & 0xFFFF) == 0)
+    table = (u >> 16).astype(np.uint16)
+    return table[np.asarray(codes, dtype=np.uint8)]
+
+
+def conv3d_acc_e4m3(x8, layout, w8, scale, stride=(1, 1, 1), pads=((0, 0, 0),) * 3,
+                    nthreads=0):
+    """fp32 accumulator of the convolution of e4m3fn operands times `scale`,
+    [N, Do, Ho, Wo, Co]: the plain convolution of the (exact) values, then one
+    fp32 rounding of scale * acc."""
+    acc = conv3d_acc(e4m3_to_bf16(x8), layout, e4m3_to_bf16(w8), stride, pads, nthreads)
+    return (acc.astype(np.float64) * float(np.float32(scale))).astype(np.float32)
+
+
+def pack_weight_e4m3(w8):
+    """OITRS e4m3fn bytes -> OTRSI with Ci zero-padded to a multiple of 128 (bytes)."""
+    w8 = np.ascontiguousarray(w8, dtype=np.uint8)
+    Co, Ci, KT, KR, KS = w8.shape
+    cp = (Ci + 127) // 128 * 128
+    out = np.zeros((Co, KT, KR, KS, cp), dtype=np.uint8)
+    out[..., :Ci] = np.transpose(w8, (0, 2, 3, 4, 1))
+    return out
+
+
 def upsample2x_nearest(x):
     """Nearest-exact x2 spatial upsampling of NDHWC bf16 bits [N, D, H, W, C] (ROCm/FlyDSL
     PR "Add Qwen-Image VAE classic conv shapes ...", "Upsample Conv2d": the decoder's

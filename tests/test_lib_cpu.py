@@ -321,3 +321,45 @@ def test_output_halo_overlap_counts_the_whole_tensor():
     assert vvc._lib().conv3d_workspace_bytes(ctypes.byref(p), ctypes.byref(ws)) == vvc.OK
     p.workspace, p.workspace_bytes = 0x40000000, ws.value
     assert fwd(p) == vvc.ERR_OVERLAP
+
+
+def test_e4m3_validation_and_plan():
+    lib = vvc._lib()
+    assert lib.conv3d_packed_weight_bytes_e4m3(96, 96, 3, 3, 3) == 96 * 27 * 128
+    assert lib.conv3d_packed_weight_bytes_e4m3(8, 130, 1, 3, 3) == 8 * 9 * 256
+    assert lib.conv3d_packed_weight_bytes_e4m3(0, 16, 3, 3, 3) == 0
+    f8 = dict(dtype=vvc.DTYPE_E4M3, fp8_scale=1.0)
+    info = _plan(_params(**f8))
+    assert info.kernel == 2 and info.paired == 0 and info.im2col == 0
+    # the same stage walk as the bf16 plan over Cin / 2 channel pairs
+    assert info.stages_per_tile == _plan(_params(Cin=8)).stages_per_tile
+    p = _params(Cin=96, Cout=96, **f8)
+    # one chunk of 48 pairs per (kt, kr) with the three W taps in one stage, never
+    # paired (bf16 96 channels pair the last chunks: 18 -> 14 stages)
+    assert _plan(p).stages_per_tile == 9 and _plan(p).paired == 0
+    bad = [
+        dict(dtype=2),                                       # unknown element type
+        dict(fp8_scale=0.0),                                 # scale must be nonzero
+        dict(fp8_scale=float("inf")),                        # and finite
+        dict(fp8_scale=float("nan")),
+        dict(layout=vvc.NCDHW),                              # e4m3 input is NDHWC
+        dict(Cin=24),                                        # 16-byte channel rows
+        dict(input_upsample=2, pad=None),                    # no fused upsample
+    ]
+    for case in bad:
+        kw = dict(f8)
+        kw.update({k: v for k, v in case.items() if k != "pad"})
+        assert fwd(_params(**kw)) == vvc.ERR_INVALID_ARG, case
+    # outside the e4m3 instances: pixel-major kernels and tiny Cout
+    p = _params(**f8)
+    assert fwd(p, vvc.Tuning(kernel=1)) == vvc.ERR_UNSUPPORTED
+    assert fwd(p, vvc.Tuning(kernel=3)) == vvc.ERR_UNSUPPORTED
+    assert fwd(_params(Cout=8, **f8)) == vvc.ERR_UNSUPPORTED
+    # buffer spans count one byte per e4m3 element: x right below y is no overlap
+    p = _params(x=0x10000000 - 16 * 4 * 12 * 12, **f8)
+    rc = fwd(p, vvc.Tuning(k_splits=1))
+    assert rc != vvc.ERR_OVERLAP
+    p = _params(x=0x10000000 - 16 * 4 * 12 * 12 + 16, **f8)
+    assert fwd(p, vvc.Tuning(k_splits=1)) == vvc.ERR_OVERLAP
+    # the bf16 call ignores the scale
+    assert _plan(_params(fp8_scale=0.0)).kernel in (1, 2)

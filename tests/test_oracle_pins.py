@@ -598,3 +598,58 @@ def test_upsample2x_conv_parity_classes(orc):
     # the oracle's fp32 accumulator of the plain definition agrees with fp64
     acc = orc.upsample2x_conv_acc(x, w)[:, 0]
     np.testing.assert_allclose(acc, direct, rtol=1e-5, atol=1e-5)
+
+
+# ---- FP8 e4m3fn operands (FlyDSL PR, "Summary" / "Test shapes": the FP8 suite) --------
+
+def test_e4m3_decode_matches_torch_and_closed_forms(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    got = orc.e4m3_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert list(np.flatnonzero(nan)) == [0x7F, 0xFF]          # only S.1111.111
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+    # closed forms of the format: bias 7, 3 mantissa bits, subnormals m/8 * 2^-6
+    assert got[0x38] == 1.0 and got[0xB8] == -1.0
+    assert got[0x7E] == 448.0 and got[0xFE] == -448.0         # 1.75 * 2^8
+    assert got[0x01] == 2.0 ** -9 and got[0x07] == 7 * 2.0 ** -9
+    assert got[0x08] == 2.0 ** -6                              # smallest normal
+    assert got[0x3C] == 1.5 and got[0x41] == 2.25
+    assert got[0x00] == 0.0 and not np.signbit(got[0x00]) and np.signbit(got[0x80])
+
+
+def test_e4m3_to_bf16_is_exact(orc):
+    codes = np.arange(256, dtype=np.uint8)
+    v = orc.e4m3_to_f64(codes)
+    b = orc.e4m3_to_bf16(codes)
+    ok = ~np.isnan(v)
+    np.testing.assert_array_equal(orc.bf16_to_f32(b)[ok].astype(np.float64), v[ok])
+    assert np.all(np.isnan(orc.bf16_to_f32(b)[~ok]))
+
+
+@pytest.mark.parametrize("case", [CASES[2], CASES[3], CASES[5]])
+def test_conv_e4m3_matches_torch(orc, case):
+    # torch's own e4m3fn decode, fp64 conv3d, then the per-tensor scale
+    N, C, D, H, W, Co, k, stride, pads = case
+    rng = np.random.default_rng(31)
+    x8 = rng.integers(0, 256, (N, D, H, W, C), dtype=np.uint8)
+    w8 = rng.integers(0, 256, (Co, C) + k, dtype=np.uint8)
+    x8[(x8 & 0x7F) == 0x7F] = 0x38                              # no NaN codes
+    w8[(w8 & 0x7F) == 0x7F] = 0xB8
+    scale = 2.0 ** -11
+    acc = orc.conv3d_acc_e4m3(x8, wl.NDHWC, w8, scale, stride, pads)
+    dec = lambda a: torch.from_numpy(a).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ref = torch_conv(np.ascontiguousarray(dec(x8).transpose(0, 4, 1, 2, 3)), dec(w8), stride,
+                     pads) * scale
+    np.testing.assert_allclose(acc, ref.astype(np.float32), rtol=2.0 ** -23, atol=0)
+
+
+def test_pack_weight_e4m3(orc):
+    rng = np.random.default_rng(32)
+    w8 = rng.integers(0, 256, (5, 140, 3, 2, 3), dtype=np.uint8)
+    p = orc.pack_weight_e4m3(w8)
+    assert p.shape == (5, 3, 2, 3, 256)
+    assert np.all(p[..., 140:] == 0)
+    for co, t, r, s in [(0, 0, 0, 0), (4, 2, 1, 2), (2, 1, 0, 1)]:
+        np.testing.assert_array_equal(p[co, t, r, s, :140], w8[co, :, t, r, s])

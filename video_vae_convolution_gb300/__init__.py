@@ -21,6 +21,8 @@ NCDHW = 0
 NDHWC = 1
 PAD_ZERO = 0
 PAD_REFLECT = 1
+DTYPE_BF16 = 0
+DTYPE_E4M3 = 1
 
 EPI_BIAS = 1
 EPI_RESIDUAL = 2
@@ -42,7 +44,7 @@ ERR_DEVICE_TIMEOUT = -7
 ERR_SCRATCH_LIMIT = -8
 
 # ABI version of the C library this binding mirrors (major * 100 + minor).
-ABI_VERSION = 300
+ABI_VERSION = 310
 
 # Every function the C header declares (checked by the tests against include/conv3d.h).
 EXPORTS = (
@@ -50,7 +52,8 @@ EXPORTS = (
     "conv3d_workspace_bytes_ex", "conv3d_fwd", "conv3d_fwd_ex", "conv3d_launch_count",
     "l2norm_silu", "conv3d_get_device_status", "conv3d_status_string", "conv3d_version",
     "conv3d_struct_size", "conv3d_fwd_static_scratch", "conv3d_plan", "l2norm_silu_pad",
-    "group_norm_workspace_bytes", "group_norm_silu",
+    "group_norm_workspace_bytes", "group_norm_silu", "conv3d_packed_weight_bytes_e4m3",
+    "conv3d_pack_weight_e4m3",
 )
 
 
@@ -82,6 +85,7 @@ class Params(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("cache_out", ctypes.c_void_p), ("history_frames", ctypes.c_int32),
         ("out_halo", Pad * 3), ("input_upsample", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("fp8_scale", ctypes.c_float),
     ]
 
 
@@ -122,6 +126,10 @@ def _lib():
                 lib.conv3d_packed_weight_bytes.restype = sz
                 lib.conv3d_pack_weight.argtypes = [vp] + [i32] * 5 + [vp, vp]
                 lib.conv3d_pack_weight.restype = ctypes.c_int
+                lib.conv3d_packed_weight_bytes_e4m3.argtypes = [i32] * 5
+                lib.conv3d_packed_weight_bytes_e4m3.restype = sz
+                lib.conv3d_pack_weight_e4m3.argtypes = [vp] + [i32] * 5 + [vp, vp]
+                lib.conv3d_pack_weight_e4m3.restype = ctypes.c_int
                 lib.conv3d_workspace_bytes.argtypes = [P, ctypes.POINTER(sz)]
                 lib.conv3d_workspace_bytes.restype = ctypes.c_int
                 lib.conv3d_workspace_bytes_ex.argtypes = [P, T, ctypes.POINTER(sz)]
@@ -201,6 +209,25 @@ def pack_weight(w: torch.Tensor, stream=None) -> torch.Tensor:
     return out
 
 
+def packed_weight_shape_e4m3(Cout, Cin, KT, KR, KS):
+    return (Cout, KT, KR, KS, (Cin + 127) // 128 * 128)
+
+
+def pack_weight_e4m3(w: torch.Tensor, stream=None) -> torch.Tensor:
+    """OITRS (or OIRS) e4m3fn CUDA weights (torch.float8_e4m3fn, or their bytes as
+    torch.uint8) -> packed OTRSI bytes (torch.uint8) for dtype=DTYPE_E4M3 calls."""
+    if w.dim() == 4:
+        w = w.unsqueeze(2)
+    assert w.dim() == 5 and w.element_size() == 1 and w.is_cuda
+    w = w.contiguous()
+    Cout, Cin, KT, KR, KS = w.shape
+    out = torch.empty(packed_weight_shape_e4m3(Cout, Cin, KT, KR, KS), dtype=torch.uint8,
+                      device=w.device)
+    _check(_lib().conv3d_pack_weight_e4m3(_ptr(w), Cout, Cin, KT, KR, KS, _ptr(out),
+                                          _stream(stream)), "conv3d_pack_weight_e4m3")
+    return out
+
+
 # ---- convolution -----------------------------------------------------------------------------
 
 def out_dims(D, H, W, kernel, stride, pads):
@@ -235,13 +262,16 @@ class Conv3d:
     x: bf16 CUDA tensor in `layout` (5-D, or 4-D with D = 1).  w_packed from
     pack_weight.  pads: ((before, after, mode) for T, H, W).  Outputs are allocated
     here unless given; the workspace is allocated here (torch) unless given.
+    dtype=DTYPE_E4M3: x holds e4m3fn bytes (NDHWC), w_packed comes from
+    pack_weight_e4m3 and the accumulator is multiplied by fp8_scale; y stays bf16.
     """
 
     def __init__(self, x, w_packed, Cout, kernel, stride=(1, 1, 1),
                  pads=((0, 0, PAD_ZERO),) * 3, layout=NDHWC, out_layout=NDHWC, epi=0,
                  bias=None, residual=None, residual_bias=None, gamma=None, y=None,
                  value_out=None, conv_out=None, workspace=None, tuning: Optional[Tuning] = None,
-                 cache_out=None, history_frames=0, out_halo=None, input_upsample=0):
+                 cache_out=None, history_frames=0, out_halo=None, input_upsample=0,
+                 dtype=DTYPE_BF16, fp8_scale=1.0):
         N, C, D, H, W = _dims(x, layout)
         KT, KR, KS = kernel
         up = 2 if input_upsample == 2 else 1  # the convolution reads the x2 upsampled grid
@@ -293,6 +323,8 @@ class Conv3d:
             for i in range(3):
                 p.out_halo[i].before, p.out_halo[i].after, p.out_halo[i].mode = out_halo[i]
         p.input_upsample = input_upsample
+        p.dtype = dtype
+        p.fp8_scale = fp8_scale
         self.out_halo = out_halo
         self.cache_out = cache_out
         self.tuning = tuning

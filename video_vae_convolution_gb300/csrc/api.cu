@@ -25,6 +25,8 @@ cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
                            size_t smem_bytes, cudaStream_t stream);
 cudaError_t conv_status_read_clear(int* status, cudaStream_t stream);
 cudaError_t conv_cm_status_read_clear(int* status);
+cudaError_t launch_pack_weight_u8(const void* w, void* out, int Co, int Ci, int taps,
+                                  cudaStream_t s);
 cudaError_t launch_pack_weight(const void* w, void* out, int Co, int Ci, int taps,
                                cudaStream_t s);
 cudaError_t launch_stage_input(const void* x, int layout, int N, int C, int Cp, long long S,
@@ -97,6 +99,8 @@ struct Plan {
   int Ck = 0;
   size_t wr_off = 0, wr_bytes = 0;
   conv3d_params q{};
+  // e4m3 operands: the kernels see a bf16-sized convolution over channel pairs (q)
+  bool f8 = false;
   bool cm = false;          // channel-major kernel (conv_cm) instead of pixel-major (conv_tc)
   ConvTCParams kp{};
   ConvCMParams cp{};
@@ -153,6 +157,13 @@ int validate_shape(const conv3d_params* p, int* Do, int* Ho, int* Wo) {
       return CONV3D_ERR_INVALID_ARG;
   }
   if (p->input_upsample != 0 && p->input_upsample != 2) return CONV3D_ERR_INVALID_ARG;
+  if (p->dtype != CONV3D_DTYPE_BF16 && p->dtype != CONV3D_DTYPE_E4M3) return CONV3D_ERR_INVALID_ARG;
+  if (p->dtype == CONV3D_DTYPE_E4M3) {
+    // FP8 e4m3 operands: channels-last bytes, 16-byte channel rows, a usable scale
+    if (p->layout != CONV3D_NDHWC || p->Cin % 16 != 0 || p->input_upsample != 0 ||
+        !std::isfinite(p->fp8_scale) || p->fp8_scale == 0.0f)
+      return CONV3D_ERR_INVALID_ARG;
+  }
   const int up = p->input_upsample == 2 ? 2 : 1;  // the convolution reads the x2 grid
   if ((long long)p->H * up > 0x3fffffffLL || (long long)p->W * up > 0x3fffffffLL)
     return CONV3D_ERR_INVALID_ARG;
@@ -266,6 +277,7 @@ void fill_epi(const conv3d_params* p, const Plan& pl, EpiParams* e) {
   e->h_mode = p->out_halo[1].mode == CONV3D_PAD_REFLECT ? 2 : 1;
   e->w_mode = p->out_halo[2].mode == CONV3D_PAD_REFLECT ? 2 : 1;
   e->up2 = p->input_upsample == 2 ? 1 : 0;
+  e->acc_scale = 1.0f;
 }
 
 // Split of the reduction so that small layers still fill the GPU.  Each split
@@ -433,6 +445,13 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
     k.box_w = tw;
     k.run_pitch = tw;
     k.N = static_cast<int>(round_up((long long)tw * rh, 16));
+    // the tile's rows are rh input rows sh apart: one copy with element stride sh along
+    // H brings them all (the rows land tw apart, as the per-row copies place them),
+    // unless a row needs the reflect-H coordinate mapping
+    const bool reflect_h =
+        p->pad[1].mode == CONV3D_PAD_REFLECT && (p->pad[1].before || p->pad[1].after);
+    k.rows_box = (rh > 1 && !reflect_h && (long long)rh * p->stride[1] <= 256 &&
+                  p->stride[1] <= 8) ? 1 : 0;
   }
   if (k.N > 256) return CONV3D_ERR_INVALID_ARG;
   // Pixel-major mode for layers with at most 128 output channels: N = Cout (rounded
@@ -944,6 +963,29 @@ int make_plan_conv(const conv3d_params* p, const conv3d_tuning* tu, Plan* pl) {
   if (rc) return rc;
   conv3d_tuning t{};
   if (tu) t = *tu;
+  if (p->dtype == CONV3D_DTYPE_E4M3) {
+    // e4m3 operands: a K step of the f8f6f4 MMA (32 one-byte channels) spans the same
+    // 32 bytes as a bf16 K step, so the channel-major plan of the same convolution over
+    // Cin / 2 two-byte channel pairs describes every copy and shared-memory layout;
+    // only the MMA kind and the accumulator scale differ
+    if (t.kernel == 1 || t.kernel == 3 || t.im2col == 1 || t.im2col == 3)
+      return CONV3D_ERR_UNSUPPORTED;
+    conv3d_params q = *p;
+    q.Cin = p->Cin / 2;
+    q.dtype = CONV3D_DTYPE_BF16;
+    conv3d_tuning t2 = t;
+    t2.pair = 2;  // one plain schedule for the e4m3 instances
+    pl->f8 = true;
+    pl->cm = true;
+    pl->Cst = q.Cin;
+    pl->q = q;
+    rc = plan_cm(&pl->q, t2, pl, 0);
+    if (rc) return rc;
+    if (pl->cp.pm || pl->cp.gather || pl->cp.up2 || pl->cp.pair) return CONV3D_ERR_UNSUPPORTED;
+    pl->cp.f8 = 1;
+    pl->cp.epi.acc_scale = p->fp8_scale;
+    return CONV3D_OK;
+  }
   if (p->input_upsample == 2) {
     // x2 upsampled input: the channel-major kernel tiles the low-resolution grid (a
     // 3x3, pad-1 convolution of it, once per parity class); the output is twice as
@@ -1059,9 +1101,11 @@ int check_pointers(const conv3d_params* p, const Plan& pl) {
     s.hi = q ? s.lo + bytes : s.lo;
     return s;
   };
+  const bool f8 = p->dtype == CONV3D_DTYPE_E4M3;
   const Span in[] = {
-      span(p->x, (size_t)p->N * p->Cin * p->D * p->H * p->W * 2),
-      span(p->w_packed, conv3d_packed_weight_bytes(p->Cout, p->Cin, p->KT, p->KR, p->KS)),
+      span(p->x, (size_t)p->N * p->Cin * p->D * p->H * p->W * (f8 ? 1 : 2)),
+      span(p->w_packed, f8 ? conv3d_packed_weight_bytes_e4m3(p->Cout, p->Cin, p->KT, p->KR, p->KS)
+                           : conv3d_packed_weight_bytes(p->Cout, p->Cin, p->KT, p->KR, p->KS)),
       span((p->epi & CONV3D_EPI_RESIDUAL) ? p->residual : nullptr, out_elems * 2),
       span((p->epi & CONV3D_EPI_BIAS) ? p->bias : nullptr, (size_t)p->Cout * 4),
       span((p->epi & CONV3D_EPI_RESIDUAL_BIAS) ? p->residual_bias : nullptr, (size_t)p->Cout * 4),
@@ -1182,6 +1226,11 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
   cuuint64_t gstrA[4] = {C * 2, C * 2 * p->W, C * 2 * p->W * p->H, C * 2 * p->W * p->H * p->D};
   cuuint32_t boxA[5] = {(cuuint32_t)kc, (cuuint32_t)act_box, 1, 1, 1};
   cuuint32_t esA[5] = {1, (cuuint32_t)es_w, 1, 1, 1};
+  if (pl.cm && pl.cp.rows_box) {
+    // direct tiles: all rh rows of the tile in one box, rows sh apart
+    boxA[2] = (cuuint32_t)(pl.cp.rh * pl.cp.sh);
+    esA[2] = (cuuint32_t)pl.cp.sh;
+  }
   cuuint32_t rankA = 5;
   if (flat && pl.cm && pl.cp.flat3) {
     // D, H and W merged into one dimension of D*H*W positions (dims C, D*H*W, 1, N)
@@ -1315,6 +1364,28 @@ size_t conv3d_packed_weight_bytes(int32_t Cout, int32_t Cin, int32_t KT, int32_t
   return (size_t)Cout * KT * KR * KS * (size_t)round_up(Cin, 64) * 2;
 }
 
+size_t conv3d_packed_weight_bytes_e4m3(int32_t Cout, int32_t Cin, int32_t KT, int32_t KR,
+                                       int32_t KS) {
+  if (Cout < 1 || Cin < 1 || KT < 1 || KR < 1 || KS < 1) return 0;
+  return (size_t)Cout * KT * KR * KS * (size_t)round_up(Cin, 128);
+}
+
+int conv3d_pack_weight_e4m3(const void* w_oitrs, int32_t Cout, int32_t Cin, int32_t KT,
+                            int32_t KR, int32_t KS, void* w_packed, conv3d_stream_t stream) {
+  if (!w_oitrs || !w_packed) return CONV3D_ERR_INVALID_ARG;
+  if (Cout < 1 || Cin < 1 || KT < 1 || KR < 1 || KS < 1) return CONV3D_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(w_oitrs) & 15u) || (reinterpret_cast<uintptr_t>(w_packed) & 15u))
+    return CONV3D_ERR_MISALIGNED;
+  const size_t in_bytes = (size_t)Cout * Cin * KT * KR * KS;
+  const size_t out_bytes = conv3d_packed_weight_bytes_e4m3(Cout, Cin, KT, KR, KS);
+  Span a{reinterpret_cast<uintptr_t>(w_oitrs), reinterpret_cast<uintptr_t>(w_oitrs) + in_bytes};
+  Span b{reinterpret_cast<uintptr_t>(w_packed), reinterpret_cast<uintptr_t>(w_packed) + out_bytes};
+  if (overlaps(a, b)) return CONV3D_ERR_OVERLAP;
+  cudaError_t err = vvc::launch_pack_weight_u8(w_oitrs, w_packed, Cout, Cin, KT * KR * KS,
+                                               reinterpret_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? CONV3D_OK : CONV3D_ERR_CUDA;
+}
+
 int conv3d_pack_weight(const void* w_oitrs, int32_t Cout, int32_t Cin, int32_t KT, int32_t KR,
                        int32_t KS, void* w_packed, conv3d_stream_t stream) {
   if (!w_oitrs || !w_packed) return CONV3D_ERR_INVALID_ARG;
@@ -1437,6 +1508,12 @@ int conv3d_fwd_ex(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_st
     q.y = yk;
     pm = &q;
     xin = dst;
+  } else if (pl.f8) {
+    q = pl.q;
+    q.x = p->x;
+    q.w_packed = p->w_packed;
+    q.y = yk;
+    pm = &q;
   } else if (pl.stage) {
     void* dst = ws + pl.stage_off;
     if (vvc::launch_stage_input(p->x, p->layout, p->N, p->Cin, pl.Cst,
@@ -1702,7 +1779,7 @@ const char* conv3d_status_string(int status) {
   }
 }
 
-int conv3d_version(void) { return 300; }
+int conv3d_version(void) { return 310; }
 
 }  // extern "C"
 

@@ -44,6 +44,40 @@ cudaError_t launch_pack_weight(const void* w, void* out, int Co, int Ci, int tap
   return cudaGetLastError();
 }
 
+// One-byte (e4m3) weights: OITRS -> OTRSI with Ci zero-padded to a multiple of 128;
+// a thread writes one 16-byte group of 16 input channels of one (co, tap).
+__global__ void pack_weight_u8_kernel(const uint8_t* __restrict__ w, uint8_t* __restrict__ out,
+                                      int Ci, int taps, int groups, long long total) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int g = static_cast<int>(i % groups);
+    const long long rest = i / groups;  // co * taps + tap
+    const int tap = static_cast<int>(rest % taps);
+    const long long co = rest / taps;
+    uint32_t v[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int ci = g * 16 + k;
+      const uint32_t b = (ci < Ci) ? w[(co * Ci + ci) * taps + tap] : 0u;
+      v[k >> 2] |= b << (8 * (k & 3));
+    }
+    *reinterpret_cast<uint4*>(out + i * 16) = make_uint4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+cudaError_t launch_pack_weight_u8(const void* w, void* out, int Co, int Ci, int taps,
+                                  cudaStream_t s) {
+  const int groups = (Ci + 127) / 128 * 8;  // 16-byte groups per (co, tap) row
+  const long long total = (long long)Co * taps * groups;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 152 * 32) blocks = 152 * 32;
+  pack_weight_u8_kernel<<<static_cast<int>(blocks), threads, 0, s>>>(
+      static_cast<const uint8_t*>(w), static_cast<uint8_t*>(out), Ci, taps, groups, total);
+  return cudaGetLastError();
+}
+
 // ---- spatial im2col staging for narrow inputs ------------------------------------------
 // For a layer with few input channels (Cin * KR * KS <= 64) the spatial taps are
 // gathered once: out[n][d][ho][wo][(r * KS + s) * C + c] = x[n, c, d, ho*sh + r - ph,

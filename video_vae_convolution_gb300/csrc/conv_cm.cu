@@ -1,7 +1,7 @@
 // Channel-major implicit-GEMM convolution: the instances without an output halo,
 // the launcher for every instance, and the status word of this translation unit.
 // The kernel itself is in conv_cm_kernel.cuh; the instances that write a haloed
-// output are compiled in conv_cm_halo.cu.
+// output are compiled in conv_cm_halo.cu, the e4m3 ones in conv_cm_f8.cu.
 #include "conv_cm_kernel.cuh"
 
 namespace vvc {
@@ -11,6 +11,11 @@ cudaError_t launch_conv_cm_halo(const CUtensorMap& tmAct, const CUtensorMap& tmW
                                 const CmHalfMaps& half, const ConvCMParams& p, int which,
                                 int grid, size_t smem_bytes, cudaStream_t stream);
 cudaError_t conv_cm_halo_status_read_clear(int* status);
+cudaError_t launch_conv_cm_f8(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
+                              const CUtensorMap& tmWgtLast, const CmOutMaps& om,
+                              const CmHalfMaps& half, const ConvCMParams& p, bool inner,
+                              int grid, size_t smem_bytes, cudaStream_t stream);
+cudaError_t conv_cm_f8_status_read_clear(int* status);
 
 cudaError_t conv_cm_status_read_clear(int* status) {
   int v = 0;
@@ -19,10 +24,12 @@ cudaError_t conv_cm_status_read_clear(int* status) {
   const int zero = 0;
   err = cudaMemcpyToSymbol(g_conv_cm_status, &zero, sizeof(int));
   if (err != cudaSuccess) return err;
-  int h = 0;
+  int h = 0, f = 0;
   err = conv_cm_halo_status_read_clear(&h);
   if (err != cudaSuccess) return err;
-  *status = v ? v : h;
+  err = conv_cm_f8_status_read_clear(&f);
+  if (err != cudaSuccess) return err;
+  *status = v ? v : (h ? h : f);
   return cudaSuccess;
 }
 
@@ -37,6 +44,9 @@ cudaError_t launch_conv_cm(const CUtensorMap& tmAct, const CUtensorMap& tmWgt,
   if (p.gather && (p.pair || p.pm)) return cudaErrorInvalidValue;
   if (p.up2 && (p.pair || p.pm || p.gather || inner || p.epi.halo || !p.halo))
     return cudaErrorInvalidValue;
+  if (p.f8)
+    return launch_conv_cm_f8(tmAct, tmWgt, tmWgtLast, om, half, p, inner, grid, smem_bytes,
+                             stream);
   const int which = p.up2 ? 5 : (p.gather ? 4 : (p.pm ? 3 : (p.pair ? 1 : (inner ? 2 : 0))));
   if (p.epi.halo)
     return launch_conv_cm_halo(tmAct, tmWgt, tmWgtLast, om, half, p, which, grid, smem_bytes,

@@ -109,6 +109,16 @@ __device__ __forceinline__ StageCoord decode_stage(const ConvCMParams& p, int it
   return c;
 }
 
+// e4m3 operands: the accumulator times the call's scale, in place (fp32, round to
+// nearest), before anything rounds it to bf16 or writes it as a partial sum.
+template <bool kF8>
+__device__ __forceinline__ void scale_acc(uint32_t (&r)[32], float s) {
+  if constexpr (kF8) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__fmul_rn(__uint_as_float(r[j]), s));
+  }
+}
+
 // Stage after c, in the order decode_stage numbers them (no divisions: the
 // issuing threads sit on the load-latency path).
 __device__ __forceinline__ void next_stage(const ConvCMParams& p, StageCoord& c) {
@@ -188,10 +198,12 @@ __device__ __forceinline__ int cta_tile(const ConvCMParams& p, int l) {
 // kGather: narrow-input gather mode (ConvCMParams::gather).  kHalo: the output goes
 // into a haloed tensor (EpiParams::halo).  kUp2: the input is read x2 upsampled
 // (ConvCMParams::up2).
+// kF8: e4m3 operands (ConvCMParams::f8): kind::f8f6f4 MMAs and the accumulator scale.
 // They are template parameters so that the plain instance keeps the shortest
 // producer and MMA-issue loops (the per-stage checks of the first two modes cost
 // 4-5 % each on layers that use neither).
-template <bool kPair, bool kInner, bool kPM, bool kGather, bool kHalo, bool kUp2>
+template <bool kPair, bool kInner, bool kPM, bool kGather, bool kHalo, bool kUp2,
+          bool kF8 = false>
 __global__ void __launch_bounds__(kMaxThreads, 1)
     conv_cm_kernel(const __grid_constant__ CUtensorMap tmAct,
                    const __grid_constant__ CUtensorMap tmWgt,
@@ -546,7 +558,11 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               // one run per output row of the tile, run_pitch rows apart: halo runs
               // of tw + KS - 1 pixels (all KS taps), or tw pixels at one tap
               const int w_start = p.halo ? (w0 - p.pw) : (w0 * p.sw + sc.sblk - p.pw);
-              for (int i = 0; i < p.rh; ++i) {
+              if (p.rows_box) {
+                // direct tile: every row of the tile in one copy (rows sh apart)
+                tma_load_5d(act, &tmAct, full, sc.ch * p.kc, w_start, h0 * p.sh + sc.r - p.ph,
+                            d_in, tc.nb);
+              } else for (int i = 0; i < p.rh; ++i) {
                 const int ho = h0 + i;
                 int h_in = ho * p.sh + sc.r - p.ph;
                 // x2 upsampled input: class row offsets (-1, 0, 0) or (0, 0, 1)
@@ -582,7 +598,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
     if (lane == 0) {
       // channel-major: A = weights (M = 128 channels), B = pixels (N = p.N);
       // pixel-major: A = pixels (M = 128 per half), B = weights (N = p.pm_n)
-      const uint32_t idesc = idesc_bf16_f32(128, kPM ? p.pm_n : p.N);
+      const uint32_t idesc = kF8 ? idesc_e4m3_f32(128, p.N) : idesc_bf16_f32(128, kPM ? p.pm_n : p.N);
       const uint32_t sbo = 8u * static_cast<uint32_t>(p.row_bytes);
       // The high descriptor word (stride, version, swizzle) is fixed; operand
       // views differ only in the start-address field (16-byte units).  The
@@ -649,7 +665,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             for (int kk = 0; kk < 2; ++kk) {
               const uint64_t adesc = (static_cast<uint64_t>(desc_hi_h) << 32) | (w_lo + 2u * kk);
               const uint64_t bdesc = (static_cast<uint64_t>(desc_hi_h) << 32) | (b_lo + 2u * kk);
-              mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+              mma_ss<kF8>(d, adesc, bdesc, idesc, acc);
               acc = 1u;
             }
           } else if (kPair && psc.np == 2 && p.KS == 3 && kk_n == 2) {
@@ -664,7 +680,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 for (int kk = 0; kk < 2; ++kk) {
                   const uint64_t adesc = (static_cast<uint64_t>(desc_hi_h) << 32) | (a_t + 2u * kk);
                   const uint64_t bdesc = (static_cast<uint64_t>(desc_hi_h) << 32) | (b_t + 2u * kk);
-                  mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+                  mma_ss<kF8>(d, adesc, bdesc, idesc, acc);
                   acc = 1u;
                 }
               }
@@ -678,7 +694,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 for (int kk = 0; kk < kk_n; ++kk) {
                   const uint64_t adesc = (static_cast<uint64_t>(desc_hi_h) << 32) | (a_t + 2u * kk);
                   const uint64_t bdesc = (static_cast<uint64_t>(desc_hi_h) << 32) | (b_t + 2u * kk);
-                  mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+                  mma_ss<kF8>(d, adesc, bdesc, idesc, acc);
                   acc = 1u;
                 }
               }
@@ -696,7 +712,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 for (int kk = 0; kk < 4; ++kk) {
                   const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (a_t + 2u * kk);
                   const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (b_t + 2u * kk);
-                  mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+                  mma_ss<kF8>(d, adesc, bdesc, idesc, acc);
                   acc = 1u;
                 }
                 return;
@@ -706,7 +722,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 for (int kk = 0; kk < 2; ++kk) {
                   const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (a_t + 2u * kk);
                   const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (b_t + 2u * kk);
-                  mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+                  mma_ss<kF8>(d, adesc, bdesc, idesc, acc);
                   acc = 1u;
                 }
                 return;
@@ -714,7 +730,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               for (int kk = 0; kk < kk_n; ++kk) {
                 const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (a_t + 2u * kk);
                 const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (b_t + 2u * kk);
-                mma_bf16_ss(d, adesc, bdesc, idesc, acc);
+                mma_ss<kF8>(d, adesc, bdesc, idesc, acc);
                 acc = 1u;
               }
             };
@@ -751,7 +767,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 for (int kk = 0; kk < KK; ++kk) {
                   const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (x_t + 2u * kk);
                   const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (w_t + 2u * kk);
-                  mma_bf16_ss(dh, adesc, bdesc, idesc, (tl | kk) ? 1u : acc0);
+                  mma_ss<kF8>(dh, adesc, bdesc, idesc, (tl | kk) ? 1u : acc0);
                 }
               }
             };
@@ -773,7 +789,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                 for (int kk = 0; kk < kk_n; ++kk) {
                   const uint64_t adesc = (static_cast<uint64_t>(desc_hi) << 32) | (x_t + 2u * kk);
                   const uint64_t bdesc = (static_cast<uint64_t>(desc_hi) << 32) | (w_t + 2u * kk);
-                  mma_bf16_ss(dh, adesc, bdesc, idesc, acc_h);
+                  mma_ss<kF8>(dh, adesc, bdesc, idesc, acc_h);
                   acc_h = 1u;
                 }
               }
@@ -969,6 +985,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           tmem_ld32(tb + static_cast<uint32_t>(j0), r);
           tmem_ld_wait();
           if (!warp_live) continue;
+          scale_acc<kF8>(r, p.epi.acc_scale);
           if (p.tma_store) {
             // the warp's previous bulk store has read the staging block
             if (lane == 0) bulk_wait_read_all();
@@ -1093,6 +1110,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
             uint32_t r[32];
             tmem_ld32(tb + static_cast<uint32_t>(j0), r);
             tmem_ld_wait();
+            scale_acc<kF8>(r, p.epi.acc_scale);
             if (warp_live) cm_norm_pass1(E, t, st, lane, j0, r, scr, Cs, ch);
           }
           tc_fence_before();

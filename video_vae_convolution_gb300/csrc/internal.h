@@ -66,6 +66,9 @@ struct EpiParams {
   // grid the tiles cover; y (and conv_out) is [N, Do, 2 Ho, 2 Wo, Cout] and the tile of
   // parity class cls writes output (2 h + cls / 2, 2 w + cls % 2)
   int up2;
+  // e4m3 operands: the fp32 accumulator is multiplied by acc_scale (round to nearest)
+  // before the first rounding to bf16; 1 otherwise
+  float acc_scale;
 };
 
 // Implicit-GEMM convolution on tcgen05 (one CTA = R M-tiles x BN output channels).
@@ -122,7 +125,9 @@ struct ConvCMParams {
                            // (needs stride 1 and no H / W padding; T zero padding reads
                            // positions outside the volume)
   int tiles_d;             // output frames in the tile index (1 with flat3)
-  int nbox;                // activation boxes per stage (halo: 1..2, direct: rh)
+  int nbox;                // activation boxes per row of the tile (halo: 1..2, direct: 1)
+  int rows_box;            // direct tiles: 1 = one box covers all rh rows (element
+                           // stride sh along H), 0 = one box per row
   int box_w;               // loaded elements per activation box
   int run_pitch;           // shared-memory rows between the runs of consecutive output
                            // rows (also the tile's pixel pitch: valid columns are < tw)
@@ -186,6 +191,11 @@ struct ConvCMParams {
   int gather, g_K, g_cpp, g_planes, g_row_bytes;
   uint32_t g_raw_off, g_wres_off;
   const uint16_t* g_wp;     // packed weights [Cout][KT][KR][KS][cp64]
+  // e4m3 operands (f8 = 1): C, kc, cp64 and every copy count two-byte channel pairs;
+  // the MMA is kind::f8f6f4 (K = 32 one-byte channels per instruction, the same 32
+  // bytes of each operand row as a bf16 K step) and epi.acc_scale scales the
+  // accumulator
+  int f8;
 };
 
 // Tensor maps of the paired last-chunk stages: 32-channel boxes, 64-byte swizzle.

@@ -178,6 +178,27 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uin
       : "memory");
 }
 
+// The same for e4m3 A and B (kind::f8f6f4; K = 32 one-byte elements, 32 bytes of each
+// operand row, as one bf16 K step), fp32 accumulator.
+__device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+template <bool kF8>
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  if constexpr (kF8)
+    mma_e4m3_ss(d_tmem, adesc, bdesc, idesc, accumulate);
+  else
+    mma_bf16_ss(d_tmem, adesc, bdesc, idesc, accumulate);
+}
+
 // Arrives once on `bar` when all previously issued tcgen05.mma of this thread complete.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
@@ -219,6 +240,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                   // D format: f32
          | (1u << 7)                                 // A format: bf16
          | (1u << 10)                                // B format: bf16
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// kind::f8f6f4 with A and B e4m3 (format code 0), fp32 D, K-major operands.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                                   // D format: f32
+         | (0u << 7)                                 // A format: e4m3
+         | (0u << 10)                                // B format: e4m3
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }

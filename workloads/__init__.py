@@ -258,6 +258,37 @@ def from_bits(a: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
 
 
+def to_e4m3_bytes(t: torch.Tensor) -> torch.Tensor:
+    """Float tensor -> e4m3fn codes as torch.uint8 (values clamped to +-448 first,
+    then torch's float8_e4m3fn conversion)."""
+    return t.float().clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+# per-tensor scale of the e4m3 activations: x / 2^-4 spreads N(0, 1) over +-64
+E4M3_X_SCALE = 2.0 ** -4
+
+
+def e4m3_weight_scale(call: "ConvCall") -> float:
+    """Power of two near a quarter of the weights' standard deviation, so that the
+    e4m3 codes of w / scale spread over about +-16 (normal range, 3 mantissa bits)."""
+    kt, kr, ks = call.kernel
+    std = 1.0 / np.sqrt(call.Cin * kt * kr * ks)
+    return float(2.0 ** np.round(np.log2(std / 4.0)))
+
+
+def make_inputs_e4m3(workload: str, call: "ConvCall", crop=None) -> dict:
+    """The bf16 recipe of make_inputs (NDHWC) quantised to e4m3fn with per-tensor
+    power-of-two scales: adds x8 (uint8 NDHWC), w8 (uint8 OITRS) and scale = the
+    product of the two scales (the accumulator factor).  bias, residual, gamma as in
+    make_inputs."""
+    base = make_inputs(workload, call, NDHWC, NDHWC, crop=crop)
+    sx, sw = E4M3_X_SCALE, e4m3_weight_scale(call)
+    base["x8"] = to_e4m3_bytes(base["x"].float() / sx).contiguous()
+    base["w8"] = to_e4m3_bytes(base["w"].float() / sw).contiguous()
+    base["scale"] = sx * sw
+    return base
+
+
 def seed_of(workload: str, call: ConvCall) -> int:
     return 1000 * WORKLOAD_IDS[workload] + call.index
 
