@@ -11,12 +11,14 @@ needed to time the convolutions).
 
 Prints one JSON line.  `value` is chain TFLOP/s (algorithmic FLOP of the 30 calls
 / device time of one chain), the chain's input resident in HBM, L2 flushed
-between steps.  `e2e` is the same metric with the chain's input copied in from
-pinned host memory and its output copied out inside the timed region.  `layers`
-holds per-call rows of the ladder (times inside the chain) and of the other
-workloads (the Wan-like chain, the fused 160 blocks, the T=1 image-VAE layers),
-each timed alone after an L2 flush.  `--impl reference` times the CPU oracle on a
-bounded sample of the ladder.
+between steps; the step replays the 30 calls recorded once as a CUDA graph
+(`ladder_eager` holds the same chain issued call by call).  `e2e` is the same
+metric with the chain's input copied in from pinned host memory and its output
+copied out inside the timed region.  `layers` holds per-call rows of the ladder
+(times inside the eager chain) and of the other workloads (the Wan-like chain, the
+fused 160 blocks, the T=1 image-VAE layers, the x2-upsample decoder convolutions,
+the ladder's layers with FP8 e4m3 operands), each timed alone after an L2 flush.
+`--impl reference` times the CPU oracle on a bounded sample of the ladder.
 """
 
 from __future__ import annotations
@@ -52,7 +54,7 @@ KERNEL_SOURCES = ["conv_cm.cu", "conv_cm_kernel.cuh", "conv_cm_halo.cu", "epilog
                   "ptx.cuh", "internal.h"]
 NCU_TRAFFIC = {
     # profiles/conv_cm_ladder_L0_halo.md: L0_0 as in the haloed ladder chain
-    ("6f5e5913bff893d0", "L0_0"): 325141760 + 253436160,
+    ("1372713c2e32f5eb", "L0_0"): 324811520 + 253700352,
 }
 
 
@@ -223,6 +225,8 @@ def workload_config(world=1, extra=None):
                        "1024->1024 x3 @[5,16,16]; conv_out 1024->48; 3x3x3, causal T pad "
                        "(2,0) zero + reflect H,W (1,1); NDHWC in and out",
            "calls_per_step": 30, "layout": "NDHWC",
+           "launch": "the 30 calls recorded once as a CUDA graph (vvc.Chain) and replayed "
+                     "each step",
            "intermediates": "each call but the last writes its output inside a haloed tensor "
                             "(2 zero frames before it, a 1-pixel reflect border around it: the "
                             "next call's padding) and the next call reads it as a valid "
@@ -496,7 +500,99 @@ def time_chain(calls, stream, flush, steps, warmup, world, sampler=None):
     return statistics.mean(step_ms), [statistics.median(t) for t in per_call], wall, chain
 
 
+def time_graph(chain, stream, flush, steps, warmup, world, sampler=None):
+    """Times `steps` replays of a recorded chain (vvc.Chain), L2 flushed before each;
+    returns (mean step ms, wall seconds)."""
+    import video_vae_convolution_gb300 as vvc
+    for _ in range(max(3, warmup)):
+        flush.zero_()
+        chain.run(stream)
+    torch.cuda.synchronize()
+    assert vvc.device_status() == 0
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    if sampler is not None:
+        sampler.begin()
+    evs = []
+    for _ in range(steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        chain.run(stream)
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - t_wall
+    if sampler is not None:
+        sampler.end()
+    status = vvc.device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status}")
+    return statistics.mean(a.elapsed_time(b) for a, b in evs), wall
+
+
+def e4m3_layers(dev, stream, flush, pk, reps):
+    """The ladder's layer classes with FP8 e4m3 operands (FlyDSL PR, the FP8 suite), each
+    as in the haloed chain (valid convolution of a haloed input, haloed output but for
+    conv_out) and timed alone; conv_in (3 input channels) has no e4m3 plan.  Rows carry
+    the fraction of the e4m3 tensor peak, taken as 2 x the measured bf16 burst peak (the
+    nominal dense fp8 / bf16 ratio, 4.5 / 2.25 PFLOP/s).  Also returns the sum over the
+    29 calls (each class time x its repeats)."""
+    import video_vae_convolution_gb300 as vvc
+    rows = []
+    total_ms = total_flop = 0.0
+    ladder = wl.ladder().calls
+    seen = {}
+    for i, call in enumerate(ladder):
+        cls = call_class(call.name)
+        seen[cls] = seen.get(cls, 0) + 1
+    done = set()
+    for i, call in enumerate(ladder):
+        cls = call_class(call.name)
+        if call.Cin % 16 or cls in done:
+            continue
+        done.add(cls)
+        g = torch.Generator(device=dev)
+        g.manual_seed(wl.seed_of("ladder", call))
+        shape = (call.N, call.D + 2, call.H + 2, call.W + 2, call.Cin)
+        x8 = wl.to_e4m3_bytes(torch.randn(shape, generator=g, device=dev) * 16.0)
+        w8 = wl.to_e4m3_bytes(torch.randn((call.Cout, call.Cin) + tuple(call.kernel),
+                                          generator=g, device=dev) * 4.0)
+        wp = vvc.pack_weight_e4m3(w8)
+        kw = {} if i == len(ladder) - 1 else {"out_halo": LADDER_HALO}
+        c = vvc.Conv3d(x8, wp, call.Cout, call.kernel, call.stride, VALID, wl.NDHWC,
+                       wl.NDHWC, call.epi, dtype=vvc.DTYPE_E4M3,
+                       fp8_scale=wl.E4M3_X_SCALE * wl.e4m3_weight_scale(call), **kw)
+        ms = time_alone(c, stream, flush, reps)
+        tf = call.flops / (ms * 1e-3) / 1e12
+        row = layer_row(call, ms, pk, c.launches, wl.NDHWC, "ladder_e4m3",
+                        {"dtype": "e4m3", "frac_e4m3": round(tf / (2 * pk["bf16_tflops"]), 3),
+                         "calls_in_ladder": seen[cls],
+                         "timed": "alone, haloed input as in the chain"})
+        del row["frac_bf16"]  # measured against the e4m3 peak instead
+        # one byte per input and weight element
+        row["gbs"] = round((call.bytes() - call.N * call.Cin * call.D * call.H * call.W -
+                            call.Cout * call.K) / (ms * 1e-3) / 1e9, 1)
+        row["frac_hbm"] = round(row["gbs"] / pk["hbm_gbs"], 3)
+        rows.append(row)
+        total_ms += ms * seen[cls]
+        total_flop += call.flops * seen[cls]
+        del c, wp, x8, w8
+    torch.cuda.empty_cache()
+    summary = {"calls": "the 29 ladder calls with Cin % 16 == 0, each layer class timed alone "
+                        "once and counted for its repeats",
+               "ms_sum": round(total_ms, 4),
+               "tflops": round(total_flop / (total_ms * 1e-3) / 1e12, 2) if total_ms else None,
+               "peak_tflops": 2 * pk["bf16_tflops"],
+               "peak_source": pk["source"] + " bf16 burst x 2 (nominal fp8 / bf16 ratio)"}
+    return rows, summary
+
+
 def run_gpu(args, rank, world):
+    import video_vae_convolution_gb300 as vvc
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
@@ -510,10 +606,13 @@ def run_gpu(args, rank, world):
     # layout staging)
     staging_launches = sum(1 for _, c in calls if c.plan.im2col == 1)
 
+    # per-call rows: the calls issued one by one, an event between each two
+    eager_ms, call_ms, _, _ = time_chain(calls, stream, flush, args.steps, args.warmup, world)
+    # the step: the 30 calls recorded once as a CUDA graph and replayed
+    graph = vvc.Chain([c for _, c in calls], stream)
     sampler = ClockSampler(dev.index)
     sampler.start()
-    ms_step, call_ms, wall, chain = time_chain(calls, stream, flush, args.steps, args.warmup,
-                                               world, sampler)
+    ms_step, wall = time_graph(graph, stream, flush, args.steps, args.warmup, world, sampler)
     clocks = sampler.stop()
     ms_step = max_over_ranks(ms_step, world)
     value = world * total_flop / (ms_step * 1e-3) / 1e12
@@ -535,7 +634,7 @@ def run_gpu(args, rank, world):
                 "kernel": f"vvc::conv_cm_kernel ({dom_cls}: {dom_call.Cin}->{dom_call.Cout} "
                           f"[{dom_call.D},{dom_call.H},{dom_call.W}], {len(members)} calls, "
                           f"{dom_c.launches} launch(es) each)",
-                "share_of_chain": round(sum(m[2] for m in members) / ms_step, 3),
+                "share_of_chain": round(sum(m[2] for m in members) / eager_ms, 3),
                 "peak_source": pk["source"] + " burst bf16",
                 "algorithmic_flop": dom_call.flops, "algorithmic_bytes": dom_call.bytes()}
 
@@ -548,7 +647,7 @@ def run_gpu(args, rank, world):
 
     def e2e_step():
         x0.copy_(host_in, non_blocking=True)
-        chain()
+        graph.run(stream)
         out_host.copy_(y_last, non_blocking=True)
 
     for _ in range(max(2, min(args.warmup, 3))):
@@ -583,16 +682,19 @@ def run_gpu(args, rank, world):
 
     # per-layer rows of the other workloads (each call alone, L2 flushed)
     other, wan = ([], None)
+    e4m3_rows, e4m3 = ([], None)
     if not args.ladder_only:
         other, wan = other_layers(dev, stream, flush, pk, reps=max(3, min(args.steps, 10)))
-    layers += other
+        e4m3_rows, e4m3 = e4m3_layers(dev, stream, flush, pk, reps=max(3, min(args.steps, 10)))
+    layers += other + e4m3_rows
     def wide_stats(rows):
         return {"calls": len(rows), "at_or_above_0.60": sum(r["frac_bf16"] >= 0.6 for r in rows),
                 "min_frac_bf16": min((r["frac_bf16"] for r in rows), default=None)}
 
-    wide = [r for r in layers if r["cin"] >= 128 and r["cout"] >= 128 and
+    bf16 = [r for r in layers if r.get("dtype", "bf16") == "bf16"]
+    wide = [r for r in bf16 if r["cin"] >= 128 and r["cout"] >= 128 and
             r["kernel"] == [3, 3, 3] and r["layout"] == "NDHWC"]
-    narrow = [r for r in layers if (min(r["cin"], r["cout"]) <= 16) and r["layout"] == "NDHWC" and
+    narrow = [r for r in bf16 if (min(r["cin"], r["cout"]) <= 16) and r["layout"] == "NDHWC" and
               r["workload"] != "ladder_per_call_padding"]
     targets = {
         "wide_3x3x3_ge128_ndhwc": wide_stats(
@@ -615,6 +717,11 @@ def run_gpu(args, rank, world):
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": launches_per_step * args.steps,
             "targets": targets, "wan_chain": wan, "ladder_per_call_padding": ladder_plain,
+            "ladder_eager": {"ms_per_step": round(max_over_ranks(eager_ms, world), 4),
+                             "tflops": round(world * total_flop / (eager_ms * 1e-3) / 1e12, 2),
+                             "launch": "the 30 calls issued one by one (the per-call rows "
+                                       "are timed this way)"},
+            "ladder_e4m3": e4m3,
             "layers": layers, "wall_s": round(wall, 3)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         r, ms, threads, desc = oracle_ladder_rate(target_s=12.0)
@@ -635,19 +742,27 @@ def run_case(args):
     work = wl.all_workloads()[args.workload]
     call = next(c for c in work.calls if c.name == args.case)
     lay = wl.NCDHW if args.layout == "ncdhw" else wl.NDHWC
-    inp = wl.make_inputs(args.workload, call, lay, lay)
+    f8 = args.e4m3
+    if f8:
+        # FP8 e4m3 operands (NDHWC), the per-tensor scales of the workloads module
+        lay = wl.NDHWC
+        inp = wl.make_inputs_e4m3(args.workload, call)
+    else:
+        inp = wl.make_inputs(args.workload, call, lay, lay)
     g = lambda k: None if inp[k] is None else inp[k].to(dev)
     tun = None
     if args.tune:
         tun = vvc.Tuning(**{k: int(v) for k, v in (kv.split("=") for kv in args.tune.split(","))})
-    wp = vvc.pack_weight(inp["w"].to(dev))
+    wp = vvc.pack_weight_e4m3(inp["w8"].to(dev)) if f8 else vvc.pack_weight(inp["w"].to(dev))
     epi, extra = call.epi, {}
+    if f8:
+        extra = {"dtype": vvc.DTYPE_E4M3, "fp8_scale": inp["scale"]}
     if args.pad_cache >= 0:
         # padded output + two-frame cache after the fused norm, P history frames
         epi |= vvc.EPI_PAD_CACHE
         extra = {"history_frames": args.pad_cache}
     out_lay = wl.NDHWC if call.upsample else lay
-    x = inp["x"].to(dev)
+    x = inp["x8" if f8 else "x"].to(dev)
     pads = call.pads
     if args.chain_halo and args.workload == "ladder":
         # as in the ladder chain: the input arrives haloed (2 zero frames, a 1-pixel
@@ -655,7 +770,7 @@ def run_case(args):
         # tensor unless this is the chain's last call
         if call.name != "conv_in":
             xp = torch.zeros((call.N, call.D + 2, call.H + 2, call.W + 2, call.Cin),
-                             dtype=torch.bfloat16, device=dev)
+                             dtype=x.dtype, device=dev)
             xp[:, 2:, 1:-1, 1:-1] = x
             x, pads = xp, VALID
         if call.name != "conv_out":
@@ -690,6 +805,8 @@ def run_case(args):
         line["pad_cache"] = args.pad_cache
     if args.chain_halo:
         line["chain_halo"] = True
+    if f8:
+        line["dtype"] = "e4m3"
     print(json.dumps(line), flush=True)
     return 0
 
@@ -798,6 +915,8 @@ def main():
     ap.add_argument("--chain-halo", action="store_true",
                     help="with --workload ladder --case: run the call as in the chained ladder "
                          "(haloed input read as a valid convolution, haloed output)")
+    ap.add_argument("--e4m3", action="store_true",
+                    help="with --case: FP8 e4m3 operands (NDHWC)")
     ap.add_argument("--ladder-only", action="store_true",
                     help="time the ladder chain only (no per-layer rows of the other workloads)")
     ap.add_argument("--pad-cache", type=int, default=-1,

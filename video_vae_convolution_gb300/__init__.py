@@ -355,6 +355,39 @@ class Conv3d:
         return self.y
 
 
+class Chain:
+    """A fixed sequence of prepared calls (Conv3d objects, e.g. the layers of an
+    encoder whose outputs feed the next call) recorded once as a CUDA graph: run()
+    replays every kernel launch of the sequence with one graph launch, without the
+    per-launch host and queue gaps of issuing the calls one by one.  The calls keep
+    their buffers, tensor maps and plans from recording time; refill their inputs in
+    place between runs.  Every call runs once eagerly first (kernel attributes, the
+    first-call device set-up), then the sequence is captured on a side stream."""
+
+    def __init__(self, calls, stream=None):
+        self.calls = list(calls)
+        s = stream if stream is not None else torch.cuda.current_stream()
+        for c in self.calls:
+            _check(c.run(s), "conv3d_fwd")
+        side = torch.cuda.Stream(device=s.device)
+        side.wait_stream(s)
+        torch.cuda.synchronize(s.device)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=side):
+            for c in self.calls:
+                _check(c.run(side), "conv3d_fwd (graph capture)")
+        torch.cuda.synchronize(s.device)
+        self.launches = sum(c.launches for c in self.calls)
+
+    def run(self, stream=None):
+        """Replays the recorded launches on `stream` (default: the current stream)."""
+        if stream is None:
+            self.graph.replay()
+        else:
+            with torch.cuda.stream(stream):
+                self.graph.replay()
+
+
 def conv3d(x, w_packed, Cout, kernel, **kw):
     """Runs one convolution; returns y (and fills value_out / conv_out if asked)."""
     c = Conv3d(x, w_packed, Cout, kernel, **kw)

@@ -351,6 +351,33 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
       q_total = q3;
     }
     tw = static_cast<int>(std::min<long long>(256, round_up(q_total, 16)));
+    // Narrower tiles when the last wave of 256-wide tiles is nearly empty: a layer runs
+    // in ceil(tiles / SMs) rounds of one tile per CTA, and a tile's time shrinks with
+    // its width down to about 208 pixels (below that the per-stage latency sets it), so
+    // the width with the fewest rounds x max(width, 208) wins when it saves at least 3 %.
+    // Only for layers with at least a wave of tiles (smaller ones split the reduction).
+    // (Ladder 256 -> 256 on [9, 64, 64]: 306 tiles = 2 waves + 2 tiles at width 256.)
+    if (tw == 256) {
+      const bool norm_units = (p->epi & CONV3D_EPI_L2NORM_SILU) != 0;
+      const long long per_q = (flat3 ? 1LL : (long long)Do) * p->N *
+                              (norm_units ? 1LL : cdiv(p->Cout, 128));
+      const int sms0 = num_sms();
+      auto cost = [&](int c) {
+        const long long units = per_q * cdiv(q_total, c);
+        return units < sms0 ? -1LL : cdiv(units, sms0) * std::max(c, 208);
+      };
+      const long long c256 = cost(256);
+      if (c256 > 0) {
+        long long best = c256;
+        for (int c = 240; c >= 208; c -= 16) {
+          const long long v = cost(c);
+          if (v > 0 && v * 100 <= c256 * 97 && v < best) {
+            best = v;
+            tw = c;
+          }
+        }
+      }
+    }
   } else if (t.tile_w > 0) {
     tw = t.tile_w;
     rh = t.tile_h > 0 ? t.tile_h : 1;
