@@ -225,8 +225,6 @@ def workload_config(world=1, extra=None):
                        "1024->1024 x3 @[5,16,16]; conv_out 1024->48; 3x3x3, causal T pad "
                        "(2,0) zero + reflect H,W (1,1); NDHWC in and out",
            "calls_per_step": 30, "layout": "NDHWC",
-           "launch": "the 30 calls recorded once as a CUDA graph (vvc.Chain) and replayed "
-                     "each step",
            "intermediates": "each call but the last writes its output inside a haloed tensor "
                             "(2 zero frames before it, a 1-pixel reflect border around it: the "
                             "next call's padding) and the next call reads it as a valid "
@@ -716,6 +714,8 @@ def run_gpu(args, rank, world):
             "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
             "gpu_launches": launches_per_step * args.steps,
+            "launch": "the 30 calls recorded once as a CUDA graph (vvc.Chain) and replayed "
+                      "each step",
             "targets": targets, "wan_chain": wan, "ladder_per_call_padding": ladder_plain,
             "ladder_eager": {"ms_per_step": round(max_over_ranks(eager_ms, world), 4),
                              "tflops": round(world * total_flop / (eager_ms * 1e-3) / 1e12, 2),
