@@ -456,27 +456,58 @@ __global__ void splitk_epilogue_kernel(const float* __restrict__ partial, int sp
 // Same reduction when the epilogue is per element (no L2 norm): one thread per
 // (pixel, 16-channel chunk), so small layers still spread over every SM; adjacent
 // threads read and write adjacent 64-byte chunks of a pixel row.
+// One thread per (pixel, `width` channels): width 8 when Cout % 8 == 0 (16-byte
+// output stores, twice the threads of width 16), else 16.  The partial sums are added
+// in split order from 0 (deterministic); the loads of four splits are issued before
+// their additions so that they overlap.
 __global__ void splitk_epilogue_chunk_kernel(const float* __restrict__ partial, int splits,
-                                             long long M, EpiParams e) {
-  const int chunks = (e.Cout + 15) / 16;
+                                             long long M, EpiParams e, int width) {
+  const int chunks = (e.Cout + width - 1) / width;
   const long long u = blockIdx.x * (long long)blockDim.x + threadIdx.x;
   Pixel px;
   px.valid = u < M * chunks;
   const long long uu = px.valid ? u : 0;
   const long long pp = uu / chunks;
-  const int c0 = static_cast<int>(uu - pp * chunks) * 16;
+  const int c0 = static_cast<int>(uu - pp * chunks) * width;
   px.w = static_cast<int>(pp % e.Wo);
   long long rest = pp / e.Wo;
   px.h = static_cast<int>(rest % e.Ho);
   rest /= e.Ho;
   px.d = static_cast<int>(rest % e.Do);
   px.n = static_cast<int>(rest / e.Do);
-  const int cnt = min(16, e.Cout - c0);
+  const int cnt = min(width, e.Cout - c0);
   const bool vec = (e.Cout % 4) == 0 && cnt == 16;
+  const bool vec8 = (e.Cout % 8) == 0 && width == 8;
   auto load = [&](int c_rel, float(&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = 0.0f;
     if (!px.valid) return;
+    if (vec8) {
+      const float* base = partial + pp * e.Cout + c0 + c_rel;
+      const long long sstride = M * e.Cout;
+      int s = 0;
+      for (; s + 4 <= splits; s += 4) {
+        float4 a[4][2];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4* q = reinterpret_cast<const float4*>(base + (s + k) * sstride);
+          a[k][0] = __ldg(q);
+          a[k][1] = __ldg(q + 1);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          v[0] += a[k][0].x; v[1] += a[k][0].y; v[2] += a[k][0].z; v[3] += a[k][0].w;
+          v[4] += a[k][1].x; v[5] += a[k][1].y; v[6] += a[k][1].z; v[7] += a[k][1].w;
+        }
+      }
+      for (; s < splits; ++s) {
+        const float4* q = reinterpret_cast<const float4*>(base + s * sstride);
+        const float4 lo = __ldg(q), hi = __ldg(q + 1);
+        v[0] += lo.x; v[1] += lo.y; v[2] += lo.z; v[3] += lo.w;
+        v[4] += hi.x; v[5] += hi.y; v[6] += hi.z; v[7] += hi.w;
+      }
+      return;
+    }
     for (int s = 0; s < splits; ++s) {
       const float* src = partial + ((long long)s * M + pp) * e.Cout + c0 + c_rel;
       if (vec) {
@@ -502,10 +533,11 @@ cudaError_t launch_splitk_epilogue(const float* partial, int splits, long long M
                                    const EpiParams& e, cudaStream_t s) {
   const int threads = 128;
   if (!(e.flags & EPI_L2NORM_SILU)) {
-    const long long units = M * ((e.Cout + 15) / 16);
+    const int width = (e.Cout % 8 == 0) ? 8 : 16;
+    const long long units = M * ((e.Cout + width - 1) / width);
     const long long blocks = (units + threads - 1) / threads;
-    splitk_epilogue_chunk_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(partial,
-                                                                                   splits, M, e);
+    splitk_epilogue_chunk_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+        partial, splits, M, e, width);
     return cudaGetLastError();
   }
   const long long blocks = (M + threads - 1) / threads;

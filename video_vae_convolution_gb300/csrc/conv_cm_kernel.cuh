@@ -966,6 +966,8 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         if (lane == 0) mbar_arrive(acce_bar(buf));
       }
     } else if (!p.norm) {
+      const bool dbl_stage = (E.flags & EPI_DEBUG_STORE_CONV) == 0;
+      int nbulk = 0;  // bulk blocks this warp has staged
       for (int local = 0;; ++local) {
         const int tile = cta_tile(p, local);
         if (tile < 0) break;
@@ -987,21 +989,37 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
           if (!warp_live) continue;
           scale_acc<kF8>(r, p.epi.acc_scale);
           if (p.tma_store) {
-            // the warp's previous bulk store has read the staging block
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
             const int qq = t.q0 + j0;
             const int ib = qq / t.pitch;
             const int jb = qq - ib * t.pitch;
             const int wr = t.woff + jb;
             int od, hr;  // output frame and row (a tile of the flattened volume spans frames)
             cm_frame_row(t, t.hoff + ib, od, hr);
-            if (!E.ndhwc && jb + 31 < t.jlim && jb + 31 < t.pitch && j0 + 31 < t.npix &&
-                hr < E.Ho && od < E.Do && wr + 31 < E.Wo && (wr & 7) == 0) {
+            const bool in_row = jb + 31 < t.jlim && jb + 31 < t.pitch && j0 + 31 < t.npix &&
+                                hr < E.Ho && od < E.Do && wr + 31 < E.Wo;
+            const bool bulk_ncdhw = !E.ndhwc && in_row && (wr & 7) == 0;
+            const bool bulk_ndhwc = E.ndhwc && in_row;
+            // Bulk blocks alternate between the two 2 KB halves of the staging block, so a
+            // block waits only for the store before the previous one to have read its half
+            // (the debug conv store takes the second half: one half then).  Any other block
+            // writes the whole staging block and waits for every store to have read it.
+            uint16_t* yt = reinterpret_cast<uint16_t*>(st);
+            if (bulk_ncdhw || bulk_ndhwc) {
+              if (dbl_stage) {
+                yt += (nbulk & 1) * 1024;
+                ++nbulk;
+                if (lane == 0) bulk_wait_read_1();
+              } else if (lane == 0) {
+                bulk_wait_read_all();
+              }
+            } else if (lane == 0) {
+              bulk_wait_read_all();
+            }
+            __syncwarp();
+            if (bulk_ncdhw) {
               // NCDHW: the block goes out as [32 channels][32 pixels] bf16, one 64-byte
               // row per thread (its channel), through bulk tensor stores.  The store's
               // innermost coordinate is the output column, so it must be a multiple of 8.
-              uint16_t* yt = reinterpret_cast<uint16_t*>(st);
               const bool bias = (E.flags & EPI_BIAS) != 0;
               uint32_t wv[16];
 #pragma unroll
@@ -1028,11 +1046,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
               }
               continue;
             }
-            if (E.ndhwc && jb + 31 < t.jlim && jb + 31 < t.pitch && j0 + 31 < t.npix &&
-                hr < E.Ho && od < E.Do && wr + 31 < E.Wo) {
+            if (bulk_ndhwc) {
               // The 32 pixels are one piece of an output row: the block goes out as
               // [32 pixels][32 channels] bf16 through bulk tensor stores.
-              uint16_t* yt = reinterpret_cast<uint16_t*>(st);
               uint16_t* ct = yt + 32 * 32;
               const bool dbg = (E.flags & EPI_DEBUG_STORE_CONV) != 0;
 #pragma unroll

@@ -56,6 +56,13 @@ __device__ __forceinline__ void store_chunk(uint16_t* base, int layout, int C, i
       b.w = v[14] | (uint32_t(v[15]) << 16);
       reinterpret_cast<uint4*>(p)[0] = a;
       reinterpret_cast<uint4*>(p)[1] = b;
+    } else if (cnt == 8 && ((reinterpret_cast<uintptr_t>(p) & 15u) == 0)) {
+      uint4 a;
+      a.x = v[0] | (uint32_t(v[1]) << 16);
+      a.y = v[2] | (uint32_t(v[3]) << 16);
+      a.z = v[4] | (uint32_t(v[5]) << 16);
+      a.w = v[6] | (uint32_t(v[7]) << 16);
+      reinterpret_cast<uint4*>(p)[0] = a;
     } else {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
@@ -224,9 +231,26 @@ __device__ __forceinline__ void epi_store16(const EpiParams& e, const Pixel& px,
   if (e.halo) {
     // NDHWC: the pixel's own position, then its reflected copies / zero neighbours
     auto put = [&](long long off, bool zero) {
+      uint16_t* q = yp + off;
+      if ((cnt == 8 || cnt == 16) && ((reinterpret_cast<uintptr_t>(q) & 15u) == 0)) {
+        // 16-byte stores of 8 channels
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          if (k * 8 >= cnt) break;
+          uint4 a = make_uint4(0u, 0u, 0u, 0u);
+          if (!zero) {
+            a.x = yb[8 * k] | (uint32_t(yb[8 * k + 1]) << 16);
+            a.y = yb[8 * k + 2] | (uint32_t(yb[8 * k + 3]) << 16);
+            a.z = yb[8 * k + 4] | (uint32_t(yb[8 * k + 5]) << 16);
+            a.w = yb[8 * k + 6] | (uint32_t(yb[8 * k + 7]) << 16);
+          }
+          reinterpret_cast<uint4*>(q)[k] = a;
+        }
+        return;
+      }
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        if (i < cnt) yp[off + i] = zero ? uint16_t(0) : yb[i];
+        if (i < cnt) q[i] = zero ? uint16_t(0) : yb[i];
     };
     put(halo_offset(e, px.n, px.d, px.h, px.w, c), false);
     halo_extras(e, px.n, px.d, px.h, px.w, c, put);

@@ -576,25 +576,26 @@ static __device__ __noinline__ void cm_halo_block(const EpiParams& e, const uint
                                 halo_offset(e, nb, od, hh, wr + (u >> 2), cw + 8 * (u & 3))) =
           zero4;
   }
-  for (int j = lane >> 2; j < 32; j += 8) {
-    const int bw = halo_bits(wr + j, e.Wo, e.w0, e.Wy - e.Wo - e.w0, e.w_mode);
-    if (!bw) continue;
+  // halo columns: each W side copies one output column (reflect: 1 and Wo - 2) or
+  // borders one (zero: 0 and Wo - 1); lanes 0-3 write that pixel's 32 channels when it
+  // lies in this block (the pixels halo_bits marks)
+  if (lane >= 4) return;
+  uint16_t* y = static_cast<uint16_t*>(e.y);
+  const bool zc = e.w_mode != 2;
+  for (int cs = 0; cs < 2; ++cs) {
+    if (!(cs ? (e.Wy - e.Wo - e.w0 > 0) : (e.w0 > 0))) continue;
+    const int j = (cs ? (zc ? e.Wo - 1 : e.Wo - 2) : (zc ? 0 : 1)) - wr;
+    if (j < 0 || j >= 32) continue;
     const uint4 val = *reinterpret_cast<const uint4*>(yt + j * 32 + 8 * part);
-    uint16_t* y = static_cast<uint16_t*>(e.y);
-    for (int cs = 0; cs < 2; ++cs) {
-      const int b = cs ? (bw >> 2) : bw;
-      if (!(b & 1)) continue;
-      const int ww = cs ? e.Wo : -1;
-      const bool zc = (b & 2) != 0;
-      *reinterpret_cast<uint4*>(y + halo_offset(e, nb, od, hr, ww, cw + 8 * part)) =
-          zc ? zero4 : val;
-      if (bh & 1)
-        *reinterpret_cast<uint4*>(y + halo_offset(e, nb, od, -1, ww, cw + 8 * part)) =
-            (zc || (bh & 2)) ? zero4 : val;
-      if (bh & 4)
-        *reinterpret_cast<uint4*>(y + halo_offset(e, nb, od, e.Ho, ww, cw + 8 * part)) =
-            (zc || (bh & 8)) ? zero4 : val;
-    }
+    const int ww = cs ? e.Wo : -1;
+    *reinterpret_cast<uint4*>(y + halo_offset(e, nb, od, hr, ww, cw + 8 * part)) =
+        zc ? zero4 : val;
+    if (bh & 1)
+      *reinterpret_cast<uint4*>(y + halo_offset(e, nb, od, -1, ww, cw + 8 * part)) =
+          (zc || (bh & 2)) ? zero4 : val;
+    if (bh & 4)
+      *reinterpret_cast<uint4*>(y + halo_offset(e, nb, od, e.Ho, ww, cw + 8 * part)) =
+          (zc || (bh & 8)) ? zero4 : val;
   }
 }
 
