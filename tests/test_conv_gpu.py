@@ -318,6 +318,31 @@ def test_paired_off_matches_oracle():
     assert gc.c.plan.paired == 0
 
 
+# The split reduction: 8 channels a thread with 16-byte stores when Cout % 8 == 0 (the
+# partial sums of four splits loaded before they are added), 16 a thread otherwise; the
+# sum always runs in split order, so the result is the same as one split's within the
+# conv tolerance and deterministic.
+SPLIT_CASES = [
+    (mk("split_cout40_w8", 1, 64, 3, 6, 50, 40, pads=P1, epi=wl.EPI_BIAS | wl.EPI_RESIDUAL,
+        index=60), 3),
+    (mk("split_cout20_w16", 1, 64, 3, 6, 50, 20, pads=P1, epi=wl.EPI_BIAS, index=61), 2),
+    (mk("split_cout136_six", 1, 128, 2, 5, 30, 136, pads=CR, epi=wl.EPI_BIAS, index=62), 6),
+]
+
+
+@pytest.mark.parametrize("case", SPLIT_CASES, ids=lambda c: c[0].name)
+@pytest.mark.parametrize("out_layout", [wl.NDHWC, wl.NCDHW], ids=["ndhwc", "ncdhw"])
+def test_split_reduction_widths(case, out_layout):
+    call, k = case
+    gc, _ = run_and_check(call, wl.NDHWC, out_layout, tuning=vvc.Tuning(k_splits=k))
+    assert gc.c.plan.k_splits == k and gc.c.launches == 2
+    # deterministic: the same call again gives the same bits
+    rc = gc.c.run()
+    assert rc == vvc.OK
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(wl.bits(gc.c.y.detach().cpu()), gc.y)
+
+
 def test_epilogue_split_k_matches():
     call = mk("epi_split", 1, 64, 3, 5, 70, 160, pads=P1,
               epi=wl.EPI_BIAS | wl.EPI_RESIDUAL | wl.EPI_L2NORM_SILU, index=17)

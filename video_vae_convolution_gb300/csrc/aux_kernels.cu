@@ -282,58 +282,39 @@ cudaError_t launch_im2col_hw(const void* x, int layout, int N, int C, int D, int
 
 // ---- input staging --------------------------------------------------------------------
 // NCDHW [N][C][S] (S = D*H*W) -> NDHWC [N][S][Cp], channels Cin..Cp-1 zero.
-// S % 8 == 0 (every channel row starts on a 16-byte boundary): a block moves up to
-// 128 channels x 128 positions through shared memory.  Each channel row is read as
-// 256 contiguous bytes in 16-byte loads, and the positions' channel rows are
-// written as consecutive 16-byte stores, so with Cp <= 128 a block writes one
-// contiguous range of the output.
-__global__ void __launch_bounds__(256) ncdhw_to_ndhwc_kernel(const uint16_t* __restrict__ x,
-                                                             uint16_t* __restrict__ out, int C,
-                                                             int Cp, long long S) {
-  constexpr int P = 128;
-  __shared__ uint16_t tile[128][P + 2];  // odd word pitch: column reads spread over banks
-  const int n = blockIdx.z;
-  const int c0 = blockIdx.y * 128;
-  const long long s0 = (long long)blockIdx.x * P;
-  const int nc = min(128, Cp - c0);  // output channels of this block (Cp % 8 == 0)
-  const uint16_t* xn = x + (long long)n * C * S;
-  uint16_t* on = out + (long long)n * Cp * S;
-  const int tid = threadIdx.x;
-  if (s0 + P <= S) {
-    // 16 threads per channel row, 8 positions each
-    const int q = (tid & 15) * 8;
-    for (int r = tid >> 4; r < nc; r += 16) {
-      const int c = c0 + r;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (c < C) v = *reinterpret_cast<const uint4*>(xn + (long long)c * S + s0 + q);
-      uint32_t* t = reinterpret_cast<uint32_t*>(&tile[r][q]);
-      t[0] = v.x;
-      t[1] = v.y;
-      t[2] = v.z;
-      t[3] = v.w;
-    }
-  } else {
-    const int pl = tid & (P - 1);
-    const long long sp = s0 + pl;
-    for (int r = tid >> 7; r < nc; r += 2) {
-      const int c = c0 + r;
-      tile[r][pl] = (c < C && sp < S) ? xn[(long long)c * S + sp] : uint16_t(0);
-    }
-  }
-  __syncthreads();
-  const int groups = nc >> 3;  // 16-byte groups per position
-  const int npos = static_cast<int>(S - s0 < P ? S - s0 : P);
-  for (int u = tid; u < npos * groups; u += 256) {
-    const int pl = u / groups, g = u - pl * groups;
-    uint16_t v[8];
+// S % 8 == 0: a thread moves an 8-channel x 8-position block in registers: eight 16-byte
+// loads (8 positions of one channel each), a transpose of the 8 x 8 bf16 block by byte
+// permutes, eight 16-byte stores (8 channels of one position each).  A warp covers 4
+// channel groups x 8 position groups, so each load instruction reads 128 contiguous
+// bytes of 4 channel rows and each store writes 64 contiguous bytes of 8 positions.
+// Grid: x = 512-position pieces, y = 32-channel pieces of Cp, z = batch.
+__global__ void __launch_bounds__(256) ncdhw_to_ndhwc_r8_kernel(const uint16_t* __restrict__ x,
+                                                                uint16_t* __restrict__ out,
+                                                                int C, int Cp, long long S) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = blockIdx.y * 4 + (lane & 3);                        // channel group
+  const long long q = (long long)blockIdx.x * 64 + warp * 8 + (lane >> 2);  // position group
+  if (8 * g >= Cp || 8 * q >= S) return;
+  const uint16_t* xn = x + (long long)blockIdx.z * C * S;
+  uint16_t* on = out + (long long)blockIdx.z * Cp * S;
+  uint4 v[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = tile[8 * g + e][pl];
-    uint4 w;
-    w.x = v[0] | (uint32_t(v[1]) << 16);
-    w.y = v[2] | (uint32_t(v[3]) << 16);
-    w.z = v[4] | (uint32_t(v[5]) << 16);
-    w.w = v[6] | (uint32_t(v[7]) << 16);
-    *reinterpret_cast<uint4*>(on + (s0 + pl) * Cp + c0 + 8 * g) = w;
+  for (int k = 0; k < 8; ++k) {
+    const int c = 8 * g + k;
+    v[k] = (c < C) ? __ldg(reinterpret_cast<const uint4*>(xn + (long long)c * S + 8 * q))
+                   : make_uint4(0u, 0u, 0u, 0u);
+  }
+  auto word = [](const uint4& a, int i) { return i == 0 ? a.x : (i == 1 ? a.y : (i == 2 ? a.z : a.w)); };
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    // position 8q + j: channel 8g + k is element j of v[k]
+    const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;
+    uint4 o;
+    o.x = __byte_perm(word(v[0], j >> 1), word(v[1], j >> 1), sel);
+    o.y = __byte_perm(word(v[2], j >> 1), word(v[3], j >> 1), sel);
+    o.z = __byte_perm(word(v[4], j >> 1), word(v[5], j >> 1), sel);
+    o.w = __byte_perm(word(v[6], j >> 1), word(v[7], j >> 1), sel);
+    *reinterpret_cast<uint4*>(on + (8 * q + j) * Cp + 8 * g) = o;
   }
 }
 
@@ -392,10 +373,10 @@ cudaError_t launch_stage_input(const void* x, int layout, int N, int C, int Cp, 
   if (layout == LAYOUT_NCDHW) {
     const bool vec = (S % 8) == 0 && (reinterpret_cast<uintptr_t>(x) % 16) == 0;
     if (vec) {
-      dim3 grid(static_cast<unsigned>((S + 127) / 128), static_cast<unsigned>((Cp + 127) / 128),
+      dim3 grid(static_cast<unsigned>((S / 8 + 63) / 64), static_cast<unsigned>((Cp + 31) / 32),
                 static_cast<unsigned>(N));
-      ncdhw_to_ndhwc_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x),
-                                                 static_cast<uint16_t*>(out), C, Cp, S);
+      ncdhw_to_ndhwc_r8_kernel<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x),
+                                                    static_cast<uint16_t*>(out), C, Cp, S);
     } else {
       dim3 grid(static_cast<unsigned>((S + 255) / 256), static_cast<unsigned>((Cp + 31) / 32),
                 static_cast<unsigned>(N));
