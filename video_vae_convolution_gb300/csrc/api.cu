@@ -392,8 +392,13 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
     long long best = -1;
     tw = 0;
     rh = 1;
+    // NCDHW output: tile widths that are multiples of 8 keep every 32-pixel block of a row
+    // on a column that is a multiple of 8, where the epilogue stores it with bulk tensor
+    // stores (a block starting elsewhere takes the per-element path)
+    const int wq = p->out_layout == CONV3D_NCDHW ? 8 : 1;
     for (int nt = 1; nt <= 16; ++nt) {
-      const int ctw = static_cast<int>(cdiv(Wo, nt));
+      const int ctw = static_cast<int>(round_up(cdiv(Wo, nt), wq));
+      if (nt > 1 && (long long)(nt - 1) * ctw >= Wo) continue;  // a tile would be empty
       const int run = ctw + p->KS - 1;
       int crh, cN;
       if (run > 256) {
