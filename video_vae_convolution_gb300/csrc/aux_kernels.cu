@@ -108,30 +108,33 @@ __device__ __forceinline__ int pad_index(int i, int L, bool reflect) {
   return i;  // out of [0, L) means zero padding
 }
 
+// The weight repack, block b of nb.
+__device__ __forceinline__ void im2col_repack_weights(const Im2colArgs& a, int b, int nb) {
+  const long long total = (long long)a.Cout * a.KT * a.cp2;
+  const int krs = a.KR * a.KS * a.C;
+  for (long long i = (long long)b * blockDim.x + threadIdx.x; i < total;
+       i += (long long)nb * blockDim.x) {
+    const int kk = static_cast<int>(i % a.cp2);
+    const long long rest = i / a.cp2;
+    const int t = static_cast<int>(rest % a.KT);
+    const long long co = rest / a.KT;
+    uint16_t v = 0;
+    if (kk < krs) {
+      const int rs = kk / a.C, c = kk - rs * a.C;
+      const int tap = t * a.KR * a.KS + rs;
+      v = a.wp[(co * a.KT * a.KR * a.KS + tap) * a.cp + c];
+    }
+    a.wr[i] = v;
+  }
+}
+
 // Grid: x = 256-pixel pieces of an output row, y = output row ho, z = n * D + d;
 // blockIdx.x past the row pieces (x >= xblocks) repacks the weights.
 __global__ void __launch_bounds__(256) im2col_hw_kernel(const Im2colArgs a) {
   const int xblocks = (a.Wo + 255) / 256;
   if (static_cast<int>(blockIdx.x) >= xblocks) {
     if (blockIdx.y != 0 || blockIdx.z != 0) return;
-    // weight repack
-    const long long total = (long long)a.Cout * a.KT * a.cp2;
-    const int krs = a.KR * a.KS * a.C;
-    const int nb = gridDim.x - xblocks;
-    for (long long i = (long long)(blockIdx.x - xblocks) * blockDim.x + threadIdx.x; i < total;
-         i += (long long)nb * blockDim.x) {
-      const int kk = static_cast<int>(i % a.cp2);
-      const long long rest = i / a.cp2;
-      const int t = static_cast<int>(rest % a.KT);
-      const long long co = rest / a.KT;
-      uint16_t v = 0;
-      if (kk < krs) {
-        const int rs = kk / a.C, c = kk - rs * a.C;
-        const int tap = t * a.KR * a.KS + rs;
-        v = a.wp[(co * a.KT * a.KR * a.KS + tap) * a.cp + c];
-      }
-      a.wr[i] = v;
-    }
+    im2col_repack_weights(a, blockIdx.x - xblocks, gridDim.x - xblocks);
     return;
   }
   const int wo = blockIdx.x * 256 + threadIdx.x;
@@ -183,9 +186,16 @@ __global__ void __launch_bounds__(256) im2col_hw_kernel(const Im2colArgs a) {
 // loads are issued before the values are packed (the loop above waits for each
 // load in turn).
 template <int C>
-__global__ void __launch_bounds__(256) im2col_3x3_kernel(const Im2colArgs a) {
+// Grid: x = 256-pixel pieces of an output row, y = output row ho, z = n * D + d, plus one
+// more z slice whose blocks (x = 0, y < wblocks) repack the weights alongside the gather.
+__global__ void __launch_bounds__(256) im2col_3x3_kernel(const Im2colArgs a, int wblocks) {
   const int xblocks = (a.Wo + 255) / 256;
-  if (static_cast<int>(blockIdx.x) >= xblocks) return;  // weights: the generic kernel's blocks
+  if (static_cast<int>(blockIdx.z) == a.N * a.D) {
+    if (blockIdx.x == 0 && static_cast<int>(blockIdx.y) < wblocks)
+      im2col_repack_weights(a, blockIdx.y, wblocks);
+    return;
+  }
+  if (static_cast<int>(blockIdx.x) >= xblocks) return;
   const int wo = blockIdx.x * 256 + threadIdx.x;
   if (wo >= a.Wo) return;
   const int ho = blockIdx.y;
@@ -257,23 +267,20 @@ cudaError_t launch_im2col_hw(const void* x, int layout, int N, int C, int D, int
   const long long wtotal = (long long)Cout * KT * a.cp2;
   const int wblocks_own =
       static_cast<int>(std::min<long long>(152, std::max<long long>(1, (wtotal + 2047) / 2048)));
-  if (KR == 3 && KS == 3 && C >= 1 && C <= 7) {
-    // gather through the unrolled kernel; the generic one only repacks the weights
-    const dim3 g(xblocks, Ho, N * D);
+  if (KR == 3 && KS == 3 && C >= 1 && C <= 7 && (long long)N * D < 65535) {
+    // gather through the unrolled kernel, the weight repack in the same launch (blocks of
+    // an extra z slice, up to Ho of them)
+    const int wb = std::min(wblocks_own, Ho);
+    const dim3 g(xblocks, Ho, N * D + 1);
     switch (C) {
-      case 1: im2col_3x3_kernel<1><<<g, 256, 0, s>>>(a); break;
-      case 2: im2col_3x3_kernel<2><<<g, 256, 0, s>>>(a); break;
-      case 3: im2col_3x3_kernel<3><<<g, 256, 0, s>>>(a); break;
-      case 4: im2col_3x3_kernel<4><<<g, 256, 0, s>>>(a); break;
-      case 5: im2col_3x3_kernel<5><<<g, 256, 0, s>>>(a); break;
-      case 6: im2col_3x3_kernel<6><<<g, 256, 0, s>>>(a); break;
-      default: im2col_3x3_kernel<7><<<g, 256, 0, s>>>(a); break;
+      case 1: im2col_3x3_kernel<1><<<g, 256, 0, s>>>(a, wb); break;
+      case 2: im2col_3x3_kernel<2><<<g, 256, 0, s>>>(a, wb); break;
+      case 3: im2col_3x3_kernel<3><<<g, 256, 0, s>>>(a, wb); break;
+      case 4: im2col_3x3_kernel<4><<<g, 256, 0, s>>>(a, wb); break;
+      case 5: im2col_3x3_kernel<5><<<g, 256, 0, s>>>(a, wb); break;
+      case 6: im2col_3x3_kernel<6><<<g, 256, 0, s>>>(a, wb); break;
+      default: im2col_3x3_kernel<7><<<g, 256, 0, s>>>(a, wb); break;
     }
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
-    Im2colArgs aw = a;
-    aw.Wo = 0;  // no row pieces: every block of this launch repacks weights
-    im2col_hw_kernel<<<dim3(wblocks_own, 1, 1), 256, 0, s>>>(aw);
     return cudaGetLastError();
   }
   im2col_hw_kernel<<<dim3(xblocks + wblocks, Ho, N * D), 256, 0, s>>>(a);
