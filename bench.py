@@ -225,10 +225,10 @@ def workload_config(world=1, extra=None):
                        "1024->1024 x3 @[5,16,16]; conv_out 1024->48; 3x3x3, causal T pad "
                        "(2,0) zero + reflect H,W (1,1); NDHWC in and out",
            "calls_per_step": 30, "layout": "NDHWC",
-           "intermediates": "each call but the last writes its output inside a haloed tensor "
-                            "(2 zero frames before it, a 1-pixel reflect border around it: the "
-                            "next call's padding) and the next call reads it as a valid "
-                            "convolution; conv_in pads the model input itself",
+           "intermediates": "each call but the last writes its output inside a tensor with a "
+                            "1-pixel reflect border (the next call's spatial padding) and the "
+                            "next call applies only the causal T padding; conv_in pads the "
+                            "model input itself",
            "l2": "flushed between steps (256 MiB write, untimed); inside a step each call "
                  "reads the previous call's output",
            "inputs": "seeded synthetic: x N(0,1) bf16, weights N(0,1/sqrt(fan_in)) bf16",
@@ -416,17 +416,19 @@ def other_layers(dev, stream, flush, pk, reps):
     return rows, wan
 
 
-LADDER_HALO = ((2, 0, wl.ZERO), (1, 1, wl.REFLECT), (1, 1, wl.REFLECT))
+# chained ladder: each intermediate carries the next call's spatial (reflect) padding as
+# a 1-pixel halo; the next call applies the causal T padding itself
+LADDER_HALO = ((0, 0, wl.ZERO), (1, 1, wl.REFLECT), (1, 1, wl.REFLECT))
+CAUSAL_T = ((2, 0, wl.ZERO), (0, 0, wl.ZERO), (0, 0, wl.ZERO))
 VALID = ((0, 0, wl.ZERO),) * 3
 
 
 def build_ladder(dev, halo):
     """The 30 ladder calls on the device, each reading the previous call's output.
-    halo: every call but the last writes its output inside a haloed tensor (two
-    zero frames before it, the reflect border around it) and every call but the
-    first reads the previous haloed tensor as a valid convolution; otherwise each
-    call applies its own causal + reflect padding.  Returns (calls, pinned host
-    copy of the chain's input)."""
+    halo: every call but the last writes its output inside a tensor with a 1-pixel
+    reflect border (the next call's spatial padding) and every call but the first reads
+    it with only the causal T padding of its own; otherwise each call applies its own
+    causal + reflect padding.  Returns (calls, pinned host copy of the chain's input)."""
     import video_vae_convolution_gb300 as vvc
     calls = []
     x = None
@@ -441,7 +443,7 @@ def build_ladder(dev, halo):
             inp = {"w": wl.make_inputs("ladder", call, wl.NDHWC, wl.NDHWC, crop=(1, 3, 3))["w"]}
         wp = vvc.pack_weight(inp["w"].to(dev))
         last = i == len(ladder) - 1
-        pads = call.pads if (i == 0 or not halo) else VALID
+        pads = call.pads if (i == 0 or not halo) else CAUSAL_T
         kw = {"out_halo": LADDER_HALO} if (halo and not last) else {}
         c = vvc.Conv3d(x, wp, call.Cout, call.kernel, call.stride, pads, wl.NDHWC, wl.NDHWC,
                        call.epi, **kw)
@@ -555,13 +557,13 @@ def e4m3_layers(dev, stream, flush, pk, reps):
         done.add(cls)
         g = torch.Generator(device=dev)
         g.manual_seed(wl.seed_of("ladder", call))
-        shape = (call.N, call.D + 2, call.H + 2, call.W + 2, call.Cin)
+        shape = (call.N, call.D, call.H + 2, call.W + 2, call.Cin)
         x8 = wl.to_e4m3_bytes(torch.randn(shape, generator=g, device=dev) * 16.0)
         w8 = wl.to_e4m3_bytes(torch.randn((call.Cout, call.Cin) + tuple(call.kernel),
                                           generator=g, device=dev) * 4.0)
         wp = vvc.pack_weight_e4m3(w8)
         kw = {} if i == len(ladder) - 1 else {"out_halo": LADDER_HALO}
-        c = vvc.Conv3d(x8, wp, call.Cout, call.kernel, call.stride, VALID, wl.NDHWC,
+        c = vvc.Conv3d(x8, wp, call.Cout, call.kernel, call.stride, CAUSAL_T, wl.NDHWC,
                        wl.NDHWC, call.epi, dtype=vvc.DTYPE_E4M3,
                        fp8_scale=wl.E4M3_X_SCALE * wl.e4m3_weight_scale(call), **kw)
         ms = time_alone(c, stream, flush, reps)
@@ -765,14 +767,14 @@ def run_case(args):
     x = inp["x8" if f8 else "x"].to(dev)
     pads = call.pads
     if args.chain_halo and args.workload == "ladder":
-        # as in the ladder chain: the input arrives haloed (2 zero frames, a 1-pixel
-        # border) and is read as a valid convolution; the output goes into a haloed
-        # tensor unless this is the chain's last call
+        # as in the ladder chain: the input arrives with a 1-pixel spatial border and
+        # the call applies the causal T padding; the output goes into a haloed tensor
+        # unless this is the chain's last call
         if call.name != "conv_in":
-            xp = torch.zeros((call.N, call.D + 2, call.H + 2, call.W + 2, call.Cin),
+            xp = torch.zeros((call.N, call.D, call.H + 2, call.W + 2, call.Cin),
                              dtype=x.dtype, device=dev)
-            xp[:, 2:, 1:-1, 1:-1] = x
-            x, pads = xp, VALID
+            xp[:, :, 1:-1, 1:-1] = x
+            x, pads = xp, CAUSAL_T
         if call.name != "conv_out":
             extra = dict(extra, out_halo=LADDER_HALO)
     c = vvc.Conv3d(x, wp, call.Cout, call.kernel, call.stride, pads, lay,

@@ -34,6 +34,11 @@ Z, R = wl.ZERO, wl.REFLECT
 CR = ((2, 0, Z), (1, 1, R), (1, 1, R))
 VALID = ((0, 0, Z),) * 3
 LADDER_HALO = ((2, 0, Z), (1, 1, R), (1, 1, R))
+# the chain form the benchmark runs: a spatial halo only, and every later call applies
+# the causal T padding itself (its kernel leaves out the all-padding temporal taps)
+HW_HALO = ((0, 0, Z), (1, 1, R), (1, 1, R))
+CAUSAL_T = ((2, 0, Z), (0, 0, Z), (0, 0, Z))
+CHAIN_FORMS = {"t_halo": (LADDER_HALO, VALID, 2), "t_pad": (HW_HALO, CAUSAL_T, 0)}
 SENTINEL = 0x40E0  # bf16 7.0: the caller's contents of the T halo frames
 
 
@@ -179,10 +184,14 @@ def test_output_halo_rejected_combinations():
                        y=torch.zeros((1, 6, 8, 18, 32), dtype=torch.bfloat16, device=dev), **kw)
 
 
-def test_ladder_chained_through_halos():
+@pytest.mark.parametrize("form", sorted(CHAIN_FORMS))
+def test_ladder_chained_through_halos(form):
     """The 30-call encoder ladder with haloed intermediates: conv_in reads the model
     input with its causal + reflect padding and writes a haloed output; every
-    later call reads the previous haloed tensor as a valid convolution."""
+    later call reads the previous haloed tensor, as a valid convolution (t_halo: two
+    zero frames lead each intermediate) or with the causal T padding applied by the
+    call itself (t_pad: spatial halo only)."""
+    halo, later_pads, lead = CHAIN_FORMS[form]
     dev = torch.device("cuda")
     w = wl.ladder()
     prev = None          # previous haloed output (device)
@@ -194,17 +203,17 @@ def test_ladder_chained_through_halos():
         if prev is None:
             x, pads = inp["x"].to(dev), call.pads
         else:
-            x, pads = prev, VALID
+            x, pads = prev, later_pads
         Do, Ho, Wo = call.out_dims()
         if last:
             c = vvc.Conv3d(x, wp, call.Cout, call.kernel, call.stride, pads, wl.NDHWC, wl.NDHWC,
                            vvc.EPI_DEBUG_STORE_CONV)
         else:
-            y = torch.full((1, Do + 2, Ho + 2, Wo + 2, call.Cout), 7.0, dtype=torch.bfloat16,
+            y = torch.full((1, Do + lead, Ho + 2, Wo + 2, call.Cout), 7.0, dtype=torch.bfloat16,
                            device=dev)
-            y[:, :2] = 0
+            y[:, :lead] = 0
             c = vvc.Conv3d(x, wp, call.Cout, call.kernel, call.stride, pads, wl.NDHWC, wl.NDHWC,
-                           vvc.EPI_DEBUG_STORE_CONV, y=y, out_halo=LADDER_HALO)
+                           vvc.EPI_DEBUG_STORE_CONV, y=y, out_halo=halo)
         if prev is not None:
             assert c.plan.launches == 1 + (1 if c.plan.k_splits > 1 else 0), call.name
         c()
@@ -212,12 +221,12 @@ def test_ladder_chained_through_halos():
         assert vvc.device_status() == 0
         conv = _bits(c.conv_out)
         out = _bits(c.y)
-        inner = out if last else out[:, 2:, 1:-1, 1:-1, :]
+        inner = out if last else out[:, lead:, 1:-1, 1:-1, :]
         # no epilogue ops: the output is B(conv) itself
         np.testing.assert_array_equal(inner, conv)
         if not last:
-            exp = _expected_halo(inner, LADDER_HALO)
-            exp[:, :2] = 0
+            exp = _expected_halo(inner, halo)
+            exp[:, :lead] = 0
             np.testing.assert_array_equal(out, exp)
         # the oracle on the unpadded input with the call's own padding
         xb = wl.bits(inp["x"])

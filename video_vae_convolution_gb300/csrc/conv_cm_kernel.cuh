@@ -183,6 +183,37 @@ __device__ __forceinline__ void stage_range(const ConvCMParams& p, int split, in
   e = min(p.stages_total, b + p.stages_per_split);
 }
 
+// The tile's stage range: its split's slice of the reduction, without the stages whose
+// temporal tap reads only T padding for every output frame of the tile (the frames next
+// to a zero-padded T edge: the causal pad makes taps 0 and 1 of output frame 0 and tap
+// 0 of frame 1 pure zeros).  Stages run in (t, r, s, chunk) order, t slowest, so those
+// stages are a prefix and a suffix of the range.  A unit left with no stage keeps its
+// first one (it reads zeros and yields the zero partial sum).  Not for the paired
+// schedule, which orders stages differently, nor the gather mode (its own producers).
+template <bool kPair, bool kGather>
+__device__ __forceinline__ void tile_stage_range(const ConvCMParams& p, const TileCoord& tc,
+                                                 int& b, int& e) {
+  stage_range(p, tc.split, b, e);
+  if (kPair || kGather || p.KT == 1) return;
+  int f_lo = tc.od, f_hi = tc.od;  // output frames of the tile
+  if (p.flat3) {
+    const int plane = p.H * p.W;
+    f_lo = (tc.twi * p.tw) / plane;
+    f_hi = (tc.twi * p.tw + p.tw - 1) / plane;
+  }
+  const int t_min = max(0, p.pt - f_hi * p.st);
+  const int t_max = min(p.KT - 1, p.D - 1 + p.pt - f_lo * p.st);
+  if (t_min == 0 && t_max == p.KT - 1) return;
+  const int s_t = p.stages_total / p.KT;
+  const int lo = max(b, t_min * s_t), hi = min(e, (t_max + 1) * s_t);
+  if (lo < hi) {
+    b = lo;
+    e = hi;
+  } else {
+    e = b + 1;
+  }
+}
+
 // The CTA's l-th tile, or -1 past its last.  CTAs take units of tpu consecutive
 // tiles round-robin (tpu > 1 keeps the channel tiles of a pixel tile together).
 __device__ __forceinline__ int cta_tile(const ConvCMParams& p, int l) {
@@ -462,7 +493,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const uint32_t tx = act_role ? p.act_tx
                                      : (last_ct ? p.tx_bytes_last : p.tx_bytes) - p.act_tx;
         int it_b, it_e;
-        stage_range(p, tc.split, it_b, it_e);
+        tile_stage_range<kPair, kGather>(p, tc, it_b, it_e);
         StageCoord sc = kPair ? pair_begin(p) : decode_stage(p, it_b);
         // weight L2 prefetch (plain schedule): pf runs wpref stages ahead of sc
         const bool pref = !kPair && !act_role && p.wpref > 0;
@@ -635,7 +666,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + static_cast<uint32_t>(buf * p.acc_cols);
         int it_b, it_e;
-        stage_range(p, tc.split, it_b, it_e);
+        tile_stage_range<kPair, kGather>(p, tc, it_b, it_e);
         uint32_t acc = 0u;
         int ch = it_b % p.n_chunks;
         StageCoord psc = pair_begin(p);  // paired schedule only
@@ -826,7 +857,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         const TileCoord tc = decode_tile(p, tile);
         const int w0 = tc.twi * p.tw;
         int it_b, it_e;
-        stage_range(p, tc.split, it_b, it_e);
+        tile_stage_range<kPair, kGather>(p, tc, it_b, it_e);
         StageCoord sc = kPair ? pair_begin(p) : decode_stage(p, it_b);
         for (int it = it_b; it < it_e; ++it, kPair ? pair_next(p, sc) : next_stage(p, sc)) {
           if (!mbar_wait(full_bar(slot), phase, abort_flag, lim)) {
