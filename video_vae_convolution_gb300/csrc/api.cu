@@ -513,6 +513,18 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   const long long act_rows = std::max<long long>((long long)k.rh * k.run_pitch,
                                                  k.N + (halo ? p->KS - 1 : 0));
   k.act_bytes = static_cast<uint32_t>(round_up(round_up(act_rows, 8) * k.row_bytes, 1024));
+  // Leading output frames whose first temporal taps read only the T padding have shorter
+  // tiles (the kernel leaves those stages out).  With long tiles (36 stages or more, taps
+  // folded into halo stages) they go last in the tile order, so that every CTA's last
+  // round takes some of them: ladder 256->256 at [17, 128, 128] 0.525 -> 0.514 ms, at
+  // [9, 64, 64] 0.105 -> 0.099 ms.  With shorter tiles the run of short tiles at the end
+  // is bound by their epilogues and the plain order is faster (128->128: 0.518 against
+  // 0.549 ms).  (Not for the paired schedule, which keeps every stage.)
+  if (!flat3 && halo && p->KT > 1 && p->pad[0].before > 0 && Do > 1 &&
+      k.stages_total >= 36) {
+    const int dc = static_cast<int>(cdiv(p->pad[0].before, p->stride[0]));
+    k.d_cheap = dc < Do ? dc : 0;
+  }
   const uint32_t wgt_bytes = static_cast<uint32_t>(k.taps_per_stage * k.wtap_rows * k.row_bytes);
   k.stage_bytes = k.act_bytes + wgt_bytes;
   k.tiles_c = static_cast<int>(cdiv(p->Cout, 128));
@@ -602,6 +614,7 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
     splits = choose_splits(t, par, total, sms, &per);
     if (splits == 1) {
       k.pair = 1;
+      k.d_cheap = 0;  // every stage of the paired schedule runs
       k.stages_total = total;
     }
   }

@@ -66,7 +66,7 @@ struct TileCoord {
 };
 
 // Tile index, fastest first: channel tile, split, output depth, W tile, H tile,
-// batch.  CTAs run consecutive tiles at the same time, so with the output depth
+// batch (with d_cheap, the output depths past the first d_cheap ones, then those).  CTAs run consecutive tiles at the same time, so with the output depth
 // next to the channel tile they share input rows across all output depths while
 // those rows are still in L2 (the 3-D layers read their input from HBM about once).
 __device__ __forceinline__ TileCoord decode_tile(const ConvCMParams& p, int tile) {
@@ -80,8 +80,24 @@ __device__ __forceinline__ TileCoord decode_tile(const ConvCMParams& p, int tile
   }
   c.split = tile % p.k_splits;
   tile /= p.k_splits;
-  c.od = tile % p.tiles_d;
-  tile /= p.tiles_d;
+  if (p.d_cheap) {
+    // the tiles of the first d_cheap output frames (shorter: they leave out temporal taps
+    // that read only padding) come after all others, so that every CTA's last round
+    // takes some of them
+    const int full = p.tiles_d - p.d_cheap;
+    const int n_full = full * p.tiles_w * p.tiles_h * p.epi.N;
+    if (tile < n_full) {
+      c.od = p.d_cheap + tile % full;
+      tile /= full;
+    } else {
+      tile -= n_full;
+      c.od = tile % p.d_cheap;
+      tile /= p.d_cheap;
+    }
+  } else {
+    c.od = tile % p.tiles_d;
+    tile /= p.tiles_d;
+  }
   c.twi = tile % p.tiles_w;
   tile /= p.tiles_w;
   c.thi = tile % p.tiles_h;
