@@ -210,7 +210,7 @@ template <bool kPair, bool kGather>
 __device__ __forceinline__ void tile_stage_range(const ConvCMParams& p, const TileCoord& tc,
                                                  int& b, int& e) {
   stage_range(p, tc.split, b, e);
-  if (kPair || kGather || p.KT == 1) return;
+  if (kPair || kGather || !p.skip_pad) return;
   int f_lo = tc.od, f_hi = tc.od;  // output frames of the tile
   if (p.flat3) {
     const int plane = p.H * p.W;

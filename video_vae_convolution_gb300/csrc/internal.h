@@ -125,6 +125,8 @@ struct ConvCMParams {
                            // (needs stride 1 and no H / W padding; T zero padding reads
                            // positions outside the volume)
   int tiles_d;             // output frames in the tile index (1 with flat3)
+  int skip_pad;            // 1: tiles leave out the stages whose temporal tap reads only
+                           // T padding
   int d_cheap;             // leading output frames whose tiles leave out all-padding
                            // temporal taps; the tile order puts them last (0 = plain order)
   int nbox;                // activation boxes per row of the tile (halo: 1..2, direct: 1)
