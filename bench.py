@@ -420,7 +420,6 @@ def other_layers(dev, stream, flush, pk, reps):
 # a 1-pixel halo; the next call applies the causal T padding itself
 LADDER_HALO = ((0, 0, wl.ZERO), (1, 1, wl.REFLECT), (1, 1, wl.REFLECT))
 CAUSAL_T = ((2, 0, wl.ZERO), (0, 0, wl.ZERO), (0, 0, wl.ZERO))
-VALID = ((0, 0, wl.ZERO),) * 3
 
 
 def build_ladder(dev, halo):
