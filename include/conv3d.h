@@ -230,6 +230,11 @@ typedef struct {
   int32_t prefetch;    /* weight L2 prefetch distance in pipeline stages: 0 auto (on for
                           layers whose CTAs run few tiles, so that every weight slice is a
                           first read from HBM), -1 off, > 0 that many stages ahead */
+  int32_t compact;     /* 0 auto, 1 on, 2 off: tiles over the flattened volume (flat = 2
+                          below) leave out the KR - 1 input rows under each frame's last
+                          output row, so that every tile position is on an output row (the
+                          activations then come through a TMA im2col map).  Auto: on when
+                          that gives fewer tiles than both other flat forms */
 } conv3d_tuning;
 
 /* ---- weight packing ([cuDNN page] "Weight Packing") ------------------------------ */
@@ -321,7 +326,8 @@ typedef struct {
                                tensor stores (channel-major kernel) */
   int32_t flat;             /* channel-major tiles: 0 rows of pixels, 1 runs of the
                                flattened H*W plane, 2 runs of the flattened D*H*W volume
-                               (tiles span frames) */
+                               (tiles span frames), 3 runs of the flattened volume of
+                               output rows only (tiles span frames) */
 } conv3d_plan_info;
 
 int conv3d_plan(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_plan_info* info);
@@ -386,7 +392,7 @@ const char* conv3d_status_string(int status);
  * history_frames, conv3d_tuning gained pair; conv3d_plan, l2norm_silu_pad and the GroupNorm
  * calls were added.  3.00: conv3d_params gained out_halo and input_upsample.  3.10:
  * conv3d_params gained dtype and fp8_scale; conv3d_pack_weight_e4m3 and
- * conv3d_packed_weight_bytes_e4m3 were added. */
+ * conv3d_packed_weight_bytes_e4m3 were added.  3.20: conv3d_tuning gained compact. */
 int conv3d_version(void);
 
 /* sizeof() of the ABI structs, for bindings to check their mirrors:

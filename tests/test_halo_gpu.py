@@ -111,30 +111,68 @@ FLAT3_CASES = [
 ]
 
 
-@pytest.mark.parametrize("case", FLAT3_CASES, ids=lambda c: c[0].name)
+# Compact volume tiles (conv3d_tuning.compact): the flattened volume without the input
+# rows below each frame's last output row, read through a TMA im2col map.  Tiles span
+# frames (and, past the last one, the next batch item's rows or the zero fill).
+COMPACT_CASES = [
+    (wl.ConvCall("compact_two_ctiles", 1, 128, 6, 12, 14, 136, pads=CAUSAL_T, epi=wl.EPI_BIAS,
+                 index=92), dict(k_splits=1)),
+    (wl.ConvCall("compact_batch2", 2, 64, 4, 10, 10, 64, pads=CAUSAL_T, index=93),
+     dict(k_splits=1)),
+    (wl.ConvCall("compact_split", 1, 256, 5, 18, 18, 128, pads=CAUSAL_T, epi=wl.EPI_BIAS,
+                 index=94), None),
+    (wl.ConvCall("compact_kt1", 1, 64, 5, 10, 12, 64, kernel=(1, 3, 3), pads=VALID, index=95),
+     dict(k_splits=1)),
+    (wl.ConvCall("compact_t_both", 1, 64, 5, 10, 10, 64, pads=((1, 1, Z), (0, 0, Z), (0, 0, Z)),
+                 index=96), None),
+]
+
+
+def _flat_form(call, inp, tune, compact):
+    tuning = vvc.Tuning(**dict(tune or {}, compact=compact))
+    gc = GpuCall(call, inp, wl.NDHWC, wl.NDHWC, tuning=tuning)
+    if compact == 1:
+        assert gc.c.plan.flat == 3, call.name
+    return gc, tuning
+
+
+@pytest.mark.parametrize("case", FLAT3_CASES + COMPACT_CASES, ids=lambda c: c[0].name)
 def test_flat_volume_tiles(case):
+    """Both forms of volume tiles on the same inputs: the tiled map over the whole
+    volume (halo rows included) and the compact im2col form; each against the oracle,
+    and bit for bit equal to each other where their stage schedules are the same."""
     call, tune = case
     inp = wl.make_inputs("test", call, wl.NDHWC, wl.NDHWC)
-    tuning = vvc.Tuning(**tune) if tune else None
-    gc = GpuCall(call, inp, wl.NDHWC, wl.NDHWC, tuning=tuning)
-    assert gc.c.plan.flat == 2, call.name
+    tiled, _ = _flat_form(call, inp, tune, 2)
+    if call.name.startswith("flat3"):
+        assert tiled.c.plan.flat == 2, call.name
     if call.name == "flat3_paired":
-        assert gc.c.plan.paired == 1
-    check_conv(gc.conv, full_reference(gc), call.name)
-    check_epilogue(gc)
+        assert tiled.c.plan.paired == 1
+    comp, tuning = _flat_form(call, inp, tune, 1)
+    assert comp.c.plan.paired == 0
+    ref = full_reference(comp)
+    check_conv(comp.conv, ref, call.name + " compact")
+    check_epilogue(comp)
+    if tiled.c.plan.paired or tiled.c.plan.k_splits != comp.c.plan.k_splits:
+        check_conv(tiled.conv, ref, call.name + " tiled")
+        check_epilogue(tiled)
+    else:
+        np.testing.assert_array_equal(comp.conv, tiled.conv)
+        np.testing.assert_array_equal(comp.y, tiled.y)
     # and into a haloed tensor: the same output inside it
     dev = torch.device("cuda")
-    Do, Ho, Wo = gc.c.out_dims
-    y = torch.full((1, Do + 2, Ho + 2, Wo + 2, call.Cout), 7.0, dtype=torch.bfloat16, device=dev)
+    Do, Ho, Wo = comp.c.out_dims
+    y = torch.full((call.N, Do + 2, Ho + 2, Wo + 2, call.Cout), 7.0, dtype=torch.bfloat16,
+                   device=dev)
     g = lambda k: None if inp[k] is None else inp[k].to(dev)
-    c = vvc.Conv3d(inp["x"].to(dev), gc.w_packed, call.Cout, call.kernel, call.stride,
+    c = vvc.Conv3d(inp["x"].to(dev), comp.w_packed, call.Cout, call.kernel, call.stride,
                    call.pads, wl.NDHWC, wl.NDHWC, call.epi, bias=g("bias"),
                    residual=g("residual"), y=y, out_halo=LADDER_HALO, tuning=tuning)
-    assert c.plan.flat == 2
+    assert c.plan.flat == 3
     c()
     torch.cuda.synchronize()
     assert vvc.device_status() == 0
-    np.testing.assert_array_equal(_bits(y), _expected_halo(gc.y, LADDER_HALO))
+    np.testing.assert_array_equal(_bits(y), _expected_halo(comp.y, LADDER_HALO))
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c[0].name)

@@ -159,6 +159,53 @@ def test_plan_paired_last_chunks():
     assert _plan(_valid(Cin=96, Cout=96, KT=1, KR=1, KS=1)).paired == 0
 
 
+def _causal(**kw):
+    p = _valid(**kw)
+    p.pad[0].before = 2
+    return p
+
+
+def test_plan_compact_volume_tiles():
+    # 256 -> 256 on [9, 64, 64] with a 1-pixel halo input and the causal T padding: the
+    # per-frame flat tiles need 17 x 9 = 153 tiles of 256 positions per channel tile
+    # (3 rounds of 306 work items on 152 SMs, so 208-wide tiles); the volume without the
+    # two halo rows under each frame needs 149 (298 work items, 2 rounds)
+    p = _causal(Cin=256, Cout=256, D=9, H=66, W=66)
+    auto, off = _plan(p), _plan(p, vvc.Tuning(compact=2))
+    assert (auto.flat, auto.mma_n, auto.k_splits) == (3, 256, 1)
+    assert (off.flat, off.mma_n) == (1, 208)
+    # 16x16 planes with a halo (the ladder's 512 -> 512 at [5, 16, 16]): 6 compact
+    # tiles against 7 volume tiles that include the halo rows
+    small = _causal(Cin=512, Cout=512, D=5, H=18, W=18)
+    assert _plan(small).flat == 3
+    assert _plan(small, vvc.Tuning(compact=2)).flat == 2
+    # forced on where it saves nothing (256^2 planes: the same 258 tiles per frame)
+    big = _causal(Cin=128, Cout=128, D=3, H=66, W=258)
+    assert _plan(big).flat == 1
+    assert _plan(big, vvc.Tuning(compact=1)).flat == 3
+    # not applicable: H zero padding in the call (flat volume tiles need none), a T
+    # padding outside the im2col corner range [-16, 15], one frame, NCDHW output, the
+    # fused norm
+    hp = _params(Cin=64, Cout=64, D=5, H=16, W=18)
+    hp.pad[2].before = hp.pad[2].after = 0
+    assert _plan(hp, vvc.Tuning(compact=1)).flat != 3
+    far = _causal(Cin=64, Cout=64, D=40, H=18, W=18, KT=1)
+    far.pad[0].before = 17
+    assert _plan(far, vvc.Tuning(compact=1)).flat != 3
+    assert _plan(_valid(Cin=64, Cout=64, D=1, H=18, W=18, KT=1),
+                 vvc.Tuning(compact=1)).flat != 3
+    nc = _causal(Cin=64, Cout=64, D=5, H=18, W=18)
+    nc.out_layout = vvc.NCDHW
+    assert _plan(nc, vvc.Tuning(compact=1)).flat != 3
+    nm = _causal(Cin=64, Cout=64, D=5, H=18, W=18)
+    nm.epi, nm.gamma = vvc.EPI_L2NORM_SILU, 0x300000
+    assert _plan(nm, vvc.Tuning(compact=1)).flat != 3
+    # never with paired last chunks (their half-width copies use the tiled map)
+    pr = _causal(Cin=96, Cout=64, D=6, H=14, W=14)
+    info = _plan(pr, vvc.Tuning(compact=1, k_splits=1))
+    assert info.flat == 3 and info.paired == 0
+
+
 def test_plan_bulk_store():
     # NCDHW output takes bulk stores when its rows are 16-byte multiples (Wo % 8 == 0)
     # and no NDHWC debug store runs beside them; NDHWC when Cout % 8 == 0

@@ -44,7 +44,7 @@ ERR_DEVICE_TIMEOUT = -7
 ERR_SCRATCH_LIMIT = -8
 
 # ABI version of the C library this binding mirrors (major * 100 + minor).
-ABI_VERSION = 310
+ABI_VERSION = 320
 
 # Every function the C header declares (checked by the tests against include/conv3d.h).
 EXPORTS = (
@@ -92,7 +92,7 @@ class Params(ctypes.Structure):
 class Tuning(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "tile_w", "tile_h", "R", "kc", "BN", "halo", "stages", "k_splits", "kernel",
-        "inject", "timeout_ms", "im2col", "pair", "prefetch")]
+        "inject", "timeout_ms", "im2col", "pair", "prefetch", "compact")]
 
     def __init__(self, **kw):
         super().__init__()

@@ -338,7 +338,16 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
                         p->out_layout == CONV3D_NDHWC &&
                         !(p->epi & CONV3D_EPI_L2NORM_SILU) && t.kernel != 3 &&
                         q3 < 0x7fffff00LL;
-  bool flat3 = false;
+  // Compact volume: the flattened volume without the KR - 1 input rows below each frame's
+  // last output row (they hold no output position), walked by a TMA im2col map whose
+  // bounding box spans W x Ho x Do.  Its corners (T: -pt and pad_after - (KT - 1), H:
+  // 0 and -(KR - 1), W: 0 and 0) must lie in [-16, 15], the im2col offsets (r, t) are
+  // 16-bit.
+  const long long qc = ((long long)(Do - 1) * Ho + (Ho - 1)) * p->W + Wo;
+  const int up_t = p->pad[0].after - (p->KT - 1);
+  const bool compact_ok = flat3_ok && t.compact != 2 && p->pad[0].before <= 16 && up_t >= -16 && up_t <= 15 &&
+                          p->KR <= 17 && Ho == p->H - (p->KR - 1) && qc < 0x7fffff00LL;
+  bool flat3 = false, compact = false;
   if (t.tile_w <= 0 && t.halo != 2 && flat_ok && q_total < 0x7fffff00LL) {
     // flattened H*W: a tile is 256 consecutive positions with row pitch W
     flat = true;
@@ -346,7 +355,25 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
     rh = 1;
     const long long tiles2 = (long long)Do * cdiv(q_total, std::min<long long>(256, round_up(q_total, 16)));
     const long long tiles3 = cdiv(q3, std::min<long long>(256, round_up(q3, 16)));
-    if (flat3_ok && Do > 1 && tiles3 < tiles2) {
+    const long long tilesc = cdiv(qc, std::min<long long>(256, round_up(qc, 16)));
+    // Automatic only when it saves a round of tiles or 3 % of them, and not where the
+    // paired last chunks would apply (the compact map has no half-width form).
+    // (Ladder 256 -> 256 on [9, 64, 64] with a 1-pixel halo: 149 tiles against 153 per
+    // channel tile, two rounds of 298 work items on 152 SMs instead of three; 512 ->
+    // 512 on [5, 16, 16]: 6 against 7.)
+    const long long best = std::min(tiles2, flat3_ok ? tiles3 : tiles2);
+    const long long ct = cdiv(p->Cout, 128);
+    const int sms_c = num_sms();
+    const int last_c = pl->Cst - (k.n_chunks - 1) * kc;
+    const bool pair_likely = t.pair != 2 && kc == 64 && last_c <= 32 && p->KT * p->KR >= 2;
+    const bool compact_gain = tilesc < best && !pair_likely &&
+                              (cdiv(tilesc * ct, sms_c) < cdiv(best * ct, sms_c) ||
+                               tilesc * 100 <= best * 97);
+    if (compact_ok && Do > 1 && (t.compact == 1 || compact_gain)) {
+      flat3 = true;
+      compact = true;
+      q_total = qc;
+    } else if (flat3_ok && Do > 1 && tiles3 < tiles2) {
       flat3 = true;
       q_total = q3;
     }
@@ -451,6 +478,7 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.halo = halo ? 1 : 0;
   k.flat = flat ? 1 : 0;
   k.flat3 = flat3 ? 1 : 0;
+  k.compact = compact ? 1 : 0;
   k.tiles_d = flat3 ? 1 : Do;
   if (flat) {
     k.nbox = static_cast<int>(cdiv(tw + p->KS - 1, 256));
@@ -612,7 +640,7 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   const int last_ch = pl->Cst - (k.n_chunks - 1) * kc;
   const bool reflect_w_pad =
       p->pad[2].mode == CONV3D_PAD_REFLECT && (p->pad[2].before || p->pad[2].after);
-  const bool pair_ok = t.pair != 2 && !pm && !up2 && halo && kc == 64 && last_ch >= 1 &&
+  const bool pair_ok = t.pair != 2 && !pm && !up2 && !compact && halo && kc == 64 && last_ch >= 1 &&
                        last_ch <= 32 && n_pairs >= 2 && !reflect_w_pad;
   int splits = 0;
   if (pair_ok) {
@@ -1211,6 +1239,25 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+using EncodeIm2colFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                    const cuuint64_t*, const cuuint64_t*, const int*, const int*,
+                                    cuuint32_t, cuuint32_t, const cuuint32_t*,
+                                    CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeIm2colFn encode_im2col_fn() {
+  static EncodeIm2colFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeIm2colFn>(ptr);
+  }
+  return fn;
+}
+
 CUtensorMapSwizzle swizzle_of(int kc) {
   return kc == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
                   : (kc == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
@@ -1284,7 +1331,9 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
     esA[2] = (cuuint32_t)pl.cp.sh;
   }
   cuuint32_t rankA = 5;
-  if (flat && pl.cm && pl.cp.flat3) {
+  if (flat && pl.cm && pl.cp.compact) {
+    // the compact form's im2col map keeps the five dimensions (encoded below)
+  } else if (flat && pl.cm && pl.cp.flat3) {
     // D, H and W merged into one dimension of D*H*W positions (dims C, D*H*W, 1, N)
     gdimA[1] = (cuuint64_t)p->D * p->H * p->W;
     gdimA[2] = 1;
@@ -1301,9 +1350,25 @@ int encode_maps(const conv3d_params* p, const Plan& pl, const void* xin, CUtenso
     gstrA[2] = gstrA[3];
     rankA = 4;
   }
-  CUresult r = enc(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rankA, const_cast<void*>(xin), gdimA,
-                   gstrA, boxA, esA, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kc),
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r;
+  if (flat && pl.cm && pl.cp.compact) {
+    // compact volume: an im2col map over (C, W, H, D, N) whose traversal walks W x Ho x
+    // Do from (0, 0, -pt); corner arrays in W, H, D order.  Box = kc channels x box_w
+    // pixels of the traversal.
+    EncodeIm2colFn enc2 = encode_im2col_fn();
+    if (!enc2) return CONV3D_ERR_CUDA;
+    const int lo[3] = {0, 0, -p->pad[0].before};
+    const int up[3] = {0, -(p->KR - 1), p->pad[0].after - (p->KT - 1)};
+    const cuuint32_t es1[5] = {1, 1, 1, 1, 1};
+    r = enc2(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(xin), gdimA, gstrA, lo,
+             up, (cuuint32_t)kc, (cuuint32_t)act_box, es1, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle_of(kc), CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    r = enc(tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rankA, const_cast<void*>(xin), gdimA, gstrA,
+            boxA, esA, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kc),
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) return CONV3D_ERR_CUDA;
   // packed weights [Cout][taps * cp64]: one box = kc channels x wgt_rows output channels
   const cuuint64_t Ktot = (cuuint64_t)p->KT * p->KR * p->KS * cp64;
@@ -1489,7 +1554,7 @@ int conv3d_plan(const conv3d_params* p, const conv3d_tuning* tuning, conv3d_plan
     r.k_splits = k.k_splits;
     r.paired = k.pair;
     r.bulk_store = k.tma_store;
-    r.flat = k.flat ? (k.flat3 ? 2 : 1) : 0;
+    r.flat = k.flat ? (k.flat3 ? (k.compact ? 3 : 2) : 1) : 0;
   } else {
     const ConvTCParams& k = pl.kp;
     r.kernel = 1;
@@ -1831,7 +1896,7 @@ const char* conv3d_status_string(int status) {
   }
 }
 
-int conv3d_version(void) { return 310; }
+int conv3d_version(void) { return 320; }
 
 }  // extern "C"
 

@@ -213,7 +213,7 @@ __device__ __forceinline__ void tile_stage_range(const ConvCMParams& p, const Ti
   if (kPair || kGather || !p.skip_pad) return;
   int f_lo = tc.od, f_hi = tc.od;  // output frames of the tile
   if (p.flat3) {
-    const int plane = p.H * p.W;
+    const int plane = (p.compact ? p.epi.Ho : p.H) * p.W;
     f_lo = (tc.twi * p.tw) / plane;
     f_hi = (tc.twi * p.tw + p.tw - 1) / plane;
   }
@@ -511,6 +511,23 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         int it_b, it_e;
         tile_stage_range<kPair, kGather>(p, tc, it_b, it_e);
         StageCoord sc = kPair ? pair_begin(p) : decode_stage(p, it_b);
+        // compact volume tiles: the traversal start (w, h, d) of each activation box; a
+        // box that would start past the volume's last position starts there instead (its
+        // positions are past the end and never stored), so every start lies inside the
+        // map's bounding box
+        int cq_w[2] = {0, 0}, cq_h[2] = {0, 0}, cq_d[2] = {0, 0};
+        if (p.compact && act_role) {
+          const int plane = p.epi.Ho * p.W;
+          const int q_last = p.epi.Do * plane - 1;
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            const int q = min(w0 + b * p.box_w, q_last);
+            cq_d[b] = q / plane;
+            const int rem = q - cq_d[b] * plane;
+            cq_h[b] = rem / p.W;
+            cq_w[b] = rem - cq_h[b] * p.W;
+          }
+        }
         // weight L2 prefetch (plain schedule): pf runs wpref stages ahead of sc
         const bool pref = !kPair && !act_role && p.wpref > 0;
         StageCoord pf = sc;
@@ -592,6 +609,17 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
                               x0 + s * p.cp64, c0);
                 }
               }
+            } else if (p.flat && p.compact) {
+              // compact volume: traversal position (w, h, d) of tap (t, r) reads input
+              // frame d - pt + t, row h + r; the KS W taps are consecutive positions of
+              // the run
+#pragma unroll
+              for (int b = 0; b < 2; ++b)
+                if (b < p.nbox)
+                  tma_load_im2col_5d(act + static_cast<uint32_t>(b * p.box_w * p.row_bytes),
+                                     &tmAct, full, sc.ch * p.kc, cq_w[b], cq_h[b],
+                                     cq_d[b] - p.pt, tc.nb, 0, static_cast<uint16_t>(sc.r),
+                                     static_cast<uint16_t>(sc.t));
             } else if (p.flat) {
               // flattened (H*W) positions: output q reads input q + (r - ph) * W + s;
               // flattened (D*H*W) positions: q + ((t - pt) * H + r - ph) * W + s
@@ -958,7 +986,7 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
       t.hoff = p.flat ? 0 : t.h0;
       t.woff = p.flat ? 0 : t.w0;
       t.jlim = p.flat ? p.W : p.tw;
-      t.vrows = p.flat3 ? p.H : 0;
+      t.vrows = p.flat3 ? (p.compact ? p.epi.Ho : p.H) : 0;
       t.cls = tc.cls;
       return t;
     };

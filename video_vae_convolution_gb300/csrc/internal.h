@@ -124,6 +124,10 @@ struct ConvCMParams {
                            // positions of the flattened volume and may span frames
                            // (needs stride 1 and no H / W padding; T zero padding reads
                            // positions outside the volume)
+  int compact;             // 1 (with flat3): the flattened volume leaves out the KR - 1
+                           // input rows below each frame's last output row, so a tile of
+                           // tw positions covers output rows only; the activation map is
+                           // an im2col map whose traversal runs over (W, Ho, Do)
   int tiles_d;             // output frames in the tile index (1 with flat3)
   int skip_pad;            // 1: tiles leave out the stages whose temporal tap reads only
                            // T padding

@@ -93,6 +93,21 @@ __device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* map, uint3
       : "memory");
 }
 
+// im2col copy of a 5-D NDHWC map: the box's pixels follow the map's traversal (W
+// fastest, then H, D and N, each within the map's bounding box) from the start
+// coordinate (c, w, h, d, n); pixel (w, h, d) of the traversal reads the input at
+// (w + ow, h + oh, d + od).  The start must lie inside the bounding box.
+__device__ __forceinline__ void tma_load_im2col_5d(uint32_t dst, const void* map, uint32_t bar,
+                                                   int c, int w, int h, int d, int n,
+                                                   uint16_t ow, uint16_t oh, uint16_t od) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2], {%8, %9, %10};" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c), "r"(w), "r"(h), "r"(d), "r"(n),
+      "h"(ow), "h"(oh), "h"(od)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, uint32_t bar, int c0,
                                             int c1, int c2, int c3) {
   asm volatile(
