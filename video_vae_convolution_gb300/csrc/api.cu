@@ -481,7 +481,8 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   k.compact = compact ? 1 : 0;
   k.tiles_d = flat3 ? 1 : Do;
   if (flat) {
-    k.nbox = static_cast<int>(cdiv(tw + p->KS - 1, 256));
+    // (an im2col box takes up to 1024 pixels: one box a stage in the compact form)
+    k.nbox = compact ? 1 : static_cast<int>(cdiv(tw + p->KS - 1, 256));
     k.box_w = k.nbox == 1 ? tw + p->KS - 1
                           : static_cast<int>(round_up(cdiv(tw + p->KS - 1, k.nbox), 8));
     k.run_pitch = k.nbox * k.box_w;

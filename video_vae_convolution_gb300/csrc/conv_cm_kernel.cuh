@@ -511,10 +511,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1)
         int it_b, it_e;
         tile_stage_range<kPair, kGather>(p, tc, it_b, it_e);
         StageCoord sc = kPair ? pair_begin(p) : decode_stage(p, it_b);
-        // compact volume tiles: the traversal start (w, h, d) of each activation box; a
-        // box that would start past the volume's last position starts there instead (its
-        // positions are past the end and never stored), so every start lies inside the
-        // map's bounding box
+        // compact volume tiles: the traversal start (w, h, d) of each activation box (one
+        // box a stage as planned; two kept for generality); a box that would start past
+        // the volume's last position starts there instead (its positions are past the end
+        // and never stored), so every start lies inside the map's bounding box
         int cq_w[2] = {0, 0}, cq_h[2] = {0, 0}, cq_d[2] = {0, 0};
         if (p.compact && act_role) {
           const int plane = p.epi.Ho * p.W;
