@@ -54,7 +54,7 @@ KERNEL_SOURCES = ["conv_cm.cu", "conv_cm_kernel.cuh", "conv_cm_halo.cu", "epilog
                   "ptx.cuh", "internal.h"]
 NCU_TRAFFIC = {
     # profiles/conv_cm_ladder_L0_halo.md: L0_0 as in the haloed ladder chain
-    ("7ec4ecfeedaf012b", "L0_0"): 290746112 + 251861760,
+    ("ff151339c2fd4ecf", "L0_0"): 290725376 + 251654144,
 }
 
 
@@ -384,6 +384,50 @@ def time_alone(c, stream, flush, reps, warm=2):
     return statistics.median(a.elapsed_time(b) for a, b in ts)
 
 
+# streaming causal convolution (cuDNN frontend doc, "Causal Conv3D with Cache"): one
+# 4-frame NCTHW chunk of the 12-channel (2x2 patchified RGB) input after two history
+# frames, 12 -> 160 at the 160-channel blocks' [104, 180] plane
+CAUSAL_CHUNK = (1, 12, 4, 104, 180)
+CAUSAL_COUT = 160
+
+
+def causal_cache_row(dev, stream, flush, pk, reps):
+    """The packing launch and the convolution of one chunk, timed together."""
+    import video_vae_convolution_gb300 as vvc
+    N, C, T, H, W = CAUSAL_CHUNK
+    Co = CAUSAL_COUT
+    g = torch.Generator(device=dev)
+    g.manual_seed(20250)
+    x = torch.randn(CAUSAL_CHUNK, generator=g, device=dev).to(torch.bfloat16)
+    prev = torch.randn((N, 2, H, W, C), generator=g, device=dev).to(torch.bfloat16)
+    w = (torch.randn((Co, C, 3, 3, 3), generator=g, device=dev) * (C * 27) ** -0.5).to(
+        torch.bfloat16)
+    cc = vvc.CausalConv3dWithCache(CAUSAL_CHUNK, vvc.pack_weight(w), Co, history_frames=2,
+                                   device=dev)
+
+    class Step:
+        def run(self, s):
+            cc(x, prev, s)
+            return 0
+
+        def __call__(self, s):
+            return self.run(s)
+
+    ms = time_alone(Step(), stream, flush, reps)
+    flop = 2.0 * N * T * H * W * Co * C * 27
+    nbytes = 2 * (x.numel() + prev.numel() + N * T * H * W * Co + N * 2 * H * W * C +
+                  w.numel())
+    tf = flop / (ms * 1e-3) / 1e12
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": "causal_cache", "name": "causal_12to160_chunk4_hist2",
+            "layout": "NCTHW in, NDHWC out", "cin": C, "cout": Co, "kernel": [3, 3, 3],
+            "stride": [1, 1, 1], "ms": round(ms, 4), "tflops": round(tf, 1),
+            "frac_bf16": round(tf / pk["bf16_tflops"], 3), "gbs": round(gbs, 1),
+            "frac_hbm": round(gbs / pk["hbm_gbs"], 3), "launches": cc.launches,
+            "timed": "packing (history, causal and spatial zeros, 12 -> 16 channels, cache) "
+                     "and the valid convolution, alone; FLOP of the 12 real channels"}
+
+
 def other_layers(dev, stream, flush, pk, reps):
     """Per-call rows of the Wan-like chain (both layouts), the fused 160 blocks, the
     T=1 image-VAE layers (both layouts) and the decoder's upsample convolutions (x2
@@ -407,6 +451,7 @@ def other_layers(dev, stream, flush, pk, reps):
                 sums[key] = sums.get(key, 0.0) + ms
                 del c, wp, inp
         torch.cuda.empty_cache()
+    rows.append(causal_cache_row(dev, stream, flush, pk, reps))
     wan_flop = sum(c.flops for c in wl.wan().calls)
     wan = {"calls": "3 shapes, each NCDHW->NCDHW and NDHWC->NDHWC, timed alone",
            "ms_ndhwc": round(sums[("wan", "NDHWC")], 4),
@@ -862,6 +907,18 @@ def run_norm_pad(args):
     return 0
 
 
+def run_causal_cache(args):
+    """The streaming causal 12 -> 160 call (packing + convolution) timed alone, as the
+    bench line's causal_cache row."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    row = causal_cache_row(dev, stream, flush, peaks(), max(3, args.steps))
+    print(json.dumps(row), flush=True)
+    return 0
+
+
 def run_group_norm(args):
     """Channels-last GroupNorm + SiLU with time-isolated groups, timed alone."""
     import video_vae_convolution_gb300 as vvc
@@ -926,10 +983,14 @@ def main():
                     help="time the standalone padded post-operations: C,T,H,W,P")
     ap.add_argument("--group-norm", default="",
                     help="time the channels-last GroupNorm + SiLU: C,D,H,W,groups")
+    ap.add_argument("--causal-cache", action="store_true",
+                    help="time the streaming causal 12 -> 160 call (packing + convolution)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl != "reference" else args.warmup
     if args.group_norm:
         return run_group_norm(args)
+    if args.causal_cache:
+        return run_causal_cache(args)
     if args.norm_pad:
         return run_norm_pad(args)
     if args.case:

@@ -360,6 +360,30 @@ int l2norm_silu_pad(const void* x, int32_t N, int32_t T, int32_t H, int32_t W, i
                     void* padded_out, void* cache_out, void* value_out,
                     conv3d_stream_t stream);
 
+/* ---- streaming causal convolution: input packing ([cuDNN page] "Causal Conv3D with
+ *      Cache", and the "CausalConv3dWithCacheSm100" row of the API table: input/history
+ *      packing with padding, then the convolution without bias) -------------------------
+ * Builds the padded channels-last input of one chunk of a causal 3x3x3 convolution and
+ * the raw history for the next chunk.
+ * x: the chunk, bf16 [N, C, T, H, W] (NCTHW) at non-negative element strides
+ *    x_strides[5] = (n, c, t, h, w); any view of device memory, 2-byte aligned.
+ * previous: raw history frames, bf16 [N, history_frames, H, W, C] contiguous, 8-byte
+ *    aligned; NULL exactly when history_frames = 0 (0, 1 or 2).
+ * padded: bf16 [N, T + 2, H + 2, W + 2, Cp] contiguous (Cp >= C, Cp % 8 == 0, Cp <= 256;
+ *    12 -> 16 on the page): planes 0 and 1 are the two frames before the chunk (history
+ *    frames, a zero plane for each missing one: the causal padding), planes 2 .. T + 1
+ *    the chunk; a one-pixel zero border in H and W; channels C .. Cp - 1 zero.
+ * cache_out: bf16 [N, min(2, T + history_frames), H, W, C] contiguous, the last frames of
+ *    [history..., chunk...] in order: the next chunk's previous.
+ * padded and cache_out 16-byte aligned, overlapping neither each other nor an input.
+ * The chunk's output is then conv3d_fwd over padded: NDHWC, Cin = Cp, valid padding,
+ * weights packed by conv3d_pack_weight from [Cout, C, 3, 3, 3] (the packed layout pads
+ * input channels to 64 with zeros, so it serves Cin = Cp as well).  One launch on
+ * `stream`; nothing is allocated. */
+int conv3d_causal_pack(const void* x, const int64_t* x_strides, int32_t N, int32_t C, int32_t T,
+                       int32_t H, int32_t W, const void* previous, int32_t history_frames,
+                       void* padded, int32_t Cp, void* cache_out, conv3d_stream_t stream);
+
 /* ---- channels-last GroupNorm (+ SiLU) ([FlyDSL issue] MiniMax-H3 comment, "An extra
  *      argument for NDHWC": the GroupNorm between the encoder's convolutions, with
  *      time-isolated groups) ------------------------------------------------------------
@@ -392,7 +416,8 @@ const char* conv3d_status_string(int status);
  * history_frames, conv3d_tuning gained pair; conv3d_plan, l2norm_silu_pad and the GroupNorm
  * calls were added.  3.00: conv3d_params gained out_halo and input_upsample.  3.10:
  * conv3d_params gained dtype and fp8_scale; conv3d_pack_weight_e4m3 and
- * conv3d_packed_weight_bytes_e4m3 were added.  3.20: conv3d_tuning gained compact. */
+ * conv3d_packed_weight_bytes_e4m3 were added.  3.20: conv3d_tuning gained compact;
+ * conv3d_causal_pack was added. */
 int conv3d_version(void);
 
 /* sizeof() of the ABI structs, for bindings to check their mirrors:

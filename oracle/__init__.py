@@ -18,7 +18,7 @@ Sources (web pages, cited by title and section):
 * [cuDNN-PO] cuDNN frontend doc "Fused Conv3D + Bias + Residual + RMSNorm +
   SiLU" — the Operation Contract (rounding points), "Weight Packing",
   "Normalization and Padding Variant", "Standalone Normalization and Padding
-  Variant", "Spatial Padding Variant".
+  Variant", "Spatial Padding Variant", "Causal Conv3D with Cache".
 
 bf16 values are carried as ``numpy.uint16`` bit patterns throughout.
 
@@ -337,6 +337,34 @@ def pad_cache_standalone(act, previous=None):
         assert prev.shape == (N, P, H, W, C) and 1 <= P <= 2
         padded[:, 2 - P:2, 1:-1, 1:-1, :] = prev
         seq = np.concatenate([prev, act], axis=1)
+    K = min(2, seq.shape[1])
+    return padded, np.ascontiguousarray(seq[:, seq.shape[1] - K:])
+
+
+def causal_pack(chunk_ncthw, previous=None, Cp=16):
+    """Input packing of the streaming causal convolution ([cuDNN-PO], "Causal Conv3D
+    with Cache": history frames inserted before the chunk, causal and spatial zeros,
+    channels padded 12 -> 16; the raw history returned for the next chunk).
+
+    chunk_ncthw: the chunk [N, C, T, H, W] (bf16 bits); previous: None or the P = 1 or
+    2 raw history frames [N, P, H, W, C].  Returns (padded [N, T + 2, H + 2, W + 2, Cp],
+    cache [N, min(2, T + P), H, W, C]): the frames [previous..., chunk...] channels-last
+    end at plane T + 1 (zero planes before the history, a zero spatial border, channels
+    C .. Cp - 1 zero), and the cache holds the last min(2, T + P) of them.  A valid
+    3x3x3 convolution over padded is the chunk's causal (T: 2 before) and zero-padded
+    (H, W: 1 each side) convolution continuing the earlier frames.
+    """
+    x = np.transpose(_u16(chunk_ncthw), (0, 2, 3, 4, 1))  # -> [N, T, H, W, C]
+    N, T, H, W, C = x.shape
+    assert C <= Cp
+    seq = x
+    if previous is not None:
+        prev = _u16(previous)
+        assert prev.shape[0] == N and prev.shape[2:] == (H, W, C) and 1 <= prev.shape[1] <= 2
+        seq = np.concatenate([prev, x], axis=1)
+    P = seq.shape[1] - T
+    padded = np.zeros((N, T + 2, H + 2, W + 2, Cp), dtype=np.uint16)
+    padded[:, 2 - P:, 1:-1, 1:-1, :C] = seq
     K = min(2, seq.shape[1])
     return padded, np.ascontiguousarray(seq[:, seq.shape[1] - K:])
 

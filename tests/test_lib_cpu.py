@@ -206,6 +206,32 @@ def test_plan_compact_volume_tiles():
     assert info.flat == 3 and info.paired == 0
 
 
+def test_causal_pack_validation():
+    lib = vvc._lib()
+    st = (ctypes.c_int64 * 5)(12 * 4 * 8 * 10, 4 * 8 * 10, 8 * 10, 10, 1)  # contiguous NCTHW
+
+    def call(x=0x100000, strides=st, N=1, C=12, T=4, H=8, W=10, prev=None, P=0,
+             padded=0x200000, Cp=16, cache=0x300000):
+        return lib.conv3d_causal_pack(x, strides, N, C, T, H, W, prev, P, padded, Cp, cache,
+                                      None)
+
+    assert call(x=None) == vvc.ERR_INVALID_ARG
+    assert call(strides=None) == vvc.ERR_INVALID_ARG
+    assert call(Cp=8) == vvc.ERR_INVALID_ARG                 # Cp < C
+    assert call(Cp=20) == vvc.ERR_INVALID_ARG                # Cp not a multiple of 8
+    assert call(P=3, prev=0x400000) == vvc.ERR_INVALID_ARG   # at most two history frames
+    assert call(P=1) == vvc.ERR_INVALID_ARG                  # history frames without history
+    assert call(prev=0x400000) == vvc.ERR_INVALID_ARG        # history without frames
+    neg = (ctypes.c_int64 * 5)(0, 1, 0, 0, -1)
+    assert call(strides=neg) == vvc.ERR_INVALID_ARG
+    assert call(x=0x100001) == vvc.ERR_MISALIGNED
+    assert call(prev=0x400004, P=2) == vvc.ERR_MISALIGNED    # history: 8-byte alignment
+    assert call(padded=0x200008) == vvc.ERR_MISALIGNED
+    assert call(cache=0x300008) == vvc.ERR_MISALIGNED
+    assert call(padded=0x100000 + 4096) == vvc.ERR_OVERLAP   # padded over the chunk
+    assert call(cache=0x200000 + 4096) == vvc.ERR_OVERLAP    # cache over padded
+
+
 def test_plan_bulk_store():
     # NCDHW output takes bulk stores when its rows are 16-byte multiples (Wo % 8 == 0)
     # and no NDHWC debug store runs beside them; NDHWC when Cout % 8 == 0

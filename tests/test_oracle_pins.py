@@ -492,6 +492,59 @@ def test_pad_cache_fused_plus_history_step_is_standalone(orc, P, Tc):
     assert np.array_equal(cache, ref_cache)
 
 
+# ---- streaming causal convolution: input packing with history (cuDNN frontend doc,
+#      "Causal Conv3D with Cache") -----------------------------------------------------
+
+def test_causal_pack_worked_example(orc):
+    # a 1-frame chunk of 3 channels, no history: two zero planes (the causal padding),
+    # then the frame channels-last inside a zero border, channels 3 .. 7 zero
+    x = np.arange(1, 1 + 3 * 2 * 2, dtype=np.uint16).reshape(1, 3, 1, 2, 2)  # [N, C, T, H, W]
+    padded, cache = orc.causal_pack(x, None, Cp=8)
+    assert padded.shape == (1, 3, 4, 4, 8) and cache.shape == (1, 1, 2, 2, 3)
+    assert not padded[:, :2].any()
+    assert padded[0, 2, 1, 1].tolist() == [1, 5, 9, 0, 0, 0, 0, 0]    # pixel (0, 0)
+    assert padded[0, 2, 2, 2].tolist() == [4, 8, 12, 0, 0, 0, 0, 0]   # pixel (1, 1)
+    assert not padded[0, 2, 0].any() and not padded[0, 2, :, 3].any()
+    assert cache[0, 0, 1, 0].tolist() == [3, 7, 11]
+    # with one history frame: plane 1 holds it, plane 0 stays zero, and the cache is
+    # [history, chunk frame]
+    prev = np.full((1, 1, 2, 2, 3), 0x4000, np.uint16)
+    padded, cache = orc.causal_pack(x, prev, Cp=8)
+    assert not padded[:, 0].any()
+    assert (padded[0, 1, 1:-1, 1:-1, :3] == 0x4000).all() and not padded[0, 1, 1:-1, 1:-1, 3:].any()
+    assert cache.shape == (1, 2, 2, 2, 3) and (cache[:, 0] == 0x4000).all()
+
+
+@pytest.mark.parametrize("chunks", [(1, 4, 4), (2, 1, 3), (5,), (1, 1, 1, 2)])
+def test_causal_pack_streaming_is_the_whole_causal_conv(orc, chunks):
+    # Chunk by chunk, each packed after the previous chunk's cache and convolved as a
+    # valid 3x3x3 convolution, the outputs are the causal (T: 2 zero frames before) and
+    # zero-padded (H, W: 1) convolution of the whole video: torch fp64 conv3d after
+    # F.pad.  The caches are the last frames of the video so far.
+    rng = np.random.default_rng(sum(chunks))
+    N, C, H, W, Co, Cp = 1, 12, 4, 5, 6, 16
+    T = sum(chunks)
+    video = rand_bf16(rng, (N, C, T, H, W))
+    w = rand_bf16(rng, (Co, C, 3, 3, 3), 0.2)
+    w16 = np.zeros((Co, Cp, 3, 3, 3), np.uint16)
+    w16[:, :C] = w
+    outs, prev, t0 = [], None, 0
+    for tc in chunks:
+        chunk = np.ascontiguousarray(video[:, :, t0:t0 + tc])
+        padded, cache = orc.causal_pack(chunk, prev, Cp=Cp)
+        outs.append(orc.conv3d_acc(padded, orc.NDHWC, w16))
+        t0 += tc
+        K = min(2, t0)
+        assert np.array_equal(cache, np.transpose(video[:, :, t0 - K:t0], (0, 2, 3, 4, 1)))
+        prev = cache
+    got = np.concatenate(outs, axis=1)
+    Z = wl.ZERO
+    ref = torch_conv(to_f64(orc, video), to_f64(orc, w), (1, 1, 1), ((2, 0, Z), (1, 1, Z), (1, 1, Z)))
+    assert got.shape == ref.shape
+    # (the oracle returns its fp64 sums rounded to fp32: half an fp32 ulp)
+    np.testing.assert_allclose(got, ref, rtol=2.0 ** -24, atol=1e-12)
+
+
 # ---- channels-last GroupNorm + SiLU (FlyDSL issue, MiniMax-H3 comment: the GroupNorm
 #      between the encoder's convolutions, time-isolated groups) -------------------------
 

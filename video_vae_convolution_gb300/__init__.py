@@ -53,7 +53,7 @@ EXPORTS = (
     "l2norm_silu", "conv3d_get_device_status", "conv3d_status_string", "conv3d_version",
     "conv3d_struct_size", "conv3d_fwd_static_scratch", "conv3d_plan", "l2norm_silu_pad",
     "group_norm_workspace_bytes", "group_norm_silu", "conv3d_packed_weight_bytes_e4m3",
-    "conv3d_pack_weight_e4m3",
+    "conv3d_pack_weight_e4m3", "conv3d_causal_pack",
 )
 
 
@@ -148,6 +148,9 @@ def _lib():
                 lib.l2norm_silu.restype = ctypes.c_int
                 lib.l2norm_silu_pad.argtypes = [vp] + [i32] * 5 + [vp] * 5 + [i32] + [vp] * 4
                 lib.l2norm_silu_pad.restype = ctypes.c_int
+                lib.conv3d_causal_pack.argtypes = ([vp, ctypes.POINTER(i64)] + [i32] * 5 +
+                                                   [vp, i32, vp, i32, vp, vp])
+                lib.conv3d_causal_pack.restype = ctypes.c_int
                 lib.group_norm_workspace_bytes.argtypes = [i32] * 7
                 lib.group_norm_workspace_bytes.restype = sz
                 lib.group_norm_silu.argtypes = ([vp] + [i32] * 7 + [ctypes.c_float, vp, vp, i32, vp,
@@ -431,6 +434,58 @@ def l2norm_silu_pad(x: torch.Tensor, gamma: torch.Tensor, input_bias=None, resid
                                   _ptr(padded), _ptr(cache), _ptr(value), _stream(stream)),
            "l2norm_silu_pad")
     return padded, cache, value
+
+
+def causal_pack(x: torch.Tensor, previous=None, Cp=None, padded=None, cache=None, stream=None):
+    """Input packing of a streaming causal 3x3x3 convolution (conv3d_causal_pack): x is
+    the chunk [N, C, T, H, W] (any strided bf16 CUDA view), previous the raw history
+    [N, P, H, W, C] (P <= 2) or None.  Returns (padded [N, T+2, H+2, W+2, Cp], cache
+    [N, min(2, T+P), H, W, C]); Cp defaults to C rounded up to 16."""
+    N, C, T, H, W = x.shape
+    P = 0 if previous is None else previous.shape[1]
+    if Cp is None:
+        Cp = (C + 15) // 16 * 16
+    if padded is None:
+        padded = torch.empty((N, T + 2, H + 2, W + 2, Cp), dtype=x.dtype, device=x.device)
+    if cache is None:
+        cache = torch.empty((N, min(2, T + P), H, W, C), dtype=x.dtype, device=x.device)
+    strides = (ctypes.c_int64 * 5)(*x.stride())
+    _check(_lib().conv3d_causal_pack(_ptr(x), strides, N, C, T, H, W, _ptr(previous), P,
+                                     _ptr(padded), Cp, _ptr(cache), _stream(stream)),
+           "conv3d_causal_pack")
+    return padded, cache
+
+
+class CausalConv3dWithCache:
+    """Streaming causal 3x3x3 convolution over chunks of an NCTHW video (cuDNN frontend
+    doc, "Causal Conv3D with Cache"): each call packs the chunk after the history of the
+    previous one (conv3d_causal_pack) and runs the valid convolution over the packed
+    input (conv3d_fwd, no bias).  Buffers are sized for one chunk shape and reused, so
+    the calls of a fixed shape can be captured in a CUDA graph.
+
+    w_packed: pack_weight of the [Cout, C, 3, 3, 3] weights.  history_frames: P of the
+    calls (0 for the first chunk of a video, then min(2, frames so far)).
+    """
+
+    def __init__(self, chunk_shape, w_packed, Cout, history_frames=0, Cp=None,
+                 device="cuda", tuning: Optional[Tuning] = None):
+        N, C, T, H, W = chunk_shape
+        self.Cp = (C + 15) // 16 * 16 if Cp is None else Cp
+        self.P = history_frames
+        self.padded = torch.empty((N, T + 2, H + 2, W + 2, self.Cp), dtype=torch.bfloat16,
+                                  device=device)
+        self.cache = torch.empty((N, min(2, T + history_frames), H, W, C), dtype=torch.bfloat16,
+                                 device=device)
+        self.conv = Conv3d(self.padded, w_packed, Cout, (3, 3, 3), (1, 1, 1),
+                           ((0, 0, PAD_ZERO),) * 3, NDHWC, NDHWC, 0, tuning=tuning)
+        self.launches = 1 + self.conv.launches
+
+    def __call__(self, x: torch.Tensor, previous=None, stream=None):
+        """Returns (output [N, T, H, W, Cout], cache [N, min(2, T+P), H, W, C])."""
+        if (0 if previous is None else previous.shape[1]) != self.P:
+            raise Conv3dError(ERR_INVALID_ARG, "CausalConv3dWithCache: history frames")
+        causal_pack(x, previous, self.Cp, self.padded, self.cache, stream)
+        return self.conv(stream), self.cache
 
 
 def group_norm_silu(x: torch.Tensor, groups: int, gamma=None, beta=None, eps=1e-6,

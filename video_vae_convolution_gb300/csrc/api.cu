@@ -1801,6 +1801,63 @@ int l2norm_silu_pad(const void* x, int32_t N, int32_t T, int32_t H, int32_t W, i
   return vvc::launch_pad_cache(a, s) == cudaSuccess ? CONV3D_OK : CONV3D_ERR_CUDA;
 }
 
+int conv3d_causal_pack(const void* x, const int64_t* x_strides, int32_t N, int32_t C, int32_t T,
+                       int32_t H, int32_t W, const void* previous, int32_t history_frames,
+                       void* padded, int32_t Cp, void* cache_out, conv3d_stream_t stream) {
+  if (!x || !x_strides || !padded || !cache_out || N < 1 || C < 1 || T < 1 || H < 1 ||
+      W < 1 || Cp < C || Cp % 8 != 0 || Cp > 256 || history_frames < 0 || history_frames > 2 ||
+      (history_frames > 0) != (previous != nullptr))
+    return CONV3D_ERR_INVALID_ARG;
+  const int64_t dims[5] = {N, C, T, H, W};
+  long long x_last = 0;  // element offset of the chunk's last element
+  for (int i = 0; i < 5; ++i) {
+    if (x_strides[i] < 0) return CONV3D_ERR_INVALID_ARG;
+    x_last += (long long)(dims[i] - 1) * x_strides[i];
+  }
+  const long long padded_px = (long long)N * (T + 2) * (H + 2) * (W + 2);
+  const int K = std::min(2, T + history_frames);
+  const long long cache_px = (long long)N * K * H * W;
+  if (padded_px > (1LL << 40) / Cp || x_last > (1LL << 42)) return CONV3D_ERR_UNSUPPORTED;
+  const uintptr_t ax = reinterpret_cast<uintptr_t>(x);
+  if ((ax & 1u) || (reinterpret_cast<uintptr_t>(previous) & 7u) ||
+      (reinterpret_cast<uintptr_t>(padded) & 15u) || (reinterpret_cast<uintptr_t>(cache_out) & 15u))
+    return CONV3D_ERR_MISALIGNED;
+  auto span = [](const void* q, size_t bytes) {
+    Span sp;
+    sp.lo = reinterpret_cast<uintptr_t>(q);
+    sp.hi = q ? sp.lo + bytes : sp.lo;
+    return sp;
+  };
+  const Span in[] = {span(x, (size_t)(x_last + 1) * 2),
+                     span(previous, (size_t)N * history_frames * H * W * C * 2)};
+  const Span out[] = {span(padded, (size_t)padded_px * Cp * 2),
+                      span(cache_out, (size_t)cache_px * C * 2)};
+  for (const Span& o : out)
+    for (const Span& sp : in)
+      if (overlaps(o, sp)) return CONV3D_ERR_OVERLAP;
+  if (overlaps(out[0], out[1])) return CONV3D_ERR_OVERLAP;
+  vvc::CausalPackArgs a{};
+  a.x = static_cast<const uint16_t*>(x);
+  a.sx_n = x_strides[0];
+  a.sx_c = x_strides[1];
+  a.sx_t = x_strides[2];
+  a.sx_h = x_strides[3];
+  a.sx_w = x_strides[4];
+  a.prev = static_cast<const uint16_t*>(previous);
+  a.padded = static_cast<uint16_t*>(padded);
+  a.cache = static_cast<uint16_t*>(cache_out);
+  a.N = N;
+  a.C = C;
+  a.Cp = Cp;
+  a.T = T;
+  a.H = H;
+  a.W = W;
+  a.P = history_frames;
+  a.K = K;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return vvc::launch_causal_pack(a, s) == cudaSuccess ? CONV3D_OK : CONV3D_ERR_CUDA;
+}
+
 namespace {
 // Geometry of a GroupNorm call; false when the shape is not supported.
 bool group_norm_shape(int32_t N, int32_t D, int32_t H, int32_t W, int32_t C, int32_t groups,

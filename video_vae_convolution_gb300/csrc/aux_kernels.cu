@@ -775,6 +775,73 @@ __global__ void pad_cache_kernel(PadCacheArgs a) {
   }
 }
 
+// One item per pixel of the padded input (all Cp channels, 16-byte stores) and per pixel
+// of the cache (C channels).  Source frame s of the sequence [history..., chunk...]:
+// padded frame f holds s = f - 2 + P (a zero plane for s < 0), cache frame k holds
+// s = T + P - K + k.  Threads run along W, so each channel's reads of an NCTHW chunk
+// with unit W stride are coalesced.
+template <class I>
+__global__ void causal_pack_kernel(CausalPackArgs a) {
+  const I Tp = a.T + 2, Hp = a.H + 2, Wp = a.W + 2;
+  const I n_pad = static_cast<I>(a.N) * Tp * Hp * Wp;
+  const I n_all = n_pad + static_cast<I>(a.N) * a.K * a.H * a.W;
+  auto src = [&](long long n, int s, int h, int w, int c) -> uint32_t {
+    if (s < a.P) return a.prev[(((n * a.P + s) * a.H + h) * a.W + w) * a.C + c];
+    return a.x[n * a.sx_n + c * a.sx_c + (s - a.P) * a.sx_t + h * a.sx_h + w * a.sx_w];
+  };
+  const I step = static_cast<I>(gridDim.x) * blockDim.x;
+  for (I i = static_cast<I>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_all; i += step) {
+    if (i < n_pad) {
+      I q = i;
+      const int wp = static_cast<int>(q % Wp);
+      q /= Wp;
+      const int hp = static_cast<int>(q % Hp);
+      q /= Hp;
+      const int tp = static_cast<int>(q % Tp);
+      const long long n = static_cast<long long>(q / Tp);
+      const int s = tp - 2 + a.P;
+      const bool zero = hp == 0 || hp == Hp - 1 || wp == 0 || wp == Wp - 1 || s < 0;
+      uint16_t* dst = a.padded + static_cast<long long>(i) * a.Cp;
+      for (int g = 0; g < a.Cp; g += 8) {
+        uint32_t v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = g + 2 * e;
+          const uint32_t lo = (!zero && c < a.C) ? src(n, s, hp - 1, wp - 1, c) : 0u;
+          const uint32_t hi = (!zero && c + 1 < a.C) ? src(n, s, hp - 1, wp - 1, c + 1) : 0u;
+          v[e] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4*>(dst + g) = make_uint4(v[0], v[1], v[2], v[3]);
+      }
+    } else {
+      I q = i - n_pad;
+      uint16_t* dst = a.cache + static_cast<long long>(q) * a.C;
+      const int w = static_cast<int>(q % a.W);
+      q /= a.W;
+      const int h = static_cast<int>(q % a.H);
+      q /= a.H;
+      const int k = static_cast<int>(q % a.K);
+      const long long n = static_cast<long long>(q / a.K);
+      const int s = a.T + a.P - a.K + k;
+      for (int c = 0; c < a.C; ++c) dst[c] = static_cast<uint16_t>(src(n, s, h, w, c));
+    }
+  }
+}
+
+cudaError_t launch_causal_pack(const CausalPackArgs& a, cudaStream_t s) {
+  const long long total = (long long)a.N * (a.T + 2) * (a.H + 2) * (a.W + 2) +
+                          (long long)a.N * a.K * a.H * a.W;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 152LL * 16) blocks = 152LL * 16;
+  if (blocks < 1) blocks = 1;
+  if (total + (long long)blocks * threads < 0xFFFFFFFFLL)
+    causal_pack_kernel<uint32_t><<<static_cast<unsigned>(blocks), threads, 0, s>>>(a);
+  else
+    causal_pack_kernel<unsigned long long><<<static_cast<unsigned>(blocks), threads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pad_cache(const PadCacheArgs& a, cudaStream_t s) {
   const long long G = a.C / 8;
   const long long total = (long long)a.N * (a.Tc + 2) * (a.Hc + 2) * (a.Wc + 2) * G +

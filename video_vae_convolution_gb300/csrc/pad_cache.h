@@ -25,6 +25,21 @@ struct PadCacheArgs {
 };
 
 cudaError_t launch_pad_cache(const PadCacheArgs& a, cudaStream_t s);
+
+// Input packing of the streaming causal convolution (cuDNN frontend doc, section
+// "Causal Conv3D with Cache"): the chunk's frames after up to two history frames, a
+// zero causal plane for each missing one, a one-pixel zero border and the channels
+// padded to Cp, channels-last; and the chunk's raw history for the next call.
+struct CausalPackArgs {
+  const uint16_t* x;                   // chunk [N, C, T, H, W] at element strides:
+  long long sx_n, sx_c, sx_t, sx_h, sx_w;
+  const uint16_t* prev;                // NULL, or [N, P, H, W, C] raw history frames
+  uint16_t* padded;                    // [N, T + 2, H + 2, W + 2, Cp]
+  uint16_t* cache;                     // [N, K, H, W, C], K = min(2, T + P)
+  int N, C, Cp, T, H, W, P, K;         // Cp % 8 == 0, C <= Cp
+};
+
+cudaError_t launch_causal_pack(const CausalPackArgs& a, cudaStream_t s);
 cudaError_t launch_l2norm_silu_pad(const void* x, int N, int T, int H, int W, const EpiParams& e,
                                    cudaStream_t s);
 
