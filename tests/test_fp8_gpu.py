@@ -95,6 +95,11 @@ CASES = [
      wl.NCDHW, None),
     (wl.ConvCall("f8_c256_512_small_m", 1, 256, 3, 8, 8, 512, pads=CR, epi=wl.EPI_BIAS,
                  index=7), wl.NDHWC, None),
+    # compact volume tiles (im2col map) with e4m3 operands: a spatially haloed input with
+    # the causal T padding in the call, tiles straddling frames
+    (wl.ConvCall("f8_c128_compact", 1, 128, 5, 18, 18, 128,
+                 pads=((2, 0, Z), (0, 0, Z), (0, 0, Z)), epi=wl.EPI_BIAS, index=13),
+     wl.NDHWC, dict(compact=1, k_splits=1)),
 ]
 
 
@@ -107,6 +112,8 @@ def test_e4m3_conv_parity(case):
     gc = F8Call(call, inp, out_layout, vvc.Tuning(**tune) if tune else None)
     if tune and "k_splits" in tune:
         assert gc.c.plan.k_splits == tune["k_splits"]
+    if tune and tune.get("compact") == 1:
+        assert gc.c.plan.flat == 3
     check_conv(gc.conv, _acc(call, inp), call.name)
     _check_epilogue(call, inp, gc.conv, gc.y, out_layout)
 

@@ -200,6 +200,9 @@ def test_plan_compact_volume_tiles():
     nm = _causal(Cin=64, Cout=64, D=5, H=18, W=18)
     nm.epi, nm.gamma = vvc.EPI_L2NORM_SILU, 0x300000
     assert _plan(nm, vvc.Tuning(compact=1)).flat != 3
+    # e4m3 operands plan the same convolution over channel pairs: the same compact tiles
+    f8 = _causal(Cin=256, Cout=256, D=9, H=66, W=66, dtype=vvc.DTYPE_E4M3, fp8_scale=1.0)
+    assert (_plan(f8).flat, _plan(f8).mma_n) == (3, 256)
     # never with paired last chunks (their half-width copies use the tiled map)
     pr = _causal(Cin=96, Cout=64, D=6, H=14, W=14)
     info = _plan(pr, vvc.Tuning(compact=1, k_splits=1))
