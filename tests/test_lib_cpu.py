@@ -192,6 +192,9 @@ def test_plan_compact_volume_tiles():
     far = _causal(Cin=64, Cout=64, D=40, H=18, W=18, KT=1)
     far.pad[0].before = 17
     assert _plan(far, vvc.Tuning(compact=1)).flat != 3
+    # im2col offsets beyond the measured 0..2 (a 5-tap temporal kernel)
+    assert _plan(_causal(Cin=64, Cout=64, D=9, H=18, W=18, KT=5),
+                 vvc.Tuning(compact=1)).flat != 3
     assert _plan(_valid(Cin=64, Cout=64, D=1, H=18, W=18, KT=1),
                  vvc.Tuning(compact=1)).flat != 3
     nc = _causal(Cin=64, Cout=64, D=5, H=18, W=18)

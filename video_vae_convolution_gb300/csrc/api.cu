@@ -341,12 +341,13 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   // Compact volume: the flattened volume without the KR - 1 input rows below each frame's
   // last output row (they hold no output position), walked by a TMA im2col map whose
   // bounding box spans W x Ho x Do.  Its corners (T: -pt and pad_after - (KT - 1), H:
-  // 0 and -(KR - 1), W: 0 and 0) must lie in [-16, 15], the im2col offsets (r, t) are
-  // 16-bit.
+  // 0 and -(KR - 1), W: 0 and 0) must lie in [-16, 15]; the im2col offsets (r, t) of a
+  // copy stay within 0..2, the range measured on the hardware (KT, KR <= 3).
   const long long qc = ((long long)(Do - 1) * Ho + (Ho - 1)) * p->W + Wo;
   const int up_t = p->pad[0].after - (p->KT - 1);
-  const bool compact_ok = flat3_ok && t.compact != 2 && p->pad[0].before <= 16 && up_t >= -16 && up_t <= 15 &&
-                          p->KR <= 17 && Ho == p->H - (p->KR - 1) && qc < 0x7fffff00LL;
+  const bool compact_ok = flat3_ok && t.compact != 2 && p->pad[0].before <= 16 &&
+                          up_t >= -16 && up_t <= 15 && p->KT <= 3 && p->KR <= 3 &&
+                          Ho == p->H - (p->KR - 1) && qc < 0x7fffff00LL;
   bool flat3 = false, compact = false;
   if (t.tile_w <= 0 && t.halo != 2 && flat_ok && q_total < 0x7fffff00LL) {
     // flattened H*W: a tile is 256 consecutive positions with row pitch W
@@ -641,8 +642,8 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   const int last_ch = pl->Cst - (k.n_chunks - 1) * kc;
   const bool reflect_w_pad =
       p->pad[2].mode == CONV3D_PAD_REFLECT && (p->pad[2].before || p->pad[2].after);
-  const bool pair_ok = t.pair != 2 && !pm && !up2 && !compact && halo && kc == 64 && last_ch >= 1 &&
-                       last_ch <= 32 && n_pairs >= 2 && !reflect_w_pad;
+  const bool pair_ok = t.pair != 2 && !pm && !up2 && !compact && halo && kc == 64 &&
+                       last_ch >= 1 && last_ch <= 32 && n_pairs >= 2 && !reflect_w_pad;
   int splits = 0;
   if (pair_ok) {
     const int total = n_pairs * (k.n_chunks - 1) + (n_pairs + 1) / 2;
