@@ -238,6 +238,49 @@ def test_causal_pack_validation():
     assert call(cache=0x200000 + 4096) == vvc.ERR_OVERLAP    # cache over padded
 
 
+# The plans of the benchmark's chained ladder (spatially haloed inputs, causal T padding
+# in each call, haloed outputs but for the last call) on 152 SMs, as measured: tile form
+# (0 rows, 1 per-frame runs, 3 compact volume runs), MMA N, stages per tile, splits.
+LADDER_PLANS = {
+    "conv_in": (1, 256, 3, 1), "L0_0": (1, 256, 18, 1), "L0s": (0, 256, 54, 1),
+    "L1a": (1, 256, 18, 1), "L1_0": (1, 256, 36, 1), "L1s": (0, 256, 108, 1),
+    "L2_0": (3, 256, 36, 1), "L2s": (0, 256, 108, 3), "L3a": (3, 256, 36, 3),
+    "L3_0": (3, 256, 72, 3), "L3s": (0, 256, 216, 7), "L4_0": (3, 256, 72, 6),
+    "L5a": (3, 256, 72, 3), "L5_0": (3, 256, 144, 3), "conv_out": (3, 256, 144, 16),
+}
+
+
+def test_ladder_chain_plans():
+    import workloads as wl
+    calls = wl.ladder().calls
+    causal_t = ((2, 0, vvc.PAD_ZERO), (0, 0, vvc.PAD_ZERO), (0, 0, vvc.PAD_ZERO))
+    halo = ((0, 0, vvc.PAD_ZERO), (1, 1, vvc.PAD_REFLECT), (1, 1, vvc.PAD_REFLECT))
+    seen = 0
+    for i, call in enumerate(calls):
+        first, last = i == 0, i == len(calls) - 1
+        p = vvc.Params()
+        p.x, p.w_packed, p.y = 0x100000000, 0x200000000, 0x400000000
+        p.workspace, p.workspace_bytes = 0x800000000, 1 << 34
+        p.layout = p.out_layout = vvc.NDHWC
+        p.N, p.Cin, p.Cout = call.N, call.Cin, call.Cout
+        p.D, p.H, p.W = call.D, call.H + (0 if first else 2), call.W + (0 if first else 2)
+        p.KT, p.KR, p.KS = call.kernel
+        pads = ([(b, a, vvc.PAD_ZERO if m == wl.ZERO else vvc.PAD_REFLECT)
+                 for b, a, m in call.pads] if first else causal_t)
+        for d in range(3):
+            p.stride[d] = call.stride[d]
+            p.pad[d].before, p.pad[d].after, p.pad[d].mode = pads[d]
+            if not last:
+                p.out_halo[d].before, p.out_halo[d].after, p.out_halo[d].mode = halo[d]
+        info = _plan(p)
+        assert info.kernel == 2, call.name
+        if call.name in LADDER_PLANS:
+            seen += 1
+            got = (info.flat, info.mma_n, info.stages_per_tile, info.k_splits)
+            assert got == LADDER_PLANS[call.name], (call.name, got)
+    assert seen == len(LADDER_PLANS)
+
+
 def test_plan_bulk_store():
     # NCDHW output takes bulk stores when its rows are 16-byte multiples (Wo % 8 == 0)
     # and no NDHWC debug store runs beside them; NDHWC when Cout % 8 == 0
