@@ -350,6 +350,11 @@ def device_inputs(call, dev, layout, seed):
     return out
 
 
+# HBM bandwidth the targets are written against (nominal; the measured copy rate is the
+# roofline denominator)
+HBM_NOMINAL_GBS = 8000.0
+
+
 def layer_row(call, ms, pk, launches, layout, workload, extra=None):
     tf = call.flops / (ms * 1e-3) / 1e12
     gbs = call.bytes() / (ms * 1e-3) / 1e9
@@ -357,8 +362,10 @@ def layer_row(call, ms, pk, launches, layout, workload, extra=None):
            "layout": "NCDHW" if layout == wl.NCDHW else "NDHWC",
            "cin": call.Cin, "cout": call.Cout, "kernel": list(call.kernel),
            "stride": list(call.stride), "ms": round(ms, 4), "tflops": round(tf, 1),
-           "frac_bf16": round(tf / pk["bf16_tflops"], 3), "gbs": round(gbs, 1),
-           "frac_hbm": round(gbs / pk["hbm_gbs"], 3), "launches": launches}
+           "frac_bf16": round(tf / pk["bf16_tflops"], 3),
+           "frac_bf16_sustained": round(tf / pk["bf16_tflops_sustained"], 3),
+           "gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3),
+           "frac_hbm_nominal": round(gbs / HBM_NOMINAL_GBS, 3), "launches": launches}
     if extra:
         row.update(extra)
     return row
@@ -422,8 +429,10 @@ def causal_cache_row(dev, stream, flush, pk, reps):
     return {"workload": "causal_cache", "name": "causal_12to160_chunk4_hist2",
             "layout": "NCTHW in, NDHWC out", "cin": C, "cout": Co, "kernel": [3, 3, 3],
             "stride": [1, 1, 1], "ms": round(ms, 4), "tflops": round(tf, 1),
-            "frac_bf16": round(tf / pk["bf16_tflops"], 3), "gbs": round(gbs, 1),
-            "frac_hbm": round(gbs / pk["hbm_gbs"], 3), "launches": cc.launches,
+            "frac_bf16": round(tf / pk["bf16_tflops"], 3),
+            "frac_bf16_sustained": round(tf / pk["bf16_tflops_sustained"], 3),
+            "gbs": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 3),
+            "frac_hbm_nominal": round(gbs / HBM_NOMINAL_GBS, 3), "launches": cc.launches,
             "timed": "packing (history, causal and spatial zeros, 12 -> 16 channels, cache) "
                      "and the valid convolution, alone; FLOP of the 12 real channels"}
 

@@ -25,3 +25,16 @@ def test_source_code_only_drops_comments_and_whitespace():
     finally:
         bench.KERNEL_SOURCES = saved
 
+
+
+def test_layer_row_fractions():
+    import workloads as wl
+    call = wl.ladder().calls[1]  # 128 -> 128 at [17, 256, 256]
+    pk = {"bf16_tflops": 2000.0, "bf16_tflops_sustained": 1600.0, "hbm_gbs": 6400.0}
+    ms = call.flops / 1000e12 * 1e3  # 1000 TFLOP/s
+    row = bench.layer_row(call, ms, pk, 1, wl.NDHWC, "ladder")
+    assert abs(row["tflops"] - 1000.0) < 0.2
+    assert row["frac_bf16"] == 0.5 and row["frac_bf16_sustained"] == 0.625
+    gbs = call.bytes() / (ms * 1e-3) / 1e9
+    assert abs(row["frac_hbm"] - gbs / 6400.0) < 1e-3
+    assert abs(row["frac_hbm_nominal"] - gbs / 8000.0) < 1e-3
