@@ -192,6 +192,9 @@ def test_plan_compact_volume_tiles():
     far = _causal(Cin=64, Cout=64, D=40, H=18, W=18, KT=1)
     far.pad[0].before = 17
     assert _plan(far, vvc.Tuning(compact=1)).flat != 3
+    # a partial last channel chunk (112 = 64 + 48 channels)
+    assert _plan(_causal(Cin=112, Cout=64, D=5, H=18, W=18),
+                 vvc.Tuning(compact=1, pair=2)).flat != 3
     # im2col offsets beyond the measured 0..2 (a 5-tap temporal kernel)
     assert _plan(_causal(Cin=64, Cout=64, D=9, H=18, W=18, KT=5),
                  vvc.Tuning(compact=1)).flat != 3
@@ -206,10 +209,11 @@ def test_plan_compact_volume_tiles():
     # e4m3 operands plan the same convolution over channel pairs: the same compact tiles
     f8 = _causal(Cin=256, Cout=256, D=9, H=66, W=66, dtype=vvc.DTYPE_E4M3, fp8_scale=1.0)
     assert (_plan(f8).flat, _plan(f8).mma_n) == (3, 256)
-    # never with paired last chunks (their half-width copies use the tiled map)
+    # never with paired last chunks (their half-width copies use the tiled map): a
+    # 96-channel input keeps the tiled volume tiles and pairs its last chunks
     pr = _causal(Cin=96, Cout=64, D=6, H=14, W=14)
     info = _plan(pr, vvc.Tuning(compact=1, k_splits=1))
-    assert info.flat == 3 and info.paired == 0
+    assert info.flat == 2 and info.paired == 1
 
 
 def test_causal_pack_validation():

@@ -342,12 +342,13 @@ int plan_cm(const conv3d_params* p, const conv3d_tuning& t, Plan* pl, size_t off
   // last output row (they hold no output position), walked by a TMA im2col map whose
   // bounding box spans W x Ho x Do.  Its corners (T: -pt and pad_after - (KT - 1), H:
   // 0 and -(KR - 1), W: 0 and 0) must lie in [-16, 15]; the im2col offsets (r, t) of a
-  // copy stay within 0..2, the range measured on the hardware (KT, KR <= 3).
+  // copy stay within 0..2, the range measured on the hardware (KT, KR <= 3); every
+  // channel chunk lies inside the tensor (the tiled maps zero-fill a partial last chunk).
   const long long qc = ((long long)(Do - 1) * Ho + (Ho - 1)) * p->W + Wo;
   const int up_t = p->pad[0].after - (p->KT - 1);
   const bool compact_ok = flat3_ok && t.compact != 2 && p->pad[0].before <= 16 &&
                           up_t >= -16 && up_t <= 15 && p->KT <= 3 && p->KR <= 3 &&
-                          Ho == p->H - (p->KR - 1) && qc < 0x7fffff00LL;
+                          pl->Cst % kc == 0 && Ho == p->H - (p->KR - 1) && qc < 0x7fffff00LL;
   bool flat3 = false, compact = false;
   if (t.tile_w <= 0 && t.halo != 2 && flat_ok && q_total < 0x7fffff00LL) {
     // flattened H*W: a tile is 256 consecutive positions with row pitch W
